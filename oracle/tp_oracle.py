@@ -1,0 +1,439 @@
+"""fp64 CPU oracle for the Megatron tensor-parallel transformer block.
+
+TEST INFRASTRUCTURE ONLY.  This module is the yardstick the CUDA path is measured
+against; it is imported by ``tests/``, by ``__graft_entry__.smoke()`` and by the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` and by nothing else.
+The product path (``tensor_transformer_block_gb300``) never imports it, and it
+never imports the product path: the two share no code.  Inputs reach it as plain
+numpy arrays (the seeded generators live in a module of their own).
+
+Everything is computed in float64 from the *unsharded* definitions, because the
+tensor-parallel method reaches exactly the same numbers (up to rounding order)
+as the plain product: the pages' block-matrix identities
+
+    column split:  X [W_0, W_1] = [X W_0, X W_1]          (io.zouht.com 张量并行 §2.1, first identity)
+    row split:     [X_0, X_1] [W_0; W_1] = X_0 W_0 + X_1 W_1  (same §2.1, second identity)
+
+say so.  The sharded re-statements at the bottom follow the split step by step;
+the tests use them to pin the identities themselves.
+
+Page short names used in the citations (the pages are Chinese web articles):
+  * "damodev 3D并行"      damodev.csdn.net/6a43867610ee7a33f284fb9e.html
+  * "zouht 张量并行"      io.zouht.com/197.html
+  * "wangyu 张量并行"     wangyu.me/posts/llm/tensor-parallelism/ (大语言模型并行策略（三）：张量并行)
+  * "guijiagi 张量并行"   guijiagi.com/tags/张量并行/
+  * "sunjinbo 并行方式"   sunjinbo.space/document/parallelism.html (大模型分布式并行方式详解)
+
+Conventions (readings where the pages are silent; each is listed in the design doc):
+  * Y = X W with W stored [in x out] (wangyu 张量并行 §两种切分方式: X is B x M,
+    W is M x N; guijiagi 张量并行 §线性层的切分: W in R^{d x h}).
+  * No biases: none of the pages' split identities carries one.
+  * Act = GeLU, tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
+    (zouht 张量并行 §2.2.1 names "Gelu(X W_1)"; the tanh form is the named workload's).
+  * Attention: per head softmax(Q K^T / sqrt(d)) V with a causal mask
+    (key position <= query position), no dropout.
+  * Shard layouts are the pages' splits: W1s[i] = W1[:, i*f/N:(i+1)*f/N]
+    (column split), W2s[i] = W2[i*f/N:(i+1)*f/N, :] (row split); shard i owns
+    heads i*H/N .. (i+1)*H/N-1 (zouht 张量并行 §2.2.1, 32 heads on 4 GPUs = 8 each).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "matmul", "gelu_tanh", "gelu_tanh_grad",
+    "concat_columns", "stack_rows", "split_columns_like", "split_rows_like",
+    "mlp_forward", "mlp_backward",
+    "mlp_forward_sharded", "mlp_forward_two_allgather", "mlp_backward_sharded",
+    "unpack_qkv", "pack_qkv",
+    "attention_forward", "attention_backward", "attention_forward_sharded",
+    "layer_forward", "layer_backward",
+    "mlp_backward_weight_columns", "attention_forward_rows",
+]
+
+SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+GELU_CUBIC = 0.044715
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def matmul(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Plain fp64 matrix product (library primitive; pinned by a brute-force
+    triple loop in the tests)."""
+    return _f64(a) @ _f64(b)
+
+
+# --------------------------------------------------------------------------
+# Activation
+# --------------------------------------------------------------------------
+def gelu_tanh(x: np.ndarray) -> np.ndarray:
+    """GeLU, tanh form: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+
+    The MLP's Act (damodev 3D并行 §1.2.1: "ReLU or GeLU"; zouht 张量并行 §2.2.1:
+    first layer Gelu(X W_1)).  Element-wise, which is what lets it run per shard.
+    """
+    x = _f64(x)
+    u = SQRT_2_OVER_PI * (x + GELU_CUBIC * x * x * x)
+    return 0.5 * x * (1.0 + np.tanh(u))
+
+
+def gelu_tanh_grad(x: np.ndarray) -> np.ndarray:
+    """d/dx of :func:`gelu_tanh`, differentiated by hand:
+    0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) sqrt(2/pi) (1 + 3*0.044715 x^2)."""
+    x = _f64(x)
+    u = SQRT_2_OVER_PI * (x + GELU_CUBIC * x * x * x)
+    t = np.tanh(u)
+    du = SQRT_2_OVER_PI * (1.0 + 3.0 * GELU_CUBIC * x * x)
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * du
+
+
+# --------------------------------------------------------------------------
+# Shard layouts <-> unsharded matrices (the pages' splits)
+# --------------------------------------------------------------------------
+def concat_columns(ws: np.ndarray) -> np.ndarray:
+    """[N][rows][cols/N] column blocks -> the unsharded [rows][cols] matrix.
+
+    Column split (damodev 3D并行 §1.1 "列切分"; wangyu 张量并行 §按列切分: each
+    W_i is M x (N/n)): W = [W_0, W_1, ..., W_{N-1}].
+    """
+    ws = _f64(ws)
+    n, rows, cols = ws.shape
+    return np.concatenate([ws[i] for i in range(n)], axis=1).reshape(rows, n * cols)
+
+
+def stack_rows(ws: np.ndarray) -> np.ndarray:
+    """[N][rows/N][cols] row blocks -> the unsharded [rows][cols] matrix.
+
+    Row split (damodev 3D并行 §1.1 "外积和切分"; wangyu 张量并行 §按行切分: each
+    W_i is (M/m) x N): W = [W_0; W_1; ...; W_{N-1}].
+    """
+    ws = _f64(ws)
+    n, rows, cols = ws.shape
+    return np.concatenate([ws[i] for i in range(n)], axis=0).reshape(n * rows, cols)
+
+
+def split_columns_like(w: np.ndarray, n: int) -> np.ndarray:
+    """Inverse of :func:`concat_columns` (used to return gradients in shard layout)."""
+    w = _f64(w)
+    rows, cols = w.shape
+    c = cols // n
+    return np.stack([w[:, i * c:(i + 1) * c] for i in range(n)])
+
+
+def split_rows_like(w: np.ndarray, n: int) -> np.ndarray:
+    """Inverse of :func:`stack_rows`."""
+    w = _f64(w)
+    rows, cols = w.shape
+    r = rows // n
+    return np.stack([w[i * r:(i + 1) * r, :] for i in range(n)])
+
+
+# --------------------------------------------------------------------------
+# MLP block
+# --------------------------------------------------------------------------
+def mlp_forward(X, W1s, W2s) -> dict:
+    """Unsharded MLP block Z = Act(X W1) W2 (damodev 3D并行 §1.2.1, eq. 1.2-1.3;
+    zouht 张量并行 §2.2.1 前馈网络).
+
+    W1 is the column concatenation of the shards W1s[i] and W2 the row stack of
+    W2s[i]; by the §2.1 identities the sharded block computes the same Z.
+    Returns Y = X W1 (pre-activation, in shard layout [N][T][f/N]),
+    A = GeLU(Y) (shard layout) and Z [T][h].
+    """
+    X = _f64(X)
+    n = W1s.shape[0]
+    W1 = concat_columns(W1s)
+    W2 = stack_rows(W2s)
+    Y = matmul(X, W1)
+    A = gelu_tanh(Y)
+    Z = matmul(A, W2)
+    return {"Y": split_columns_like(Y, n), "A": split_columns_like(A, n), "Z": Z}
+
+
+def mlp_backward(X, W1s, W2s, dZ) -> dict:
+    """Gradients of L = <dZ, Z> for the unsharded block, by the chain rule.
+
+    dA = dZ W2^T, dY = dA * GeLU'(Y), dW2 = A^T dZ, dW1 = X^T dY, dX = dY W1^T.
+    The pages give the sharded forms (wangyu 张量并行 §通信模式: for the column
+    split dW_i = X^T dY_i and dX = sum_i dY_i W_i^T, the all-reduce; for the row
+    split dL/dY_i = dL/dY, dW_i = X_i^T dY); the unsharded product is the same
+    numbers.  Weight gradients come back in shard layout.
+    """
+    X, dZ = _f64(X), _f64(dZ)
+    n = W1s.shape[0]
+    W1 = concat_columns(W1s)
+    W2 = stack_rows(W2s)
+    Y = matmul(X, W1)
+    A = gelu_tanh(Y)
+    dA = matmul(dZ, W2.T)
+    dY = dA * gelu_tanh_grad(Y)
+    dW2 = matmul(A.T, dZ)
+    dW1 = matmul(X.T, dY)
+    dX = matmul(dY, W1.T)
+    return {"dX": dX, "dW1s": split_columns_like(dW1, n), "dW2s": split_rows_like(dW2, n),
+            "dY": split_columns_like(dY, n)}
+
+
+def mlp_forward_sharded(X, W1s, W2s) -> dict:
+    """The pages' tensor-parallel MLP, shard by shard (damodev 3D并行 §1.2.1;
+    wangyu 张量并行 §多层感知机（MLP）中的张量并行):
+
+      shard i:  Y_i = X W1_i  (column split, X replicated),
+                A_i = Act(Y_i)  (element-wise, so no communication),
+                P_i = A_i W2_i  (row split; A_i is already X's column block i),
+      all-reduce: Z = sum_i P_i.
+    """
+    X = _f64(X)
+    n = W1s.shape[0]
+    Ys, As, Ps = [], [], []
+    for i in range(n):
+        Yi = matmul(X, W1s[i])
+        Ai = gelu_tanh(Yi)
+        Ys.append(Yi)
+        As.append(Ai)
+        Ps.append(matmul(Ai, W2s[i]))
+    Z = Ps[0].copy()
+    for i in range(1, n):
+        Z = Z + Ps[i]
+    return {"Y": np.stack(Ys), "A": np.stack(As), "Z": Z, "partials": np.stack(Ps)}
+
+
+def mlp_forward_two_allgather(X, W1s, W2s) -> np.ndarray:
+    """The naive variant the damodev page rejects (§1.2.1, eq. 1.4-1.5): column
+    split of both GEMMs with an all-gather after each.  Same Z, two gathers."""
+    X = _f64(X)
+    n = W1s.shape[0]
+    A = np.concatenate([gelu_tanh(matmul(X, W1s[i])) for i in range(n)], axis=1)  # all-gather 1
+    W2 = stack_rows(W2s)
+    h = W2.shape[1]
+    c = h // n if h % n == 0 else None
+    if c is None:  # the column split of W2 needs n | h; fall back to one block
+        return matmul(A, W2)
+    return np.concatenate([matmul(A, W2[:, i * c:(i + 1) * c]) for i in range(n)], axis=1)  # all-gather 2
+
+
+def mlp_backward_sharded(X, W1s, W2s, dZ) -> dict:
+    """Sharded backward as the pages state it (wangyu 张量并行 §通信模式):
+    row-split layer: dL/dP_i = dL/dZ (broadcast), dW2_i = A_i^T dZ, dA_i = dZ W2_i^T;
+    column-split layer: dW1_i = X^T dY_i, dX = sum_i dY_i W1_i^T (the all-reduce)."""
+    X, dZ = _f64(X), _f64(dZ)
+    n = W1s.shape[0]
+    dW1s, dW2s, parts = [], [], []
+    for i in range(n):
+        Yi = matmul(X, W1s[i])
+        Ai = gelu_tanh(Yi)
+        dW2s.append(matmul(Ai.T, dZ))
+        dYi = matmul(dZ, _f64(W2s[i]).T) * gelu_tanh_grad(Yi)
+        dW1s.append(matmul(X.T, dYi))
+        parts.append(matmul(dYi, _f64(W1s[i]).T))
+    dX = parts[0].copy()
+    for i in range(1, n):
+        dX = dX + parts[i]
+    return {"dX": dX, "dW1s": np.stack(dW1s), "dW2s": np.stack(dW2s)}
+
+
+# --------------------------------------------------------------------------
+# Self-attention block
+# --------------------------------------------------------------------------
+def unpack_qkv(Wqkv) -> tuple:
+    """Shard-major [N][h][3][H/N][d] -> unsharded Wq, Wk, Wv, each [h][H*d].
+
+    Q/K/V are split by columns, head by head (zouht 张量并行 §2.2.1 多头注意力机制;
+    wangyu 张量并行 §注意力机制中的张量并行: split by the head dimension, which is
+    a column split); shard i holds heads i*H/N .. (i+1)*H/N-1, Q then K then V.
+    """
+    W = _f64(Wqkv)
+    n, h, three, hn, d = W.shape
+    assert three == 3
+    full = np.transpose(W, (1, 2, 0, 3, 4)).reshape(h, 3, n * hn * d)
+    return full[:, 0, :].copy(), full[:, 1, :].copy(), full[:, 2, :].copy()
+
+
+def pack_qkv(Wq, Wk, Wv, n: int, d: int) -> np.ndarray:
+    """Inverse of :func:`unpack_qkv`."""
+    h, hd = Wq.shape
+    H = hd // d
+    full = np.stack([_f64(Wq), _f64(Wk), _f64(Wv)], axis=1).reshape(h, 3, n, H // n, d)
+    return np.ascontiguousarray(np.transpose(full, (2, 0, 1, 3, 4)))
+
+
+def _causal_scores(q, k, d, causal):
+    s = matmul(q, k.T) / math.sqrt(d)
+    if causal:
+        S = s.shape[0]
+        s = np.where(np.tril(np.ones((S, S), dtype=bool)), s, -np.inf)
+    return s
+
+
+def _softmax_rows(s):
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=1, keepdims=True)
+    return e / z, (m + np.log(z))[:, 0]
+
+
+def attention_forward(X, Wqkv, Wo, B: int, S: int, causal: bool = True) -> dict:
+    """Unsharded multi-head self-attention block.
+
+    Per batch b and head j (damodev 3D并行 §1.2.2, eq. 1.12 stripped from the
+    page; wangyu 张量并行 §注意力机制中的张量并行):
+        Q = X_b Wq_j, K = X_b Wk_j, V = X_b Wv_j,
+        head_j = softmax(mask(Q K^T / sqrt(d))) V,
+    then Z = concat_j(head_j) Wo (damodev §1.2.2, eq. 1.13).  Returns Z [T][h],
+    QKV in shard layout [N][T][3][H/N][d], O in shard layout [N][T][H/N*d] and
+    LSE [B][H][S] = log sum_k exp(scores) (natural log of the scaled scores).
+    """
+    X = _f64(X)
+    n, h, _, hn, d = Wqkv.shape
+    H = n * hn
+    T = B * S
+    Wq, Wk, Wv = unpack_qkv(Wqkv)
+    Wo_full = stack_rows(Wo)
+    Q, K, V = matmul(X, Wq), matmul(X, Wk), matmul(X, Wv)
+    O = np.zeros((T, H * d))
+    LSE = np.zeros((B, H, S))
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        for j in range(H):
+            c = slice(j * d, (j + 1) * d)
+            P, lse = _softmax_rows(_causal_scores(Q[r, c], K[r, c], d, causal))
+            O[r, c] = matmul(P, V[r, c])
+            LSE[b, j] = lse
+    Z = matmul(O, Wo_full)
+    QKV = np.stack([Q, K, V], axis=1).reshape(T, 3, n, hn, d).transpose(2, 0, 1, 3, 4)
+    Osh = O.reshape(T, n, hn * d).transpose(1, 0, 2)
+    return {"Z": Z, "QKV": np.ascontiguousarray(QKV).reshape(n, T, 3 * hn * d),
+            "O": np.ascontiguousarray(Osh), "LSE": LSE}
+
+
+def attention_backward(X, Wqkv, Wo, dZ, B: int, S: int, causal: bool = True) -> dict:
+    """Gradients of L = <dZ, Z> for :func:`attention_forward`.
+
+    The pages give no attention backward; this is the chain rule through the
+    definition, with the textbook softmax Jacobian dS = P * (dP - rowsum(dP * P)).
+    """
+    X, dZ = _f64(X), _f64(dZ)
+    n, h, _, hn, d = Wqkv.shape
+    H = n * hn
+    T = B * S
+    Wq, Wk, Wv = unpack_qkv(Wqkv)
+    Wo_full = stack_rows(Wo)
+    Q, K, V = matmul(X, Wq), matmul(X, Wk), matmul(X, Wv)
+    O = np.zeros((T, H * d))
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        for j in range(H):
+            c = slice(j * d, (j + 1) * d)
+            P, _ = _softmax_rows(_causal_scores(Q[r, c], K[r, c], d, causal))
+            O[r, c] = matmul(P, V[r, c])
+    dWo = matmul(O.T, dZ)
+    dO = matmul(dZ, Wo_full.T)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        for j in range(H):
+            c = slice(j * d, (j + 1) * d)
+            # P is recomputed from its definition rather than kept per head
+            P, _ = _softmax_rows(_causal_scores(Q[r, c], K[r, c], d, causal))
+            dV[r, c] = matmul(P.T, dO[r, c])
+            dP = matmul(dO[r, c], V[r, c].T)
+            dS = P * (dP - np.sum(dP * P, axis=1, keepdims=True))
+            dQ[r, c] = matmul(dS, K[r, c]) / math.sqrt(d)
+            dK[r, c] = matmul(dS.T, Q[r, c]) / math.sqrt(d)
+    dWq, dWk, dWv = matmul(X.T, dQ), matmul(X.T, dK), matmul(X.T, dV)
+    dX = matmul(dQ, Wq.T) + matmul(dK, Wk.T) + matmul(dV, Wv.T)
+    return {"dX": dX, "dWqkv": pack_qkv(dWq, dWk, dWv, n, d), "dWo": split_rows_like(dWo, n)}
+
+
+def attention_forward_sharded(X, Wqkv, Wo, B: int, S: int, causal: bool = True) -> np.ndarray:
+    """Head-sharded attention as the pages split it (zouht 张量并行 §2.2.1; wangyu
+    张量并行 §注意力机制中的张量并行): shard i computes its own heads' Q/K/V with
+    its column block of Wqkv, runs attention on those heads, multiplies its O_i by
+    its row block Wo_i; an all-reduce sums the N partial outputs."""
+    X = _f64(X)
+    n, h, _, hn, d = Wqkv.shape
+    T = B * S
+    Z = None
+    for i in range(n):
+        Wi = _f64(Wqkv[i]).reshape(h, 3 * hn * d)
+        qkv = matmul(X, Wi).reshape(T, 3, hn, d)
+        Oi = np.zeros((T, hn * d))
+        for b in range(B):
+            r = slice(b * S, (b + 1) * S)
+            for jj in range(hn):
+                q, k, v = qkv[r, 0, jj], qkv[r, 1, jj], qkv[r, 2, jj]
+                P, _ = _softmax_rows(_causal_scores(q, k, d, causal))
+                Oi[r, jj * d:(jj + 1) * d] = matmul(P, v)
+        part = matmul(Oi, Wo[i])
+        Z = part if Z is None else Z + part
+    return Z
+
+
+# --------------------------------------------------------------------------
+# Full layer: attention block then MLP block
+# --------------------------------------------------------------------------
+def layer_forward(X, Wqkv, Wo, W1s, W2s, B: int, S: int, causal: bool = True) -> dict:
+    """Z = MLP(Attn(X)).  The pages place LayerNorm, dropout and residuals outside
+    the tensor-parallel regions (zouht 张量并行 §2.2.2) and give no layer formula;
+    the layer here is the two TP blocks in sequence, attention first."""
+    a = attention_forward(X, Wqkv, Wo, B, S, causal)
+    m = mlp_forward(a["Z"], W1s, W2s)
+    return {"Z": m["Z"], "H": a["Z"], "attn": a, "mlp": m}
+
+
+def layer_backward(X, Wqkv, Wo, W1s, W2s, dZ, B: int, S: int, causal: bool = True) -> dict:
+    """Gradients of L = <dZ, layer_forward(X)["Z"]>: MLP backward, then the
+    attention backward fed with the MLP's input gradient."""
+    a = attention_forward(X, Wqkv, Wo, B, S, causal)
+    gm = mlp_backward(a["Z"], W1s, W2s, dZ)
+    ga = attention_backward(X, Wqkv, Wo, gm["dX"], B, S, causal)
+    return {"dX": ga["dX"], "dWqkv": ga["dWqkv"], "dWo": ga["dWo"],
+            "dW1s": gm["dW1s"], "dW2s": gm["dW2s"], "dH": gm["dX"]}
+
+
+# --------------------------------------------------------------------------
+# Restrictions of the same definitions to a subset of outputs (for sampled
+# checks at full size, where the whole product would take the CPU too long)
+# --------------------------------------------------------------------------
+def mlp_backward_weight_columns(X, W1s, W2s, dZ, cols) -> dict:
+    """dW1[:, cols] and dW2[cols, :] of :func:`mlp_backward`, for global FFN
+    column indices ``cols``.  Column c of dY only needs column c of Y and of dA:
+    dY[:, c] = (dZ W2[c, :]^T) * GeLU'(X W1[:, c]); dW1[:, c] = X^T dY[:, c];
+    dW2[c, :] = A[:, c]^T dZ with A[:, c] = GeLU(X W1[:, c])."""
+    X, dZ = _f64(X), _f64(dZ)
+    cols = np.asarray(cols, dtype=np.int64)
+    W1 = concat_columns(W1s)[:, cols]
+    W2 = stack_rows(W2s)[cols, :]
+    Y = matmul(X, W1)
+    dY = matmul(dZ, W2.T) * gelu_tanh_grad(Y)
+    return {"dW1_cols": matmul(X.T, dY), "dW2_rows": matmul(gelu_tanh(Y).T, dZ)}
+
+
+def attention_forward_rows(X, Wqkv, Wo, B: int, S: int, rows, causal: bool = True) -> dict:
+    """Z[rows] and O[rows] of :func:`attention_forward` for global token indices
+    ``rows``: each query row needs its own Q row and the K/V rows of its batch."""
+    X = _f64(X)
+    n, h, _, hn, d = Wqkv.shape
+    H = n * hn
+    rows = np.asarray(rows, dtype=np.int64)
+    Wq, Wk, Wv = unpack_qkv(Wqkv)
+    Wo_full = stack_rows(Wo)
+    K, V = matmul(X, Wk), matmul(X, Wv)
+    Q = matmul(X[rows], Wq)
+    O = np.zeros((len(rows), H * d))
+    LSE = np.zeros((len(rows), H))
+    for ri, t in enumerate(rows):
+        b, s = divmod(int(t), S)
+        last = s + 1 if causal else S
+        kr = slice(b * S, b * S + last)
+        for j in range(H):
+            c = slice(j * d, (j + 1) * d)
+            sc = matmul(Q[ri:ri + 1, c], K[kr, c].T) / math.sqrt(d)
+            P, lse = _softmax_rows(sc)
+            O[ri, c] = matmul(P, V[kr, c])[0]
+            LSE[ri, j] = lse[0]
+    return {"Z": matmul(O, Wo_full), "O": O, "LSE": LSE}

@@ -1,0 +1,155 @@
+"""Seeded synthetic inputs for the tensor-parallel block, shared by the CUDA path's
+tests/benchmark and by the fp64 oracle.
+
+This module draws random numbers and arranges them in the shard-major layouts of
+the boundary; it contains none of the block's arithmetic.  Draws are fp32 normals
+from a CPU ``torch.Generator`` seeded once, in a fixed order (MLP: X, W1, W2, dZ;
+attention: X, Wqkv, Wo, dZ; layer: X, Wqkv, Wo, W1, W2, dZ), scaled by the stated
+standard deviation and cast to the workload's dtype once.  The GPU and the oracle
+then consume the identical values (the oracle upcasts them to float64).
+
+Weights are drawn unsharded in the pages' [in x out] orientation and then cut the
+way the pages cut them:
+  * W1 [h x f] -> W1s [N][h][f/N]           (column split)
+  * W2 [f x h] -> W2s [N][f/N][h]           (row split; bit-identical to W2)
+  * Wqkv [h x 3*H*d] (Q heads | K heads | V heads) -> [N][h][3][H/N][d]
+  * Wo [H*d x h] -> [N][H/N*d][h]           (row split by head)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+__all__ = ["Workload", "WORKLOADS", "mlp_inputs", "attn_inputs", "layer_inputs",
+           "split_columns", "split_rows", "split_qkv_heads"]
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One of the synthetic workloads the block is checked and measured on."""
+    name: str
+    kind: str            # "mlp", "attn" or "layer"
+    dtype: str           # "f32" or "bf16"
+    backward: bool
+    T: int = 0           # tokens = B*S
+    h: int = 0
+    f: int = 0
+    N: int = 1
+    B: int = 1
+    S: int = 0
+    H: int = 0
+    d: int = 0
+    causal: bool = True
+    x_std: float = 1.0
+    w_std: float = 0.02
+    seed: int = 0
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k in self.__dataclass_fields__}
+
+
+# The five workloads: MLP fp32 forward; MLP bf16 fwd+bwd (small and h=4096);
+# attention bf16 forward; full layer bf16 fwd+bwd.
+WORKLOADS = {
+    "mlp_f32_T64_h256_f1024_N2": Workload("mlp_f32_T64_h256_f1024_N2", "mlp", "f32", False,
+                                          T=64, h=256, f=1024, N=2),
+    "mlp_bf16_T2048_h1024_f4096_N4": Workload("mlp_bf16_T2048_h1024_f4096_N4", "mlp", "bf16", True,
+                                              T=2048, h=1024, f=4096, N=4),
+    "mlp_bf16_T8192_h4096_f16384_N8": Workload("mlp_bf16_T8192_h4096_f16384_N8", "mlp", "bf16", True,
+                                               T=8192, h=4096, f=16384, N=8),
+    "attn_bf16_B2_S2048_h4096_H32_d128_N8": Workload("attn_bf16_B2_S2048_h4096_H32_d128_N8", "attn",
+                                                     "bf16", False, T=4096, h=4096, N=8, B=2,
+                                                     S=2048, H=32, d=128),
+    "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
+        "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "layer", "bf16", True,
+        T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
+}
+
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _draw(gen: torch.Generator, shape, std: float, dtype: str) -> torch.Tensor:
+    x = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    return x.to(_DT[dtype]).contiguous()
+
+
+def split_columns(w: torch.Tensor, n: int) -> torch.Tensor:
+    """[rows][cols] -> [n][rows][cols/n]: block i holds columns i*cols/n..(i+1)*cols/n-1."""
+    rows, cols = w.shape
+    return w.reshape(rows, n, cols // n).permute(1, 0, 2).contiguous()
+
+
+def split_rows(w: torch.Tensor, n: int) -> torch.Tensor:
+    """[rows][cols] -> [n][rows/n][cols] (same bytes as the input)."""
+    rows, cols = w.shape
+    return w.reshape(n, rows // n, cols).contiguous()
+
+
+def split_qkv_heads(w: torch.Tensor, n: int, H: int, d: int) -> torch.Tensor:
+    """[h][3*H*d] laid out (Q heads | K heads | V heads) -> [n][h][3][H/n][d]."""
+    h = w.shape[0]
+    return w.reshape(h, 3, n, H // n, d).permute(2, 0, 1, 3, 4).contiguous()
+
+
+def mlp_inputs(T: int, h: int, f: int, N: int, dtype: str = "bf16", seed: int = 0,
+               x_std: float = 1.0, w_std: float = 0.02, backward: bool = True) -> dict:
+    """X [T][h], W1s [N][h][f/N], W2s [N][f/N][h] and (if ``backward``) dZ [T][h],
+    all CPU tensors of ``dtype``."""
+    if N < 1 or f % N:
+        raise ValueError("N must divide f")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (T, h), x_std, dtype)
+    W1 = _draw(gen, (h, f), w_std, dtype)
+    W2 = _draw(gen, (f, h), w_std, dtype)
+    out = {"X": X, "W1s": split_columns(W1, N), "W2s": split_rows(W2, N)}
+    if backward:
+        out["dZ"] = _draw(gen, (T, h), 1.0, dtype)
+    return out
+
+
+def attn_inputs(B: int, S: int, h: int, H: int, d: int, N: int, dtype: str = "bf16",
+                seed: int = 0, x_std: float = 1.0, w_std: float = 0.02,
+                backward: bool = True) -> dict:
+    """X [B*S][h], Wqkv [N][h][3][H/N][d], Wo [N][H/N*d][h] and dZ [B*S][h]."""
+    if N < 1 or H % N:
+        raise ValueError("N must divide H")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (B * S, h), x_std, dtype)
+    Wqkv = _draw(gen, (h, 3 * H * d), w_std, dtype)
+    Wo = _draw(gen, (H * d, h), w_std, dtype)
+    out = {"X": X, "Wqkv": split_qkv_heads(Wqkv, N, H, d), "Wo": split_rows(Wo, N)}
+    if backward:
+        out["dZ"] = _draw(gen, (B * S, h), 1.0, dtype)
+    return out
+
+
+def layer_inputs(B: int, S: int, h: int, H: int, d: int, f: int, N: int, dtype: str = "bf16",
+                 seed: int = 0, x_std: float = 1.0, w_std: float = 0.02) -> dict:
+    """Inputs of the attention block followed by the MLP block."""
+    if N < 1 or H % N or f % N:
+        raise ValueError("N must divide H and f")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (B * S, h), x_std, dtype)
+    Wqkv = _draw(gen, (h, 3 * H * d), w_std, dtype)
+    Wo = _draw(gen, (H * d, h), w_std, dtype)
+    W1 = _draw(gen, (h, f), w_std, dtype)
+    W2 = _draw(gen, (f, h), w_std, dtype)
+    dZ = _draw(gen, (B * S, h), 1.0, dtype)
+    return {"X": X, "Wqkv": split_qkv_heads(Wqkv, N, H, d), "Wo": split_rows(Wo, N),
+            "W1s": split_columns(W1, N), "W2s": split_rows(W2, N), "dZ": dZ}
+
+
+def workload_inputs(w: Workload, **overrides) -> dict:
+    """Inputs for a :class:`Workload` (shape fields may be overridden)."""
+    p = {**w.as_dict(), **overrides}
+    if p["kind"] == "mlp":
+        return mlp_inputs(p["T"], p["h"], p["f"], p["N"], p["dtype"], p["seed"], p["x_std"],
+                          p["w_std"], p["backward"])
+    if p["kind"] == "attn":
+        return attn_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["N"], p["dtype"], p["seed"],
+                           p["x_std"], p["w_std"], p["backward"])
+    return layer_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["f"], p["N"], p["dtype"],
+                        p["seed"], p["x_std"], p["w_std"])

@@ -1,0 +1,432 @@
+"""Pins for the fp64 oracle: each checks it against something other than itself.
+
+* brute-force pure-Python loops on tiny inputs (no numpy, no BLAS);
+* the pages' block-matrix identities, on small-integer matrices where float64
+  arithmetic is exact, so that "equal" means bit-equal;
+* independent library routines (torch fp64 GeLU, SDPA, autograd);
+* closed forms and invariants (softmax rows sum to 1, causal row 0, uniform
+  attention when Wq = 0, the odd part of the tanh-GeLU);
+* central finite differences of L = <dZ, Z> for every gradient.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tp_oracle as O
+
+RNG = np.random.default_rng(1234)
+
+
+def rel(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+# ---------------------------------------------------------------- GEMM core
+def brute_matmul(a, b):
+    M, K = len(a), len(a[0])
+    N = len(b[0])
+    out = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += float(a[i][k]) * float(b[k][j])
+            out[i][j] = s
+    return out
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 1), (5, 8, 12), (7, 3, 9), (4, 16, 2)])
+def test_matmul_vs_triple_loop(M, K, N):
+    a = RNG.standard_normal((M, K))
+    b = RNG.standard_normal((K, N))
+    ref = np.array(brute_matmul(a.tolist(), b.tolist()))
+    assert rel(O.matmul(a, b), ref) < 1e-14
+
+
+def test_matmul_integer_exact():
+    a = RNG.integers(-9, 10, (6, 10)).astype(np.float64)
+    b = RNG.integers(-9, 10, (10, 7)).astype(np.float64)
+    ref = np.array(brute_matmul(a.tolist(), b.tolist()))
+    assert np.array_equal(O.matmul(a, b), ref)
+
+
+# ---------------------------------------------------------------- GeLU
+def test_gelu_special_values():
+    assert O.gelu_tanh(np.array([0.0]))[0] == 0.0
+    big = np.array([10.0, 30.0, 100.0])
+    assert np.allclose(O.gelu_tanh(big), big, rtol=0, atol=1e-12)
+    assert np.allclose(O.gelu_tanh(-big), 0.0, atol=1e-12)
+
+
+def test_gelu_odd_part_identity():
+    # 0.5x(1+tanh u) - (-0.5x)(1+tanh(-u)) = x for the tanh form, any constants
+    x = RNG.standard_normal(1000) * 4
+    assert np.allclose(O.gelu_tanh(x) - O.gelu_tanh(-x), x, rtol=0, atol=1e-13)
+
+
+def test_gelu_scalar_by_hand():
+    # written out with math.tanh, one scalar at a time
+    for x in [-3.0, -1.0, -0.25, 0.5, 1.0, 2.5]:
+        u = math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)
+        ref = 0.5 * x * (1.0 + math.tanh(u))
+        assert abs(O.gelu_tanh(np.array([x]))[0] - ref) < 1e-15
+
+
+def test_gelu_vs_torch():
+    x = RNG.standard_normal(4096) * 5
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    assert np.max(np.abs(O.gelu_tanh(x) - ref)) < 1e-14
+
+
+def test_gelu_is_not_erf_gelu():
+    # the tanh form differs from the exact (erf) GeLU by ~1e-4 somewhere
+    x = np.linspace(-4, 4, 801)
+    erf = torch.nn.functional.gelu(torch.from_numpy(x)).numpy()
+    assert np.max(np.abs(O.gelu_tanh(x) - erf)) > 1e-5
+
+
+def test_gelu_grad_finite_difference_and_autograd():
+    x = RNG.standard_normal(512) * 3
+    eps = 1e-6
+    fd = (O.gelu_tanh(x + eps) - O.gelu_tanh(x - eps)) / (2 * eps)
+    assert np.max(np.abs(O.gelu_tanh_grad(x) - fd)) < 1e-8
+    t = torch.from_numpy(x.copy()).requires_grad_(True)
+    torch.nn.functional.gelu(t, approximate="tanh").sum().backward()
+    assert np.max(np.abs(O.gelu_tanh_grad(x) - t.grad.numpy())) < 1e-13
+
+
+# ---------------------------------------------------------------- split identities
+def divisors(n):
+    return [k for k in range(1, n + 1) if n % k == 0]
+
+
+@pytest.mark.parametrize("f", [12, 8])
+def test_column_split_concat_exact(f):
+    """X [W_0, W_1, ...] = [X W_0, X W_1, ...], bit-exact on integer data, every N | f."""
+    T, h = 5, 8
+    X = RNG.integers(-5, 6, (T, h)).astype(np.float64)
+    W = RNG.integers(-5, 6, (h, f)).astype(np.float64)
+    full = np.array(brute_matmul(X.tolist(), W.tolist()))
+    for n in divisors(f):
+        Ws = np.stack([W[:, i * (f // n):(i + 1) * (f // n)] for i in range(n)])
+        assert np.array_equal(O.concat_columns(Ws), W)
+        parts = [O.matmul(X, Ws[i]) for i in range(n)]
+        assert np.array_equal(np.concatenate(parts, axis=1), full)
+
+
+@pytest.mark.parametrize("f", [12, 8])
+def test_row_split_sum_exact(f):
+    """[X_0, X_1, ...][W_0; W_1; ...] = sum_i X_i W_i, bit-exact on integer data."""
+    T, h = 5, 7
+    A = RNG.integers(-5, 6, (T, f)).astype(np.float64)
+    W = RNG.integers(-5, 6, (f, h)).astype(np.float64)
+    full = np.array(brute_matmul(A.tolist(), W.tolist()))
+    for n in divisors(f):
+        c = f // n
+        Ws = np.stack([W[i * c:(i + 1) * c, :] for i in range(n)])
+        assert np.array_equal(O.stack_rows(Ws), W)
+        s = np.zeros((T, h))
+        for i in range(n):
+            s += O.matmul(A[:, i * c:(i + 1) * c], Ws[i])
+        assert np.array_equal(s, full)
+
+
+def _mlp_inputs(T, h, f, n, seed=0):
+    r = np.random.default_rng(seed)
+    X = r.standard_normal((T, h))
+    W1 = r.standard_normal((h, f)) * 0.3
+    W2 = r.standard_normal((f, h)) * 0.3
+    dZ = r.standard_normal((T, h))
+    W1s = np.stack([W1[:, i * (f // n):(i + 1) * (f // n)] for i in range(n)])
+    W2s = np.stack([W2[i * (f // n):(i + 1) * (f // n), :] for i in range(n)])
+    return X, W1, W2, W1s, W2s, dZ
+
+
+def brute_mlp(X, W1, W2):
+    T, h = len(X), len(X[0])
+    f = len(W1[0])
+    Z = [[0.0] * h for _ in range(T)]
+    for t in range(T):
+        a = []
+        for j in range(f):
+            y = sum(X[t][k] * W1[k][j] for k in range(h))
+            u = math.sqrt(2.0 / math.pi) * (y + 0.044715 * y * y * y)
+            a.append(0.5 * y * (1.0 + math.tanh(u)))
+        for c in range(h):
+            Z[t][c] = sum(a[j] * W2[j][c] for j in range(f))
+    return Z
+
+
+def test_mlp_forward_vs_brute_force():
+    X, W1, W2, W1s, W2s, _ = _mlp_inputs(4, 6, 10, 2)
+    ref = np.array(brute_mlp(X.tolist(), W1.tolist(), W2.tolist()))
+    assert rel(O.mlp_forward(X, W1s, W2s)["Z"], ref) < 1e-13
+
+
+@pytest.mark.parametrize("n", divisors(12))
+def test_mlp_sharded_equals_unsharded_every_n(n):
+    X, W1, W2, W1s, W2s, dZ = _mlp_inputs(5, 8, 12, n)
+    a = O.mlp_forward(X, W1s, W2s)
+    b = O.mlp_forward_sharded(X, W1s, W2s)
+    assert rel(b["Z"], a["Z"]) < 1e-13
+    assert np.array_equal(b["Y"], a["Y"]) or rel(b["Y"], a["Y"]) < 1e-14
+    # Act commutes with the column split: A_i = GeLU(Y_i) is GeLU(Y)'s block i
+    assert rel(b["A"], a["A"]) < 1e-14
+    # the naive two-all-gather formulation gives the same numbers
+    if 8 % n == 0:
+        assert rel(O.mlp_forward_two_allgather(X, W1s, W2s), a["Z"]) < 1e-13
+    gb = O.mlp_backward_sharded(X, W1s, W2s, dZ)
+    ga = O.mlp_backward(X, W1s, W2s, dZ)
+    for k in ("dX", "dW1s", "dW2s"):
+        assert rel(gb[k], ga[k]) < 1e-13, k
+
+
+def _loss_mlp(X, W1s, W2s, dZ):
+    return float(np.sum(dZ * O.mlp_forward(X, W1s, W2s)["Z"]))
+
+
+def test_mlp_backward_finite_differences():
+    X, _, _, W1s, W2s, dZ = _mlp_inputs(3, 4, 6, 2, seed=7)
+    g = O.mlp_backward(X, W1s, W2s, dZ)
+    eps = 1e-6
+    for name, arr, grad in (("X", X, g["dX"]), ("W1s", W1s, g["dW1s"]), ("W2s", W2s, g["dW2s"])):
+        fd = np.zeros_like(arr)
+        for idx in itertools.product(*[range(s) for s in arr.shape]):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = _loss_mlp(X, W1s, W2s, dZ)
+            arr[idx] = old - eps
+            lm = _loss_mlp(X, W1s, W2s, dZ)
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert rel(grad, fd) < 1e-6, name
+
+
+def test_mlp_backward_vs_torch_autograd():
+    X, W1, W2, W1s, W2s, dZ = _mlp_inputs(6, 8, 16, 4, seed=3)
+    tX, tW1, tW2 = (torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, W1, W2))
+    Z = torch.nn.functional.gelu(tX @ tW1, approximate="tanh") @ tW2
+    (Z * torch.from_numpy(dZ)).sum().backward()
+    g = O.mlp_backward(X, W1s, W2s, dZ)
+    assert rel(g["dX"], tX.grad.numpy()) < 1e-13
+    assert rel(O.concat_columns(g["dW1s"]), tW1.grad.numpy()) < 1e-13
+    assert rel(O.stack_rows(g["dW2s"]), tW2.grad.numpy()) < 1e-13
+
+
+def test_mlp_weight_column_restriction():
+    X, _, _, W1s, W2s, dZ = _mlp_inputs(9, 8, 12, 3, seed=5)
+    g = O.mlp_backward(X, W1s, W2s, dZ)
+    cols = np.array([0, 3, 4, 11])
+    r = O.mlp_backward_weight_columns(X, W1s, W2s, dZ, cols)
+    assert rel(r["dW1_cols"], O.concat_columns(g["dW1s"])[:, cols]) < 1e-13
+    assert rel(r["dW2_rows"], O.stack_rows(g["dW2s"])[cols, :]) < 1e-13
+
+
+# ---------------------------------------------------------------- attention
+def _attn_inputs(B, S, H, d, n, h=None, seed=0, wstd=0.3):
+    r = np.random.default_rng(seed)
+    h = h or H * d
+    X = r.standard_normal((B * S, h))
+    Wq, Wk, Wv = (r.standard_normal((h, H * d)) * wstd for _ in range(3))
+    Wo = r.standard_normal((H * d, h)) * wstd
+    dZ = r.standard_normal((B * S, h))
+    Wqkv = O.pack_qkv(Wq, Wk, Wv, n, d)
+    Wos = np.stack([Wo[i * (H // n) * d:(i + 1) * (H // n) * d] for i in range(n)])
+    return X, Wq, Wk, Wv, Wo, Wqkv, Wos, dZ
+
+
+def test_qkv_pack_layout():
+    B, S, H, d, n = 1, 3, 4, 2, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n)
+    # shard i, part p, local head jj is global head i*H/n+jj's column block
+    for i in range(n):
+        for jj in range(H // n):
+            j = i * (H // n) + jj
+            assert np.array_equal(Wqkv[i, :, 0, jj, :], Wq[:, j * d:(j + 1) * d])
+            assert np.array_equal(Wqkv[i, :, 1, jj, :], Wk[:, j * d:(j + 1) * d])
+            assert np.array_equal(Wqkv[i, :, 2, jj, :], Wv[:, j * d:(j + 1) * d])
+    q, k, v = O.unpack_qkv(Wqkv)
+    assert np.array_equal(q, Wq) and np.array_equal(k, Wk) and np.array_equal(v, Wv)
+
+
+def brute_attention(X, Wq, Wk, Wv, Wo, B, S, H, d, causal):
+    T, h = X.shape
+    Q, K, V = X @ Wq, X @ Wk, X @ Wv
+    Ocat = np.zeros((T, H * d))
+    for b in range(B):
+        for j in range(H):
+            for s in range(S):
+                t = b * S + s
+                keys = range(s + 1) if causal else range(S)
+                sc = []
+                for s2 in keys:
+                    t2 = b * S + s2
+                    sc.append(sum(Q[t, j * d + e] * K[t2, j * d + e] for e in range(d)) / math.sqrt(d))
+                m = max(sc)
+                w = [math.exp(x - m) for x in sc]
+                z = sum(w)
+                for e in range(d):
+                    Ocat[t, j * d + e] = sum(w[i] / z * V[b * S + s2, j * d + e]
+                                             for i, s2 in enumerate(keys))
+    return Ocat @ Wo
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_vs_brute_force(causal):
+    B, S, H, d, n = 2, 5, 4, 3, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n)
+    ref = brute_attention(X, Wq, Wk, Wv, Wo, B, S, H, d, causal)
+    assert rel(O.attention_forward(X, Wqkv, Wos, B, S, causal)["Z"], ref) < 1e-13
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_vs_torch_sdpa(causal):
+    B, S, H, d, n = 2, 9, 4, 8, 4
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n, seed=2)
+    t = lambda a: torch.from_numpy(a)
+    q = (t(X) @ t(Wq)).reshape(B, S, H, d).transpose(1, 2)
+    k = (t(X) @ t(Wk)).reshape(B, S, H, d).transpose(1, 2)
+    v = (t(X) @ t(Wv)).reshape(B, S, H, d).transpose(1, 2)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal)
+    Z = (o.transpose(1, 2).reshape(B * S, H * d) @ t(Wo)).numpy()
+    out = O.attention_forward(X, Wqkv, Wos, B, S, causal)
+    assert rel(out["Z"], Z) < 1e-13
+    # LSE against torch.logsumexp of the masked scaled scores
+    sc = (q @ k.transpose(-1, -2)) / math.sqrt(d)
+    if causal:
+        sc = sc.masked_fill(~torch.tril(torch.ones(S, S, dtype=torch.bool)), float("-inf"))
+    assert np.max(np.abs(out["LSE"] - torch.logsumexp(sc, dim=-1).numpy())) < 1e-12
+
+
+def test_attention_causal_row0_and_uniform_closed_forms():
+    B, S, H, d, n = 2, 6, 4, 4, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n, seed=9)
+    out = O.attention_forward(X, Wqkv, Wos, B, S, True)
+    V = X @ Wv
+    Ocat = np.concatenate([out["O"][i] for i in range(n)], axis=1)
+    for b in range(B):
+        # query 0 sees only key 0: its output is V[0] for every head
+        assert np.allclose(Ocat[b * S], V[b * S], atol=1e-13)
+    # Wq = 0: every visible key gets the same weight, O[s] = mean(V[0..s])
+    Wqkv0 = O.pack_qkv(np.zeros_like(Wq), Wk, Wv, n, d)
+    out0 = O.attention_forward(X, Wqkv0, Wos, B, S, True)
+    O0 = np.concatenate([out0["O"][i] for i in range(n)], axis=1)
+    for b in range(B):
+        for s in range(S):
+            assert np.allclose(O0[b * S + s], V[b * S:b * S + s + 1].mean(axis=0), atol=1e-13)
+        # and LSE = log(number of visible keys)
+        assert np.allclose(out0["LSE"][b], np.log(np.arange(1, S + 1))[None, :], atol=1e-13)
+
+
+def test_attention_softmax_rows_sum_to_one():
+    s = RNG.standard_normal((7, 7)) * 3
+    s = np.where(np.tril(np.ones((7, 7), bool)), s, -np.inf)
+    P, _ = O._softmax_rows(s)
+    assert np.allclose(P.sum(axis=1), 1.0, atol=1e-15)
+    assert np.all(P[np.triu_indices(7, 1)] == 0.0)
+
+
+@pytest.mark.parametrize("n", [1, 2, 4])
+def test_attention_head_sharded_equals_unsharded(n):
+    B, S, H, d = 2, 5, 4, 3
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n, seed=4)
+    a = O.attention_forward(X, Wqkv, Wos, B, S, True)["Z"]
+    b = O.attention_forward_sharded(X, Wqkv, Wos, B, S, True)
+    assert rel(b, a) < 1e-13
+
+
+def test_attention_rows_restriction():
+    B, S, H, d, n = 2, 7, 4, 3, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n, seed=8)
+    full = O.attention_forward(X, Wqkv, Wos, B, S, True)
+    rows = np.array([0, 3, 6, 7, 13])
+    r = O.attention_forward_rows(X, Wqkv, Wos, B, S, rows, True)
+    assert rel(r["Z"], full["Z"][rows]) < 1e-13
+    Ocat = np.concatenate([full["O"][i] for i in range(n)], axis=1)
+    assert rel(r["O"], Ocat[rows]) < 1e-13
+    lse = full["LSE"].transpose(0, 2, 1).reshape(B * S, -1)
+    assert np.max(np.abs(r["LSE"] - lse[rows])) < 1e-12
+
+
+def test_attention_backward_finite_differences():
+    B, S, H, d, n = 1, 4, 2, 2, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, dZ = _attn_inputs(B, S, H, d, n, seed=11)
+    g = O.attention_backward(X, Wqkv, Wos, dZ, B, S, True)
+    loss = lambda: float(np.sum(dZ * O.attention_forward(X, Wqkv, Wos, B, S, True)["Z"]))
+    eps = 1e-6
+    for name, arr, grad in (("X", X, g["dX"]), ("Wqkv", Wqkv, g["dWqkv"]), ("Wo", Wos, g["dWo"])):
+        fd = np.zeros_like(arr)
+        for idx in itertools.product(*[range(s) for s in arr.shape]):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = loss()
+            arr[idx] = old - eps
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert rel(grad, fd) < 1e-6, name
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_backward_vs_torch_autograd(causal):
+    B, S, H, d, n = 2, 6, 4, 4, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, dZ = _attn_inputs(B, S, H, d, n, seed=12)
+    tX, tq, tk, tv, to = (torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, Wq, Wk, Wv, Wo))
+    shp = lambda a: a.reshape(B, S, H, d).transpose(1, 2)
+    o = torch.nn.functional.scaled_dot_product_attention(shp(tX @ tq), shp(tX @ tk), shp(tX @ tv),
+                                                         is_causal=causal)
+    Z = o.transpose(1, 2).reshape(B * S, H * d) @ to
+    (Z * torch.from_numpy(dZ)).sum().backward()
+    g = O.attention_backward(X, Wqkv, Wos, dZ, B, S, causal)
+    assert rel(g["dX"], tX.grad.numpy()) < 1e-12
+    q, k, v = O.unpack_qkv(g["dWqkv"])
+    assert rel(q, tq.grad.numpy()) < 1e-12
+    assert rel(k, tk.grad.numpy()) < 1e-12
+    assert rel(v, tv.grad.numpy()) < 1e-12
+    assert rel(O.stack_rows(g["dWo"]), to.grad.numpy()) < 1e-12
+
+
+# ---------------------------------------------------------------- layer
+def test_layer_backward_finite_differences():
+    B, S, H, d, n, f = 1, 3, 2, 2, 2, 6
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, dZ = _attn_inputs(B, S, H, d, n, seed=13)
+    h = X.shape[1]
+    r = np.random.default_rng(14)
+    W1s = np.stack(np.split(r.standard_normal((h, f)) * 0.3, n, axis=1))
+    W2s = np.stack(np.split(r.standard_normal((f, h)) * 0.3, n, axis=0))
+    g = O.layer_backward(X, Wqkv, Wos, W1s, W2s, dZ, B, S, True)
+    loss = lambda: float(np.sum(dZ * O.layer_forward(X, Wqkv, Wos, W1s, W2s, B, S, True)["Z"]))
+    eps = 1e-6
+    for name, arr in (("dX", X), ("dWqkv", Wqkv), ("dWo", Wos), ("dW1s", W1s), ("dW2s", W2s)):
+        fd = np.zeros_like(arr)
+        for idx in itertools.product(*[range(s) for s in arr.shape]):
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = loss()
+            arr[idx] = old - eps
+            lm = loss()
+            arr[idx] = old
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert rel(g[name], fd) < 1e-6, name
+
+
+# ---------------------------------------------------------------- planted mistakes
+def test_planted_mistakes_are_caught(monkeypatch):
+    """A plausible slip in the oracle must fail a pin: drop the cubic GeLU term,
+    or use the wrong attention scale, and the library cross-checks disagree."""
+    x = RNG.standard_normal(256) * 3
+    ref = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    monkeypatch.setattr(O, "GELU_CUBIC", 0.0)
+    assert np.max(np.abs(O.gelu_tanh(x) - ref)) > 1e-4
+    monkeypatch.setattr(O, "GELU_CUBIC", 0.044715)
+    B, S, H, d, n = 1, 5, 2, 4, 2
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, _ = _attn_inputs(B, S, H, d, n, seed=21)
+    good = O.attention_forward(X, Wqkv, Wos, B, S, True)["Z"]
+    bad_scores = lambda q, k, dd, causal: O.matmul(q, k.T) / dd + np.where(
+        np.tril(np.ones((q.shape[0], k.shape[0]), bool)), 0.0, -np.inf)
+    monkeypatch.setattr(O, "_causal_scores", bad_scores)
+    assert rel(O.attention_forward(X, Wqkv, Wos, B, S, True)["Z"], good) > 1e-3
