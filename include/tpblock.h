@@ -1,0 +1,172 @@
+/*
+ * libtpblock — the Megatron tensor-parallel transformer block on one GB300 (sm_103a).
+ *
+ * The block is the pair of matrix splits the pages describe: a column-split GEMM
+ * whose shards apply the element-wise activation on their own, followed by a
+ * row-split ("outer-product-sum") GEMM whose per-shard partial products are added
+ * (damodev 3D并行 §1.1 and §1.2.1; io.zouht.com 张量并行 §2.1 and §2.2.1; wangyu.me
+ * 张量并行 §两种切分方式 and §多层感知机（MLP）中的张量并行).  The N shards here are
+ * logical partitions on ONE GPU: where the pages place an all-reduce, this library
+ * adds the N partial sums on the device, inside one fp32 accumulator, in the fixed
+ * order shard 0, 1, ..., N-1.  There is no inter-GPU communication.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Y = X W with W stored [in x out], row-major and dense (wangyu.me 张量并行
+ *    §两种切分方式: X is B x M, W is M x N).  T = tokens (= B*S), h = hidden size,
+ *    f = FFN size, H = heads, d = head dim, N = shard count.
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller, 16-byte aligned
+ *    (TP_ERR_ALIGN otherwise).  The library never allocates device memory that the
+ *    caller sees; scratch space is the caller's workspace ``ws`` (256-byte
+ *    aligned, at least the size the matching *_workspace_bytes call returns).
+ *  - Weights are passed shard-major, exactly as the pages split them:
+ *      column split  W1s [N][h][f/N]     block i = columns i*f/N..(i+1)*f/N-1 of W1
+ *      row split     W2s [N][f/N][h]     block i = rows of W2 (same bytes as W2)
+ *      attention     Wqkv [N][h][3][H/N][d]  shard i = the Q, K and V columns of
+ *                    heads i*H/N..(i+1)*H/N-1 (column split by head)
+ *                    Wo [N][(H/N)*d][h]  row split by head (same bytes as Wo)
+ *  - N must divide f (MLP) and H (attention); a shard count that does not divide
+ *    the head count is an error (io.zouht.com 张量并行 §2.2.1, 32 heads on 5 GPUs).
+ *  - Row lengths that TMA moves must be multiples of 8 elements (16 bytes):
+ *    h, f/N, (H/N)*d, and d must be a multiple of 64 with d <= 128 for attention.
+ *  - ``stream`` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *    asynchronous: the return code reports validation and launch errors only.
+ *    Errors detected on the device (a bounded wait that ran out) are latched in a
+ *    device error word and surface through tp_sync_status().
+ *  - dtype: TP_BF16 (bf16 storage, fp32 accumulation) everywhere; TP_F32 (fp32
+ *    FFMA, no TF32) is accepted by tp_mlp_fwd only.
+ */
+#ifndef TPBLOCK_H
+#define TPBLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_NULL = 1,      /* a required pointer is NULL */
+  TP_ERR_SHAPE = 2,     /* a size < 1, N does not divide f or H, a row length not a multiple of 8 */
+  TP_ERR_DTYPE = 3,     /* dtype not supported by this call */
+  TP_ERR_WORKSPACE = 4, /* ws is NULL or smaller than the *_workspace_bytes figure */
+  TP_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed (launch, tensor-map encode, sync) */
+  TP_ERR_TIMEOUT = 6,   /* a kernel's bounded wait ran out (reported by tp_sync_status) */
+  TP_ERR_ALIGN = 7,     /* a pointer is not 16-byte aligned (ws: 256-byte) */
+  TP_ERR_DEVICE = 8     /* the current device is not a compute capability 10.3 (sm_103) GPU */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+/* Library version, (major << 16) | minor. */
+TP_API int tp_version(void);
+
+/* Static string for a tp_status value ("unknown status" for anything else). */
+TP_API const char* tp_status_string(int status);
+
+/* TP_OK if the current CUDA device is sm_103 and the kernels can run on it,
+ * TP_ERR_DEVICE if not, TP_ERR_CUDA if no device can be queried. */
+TP_API int tp_device_check(void);
+
+/* Waits for ``stream``, then reads and clears the device error word.
+ * Returns TP_ERR_TIMEOUT if any kernel since the last call gave up on a bounded
+ * wait, TP_ERR_CUDA if the synchronisation itself failed, TP_OK otherwise. */
+TP_API int tp_sync_status(void* stream);
+
+/* ---------------------------------------------------------------- MLP block */
+
+/* Bytes of scratch that tp_mlp_fwd (with A_save == NULL) and tp_mlp_bwd need:
+ * one [N][T][f/N] activation-sized buffer plus alignment.  0 for invalid sizes. */
+TP_API size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N);
+
+/* MLP block forward, Z = sum_i GeLU(X W1_i) W2_i.
+ * (damodev 3D并行 §1.2.1: column split of the first GEMM, element-wise Act per
+ *  shard, row split of the second GEMM, one all-reduce; io.zouht.com 张量并行
+ *  §2.2.1 前馈网络: Gelu(X W_1) split by columns, the second layer by rows.)
+ *   X      [T][h]                 input (read)
+ *   W1s    [N][h][f/N]            column blocks of W1 (read)
+ *   W2s    [N][f/N][h]            row blocks of W2 (read)
+ *   Y_save [N][T][f/N] or NULL    pre-activation Y_i = X W1_i (written if not NULL;
+ *                                 tp_mlp_bwd needs it)
+ *   A_save [N][T][f/N] or NULL    A_i = GeLU_tanh(Y_i) (written; if NULL it lives in ws)
+ *   Z      [T][h]                 output, the shard partial sums added on the device
+ *                                 in order i = 0..N-1 in one fp32 accumulator
+ * GeLU_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated in fp32.
+ * TP_F32: every tensor fp32, FFMA accumulation.  TP_BF16: bf16 tensors, fp32
+ * accumulation, outputs rounded to bf16 once. */
+TP_API int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
+               const void* X, const void* W1s, const void* W2s,
+               void* Y_save, void* A_save, void* Z,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* MLP block backward for an upstream gradient dZ (bf16 only).
+ * (wangyu.me 张量并行 §通信模式: for the row split dL/dY_i = dL/dY and
+ *  dW_i = X_i^T dY; for the column split dW_i = X^T dY_i and dX = sum_i dY_i W_i^T,
+ *  the all-reduce of io.zouht.com 张量并行 §2.3 f in the backward pass.)
+ *   dY_i  = (dZ W2_i^T) * GeLU'(Y_i)   kept in ws [N][T][f/N]
+ *   dW2_i = A_i^T dZ      -> dW2s [N][f/N][h]
+ *   dW1_i = X^T dY_i      -> dW1s [N][h][f/N]
+ *   dX    = sum_i dY_i W1_i^T  -> dX [T][h], shard sum on the device, order 0..N-1
+ * Y_save and A_save are the tensors tp_mlp_fwd wrote for the same X, W1s. */
+TP_API int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
+               const void* X, const void* W1s, const void* W2s,
+               const void* Y_save, const void* A_save, const void* dZ,
+               void* dX, void* dW1s, void* dW2s,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- attention block */
+
+/* Bytes of scratch tp_attn_fwd (with NULL saves) and tp_attn_bwd need. */
+TP_API size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N);
+
+/* Self-attention block forward (bf16), heads split over N shards.
+ * (damodev 3D并行 §1.2.2; io.zouht.com 张量并行 §2.2.1 多头注意力机制: Q/K/V split
+ *  by columns so each shard owns whole heads, W_O split by rows, one all-reduce;
+ *  wangyu.me 张量并行 §注意力机制中的张量并行.)
+ *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][3][H/N][d] (or ws)
+ *   O_j   = softmax(mask(Q_j K_j^T / sqrt(d))) V_j, per batch and head j
+ *                                          -> O_save [N][T][(H/N)*d] (or ws)
+ *   LSE   = log sum_k exp(Q_j K_j^T/sqrt(d)) per query -> LSE_save [B][H][S] fp32 (or ws)
+ *   Z     = sum_i O_i Wo_i                 -> Z [T][h], shard sum on the device
+ * X is [B*S][h] (token t = b*S + s).  causal != 0 masks keys after the query. */
+TP_API int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal,
+                const void* X, const void* Wqkv, const void* Wo,
+                void* QKV_save, void* O_save, float* LSE_save, void* Z,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* Self-attention block backward (bf16) for an upstream gradient dZ.
+ * The pages give no attention backward; this is the chain rule through the
+ * forward's definition:
+ *   dO_i  = dZ Wo_i^T,  dWo_i = O_i^T dZ
+ *   per head: D = rowsum(dO * O), P = exp(S/sqrt(d) - LSE), dV = P^T dO,
+ *             dP = dO V^T, dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
+ *   dWqkv_i = X^T dQKV_i,  dX = sum_i dQKV_i Wqkv_i^T (shard sum on the device)
+ * QKV_save, O_save, LSE_save are what tp_attn_fwd wrote for the same inputs. */
+TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal,
+                const void* X, const void* Wqkv, const void* Wo,
+                const void* QKV_save, const void* O_save, const float* LSE_save,
+                const void* dZ, void* dX, void* dWqkv, void* dWo,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Launches one block whose single thread waits on a shared-memory barrier that
+ * nothing ever signals, with the same bounded wait the GEMM and attention kernels
+ * use, limited to ``timeout_ns``.  The wait runs out, the kernel latches
+ * TP_ERR_TIMEOUT in the device error word and returns; the context stays usable.
+ * Used to test the timeout path (tp_sync_status must then report TP_ERR_TIMEOUT). */
+TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPBLOCK_H */

@@ -1,0 +1,16 @@
+"""GB300-native Megatron tensor-parallel transformer block.
+
+The compute lives in ``libtpblock.so`` (hand-written sm_103a CUDA: tcgen05/TMEM
+tensor-core GEMMs fed by TMA, fused GeLU epilogues, on-device shard reduction,
+fused attention).  This package is its ctypes binding (same function names as
+the C header ``include/tpblock.h``), the in-tree build, a small convenience layer
+that allocates outputs with torch (``block``), and the seeded synthetic inputs
+(``inputs``).
+"""
+from ._binding import (  # noqa: F401
+    HEADER_PATH, LIB_PATH, STATUS, TP_BF16, TP_F32, TPError, header_functions, load_library,
+    tp_attn_bwd, tp_attn_fwd, tp_attn_workspace_bytes, tp_debug_timeout_probe, tp_device_check,
+    tp_mlp_bwd, tp_mlp_fwd, tp_mlp_workspace_bytes, tp_status_string, tp_sync_status, tp_version,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,203 @@
+"""ctypes binding of libtpblock: one Python function per C entry point, same names.
+
+Marshalling only: tensors become device pointers, sizes become int64, the stream
+defaults to torch's current stream.  Before a call the binding checks that every
+tensor is a contiguous CUDA tensor of the right dtype and at least the number of
+elements the C call will touch (the C side only sees pointers and sizes).  A
+non-zero status raises :class:`TPError`.  There is no fallback: if the shared
+library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libtpblock.so")
+HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "tpblock.h")
+
+TP_F32, TP_BF16 = 0, 1
+STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_WORKSPACE",
+          5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE"}
+_TORCH_DT = {TP_F32: torch.float32, TP_BF16: torch.bfloat16}
+
+_lib = None
+
+i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+_SIGS = {
+    "tp_version": ([], i32),
+    "tp_status_string": ([i32], ctypes.c_char_p),
+    "tp_device_check": ([], i32),
+    "tp_sync_status": ([vp], i32),
+    "tp_debug_timeout_probe": ([i64, vp], i32),
+    "tp_mlp_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
+    "tp_mlp_fwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_mlp_bwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_attn_workspace_bytes": ([i32, i64, i64, i64, i32, i32, i32], sz),
+    "tp_attn_fwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_attn_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                     vp], i32),
+}
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call} failed: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """dlopens libtpblock.so (built by ``build()``) and declares every signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built: run tensor_transformer_block_gb300.build.build() "
+                          "(the block has no non-CUDA implementation)")
+    lib = ctypes.CDLL(path)
+    for name, (args, res) in _SIGS.items():
+        if not hasattr(lib, name):  # TEMP until attention lands
+            continue
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/tpblock.h declares."""
+    text = open(HEADER_PATH).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(tp_[a-z0-9_]+)\s*\(", text)
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().tp_status_string(status).decode()
+    except ImportError:
+        return STATUS.get(status, "unknown status")
+
+
+def _check(status: int, call: str) -> int:
+    if status != 0:
+        raise TPError(status, call)
+    return status
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _p(t, name: str, dtype, numel: int | None, required: bool = True):
+    """Device pointer of ``t`` after checking it (None -> NULL if optional)."""
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return None
+    if isinstance(t, int):  # raw device address supplied by the caller
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} has {t.numel()} elements, needs {numel}")
+    return t.data_ptr()
+
+
+def _ws(ws, need: int):
+    if ws is None:
+        return None, 0
+    if isinstance(ws, int):
+        return ws, need
+    if not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous CUDA tensor")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+# ---------------------------------------------------------------- plain calls
+def tp_version() -> int:
+    return load_library().tp_version()
+
+
+def tp_status_string(status: int) -> str:
+    return load_library().tp_status_string(status).decode()
+
+
+def tp_device_check() -> int:
+    return load_library().tp_device_check()
+
+
+def tp_sync_status(stream=None) -> int:
+    return load_library().tp_sync_status(_stream(stream))
+
+
+def tp_debug_timeout_probe(timeout_ns: int, stream=None) -> int:
+    return _check(load_library().tp_debug_timeout_probe(timeout_ns, _stream(stream)), "tp_debug_timeout_probe")
+
+
+# ---------------------------------------------------------------- MLP block
+def tp_mlp_workspace_bytes(dtype: int, T: int, h: int, f: int, N: int) -> int:
+    return load_library().tp_mlp_workspace_bytes(dtype, T, h, f, N)
+
+
+def tp_mlp_fwd(dtype, T, h, f, N, X, W1s, W2s, Y_save, A_save, Z, ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    act = T * f
+    wptr, wbytes = _ws(ws, tp_mlp_workspace_bytes(dtype, T, h, f, N))
+    return _check(load_library().tp_mlp_fwd(
+        dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
+        _p(Y_save, "Y_save", dt, act, False), _p(A_save, "A_save", dt, act, False), _p(Z, "Z", dt, T * h),
+        wptr, wbytes, _stream(stream)), "tp_mlp_fwd")
+
+
+def tp_mlp_bwd(dtype, T, h, f, N, X, W1s, W2s, Y_save, A_save, dZ, dX, dW1s, dW2s, ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    act = T * f
+    wptr, wbytes = _ws(ws, tp_mlp_workspace_bytes(dtype, T, h, f, N))
+    return _check(load_library().tp_mlp_bwd(
+        dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
+        _p(Y_save, "Y_save", dt, act), _p(A_save, "A_save", dt, act), _p(dZ, "dZ", dt, T * h),
+        _p(dX, "dX", dt, T * h), _p(dW1s, "dW1s", dt, h * f), _p(dW2s, "dW2s", dt, f * h),
+        wptr, wbytes, _stream(stream)), "tp_mlp_bwd")
+
+
+# ---------------------------------------------------------------- attention block
+def tp_attn_workspace_bytes(dtype: int, B: int, S: int, h: int, H: int, d: int, N: int) -> int:
+    return load_library().tp_attn_workspace_bytes(dtype, B, S, h, H, d, N)
+
+
+def tp_attn_fwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, Z, ws=None,
+                stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    wptr, wbytes = _ws(ws, tp_attn_workspace_bytes(dtype, B, S, h, H, d, N))
+    return _check(load_library().tp_attn_fwd(
+        dtype, B, S, h, H, d, N, int(causal), _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, h * 3 * H * d),
+        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * 3 * H * d, False),
+        _p(O_save, "O_save", dt, T * H * d, False), _p(LSE_save, "LSE_save", torch.float32, T * H, False),
+        _p(Z, "Z", dt, T * h), wptr, wbytes, _stream(stream)), "tp_attn_fwd")
+
+
+def tp_attn_bwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, dZ, dX, dWqkv, dWo,
+                ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    wptr, wbytes = _ws(ws, tp_attn_workspace_bytes(dtype, B, S, h, H, d, N))
+    return _check(load_library().tp_attn_bwd(
+        dtype, B, S, h, H, d, N, int(causal), _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, h * 3 * H * d),
+        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * 3 * H * d),
+        _p(O_save, "O_save", dt, T * H * d), _p(LSE_save, "LSE_save", torch.float32, T * H),
+        _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h), _p(dWqkv, "dWqkv", dt, h * 3 * H * d),
+        _p(dWo, "dWo", dt, H * d * h), wptr, wbytes, _stream(stream)), "tp_attn_bwd")

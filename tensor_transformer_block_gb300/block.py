@@ -1,0 +1,90 @@
+"""Convenience layer over the C-ABI: allocates outputs and scratch with torch
+(device memory is torch's job) and calls the libtpblock entry points.  No
+arithmetic happens here; every step of the block runs in the CUDA library."""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+_DT = {torch.float32: B.TP_F32, torch.bfloat16: B.TP_BF16}
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return _DT[t.dtype]
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A 256-byte aligned scratch buffer of at least ``nbytes`` bytes."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def mlp_forward(X, W1s, W2s, save: bool = True, ws=None, stream=None) -> dict:
+    """Z = sum_i GeLU(X W1_i) W2_i.  With ``save`` the pre-activation Y and the
+    activation A (both [N][T][f/N]) are returned for the backward."""
+    N, h, fN = W1s.shape
+    T = X.shape[0]
+    f = N * fN
+    dt = _dtype(X)
+    dev = X.device
+    Z = torch.empty(T, h, dtype=X.dtype, device=dev)
+    Y = torch.empty(N, T, fN, dtype=X.dtype, device=dev) if save else None
+    A = torch.empty(N, T, fN, dtype=X.dtype, device=dev) if save else None
+    if A is None and ws is None:
+        ws = workspace(B.tp_mlp_workspace_bytes(dt, T, h, f, N), dev)
+    B.tp_mlp_fwd(dt, T, h, f, N, X, W1s, W2s, Y, A, Z, ws, stream)
+    return {"Z": Z, "Y": Y, "A": A}
+
+
+def mlp_backward(X, W1s, W2s, Y, A, dZ, ws=None, stream=None, out=None) -> dict:
+    """dX, dW1s, dW2s of L = <dZ, Z> for the block whose forward saved Y and A."""
+    N, h, fN = W1s.shape
+    T = X.shape[0]
+    f = N * fN
+    dt = _dtype(X)
+    dev = X.device
+    if out is None:
+        out = {"dX": torch.empty(T, h, dtype=X.dtype, device=dev),
+               "dW1s": torch.empty(N, h, fN, dtype=X.dtype, device=dev),
+               "dW2s": torch.empty(N, fN, h, dtype=X.dtype, device=dev)}
+    if ws is None:
+        ws = workspace(B.tp_mlp_workspace_bytes(dt, T, h, f, N), dev)
+    B.tp_mlp_bwd(dt, T, h, f, N, X, W1s, W2s, Y, A, dZ, out["dX"], out["dW1s"], out["dW2s"], ws, stream)
+    return out
+
+
+def attn_forward(X, Wqkv, Wo, B_: int, S: int, causal: bool = True, save: bool = True, ws=None,
+                 stream=None) -> dict:
+    """Z = sum_i O_i Wo_i with O the per-head causal attention of X Wqkv_i."""
+    N, h, _, hN, d = Wqkv.shape
+    H = N * hN
+    T = B_ * S
+    dt = _dtype(X)
+    dev = X.device
+    Z = torch.empty(T, h, dtype=X.dtype, device=dev)
+    QKV = torch.empty(N, T, 3 * hN * d, dtype=X.dtype, device=dev) if save else None
+    O = torch.empty(N, T, hN * d, dtype=X.dtype, device=dev) if save else None
+    LSE = torch.empty(B_, H, S, dtype=torch.float32, device=dev) if save else None
+    if ws is None:
+        ws = workspace(B.tp_attn_workspace_bytes(dt, B_, S, h, H, d, N), dev)
+    B.tp_attn_fwd(dt, B_, S, h, H, d, N, causal, X, Wqkv, Wo, QKV, O, LSE, Z, ws, stream)
+    return {"Z": Z, "QKV": QKV, "O": O, "LSE": LSE}
+
+
+def attn_backward(X, Wqkv, Wo, QKV, O, LSE, dZ, B_: int, S: int, causal: bool = True, ws=None, stream=None,
+                  out=None) -> dict:
+    N, h, _, hN, d = Wqkv.shape
+    H = N * hN
+    T = B_ * S
+    dt = _dtype(X)
+    dev = X.device
+    if out is None:
+        out = {"dX": torch.empty(T, h, dtype=X.dtype, device=dev),
+               "dWqkv": torch.empty_like(Wqkv), "dWo": torch.empty_like(Wo)}
+    if ws is None:
+        ws = workspace(B.tp_attn_workspace_bytes(dt, B_, S, h, H, d, N), dev)
+    B.tp_attn_bwd(dt, B_, S, h, H, d, N, causal, X, Wqkv, Wo, QKV, O, LSE, dZ, out["dX"], out["dWqkv"],
+                  out["dWo"], ws, stream)
+    return out

@@ -1,0 +1,248 @@
+// C-ABI entry points of libtpblock (declared in include/tpblock.h): argument
+// validation, workspace carving and the kernel sequence of each call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/tpblock.h"
+#include "gemm_simt.cuh"
+#include "gemm_tc.cuh"
+#include "host_util.cuh"
+#include "ptx.cuh"
+
+// Device error word: kernels latch bits here (atomicOr); tp_sync_status reads and clears it.
+__device__ unsigned g_tp_error_word;
+
+namespace {
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
+constexpr int kMaxDev = 64;
+int g_dev_ok[kMaxDev];            // 0 unknown, 1 ok, -1 not sm_103
+unsigned* g_err_ptr[kMaxDev];
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDev) return -1;
+  return d;
+}
+
+int check_device(unsigned** err) {
+  const int d = current_device();
+  if (d < 0) return TP_ERR_CUDA;
+  if (g_dev_ok[d] == 0) {
+    const int cc = tpb::device_cc();
+    if (cc < 0) return TP_ERR_CUDA;
+    if (cc != 103) {
+      g_dev_ok[d] = -1;
+    } else {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_tp_error_word) != cudaSuccess) return TP_ERR_CUDA;
+      g_err_ptr[d] = static_cast<unsigned*>(p);
+      g_dev_ok[d] = 1;
+    }
+  }
+  if (g_dev_ok[d] < 0) return TP_ERR_DEVICE;
+  if (err) *err = g_err_ptr[d];
+  return TP_OK;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int gemm_status(int rc) { return rc == 0 ? TP_OK : (rc == 1 ? TP_ERR_SHAPE : TP_ERR_CUDA); }
+
+__global__ void k_timeout_probe(unsigned* err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tpb::mbar_init(tpb::smem_u32(&bar), 1);
+    abort_flag = 0;
+    tpb::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const tpb::WaitCtx w{err, &abort_flag, timeout_ns};
+    tpb::mbar_wait(tpb::smem_u32(&bar), 0, w);  // nothing arrives: runs out, latches kErrTimeout
+  }
+}
+
+// Shape rules of the MLP block (bf16 needs 16-byte rows for TMA).
+int mlp_shape_check(int dtype, int64_t T, int64_t h, int64_t f, int N) {
+  if (dtype != TP_F32 && dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (T < 1 || h < 1 || f < 1 || N < 1) return TP_ERR_SHAPE;
+  if (f % N) return TP_ERR_SHAPE;
+  if (T > (1ll << 31) - 1 || h > (1ll << 31) - 1 || f > (1ll << 31) - 1) return TP_ERR_SHAPE;
+  if (dtype == TP_BF16 && ((h % 8) || ((f / N) % 8))) return TP_ERR_SHAPE;
+  return TP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tp_version(void) { return (0 << 16) | 3; }
+
+const char* tp_status_string(int s) {
+  switch (s) {
+    case TP_OK: return "ok";
+    case TP_ERR_NULL: return "a required pointer is NULL";
+    case TP_ERR_SHAPE: return "invalid shape (size < 1, N does not divide f or H, or row length not a multiple of 8)";
+    case TP_ERR_DTYPE: return "dtype not supported by this call";
+    case TP_ERR_WORKSPACE: return "workspace missing or too small";
+    case TP_ERR_CUDA: return "CUDA error";
+    case TP_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    case TP_ERR_ALIGN: return "pointer not aligned (16 bytes; workspace 256 bytes)";
+    case TP_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    default: return "unknown status";
+  }
+}
+
+int tp_device_check(void) { return check_device(nullptr); }
+
+int tp_sync_status(void* stream) {
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TP_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tp_error_word, sizeof(v)) != cudaSuccess) return TP_ERR_CUDA;
+  if (v) {
+    const unsigned z = 0;
+    if (cudaMemcpyToSymbol(g_tp_error_word, &z, sizeof(z)) != cudaSuccess) return TP_ERR_CUDA;
+  }
+  if (v & tpb::kErrTimeout) return TP_ERR_TIMEOUT;
+  return TP_OK;
+}
+
+int tp_debug_timeout_probe(int64_t timeout_ns, void* stream) {
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  if (timeout_ns < 1) return TP_ERR_SHAPE;
+  k_timeout_probe<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, static_cast<unsigned long long>(timeout_ns));
+  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ MLP block
+size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N) {
+  if (mlp_shape_check(dtype, T, h, f, N) != TP_OK) return 0;
+  const size_t esz = dtype == TP_F32 ? 4 : 2;
+  return round_up(static_cast<size_t>(T) * static_cast<size_t>(f) * esz, 256);
+}
+
+int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
+               const void* W2s, void* Y_save, void* A_save, void* Z, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = mlp_shape_check(dtype, T, h, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Z) || !al16(Y_save) || !al16(A_save)) return TP_ERR_ALIGN;
+  void* Abuf = A_save;
+  if (!Abuf) {
+    if (!ws || ws_bytes < tp_mlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+    if (!al256(ws)) return TP_ERR_ALIGN;
+    Abuf = ws;
+  }
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t fN = f / N;
+
+  if (dtype == TP_F32) {
+    tpb::SimtArgs a1{};
+    a1.A = static_cast<const float*>(X);
+    a1.B = static_cast<const float*>(W1s);
+    a1.C = static_cast<float*>(Abuf);
+    a1.Yout = static_cast<float*>(Y_save);
+    a1.M = static_cast<int>(T);
+    a1.N = static_cast<int>(fN);
+    a1.K = static_cast<int>(h);
+    a1.G = N;
+    a1.S = 1;
+    a1.b_sg = h * fN;
+    a1.c_sg = T * fN;
+    a1.lda = h;
+    a1.ldb = fN;
+    a1.ldc = fN;
+    a1.gelu = 1;
+    int rc = tpb::launch_gemm_f32(a1, st);
+    if (rc) return gemm_status(rc);
+    tpb::SimtArgs a2{};
+    a2.A = static_cast<const float*>(Abuf);
+    a2.B = static_cast<const float*>(W2s);
+    a2.C = static_cast<float*>(Z);
+    a2.M = static_cast<int>(T);
+    a2.N = static_cast<int>(h);
+    a2.K = static_cast<int>(fN);
+    a2.G = 1;
+    a2.S = N;
+    a2.a_ss = T * fN;
+    a2.b_ss = fN * h;
+    a2.lda = fN;
+    a2.ldb = h;
+    a2.ldc = h;
+    return gemm_status(tpb::launch_gemm_f32(a2, st));
+  }
+
+  // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard)
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
+                                 kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
+  const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opW2, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st);
+  return gemm_status(rc);
+}
+
+int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
+               const void* W2s, const void* Y_save, const void* A_save, const void* dZ, void* dX, void* dW1s,
+               void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = mlp_shape_check(dtype, T, h, f, N);
+  if (sc != TP_OK) return sc;
+  if (dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (!X || !W1s || !W2s || !Y_save || !A_save || !dZ || !dX || !dW1s || !dW2s) return TP_ERR_NULL;
+  if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Y_save) || !al16(A_save) || !al16(dZ) || !al16(dX) ||
+      !al16(dW1s) || !al16(dW2s))
+    return TP_ERR_ALIGN;
+  if (!ws || ws_bytes < tp_mlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+  if (!al256(ws)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t fN = f / N;
+  void* dY = ws;
+
+  // a3: dY_i = (dZ W2_i^T) * GeLU'(Y_i)   (the row-split backward needs no reduction)
+  const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW2k{W2s, h, fN, N, false, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiDGelu, opdZk, opW2k, dY, Y_save, false, T, fN, N, 1, h, err,
+                                 kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // a4: dW2_i = A_i^T dZ
+  const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
+  const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opAt, opdZn, dW2s, nullptr, false, fN, h, N, 1, T, err, kWaitTimeoutNs,
+                             st);
+  if (rc) return gemm_status(rc);
+  // a5: dW1_i = X^T dY_i
+  const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
+  const tpb::GemmOperand opdYn{dY, fN, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdYn, dW1s, nullptr, false, h, fN, N, 1, T, err, kWaitTimeoutNs,
+                             st);
+  if (rc) return gemm_status(rc);
+  // a6: dX = sum_i dY_i W1_i^T   (the column split's backward all-reduce, done in the accumulator)
+  const tpb::GemmOperand opdYk{dY, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
+                             st);
+  return gemm_status(rc);
+}
+
+}  // extern "C"

@@ -1,0 +1,57 @@
+// Persistent, warp-specialised tcgen05 GEMM for the tensor-parallel block.
+//
+// One launch computes, for g = 0..G-1,
+//     C[g] (M x N) = sum_{s=0}^{S-1} A(g, s) (M x Ks) * B(g, s) (Ks x N)
+// with bf16 operands, an fp32 accumulator in TMEM and a fused epilogue.
+//   * G > 1, S = 1 is the column-parallel GEMM: one output block per shard
+//     (Y_i = X W1_i; damodev 3D并行 §1.2.1 列切分).
+//   * G = 1, S = N is the row-parallel GEMM: the K loop walks shard 0's K tiles,
+//     then shard 1's, ..., all into ONE accumulator, so the shard partial sums
+//     (the pages' all-reduce, damodev 3D并行 §1.1 外积和切分) are added in TMEM in
+//     a fixed order and never written out.
+// Every operand is addressed through a 3-D TMA map whose outer coordinate is the
+// shard index z = g*zg + s*zs, so shard-major layouts need no repacking, and
+// K-ragged shards read zeros past their end.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace tpb {
+
+enum GemmEpi : int {
+  kEpiStore = 0,  // C = bf16(acc)
+  kEpiGelu = 1,   // C = bf16(GeLU_tanh(acc)); optionally Yout = bf16(acc)
+  kEpiDGelu = 2,  // C = bf16(acc * GeLU_tanh'(Yin)), Yin read through a TMA map
+};
+
+struct GemmShape {
+  int M, N;        // output rows / cols per group
+  int G;           // independent output groups
+  int S;           // segments added into one output
+  int kb_per_seg;  // 64-wide K blocks per segment
+  int tiles_m, tiles_n;
+  int a_zg, a_zs, b_zg, b_zs;  // outer TMA coordinate = g*zg + s*zs
+  int store_y;                 // kEpiGelu: also write the pre-activation
+  unsigned* err;
+  unsigned long long timeout_ns;
+};
+
+// One operand as the host describes it: a row-major [d2][d1][d0] bf16 tensor
+// (d0 contiguous).  K-major: d0 runs along K, d1 along M (or N).  MN-major: d0
+// runs along M (or N), d1 along K.
+struct GemmOperand {
+  const void* ptr;
+  int64_t d0, d1, d2;
+  bool mn_major;
+  int zg, zs;
+};
+
+// Host launcher (gemm_tc.cu).  C and Yaux are [G][M][N] bf16 tensors.
+int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
+                     bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,
+                     unsigned long long timeout_ns, cudaStream_t stream);
+
+}  // namespace tpb
