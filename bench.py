@@ -1,0 +1,497 @@
+#!/usr/bin/env python3
+"""Throughput of the tensor-parallel block on GB300 through libtpblock.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one pass of the block over one batch of synthetic input: for the
+default workload (MLP block, T=8192 tokens, h=4096, f=16384, N=8 logical shards)
+the forward and the backward call.  The metric is algorithmic TFLOP/s (2 flop per
+multiply-add; the causal half of attention only; softmax/GeLU not counted).
+Prints one JSON line on rank 0.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the shards are logical; there is no data-path collective): value = all ranks'
+flops / the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TFLOP/s (fwd+bwd) of TP-sharded MLP/attention block, 1 GB300; % BF16 peak"
+DEFAULT_WORKLOAD = "mlp_bf16_T8192_h4096_f16384_N8"
+
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel, with
+# the sha256 of the kernel source it was taken on; reported as null once the
+# source has changed.  Filled from the summaries under profiles/.
+NCU_TRAFFIC: dict = {}
+
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"bf16_tflops": float(d["bf16_tflops"]), "bf16_tflops_sustained": float(d["bf16_tflops_sustained"]),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ flop counts
+def kernel_flops(w) -> dict:
+    """Algorithmic flops per launch of each kernel kind of the workload."""
+    T, h, f = w.T, w.h, w.f
+    out = {}
+    if w.kind in ("mlp", "layer"):
+        g = 2.0 * T * h * f
+        out.update({"mlp.fc1_col_gemm_gelu": g, "mlp.fc2_row_gemm_shard_sum": g, "mlp.bwd_dA_gemm_dgelu": g,
+                    "mlp.bwd_dW2_gemm": g, "mlp.bwd_dW1_gemm": g, "mlp.bwd_dX_row_gemm_shard_sum": g,
+                    "mlp.f32_fc1_col_gemm_gelu": g, "mlp.f32_fc2_row_gemm": g})
+    if w.kind in ("attn", "layer"):
+        Hd = w.H * w.d
+        pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d  # (causal half) x d
+        out.update({"attn.qkv_col_gemm": 2.0 * T * h * 3 * Hd, "attn.core_fwd": 2.0 * pairs,
+                    "attn.out_row_gemm_shard_sum": 2.0 * T * Hd * h, "attn.bwd_dO_gemm": 2.0 * T * h * Hd,
+                    "attn.bwd_dWo_gemm": 2.0 * T * Hd * h, "attn.bwd_core_dkdv": 3.0 * pairs,
+                    "attn.bwd_core_dq": 1.0 * pairs, "attn.bwd_dWqkv_gemm": 2.0 * T * h * 3 * Hd,
+                    "attn.bwd_dX_row_gemm_shard_sum": 2.0 * T * 3 * Hd * h})
+    return out
+
+
+def step_flops(w) -> float:
+    T, h, f = w.T, w.h, w.f
+    tot = 0.0
+    if w.kind in ("mlp", "layer"):
+        tot += (12.0 if w.backward else 4.0) * T * h * f
+    if w.kind in ("attn", "layer"):
+        Hd = w.H * w.d
+        core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
+        tot += 8.0 * T * h * Hd + core
+        if w.backward:
+            tot += 16.0 * T * h * Hd + 2.0 * core
+    return tot
+
+
+def describe(w) -> str:
+    if w.kind == "mlp":
+        return (f"MLP block {'fwd+bwd' if w.backward else 'fwd'}, {w.dtype}, T={w.T} tokens, h={w.h}, f={w.f}, "
+                f"N={w.N} logical shards")
+    if w.kind == "attn":
+        return (f"self-attention block fwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
+                f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
+    return (f"attention + MLP layer fwd+bwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
+            f"f={w.f}, causal, N={w.N} logical shards")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+            return self
+        # nvidia-smi's start-up must not overlap the timed work: wait for its first sample
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            time.sleep(0.02)
+        self.skip = len(self.lines)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self) -> dict | None:
+        rows = []
+        lines = self.lines[getattr(self, "skip", 0):] or self.lines
+        for ln in lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hwt": parts[6], "swt": parts[7], "swpc": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("swpc", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+
+
+def clocks_rejected(c: dict | None) -> bool:
+    if not c:
+        return False
+    bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+    if bad & set(c["reasons"]):
+        return True
+    # stuck well below max with no reason at all: a leftover clock lock
+    return c["sm_mhz"] < 0.5 * c["sm_max_mhz"] and not c["reasons"]
+
+
+# ------------------------------------------------------------------ oracle arm
+def oracle_step(w, inp_np: dict, rows: int) -> float:
+    """Runs the fp64 oracle as it stands on the first ``rows`` tokens of the
+    workload (or the first ``rows`` sequence positions of batch 0 for attention);
+    returns the algorithmic flops that sample stands for."""
+    from oracle import tp_oracle as O
+    if w.kind == "mlp":
+        X, dZ = inp_np["X"][:rows], inp_np.get("dZ")
+        O.mlp_forward(X, inp_np["W1s"], inp_np["W2s"])
+        if w.backward:
+            O.mlp_backward(X, inp_np["W1s"], inp_np["W2s"], dZ[:rows])
+        return (12.0 if w.backward else 4.0) * rows * w.h * w.f
+    import dataclasses
+    sub = dataclasses.replace(w, B=1, S=rows, T=rows)
+    X = inp_np["X"][:rows]
+    if w.kind == "attn":
+        O.attention_forward(X, inp_np["Wqkv"], inp_np["Wo"], 1, rows, w.causal)
+    else:
+        O.layer_forward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["W1s"], inp_np["W2s"], 1, rows, True)
+        O.layer_backward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["W1s"], inp_np["W2s"], inp_np["dZ"][:rows], 1,
+                         rows, True)
+    return step_flops(sub)
+
+
+def oracle_inputs(w) -> dict:
+    from tensor_transformer_block_gb300 import inputs
+    import torch
+    inp = inputs.workload_inputs(w)
+    return {k: v.to(torch.float64).numpy() for k, v in inp.items()}
+
+
+def oracle_cores() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def calibrate_rows(w, inp_np, target_s: float) -> int:
+    rows = 128 if w.kind != "mlp" else 256
+    t0 = time.perf_counter()
+    oracle_step(w, inp_np, rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    limit = w.T if w.kind == "mlp" else w.S
+    return int(max(64, min(limit, rows * target_s / dt)))
+
+
+def cpu_baseline(w, inp_np, target_s: float = 15.0) -> dict:
+    rows = calibrate_rows(w, inp_np, target_s)
+    t0 = time.perf_counter()
+    fl = oracle_step(w, inp_np, rows)
+    dt = time.perf_counter() - t0
+    unit = "tokens" if w.kind == "mlp" else "sequence positions of batch 0"
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle on the first {rows} {unit} of the same workload ({dt:.1f} s)",
+            "seconds": dt}
+
+
+def run_reference(args, w) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp_np = oracle_inputs(w)
+    rows = calibrate_rows(w, inp_np, 3.0)
+    for _ in range(args.warmup):
+        oracle_step(w, inp_np, rows)
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(args.steps):
+        fl += oracle_step(w, inp_np, rows)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    unit = "tokens" if w.kind == "mlp" else "sequence positions of batch 0"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normals, same draws as the GPU arm)",
+            "config": {"workload": w.name, "description": describe(w), "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_cores(), "kind": "oracle",
+                             "sample": f"each step: fp64 oracle on the first {rows} {unit}"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def source_sha(kind: str) -> str:
+    f = "gemm_tc.cu" if "gemm" in kind else ("attn_fwd.cu" if kind == "attn.core_fwd" else "attn_bwd.cu")
+    p = os.path.join(ROOT, "tensor_transformer_block_gb300", "csrc", f)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def run_gpu(args, w) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import tensor_transformer_block_gb300 as tp
+    from tensor_transformer_block_gb300 import block, inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    tp.load_library()
+    if tp.tp_device_check() != 0:
+        raise RuntimeError("not an sm_103 GPU")
+
+    inp = inputs.workload_inputs(w)
+    d = {k: v.to(dev) for k, v in inp.items()}
+    stream = torch.cuda.current_stream(dev)
+    dt = tp.TP_BF16 if w.dtype == "bf16" else tp.TP_F32
+    T, h, f, N = w.T, w.h, w.f, w.N
+    buf = {}
+    if w.kind in ("mlp", "layer"):
+        fN = f // N
+        xin = d["X"] if w.kind == "mlp" else None
+        buf["Y"] = torch.empty(N, T, fN, dtype=d["W1s"].dtype, device=dev)
+        buf["A"] = torch.empty_like(buf["Y"])
+        buf["Z"] = torch.empty(T, h, dtype=d["W1s"].dtype, device=dev)
+        buf["dX"] = torch.empty(T, h, dtype=d["W1s"].dtype, device=dev)
+        buf["dW1s"] = torch.empty_like(d["W1s"])
+        buf["dW2s"] = torch.empty_like(d["W2s"])
+        buf["mws"] = block.workspace(tp.tp_mlp_workspace_bytes(dt, T, h, f, N), dev)
+    if w.kind in ("attn", "layer"):
+        hN = w.H // N
+        buf["QKV"] = torch.empty(N, T, tp.QKV_PLANES * hN * w.d, dtype=torch.bfloat16, device=dev)
+        buf["O"] = torch.empty(N, T, hN * w.d, dtype=torch.bfloat16, device=dev)
+        buf["LSE"] = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+        buf["H"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["aws"] = block.workspace(tp.tp_attn_workspace_bytes(dt, w.B, w.S, h, w.H, w.d, N), dev)
+        if w.kind == "layer":
+            buf["dH"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+            buf["dWqkv"] = torch.empty_like(d["Wqkv"])
+            buf["dWo"] = torch.empty_like(d["Wo"])
+            buf["dXa"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+
+    def step(X, dZ):
+        if w.kind == "mlp":
+            tp.tp_mlp_fwd(dt, T, h, f, N, X, d["W1s"], d["W2s"], buf["Y"], buf["A"], buf["Z"], buf["mws"], stream)
+            if w.backward:
+                tp.tp_mlp_bwd(dt, T, h, f, N, X, d["W1s"], d["W2s"], buf["Y"], buf["A"], dZ, buf["dX"], buf["dW1s"],
+                              buf["dW2s"], buf["mws"], stream)
+            return buf["Z"], buf["dX"] if w.backward else None
+        if w.kind == "attn":
+            tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
+                           buf["LSE"], buf["H"], buf["aws"], stream)
+            return buf["H"], None
+        tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, True, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"], buf["LSE"],
+                       buf["H"], buf["aws"], stream)
+        tp.tp_mlp_fwd(dt, T, h, f, N, buf["H"], d["W1s"], d["W2s"], buf["Y"], buf["A"], buf["Z"], buf["mws"], stream)
+        tp.tp_mlp_bwd(dt, T, h, f, N, buf["H"], d["W1s"], d["W2s"], buf["Y"], buf["A"], dZ, buf["dH"], buf["dW1s"],
+                      buf["dW2s"], buf["mws"], stream)
+        tp.tp_attn_bwd(dt, w.B, w.S, h, w.H, w.d, N, True, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"], buf["LSE"],
+                       buf["dH"], buf["dXa"], buf["dWqkv"], buf["dWo"], buf["aws"], stream)
+        return buf["Z"], buf["dXa"]
+
+    # L2: flush between steps unless one step's working set is far above L2
+    work_bytes = sum(t.numel() * t.element_size() for t in list(d.values()) + list(buf.values()))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < 4 * (129 << 20) else None
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step(d["X"], d.get("dZ"))
+    torch.cuda.synchronize(dev)
+    if tp.tp_sync_status(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    gpu_id = None
+    try:
+        gpu_id = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = gpu_id if gpu_id.startswith("GPU-") else "GPU-" + gpu_id
+    except Exception:
+        gpu_id = None
+
+    def timed_region():
+        tp.tp_timing_enable(True)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_id) as cs:
+            e0.record(stream)
+            for _ in range(args.steps):
+                if flush is not None:
+                    flush.zero_()
+                step(d["X"], d.get("dZ"))
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        barrier()
+        ms = e0.elapsed_time(e1)
+        rep = tp.timing_report()
+        tp.tp_timing_enable(False)
+        return ms, rep, cs.summary()
+
+    ms, rep, clocks = timed_region()
+    if clocks_rejected(clocks):
+        ms, rep, clocks = timed_region()  # re-measured once
+    if tp.tp_sync_status(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = step_flops(w)
+    value = world * flops * args.steps / (ms / 1e3) / 1e12
+
+    # the dominant kernel: largest share of event-measured time in the timed region
+    pk = peaks()
+    kfl = kernel_flops(w)
+    gemm_kinds = {k: v for k, v in rep.items() if k in kfl}
+    dom = max(gemm_kinds, key=lambda k: gemm_kinds[k][1]) if gemm_kinds else None
+    roof = None
+    if dom:
+        n, tot = rep[dom]
+        avg_ms = tot / n
+        achieved = kfl[dom] / (avg_ms / 1e3) / 1e12
+        tr = NCU_TRAFFIC.get(dom)
+        traffic = tr["bytes"] if tr and tr.get("sha") == source_sha(dom) and tr.get("workload") == w.name else None
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops_sustained"], "traffic": traffic, "kernel": dom,
+                "avg_launch_ms": avg_ms, "flops_per_launch": kfl[dom],
+                "peak_source": f"bf16_tflops_sustained ({pk['source']}; kernel timed inside the step loop)"}
+    launches = sum(v[0] for v in rep.values())
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = None
+    if w.kind in ("mlp", "layer") or w.kind == "attn":
+        hX = inp["X"].pin_memory()
+        hdZ = inp["dZ"].pin_memory() if "dZ" in inp and w.backward else None
+        dX_in = torch.empty_like(d["X"])
+        dZ_in = torch.empty_like(d["dZ"]) if hdZ is not None else None
+        out_z = torch.empty(T, h, dtype=d["X"].dtype).pin_memory()
+        out_dx = torch.empty(T, h, dtype=d["X"].dtype).pin_memory() if w.backward else None
+        h2d = hX.numel() * hX.element_size() + (hdZ.numel() * hdZ.element_size() if hdZ is not None else 0)
+        d2h = out_z.numel() * out_z.element_size() + (out_dx.numel() * out_dx.element_size() if out_dx is not None else 0)
+
+        def e2e_step():
+            dX_in.copy_(hX, non_blocking=True)
+            if dZ_in is not None:
+                dZ_in.copy_(hdZ, non_blocking=True)
+            z, dx = step(dX_in, dZ_in)
+            out_z.copy_(z, non_blocking=True)
+            if out_dx is not None:
+                out_dx.copy_(dx, non_blocking=True)
+
+        for _ in range(max(1, args.warmup // 2)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        t0 = time.perf_counter()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * flops * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
+               "path": "pinned host -> device copies, tp_* C-ABI calls, device -> pinned host copies of the block "
+                       "outputs, one stream"}
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        import torch as _t  # noqa: F401
+        cpu = cpu_baseline(w, {k: v.to(torch.float64).numpy() for k, v in inp.items()}, args.cpu_seconds)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded normals; weights random-init)",
+                "config": {"workload": w.name, "description": describe(w), "parallelism": "tp" + str(N) +
+                           " logical shards on one GPU" + (f", {world} independent replicas" if world > 1 else ""),
+                           "flops_per_step": flops,
+                           "l2": ("flushed between steps (256 MiB write)" if flush is not None else
+                                  f"inputs larger than L2 (step working set {work_bytes / 2**30:.2f} GiB); no flush")},
+                "pct_of_peak": {"of_measured_burst": value / world / pk["bf16_tflops"],
+                                "of_measured_sustained": value / world / pk["bf16_tflops_sustained"],
+                                "peaks": pk["source"]},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "kernels": {k: {"launches": v[0], "ms_total": v[1]} for k, v in rep.items()},
+                "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="tpblock", choices=["tpblock", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    from tensor_transformer_block_gb300.inputs import WORKLOADS
+    if args.workload not in WORKLOADS:
+        raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -131,7 +131,11 @@ TP_API size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h
  * (damodev 3D并行 §1.2.2; io.zouht.com 张量并行 §2.2.1 多头注意力机制: Q/K/V split
  *  by columns so each shard owns whole heads, W_O split by rows, one all-reduce;
  *  wangyu.me 张量并行 §注意力机制中的张量并行.)
- *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][3][H/N][d] (or ws)
+ *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][5][H/N][d] (or ws): planes
+ *                                             Q, K, V, then Q - bf16(Q) and K - bf16(K)
+ *                                             (the scores are formed split-bf16,
+ *                                             Qh Kh^T + Qh Kl^T + Ql Kh^T, so that Q K^T
+ *                                             keeps ~16 bits before the softmax)
  *   O_j   = softmax(mask(Q_j K_j^T / sqrt(d))) V_j, per batch and head j
  *                                          -> O_save [N][T][(H/N)*d] (or ws)
  *   LSE   = log sum_k exp(Q_j K_j^T/sqrt(d)) per query -> LSE_save [B][H][S] fp32 (or ws)
@@ -149,6 +153,7 @@ TP_API int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  *   per head: D = rowsum(dO * O), P = exp(S/sqrt(d) - LSE), dV = P^T dO,
  *             dP = dO V^T, dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
  *   dWqkv_i = X^T dQKV_i,  dX = sum_i dQKV_i Wqkv_i^T (shard sum on the device)
+ *   (dQKV [N][T][3][H/N][d] lives in ws; P is recomputed with the same split scores)
  * QKV_save, O_save, LSE_save are what tp_attn_fwd wrote for the same inputs. */
 TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal,
                 const void* X, const void* Wqkv, const void* Wo,
@@ -164,6 +169,24 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  * TP_ERR_TIMEOUT in the device error word and returns; the context stays usable.
  * Used to test the timeout path (tp_sync_status must then report TP_ERR_TIMEOUT). */
 TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
+
+/* ---------------------------------------------------------- kernel timing */
+
+/* Every kernel the library launches is counted per kind.  With timing on, a
+ * pair of CUDA events is also recorded on the launch stream around each launch.
+ * tp_timing_enable() clears the counts and the recorded times. */
+TP_API int tp_timing_enable(int on);
+
+/* Number of kernel kinds (indices 0 .. n-1 for the calls below). */
+TP_API int tp_timing_kinds(void);
+
+/* Static name of kernel kind ``kind`` (NULL if out of range). */
+TP_API const char* tp_timing_name(int kind);
+
+/* Launch count since the last tp_timing_enable() and, if timing was on, the sum
+ * of the launches' event-measured durations in milliseconds (waits for the
+ * events).  TP_ERR_SHAPE for a bad index, TP_ERR_CUDA if an event query fails. */
+TP_API int tp_timing_read(int kind, int64_t* launches, double* total_ms);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(HERE, "libtpblock.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "tpblock.h")
 
 TP_F32, TP_BF16 = 0, 1
+QKV_PLANES = 5  # Q, K, V, Q - bf16(Q), K - bf16(K) per (token, head)
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_WORKSPACE",
           5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE"}
 _TORCH_DT = {TP_F32: torch.float32, TP_BF16: torch.bfloat16}
@@ -40,6 +41,10 @@ _SIGS = {
     "tp_attn_fwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
     "tp_attn_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                      vp], i32),
+    "tp_timing_enable": ([i32], i32),
+    "tp_timing_kinds": ([], i32),
+    "tp_timing_name": ([i32], ctypes.c_char_p),
+    "tp_timing_read": ([i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double)], i32),
 }
 
 
@@ -60,8 +65,6 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                           "(the block has no non-CUDA implementation)")
     lib = ctypes.CDLL(path)
     for name, (args, res) in _SIGS.items():
-        if not hasattr(lib, name):  # TEMP until attention lands
-            continue
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = res
@@ -185,7 +188,7 @@ def tp_attn_fwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, 
     wptr, wbytes = _ws(ws, tp_attn_workspace_bytes(dtype, B, S, h, H, d, N))
     return _check(load_library().tp_attn_fwd(
         dtype, B, S, h, H, d, N, int(causal), _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, h * 3 * H * d),
-        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * 3 * H * d, False),
+        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * QKV_PLANES * H * d, False),
         _p(O_save, "O_save", dt, T * H * d, False), _p(LSE_save, "LSE_save", torch.float32, T * H, False),
         _p(Z, "Z", dt, T * h), wptr, wbytes, _stream(stream)), "tp_attn_fwd")
 
@@ -197,7 +200,38 @@ def tp_attn_bwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, 
     wptr, wbytes = _ws(ws, tp_attn_workspace_bytes(dtype, B, S, h, H, d, N))
     return _check(load_library().tp_attn_bwd(
         dtype, B, S, h, H, d, N, int(causal), _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, h * 3 * H * d),
-        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * 3 * H * d),
+        _p(Wo, "Wo", dt, H * d * h), _p(QKV_save, "QKV_save", dt, T * QKV_PLANES * H * d),
         _p(O_save, "O_save", dt, T * H * d), _p(LSE_save, "LSE_save", torch.float32, T * H),
         _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h), _p(dWqkv, "dWqkv", dt, h * 3 * H * d),
         _p(dWo, "dWo", dt, H * d * h), wptr, wbytes, _stream(stream)), "tp_attn_bwd")
+
+
+# ---------------------------------------------------------------- kernel timing
+def tp_timing_enable(on: bool) -> int:
+    return _check(load_library().tp_timing_enable(1 if on else 0), "tp_timing_enable")
+
+
+def tp_timing_kinds() -> int:
+    return load_library().tp_timing_kinds()
+
+
+def tp_timing_name(kind: int) -> str:
+    r = load_library().tp_timing_name(kind)
+    return r.decode() if r else ""
+
+
+def tp_timing_read(kind: int) -> tuple[int, float]:
+    n = ctypes.c_int64(0)
+    t = ctypes.c_double(0.0)
+    _check(load_library().tp_timing_read(kind, ctypes.byref(n), ctypes.byref(t)), "tp_timing_read")
+    return int(n.value), float(t.value)
+
+
+def timing_report() -> dict:
+    """{kernel kind name: (launches, total event-measured ms)} for every kind launched."""
+    out = {}
+    for k in range(tp_timing_kinds()):
+        n, ms = tp_timing_read(k)
+        if n:
+            out[tp_timing_name(k)] = (n, ms)
+    return out

@@ -64,7 +64,7 @@ def attn_forward(X, Wqkv, Wo, B_: int, S: int, causal: bool = True, save: bool =
     dt = _dtype(X)
     dev = X.device
     Z = torch.empty(T, h, dtype=X.dtype, device=dev)
-    QKV = torch.empty(N, T, 3 * hN * d, dtype=X.dtype, device=dev) if save else None
+    QKV = torch.empty(N, T, B.QKV_PLANES * hN * d, dtype=X.dtype, device=dev) if save else None
     O = torch.empty(N, T, hN * d, dtype=X.dtype, device=dev) if save else None
     LSE = torch.empty(B_, H, S, dtype=torch.float32, device=dev) if save else None
     if ws is None:

@@ -7,6 +7,7 @@
 #include <cstring>
 
 #include "../../include/tpblock.h"
+#include "attn.cuh"
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
 #include "host_util.cuh"
@@ -79,6 +80,32 @@ int mlp_shape_check(int dtype, int64_t T, int64_t h, int64_t f, int N) {
   return TP_OK;
 }
 
+// Shape rules of the attention block.
+int attn_shape_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N) {
+  if (dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (B < 1 || S < 1 || h < 1 || H < 1 || d < 1 || N < 1) return TP_ERR_SHAPE;
+  if (H % N) return TP_ERR_SHAPE;
+  if (d != 64 && d != 128) return TP_ERR_SHAPE;
+  if (h % 8) return TP_ERR_SHAPE;
+  if (B > 65535 || H > 65535 || B * S > (1ll << 31) - 1 || h > (1ll << 31) - 1) return TP_ERR_SHAPE;
+  return TP_OK;
+}
+
+// Workspace of the attention block: [QKV (5 planes) | O | LSE] in the forward;
+// [dQKV (3 planes) | dO | Dsum] in the backward fits the same regions.
+struct AttnWs {
+  size_t qkv, o, lse, total;
+};
+AttnWs attn_ws(int64_t B, int64_t S, int H, int d) {
+  const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  AttnWs w;
+  w.qkv = round_up(T * tpb::kQkvPlanes * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
+  w.o = round_up(T * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
+  w.lse = round_up(T * static_cast<size_t>(H) * 4, 256);
+  w.total = w.qkv + w.o + w.lse;
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
@@ -122,8 +149,11 @@ int tp_debug_timeout_probe(int64_t timeout_ns, void* stream) {
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
   if (timeout_ns < 1) return TP_ERR_SHAPE;
+  const int slot = tpb::timing_begin(tpb::kKProbe, static_cast<cudaStream_t>(stream));
   k_timeout_probe<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, static_cast<unsigned long long>(timeout_ns));
-  return cudaGetLastError() == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  tpb::timing_end(slot, static_cast<cudaStream_t>(stream));
+  return ok ? TP_OK : TP_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ MLP block
@@ -168,7 +198,7 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
     a1.ldb = fN;
     a1.ldc = fN;
     a1.gelu = 1;
-    int rc = tpb::launch_gemm_f32(a1, st);
+    int rc = tpb::launch_gemm_f32(a1, st, tpb::kKMlpF32Fc1);
     if (rc) return gemm_status(rc);
     tpb::SimtArgs a2{};
     a2.A = static_cast<const float*>(Abuf);
@@ -184,19 +214,19 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
     a2.lda = fN;
     a2.ldb = h;
     a2.ldc = h;
-    return gemm_status(tpb::launch_gemm_f32(a2, st));
+    return gemm_status(tpb::launch_gemm_f32(a2, st, tpb::kKMlpF32Fc2));
   }
 
   // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard)
   const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
   const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
   int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st);
+                                 kWaitTimeoutNs, st, tpb::kKMlpFc1);
   if (rc) return gemm_status(rc);
   // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
   const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
   const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opW2, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st);
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opW2, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2);
   return gemm_status(rc);
 }
 
@@ -223,26 +253,159 @@ int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
   const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
   const tpb::GemmOperand opW2k{W2s, h, fN, N, false, 1, 0};
   int rc = tpb::launch_gemm_bf16(tpb::kEpiDGelu, opdZk, opW2k, dY, Y_save, false, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st);
+                                 kWaitTimeoutNs, st, tpb::kKMlpDgelu);
   if (rc) return gemm_status(rc);
   // a4: dW2_i = A_i^T dZ
   const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
   const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opAt, opdZn, dW2s, nullptr, false, fN, h, N, 1, T, err, kWaitTimeoutNs,
-                             st);
+                             st, tpb::kKMlpDw2);
   if (rc) return gemm_status(rc);
   // a5: dW1_i = X^T dY_i
   const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
   const tpb::GemmOperand opdYn{dY, fN, T, N, true, 1, 0};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdYn, dW1s, nullptr, false, h, fN, N, 1, T, err, kWaitTimeoutNs,
-                             st);
+                             st, tpb::kKMlpDw1);
   if (rc) return gemm_status(rc);
   // a6: dX = sum_i dY_i W1_i^T   (the column split's backward all-reduce, done in the accumulator)
   const tpb::GemmOperand opdYk{dY, fN, T, N, false, 0, 1};
   const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
-                             st);
+                             st, tpb::kKMlpDx);
   return gemm_status(rc);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ attention block
+extern "C" {
+
+size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N) {
+  if (attn_shape_check(dtype, B, S, h, H, d, N) != TP_OK) return 0;
+  return attn_ws(B, S, H, d).total;
+}
+
+int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
+                const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
+                size_t ws_bytes, void* stream) {
+  const int sc = attn_shape_check(dtype, B, S, h, H, d, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wqkv || !Wo || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(Z) || !al16(QKV_save) || !al16(O_save) || !al16(LSE_save))
+    return TP_ERR_ALIGN;
+  const AttnWs w = attn_ws(B, S, H, d);
+  char* wsb = static_cast<char*>(ws);
+  if (!QKV_save || !O_save || !LSE_save) {
+    if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
+    if (!al256(ws)) return TP_ERR_ALIGN;
+  }
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int hN = H / N;
+  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
+  void* QKV = QKV_save ? QKV_save : static_cast<void*>(wsb);
+  void* Ob = O_save ? O_save : static_cast<void*>(wsb + w.qkv);
+  float* LSE = LSE_save ? LSE_save : reinterpret_cast<float*>(wsb + w.qkv + w.o);
+
+  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
+  // writes the bf16 residuals of Q and K as planes 3 and 4 (split-bf16 scores)
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW{Wqkv, 3 * hNd, h, N, true, 1, 0};
+  tpb::GemmExtra split;
+  split.ldc = tpb::kQkvPlanes * hNd;
+  split.split_cols = 2 * hNd;
+  split.lo_off = 3 * hNd;
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, 3 * hNd, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
+  if (rc) return gemm_status(rc);
+  // a8: per-head causal attention
+  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
+  rc = tpb::launch_attn_fwd(ad, QKV, Ob, LSE, err, kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // a9: Z = sum_i O_i Wo_i  (row-parallel, shard sum in the accumulator)
+  const tpb::GemmOperand opO{Ob, hNd, T, N, false, 0, 1};
+  const tpb::GemmOperand opWo{Wo, h, hNd, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opO, opWo, Z, nullptr, false, T, h, 1, N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut);
+  return gemm_status(rc);
+}
+
+int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
+                const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
+                const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = attn_shape_check(dtype, B, S, h, H, d, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wqkv || !Wo || !QKV_save || !O_save || !LSE_save || !dZ || !dX || !dWqkv || !dWo) return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(QKV_save) || !al16(O_save) || !al16(LSE_save) || !al16(dZ) ||
+      !al16(dX) || !al16(dWqkv) || !al16(dWo))
+    return TP_ERR_ALIGN;
+  const AttnWs w = attn_ws(B, S, H, d);
+  if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
+  if (!al256(ws)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int hN = H / N;
+  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
+  char* wsb = static_cast<char*>(ws);
+  void* dQKV = wsb;
+  void* dO = wsb + w.qkv;
+  float* dsum = reinterpret_cast<float*>(wsb + w.qkv + w.o);
+
+  // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ)
+  const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opWok{Wo, h, hNd, N, false, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdZk, opWok, dO, nullptr, false, T, hNd, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKAttnDo);
+  if (rc) return gemm_status(rc);
+  // dWo_i = O_i^T dZ
+  const tpb::GemmOperand opOt{O_save, hNd, T, N, true, 1, 0};
+  const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opOt, opdZn, dWo, nullptr, false, hNd, h, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKAttnDwo);
+  if (rc) return gemm_status(rc);
+  // attention core backward -> dQKV
+  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
+  rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // dWqkv_i = X^T dQKV_i
+  const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
+  const tpb::GemmOperand opdQn{dQKV, 3 * hNd, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, 3 * hNd, N, 1, T, err,
+                             kWaitTimeoutNs, st, tpb::kKAttnDwqkv);
+  if (rc) return gemm_status(rc);
+  // dX = sum_i dQKV_i Wqkv_i^T  (the column split's backward all-reduce, in the accumulator)
+  const tpb::GemmOperand opdQk{dQKV, 3 * hNd, T, N, false, 0, 1};
+  const tpb::GemmOperand opWk{Wqkv, 3 * hNd, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, 3 * hNd, err,
+                             kWaitTimeoutNs, st, tpb::kKAttnDx);
+  return gemm_status(rc);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ kernel timing
+extern "C" {
+
+int tp_timing_enable(int on) {
+  tpb::timing_enable(on != 0);
+  return TP_OK;
+}
+
+int tp_timing_kinds(void) { return tpb::kNumKernelKinds; }
+
+const char* tp_timing_name(int kind) { return tpb::kernel_kind_name(kind); }
+
+int tp_timing_read(int kind, int64_t* launches, double* total_ms) {
+  if (kind < 0 || kind >= tpb::kNumKernelKinds) return TP_ERR_SHAPE;
+  long long n = 0;
+  double t = 0.0;
+  if (!tpb::timing_read(kind, &n, &t)) return TP_ERR_CUDA;
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = t;
+  return TP_OK;
 }
 
 }  // extern "C"

@@ -10,6 +10,7 @@
 #include <cstdint>
 
 #include "gemm_simt.cuh"
+#include "host_util.cuh"
 
 namespace tpb {
 namespace {
@@ -81,12 +82,15 @@ __global__ void __launch_bounds__(256) k_gemm_f32(SimtArgs a) {
 
 }  // namespace
 
-int launch_gemm_f32(const SimtArgs& a, cudaStream_t stream) {
+int launch_gemm_f32(const SimtArgs& a, cudaStream_t stream, int kind) {
   if (a.M < 1 || a.N < 1 || a.K < 1 || a.G < 1 || a.S < 1) return 1;
   dim3 grid((a.N + TN - 1) / TN, (a.M + TM - 1) / TM, a.G);
   if (grid.y > 65535 || grid.z > 65535) return 1;
+  const int slot = timing_begin(kind, stream);
   k_gemm_f32<<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  timing_end(slot, stream);
+  return ok ? 0 : 2;
 }
 
 }  // namespace tpb

@@ -19,6 +19,6 @@ struct SimtArgs {
   int gelu;
 };
 
-int launch_gemm_f32(const SimtArgs& a, cudaStream_t stream);
+int launch_gemm_f32(const SimtArgs& a, cudaStream_t stream, int kind);
 
 }  // namespace tpb

@@ -280,6 +280,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               bulk_commit();
             }
             ++ecount;
+          } else if (EPI == kEpiSplit) {
+            const bool with_lo = ccol < p.split_cols;
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t* v = (c < 4) ? &r0[8 * c] : &r1[8 * (c - 4)];
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
+                hi[e] = pack_bf16x2(x0, x1);
+                lo[e] = pack_bf16x2(x0 - bf16lo_to_f32(hi[e]), x1 - bf16hi_to_f32(hi[e]));
+              }
+              const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+              st_shared_v4(ebuf[0] + off, hi[0], hi[1], hi[2], hi[3]);
+              if (with_lo) st_shared_v4(ebuf[1] + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, ebuf[0], ccol, row0, g);
+              if (with_lo) tma_store_3d(&tmC, ebuf[1], ccol + p.lo_off, row0, g);
+              bulk_commit();
+            }
           } else if (EPI == kEpiGelu) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
@@ -383,6 +408,7 @@ KernelFn get_kernel() {
 KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
   if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<false, true, kEpiGelu>();
   if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<false, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<false, true, kEpiSplit>();
   if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<false, false, kEpiDGelu>();
   if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<false, false, kEpiStore>();
   if (a_mn && b_mn && epi == kEpiStore) return get_kernel<true, true, kEpiStore>();
@@ -400,15 +426,19 @@ bool operand_map(CUtensorMap* m, const GemmOperand& o, bool is_a) {
 
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
                      bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,
-                     unsigned long long timeout_ns, cudaStream_t stream) {
+                     unsigned long long timeout_ns, cudaStream_t stream, int kind, const GemmExtra& extra) {
   // returns 0 on success, 1 for bad arguments, 2 for a CUDA failure
   if (M < 1 || N < 1 || G < 1 || S < 1 || Ks < 1) return 1;
-  if ((A.d0 % 8) || (B.d0 % 8) || (N % 8)) return 1;
+  const int64_t ldc = extra.ldc > 0 ? extra.ldc : N;
+  if ((A.d0 % 8) || (B.d0 % 8) || (N % 8) || (ldc % 8) || ldc < N) return 1;
+  if (ldc != N && (N % 64)) return 1;  // a partial last chunk would not be clipped at N
+  if (epi == kEpiSplit && ((extra.split_cols % 64) || extra.lo_off < N || extra.lo_off + extra.split_cols > ldc))
+    return 1;
   KernelFn fn = pick_kernel(A.mn_major, B.mn_major, epi);
   if (!fn) return 2;
   CUtensorMap ta, tb, tc, ty;
   if (!operand_map(&ta, A, true) || !operand_map(&tb, B, false)) return 2;
-  const uint64_t cdims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
+  const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
   const uint32_t cbox[3] = {64u, 32u, 1u};
   if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
   if (Yaux) {
@@ -430,14 +460,19 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.b_zg = B.zg;
   p.b_zs = B.zs;
   p.store_y = (store_y && Yaux) ? 1 : 0;
+  p.split_cols = static_cast<int>(extra.split_cols);
+  p.lo_off = static_cast<int>(extra.lo_off);
   p.err = err;
   p.timeout_ns = timeout_ns;
   const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;
   const int sms = device_sm_count();
   if (sms <= 0) return 2;
   const int grid = static_cast<int>(total < sms ? total : sms);
+  const int slot = timing_begin(kind, stream);
   fn<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ta, tb, tc, ty, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : 2;
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  timing_end(slot, stream);
+  return ok ? 0 : 2;
 }
 
 }  // namespace tpb

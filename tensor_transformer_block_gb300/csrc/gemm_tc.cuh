@@ -25,6 +25,8 @@ enum GemmEpi : int {
   kEpiStore = 0,  // C = bf16(acc)
   kEpiGelu = 1,   // C = bf16(GeLU_tanh(acc)); optionally Yout = bf16(acc)
   kEpiDGelu = 2,  // C = bf16(acc * GeLU_tanh'(Yin)), Yin read through a TMA map
+  kEpiSplit = 3,  // C = bf16(acc); for columns < split_cols also the residual
+                  // bf16(acc - bf16(acc)) at column + lo_off of the same row
 };
 
 struct GemmShape {
@@ -35,6 +37,7 @@ struct GemmShape {
   int tiles_m, tiles_n;
   int a_zg, a_zs, b_zg, b_zs;  // outer TMA coordinate = g*zg + s*zs
   int store_y;                 // kEpiGelu: also write the pre-activation
+  int split_cols, lo_off;      // kEpiSplit
   unsigned* err;
   unsigned long long timeout_ns;
 };
@@ -49,9 +52,16 @@ struct GemmOperand {
   int zg, zs;
 };
 
-// Host launcher (gemm_tc.cu).  C and Yaux are [G][M][N] bf16 tensors.
+// Host launcher (gemm_tc.cu).  C and Yaux are [G][M][ldc] bf16 tensors of which
+// columns 0..N-1 are computed (ldc = 0 means ldc = N).
+struct GemmExtra {
+  int64_t ldc = 0;
+  int64_t split_cols = 0;  // kEpiSplit
+  int64_t lo_off = 0;      // kEpiSplit
+};
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
                      bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,
-                     unsigned long long timeout_ns, cudaStream_t stream);
+                     unsigned long long timeout_ns, cudaStream_t stream, int kind,
+                     const GemmExtra& extra = GemmExtra());
 
 }  // namespace tpb

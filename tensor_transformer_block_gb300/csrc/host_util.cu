@@ -1,6 +1,7 @@
 #include "host_util.cuh"
 
 #include <mutex>
+#include <vector>
 
 namespace tpb {
 
@@ -65,6 +66,86 @@ int device_cc() {
   if (cudaDeviceGetAttribute(&ma, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&mi, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return -1;
   return ma * 10 + mi;
+}
+
+namespace {
+
+const char* const kKindNames[kNumKernelKinds] = {
+    "mlp.fc1_col_gemm_gelu", "mlp.fc2_row_gemm_shard_sum", "mlp.bwd_dA_gemm_dgelu", "mlp.bwd_dW2_gemm",
+    "mlp.bwd_dW1_gemm", "mlp.bwd_dX_row_gemm_shard_sum", "mlp.f32_fc1_col_gemm_gelu", "mlp.f32_fc2_row_gemm",
+    "attn.qkv_col_gemm", "attn.core_fwd", "attn.out_row_gemm_shard_sum", "attn.bwd_dO_gemm", "attn.bwd_dWo_gemm",
+    "attn.bwd_dsum", "attn.bwd_core_dkdv", "attn.bwd_core_dq", "attn.bwd_dWqkv_gemm",
+    "attn.bwd_dX_row_gemm_shard_sum", "debug.timeout_probe"};
+
+struct Slot {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+std::mutex g_tmu;
+bool g_timing = false;
+long long g_launches[kNumKernelKinds] = {0};
+std::vector<Slot> g_slots;      // recorded this timing window
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+const char* kernel_kind_name(int k) { return (k >= 0 && k < kNumKernelKinds) ? kKindNames[k] : nullptr; }
+
+int timing_begin(int kind, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (kind < 0 || kind >= kNumKernelKinds) return -1;
+  ++g_launches[kind];
+  if (!g_timing) return -1;
+  Slot s{kind, take_event(), take_event()};
+  if (!s.a || !s.b || cudaEventRecord(s.a, st) != cudaSuccess) return -1;
+  g_slots.push_back(s);
+  return static_cast<int>(g_slots.size()) - 1;
+}
+
+void timing_end(int slot, cudaStream_t st) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (slot < static_cast<int>(g_slots.size())) cudaEventRecord(g_slots[slot].b, st);
+}
+
+void timing_enable(bool on) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  for (auto& s : g_slots) {
+    cudaEventSynchronize(s.b);
+    g_pool.push_back(s.a);
+    g_pool.push_back(s.b);
+  }
+  g_slots.clear();
+  for (auto& c : g_launches) c = 0;
+  g_timing = on;
+}
+
+bool timing_read(int kind, long long* launches, double* total_ms) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (kind < 0 || kind >= kNumKernelKinds) return false;
+  double t = 0.0;
+  for (auto& s : g_slots) {
+    if (s.kind != kind) continue;
+    if (cudaEventSynchronize(s.b) != cudaSuccess) return false;
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, s.a, s.b) != cudaSuccess) return false;
+    t += ms;
+  }
+  if (launches) *launches = g_launches[kind];
+  if (total_ms) *total_ms = t;
+  return true;
 }
 
 }  // namespace tpb

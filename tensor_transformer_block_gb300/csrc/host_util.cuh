@@ -22,4 +22,35 @@ int device_sm_count();
 // Current device's compute capability as major*10+minor, or -1.
 int device_cc();
 
+// Kernel launch registry.  Every launch is counted per kernel kind; while
+// timing is on, a pair of CUDA events is recorded on the launch stream around
+// it, and timing_read() sums the elapsed times per kind.
+enum KernelKind : int {
+  kKMlpFc1 = 0,     // column-parallel GEMM + GeLU (Y_i = X W1_i)
+  kKMlpFc2,         // row-parallel GEMM, shard sum in the accumulator (Z = sum_i A_i W2_i)
+  kKMlpDgelu,       // dY_i = (dZ W2_i^T) * GeLU'(Y_i)
+  kKMlpDw2,         // dW2_i = A_i^T dZ
+  kKMlpDw1,         // dW1_i = X^T dY_i
+  kKMlpDx,          // dX = sum_i dY_i W1_i^T
+  kKMlpF32Fc1,      // fp32 column GEMM + GeLU
+  kKMlpF32Fc2,      // fp32 row GEMM
+  kKAttnQkv,        // [Q K V]_i = X Wqkv_i
+  kKAttnCore,       // per-head causal attention forward
+  kKAttnOut,        // Z = sum_i O_i Wo_i
+  kKAttnDo,         // dO_i = dZ Wo_i^T
+  kKAttnDwo,        // dWo_i = O_i^T dZ
+  kKAttnDsum,       // rowsum(dO * O)
+  kKAttnDkdv,       // dK, dV per key block
+  kKAttnDq,         // dQ per query block
+  kKAttnDwqkv,      // dWqkv_i = X^T dQKV_i
+  kKAttnDx,         // dX = sum_i dQKV_i Wqkv_i^T
+  kKProbe,          // timeout probe
+  kNumKernelKinds
+};
+const char* kernel_kind_name(int k);
+int timing_begin(int kind, cudaStream_t st);  // returns a slot (or -1)
+void timing_end(int slot, cudaStream_t st);
+void timing_enable(bool on);                   // also clears counts and times
+bool timing_read(int kind, long long* launches, double* total_ms);
+
 }  // namespace tpb
