@@ -122,6 +122,30 @@ TP_API int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
                void* dX, void* dW1s, void* dW2s,
                void* ws, size_t ws_bytes, void* stream);
 
+/* Size of the fixed device array tp_mlp_fwd_noalloc keeps its scratch in (32 MiB). */
+#define TP_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* MLP block forward for callers that cannot allocate device memory.
+ * The method on the pages has no counterpart to this call; it exists for the
+ * software around it.  Some callers cannot call cudaMalloc at the point where
+ * they run the block: a plug-in inside a host framework that owns every device
+ * allocation and plans memory ahead of time, or a runtime with a fixed memory
+ * budget that forbids allocation once serving has started (cudaMalloc can also
+ * synchronise the device, which such callers must avoid).  This call computes
+ * the same Z as tp_mlp_fwd with Y_save = A_save = NULL, but keeps the activation
+ * A in a fixed array of TP_NOALLOC_SCRATCH_BYTES in the library's own device
+ * memory instead of a caller's workspace; the caller still passes X, W1s, W2s
+ * and Z.  It calls neither cudaMalloc nor cudaFree nor any allocating routine.
+ *  - Limit: T * f * sizeof(element) <= TP_NOALLOC_SCRATCH_BYTES, else
+ *    TP_ERR_WORKSPACE (every other check as in tp_mlp_fwd).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls on a device share the one array.  The array is written before it
+ *    is read in every call (nothing in it has to start at zero), but calls whose
+ *    kernels overlap on the GPU, such as calls on two streams at once, race on it. */
+TP_API int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N,
+                              const void* X, const void* W1s, const void* W2s, void* Z, void* stream);
+
 /* ---------------------------------------------------------- attention block */
 
 /* Bytes of scratch tp_attn_fwd (with NULL saves) and tp_attn_bwd need. */

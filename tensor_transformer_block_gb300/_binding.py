@@ -41,6 +41,7 @@ _SIGS = {
     "tp_attn_fwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
     "tp_attn_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                      vp], i32),
+    "tp_mlp_fwd_noalloc": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
     "tp_timing_name": ([i32], ctypes.c_char_p),
@@ -174,6 +175,15 @@ def tp_mlp_bwd(dtype, T, h, f, N, X, W1s, W2s, Y_save, A_save, dZ, dX, dW1s, dW2
         _p(Y_save, "Y_save", dt, act), _p(A_save, "A_save", dt, act), _p(dZ, "dZ", dt, T * h),
         _p(dX, "dX", dt, T * h), _p(dW1s, "dW1s", dt, h * f), _p(dW2s, "dW2s", dt, f * h),
         wptr, wbytes, _stream(stream)), "tp_mlp_bwd")
+
+
+def tp_mlp_fwd_noalloc(dtype, T, h, f, N, X, W1s, W2s, Z, stream=None) -> int:
+    """Z of the MLP block with the activation kept in the library's fixed device
+    array (no allocation anywhere on the call's path)."""
+    dt = _TORCH_DT.get(dtype)
+    return _check(load_library().tp_mlp_fwd_noalloc(
+        dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
+        _p(Z, "Z", dt, T * h), _stream(stream)), "tp_mlp_fwd_noalloc")
 
 
 # ---------------------------------------------------------------- attention block

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/tpblock.h"
 #include "attn.cuh"
@@ -406,6 +407,98 @@ int tp_timing_read(int kind, int64_t* launches, double* total_ms) {
   if (launches) *launches = n;
   if (total_ms) *total_ms = t;
   return TP_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------- MLP forward without allocation
+// A fixed scratch array in device memory for callers that may not allocate: the
+// activation A of tp_mlp_fwd_noalloc lives here instead of in a caller's
+// workspace.  Every GPU that loads the library holds these bytes until exit.
+static __device__ __align__(256) unsigned char g_tp_noalloc_scratch[TP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDev];  // device address of the array, per device (set up on first use)
+
+// The array's name is only a host-side stand-in in host code; its device address
+// comes from the runtime, once per device, with that device current.
+int noalloc_scratch(void** out) {
+  const int d = current_device();
+  if (d < 0) return TP_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tp_noalloc_scratch) != cudaSuccess || !p) return TP_ERR_CUDA;
+    g_noalloc_ptr[d] = p;
+  }
+  *out = g_noalloc_ptr[d];
+  return TP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
+                       const void* W2s, void* Z, void* stream) {
+  const int sc = mlp_shape_check(dtype, T, h, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Z)) return TP_ERR_ALIGN;
+  if (tp_mlp_workspace_bytes(dtype, T, h, f, N) > static_cast<size_t>(TP_NOALLOC_SCRATCH_BYTES))
+    return TP_ERR_WORKSPACE;  // the activation does not fit the fixed scratch array
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  void* Abuf = nullptr;
+  const int ss = noalloc_scratch(&Abuf);
+  if (ss != TP_OK) return ss;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t fN = f / N;
+  if (dtype == TP_F32) {
+    tpb::SimtArgs a1{};
+    a1.A = static_cast<const float*>(X);
+    a1.B = static_cast<const float*>(W1s);
+    a1.C = static_cast<float*>(Abuf);
+    a1.M = static_cast<int>(T);
+    a1.N = static_cast<int>(fN);
+    a1.K = static_cast<int>(h);
+    a1.G = N;
+    a1.S = 1;
+    a1.b_sg = h * fN;
+    a1.c_sg = T * fN;
+    a1.lda = h;
+    a1.ldb = fN;
+    a1.ldc = fN;
+    a1.gelu = 1;
+    int rc = tpb::launch_gemm_f32(a1, st, tpb::kKMlpF32Fc1);
+    if (rc) return gemm_status(rc);
+    tpb::SimtArgs a2{};
+    a2.A = static_cast<const float*>(Abuf);
+    a2.B = static_cast<const float*>(W2s);
+    a2.C = static_cast<float*>(Z);
+    a2.M = static_cast<int>(T);
+    a2.N = static_cast<int>(h);
+    a2.K = static_cast<int>(fN);
+    a2.G = 1;
+    a2.S = N;
+    a2.a_ss = T * fN;
+    a2.b_ss = fN * h;
+    a2.lda = fN;
+    a2.ldb = h;
+    a2.ldc = h;
+    return gemm_status(tpb::launch_gemm_f32(a2, st, tpb::kKMlpF32Fc2));
+  }
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, nullptr, false, T, fN, N, 1, h, err, kWaitTimeoutNs,
+                                 st, tpb::kKMlpFc1);
+  if (rc) return gemm_status(rc);
+  const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opW2, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st,
+                             tpb::kKMlpFc2);
+  return gemm_status(rc);
 }
 
 }  // extern "C"
