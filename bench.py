@@ -480,6 +480,8 @@ def main() -> None:
     ap.add_argument("--impl", default="tpblock", choices=["tpblock", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--override", action="append", default=[],
+                    help="KEY=VALUE shape override of the workload (a smaller case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -487,6 +489,15 @@ def main() -> None:
     if args.workload not in WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; choose from {sorted(WORKLOADS)}")
     w = WORKLOADS[args.workload]
+    if args.override:
+        import dataclasses
+        kv = {}
+        for item in args.override:
+            k, v = item.split("=", 1)
+            kv[k] = type(getattr(w, k))(v)
+        if "B" in kv or "S" in kv:
+            kv.setdefault("T", kv.get("B", w.B) * kv.get("S", w.S))
+        w = dataclasses.replace(w, name=w.name + "+" + ",".join(args.override), **kv)
     if args.impl == "reference":
         run_reference(args, w)
     else:
