@@ -281,6 +281,7 @@ def run_gpu(args, w) -> None:
     tp.load_library()
     if tp.tp_device_check() != 0:
         raise RuntimeError("not an sm_103 GPU")
+    tp.tp_set_gemm_tiling(args.gemm_tiling)
 
     inp = inputs.workload_inputs(w)
     d = {k: v.to(dev) for k, v in inp.items()}
@@ -480,6 +481,8 @@ def main() -> None:
     ap.add_argument("--impl", default="tpblock", choices=["tpblock", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--gemm-tiling", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile")
     ap.add_argument("--override", action="append", default=[],
                     help="KEY=VALUE shape override of the workload (a smaller case for profiling)")
     args = ap.parse_args()

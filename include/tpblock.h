@@ -194,6 +194,15 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  * Used to test the timeout path (tp_sync_status must then report TP_ERR_TIMEOUT). */
 TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
 
+/* ------------------------------------------------------------ GEMM tiling */
+
+/* Tiling of every GEMM the library launches (process-wide; for tests and
+ * measurement): 0 = automatic (default: a CTA pair per 256 x 256 tile through
+ * tcgen05 cta_group::2 when there are at least #SM/2 such tiles, else one CTA
+ * per 128 x 256 tile), 1 = always one CTA per tile, 2 = always CTA pairs.
+ * Both tilings compute the same products; TP_ERR_SHAPE for another value. */
+TP_API int tp_set_gemm_tiling(int mode);
+
 /* ---------------------------------------------------------- kernel timing */
 
 /* Every kernel the library launches is counted per kind.  With timing on, a

@@ -42,6 +42,7 @@ _SIGS = {
     "tp_attn_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                      vp], i32),
     "tp_mlp_fwd_noalloc": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp], i32),
+    "tp_set_gemm_tiling": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
     "tp_timing_name": ([i32], ctypes.c_char_p),
@@ -214,6 +215,11 @@ def tp_attn_bwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, 
         _p(O_save, "O_save", dt, T * H * d), _p(LSE_save, "LSE_save", torch.float32, T * H),
         _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h), _p(dWqkv, "dWqkv", dt, h * 3 * H * d),
         _p(dWo, "dWo", dt, H * d * h), wptr, wbytes, _stream(stream)), "tp_attn_bwd")
+
+
+def tp_set_gemm_tiling(mode: int) -> int:
+    """0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile."""
+    return _check(load_library().tp_set_gemm_tiling(mode), "tp_set_gemm_tiling")
 
 
 # ---------------------------------------------------------------- kernel timing

@@ -390,6 +390,12 @@ int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
 // ------------------------------------------------------------ kernel timing
 extern "C" {
 
+int tp_set_gemm_tiling(int mode) {
+  if (mode < 0 || mode > 2) return TP_ERR_SHAPE;
+  tpb::set_gemm_tiling_mode(mode);
+  return TP_OK;
+}
+
 int tp_timing_enable(int on) {
   tpb::timing_enable(on != 0);
   return TP_OK;

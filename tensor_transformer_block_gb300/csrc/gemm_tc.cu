@@ -1,15 +1,27 @@
 // tcgen05 GEMM with TMA multi-stage pipeline and fused epilogues (see gemm_tc.cuh).
 //
-// CTA = 6 warps, one CTA per SM, persistent over output tiles of 128 x 256:
-//   warp 4  TMA producer: fills a 4-stage ring of (A 128x64, B 256x64) bf16 tiles,
+// CTA = 6 warps, one CTA per SM, persistent over output tiles:
+//   warp 8  TMA producer: fills a ring of (A 128x64, B 64-deep) bf16 stages,
 //           128-byte swizzled, K-major or MN-major as the operand is stored;
-//   warp 5  MMA issuer: 4 x tcgen05.mma (M=128, N=256, K=16) per stage into one of
-//           two TMEM accumulators (2 x 256 fp32 columns), so the epilogue of tile t
+//   warp 9  MMA issuer: 4 x tcgen05.mma (K=16) per stage into one of two TMEM
+//           accumulators (2 x 256 fp32 columns), so the epilogue of tile t
 //           overlaps the main loop of tile t+1;
-//   warps 0-3 epilogue: tcgen05.ld 32 rows each, fused GeLU / GeLU' in fp32,
-//           bf16 pack into a swizzled staging box, TMA store (coalesced 128-byte rows).
+//   warps 0-7 epilogue: warp w reads TMEM lanes 32*(w%4).. (its row quadrant) and
+//           columns 128*(w/4).. (its half), so every SM sub-partition runs two
+//           epilogue warps to hide the latency of the fused math; fused GeLU /
+//           GeLU' in fp32, bf16 pack into a swizzled staging box, TMA store.
+// Two tilings:
+//   single: one CTA per 128 x 256 tile (cta_group::1, M=128 N=256); 3 stages of 48 KB.
+//   pair:   a cluster of two CTAs per 256 x 256 tile (cta_group::2, M=256 N=256):
+//           each CTA stages its 128 rows of A and half (128 columns) of B, so each
+//           SM moves 32 KB per k-block instead of 48; 5 stages.  The even CTA issues
+//           the MMAs; both CTAs' TMA loads count on its full barrier; its commits
+//           multicast to both CTAs' empty / accumulator-ready barriers; both CTAs'
+//           epilogue warps release an accumulator on the even CTA's barrier.
 // Every wait is bounded; on a timeout the CTA latches an error, drains its own
 // copies and MMAs, frees TMEM and returns.
+#include <cstdlib>
+
 #include "gemm_tc.cuh"
 #include "host_util.cuh"
 #include "ptx.cuh"
@@ -17,33 +29,39 @@
 namespace tpb {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 4;
+constexpr int BN = 256;  // MMA N (tile columns)
+constexpr int EPI_WARPS = 8;
 constexpr int EPI_BUF = 32 * 128;  // one 32-row x 64-column bf16 box
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 
-constexpr int BAR_FULL = 0;
-constexpr int BAR_EMPTY = STAGES;
-constexpr int BAR_TFULL = 2 * STAGES;
-constexpr int BAR_TEMPTY = 2 * STAGES + 2;
-constexpr int BAR_Y = 2 * STAGES + 4;
-constexpr int BAR_DRAIN = BAR_Y + 2 * EPI_WARPS;
-constexpr int NUM_BARS = BAR_DRAIN + 1;
-
-constexpr int SMEM_EPI_OFF = STAGES * STAGE_BYTES;
-constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * 2 * EPI_BUF;
-constexpr int SMEM_MISC_OFF = SMEM_BAR_OFF + NUM_BARS * 8;
-constexpr int SMEM_USED = SMEM_MISC_OFF + 16;
-constexpr int SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+template <bool PAIR>
+struct Cfg {
+  static constexpr int BM = 128;                      // accumulator rows per CTA
+  static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per output tile
+  static constexpr int BN_CTA = PAIR ? 128 : 256;     // B columns staged per CTA
+  static constexpr int STAGES = PAIR ? 5 : 3;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN_CTA * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BAR_FULL = 0;
+  static constexpr int BAR_EMPTY = STAGES;
+  static constexpr int BAR_TFULL = 2 * STAGES;
+  static constexpr int BAR_TEMPTY = 2 * STAGES + 2;
+  static constexpr int BAR_Y = 2 * STAGES + 4;
+  static constexpr int BAR_DRAIN = BAR_Y + 2 * EPI_WARPS;
+  static constexpr int NUM_BARS = BAR_DRAIN + 1;
+  static constexpr int SMEM_EPI_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int SMEM_MISC_OFF = SMEM_BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_USED = SMEM_MISC_OFF + 16;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+  static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
 
 __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, int& mb, int& nb) {
   const int per_g = p.tiles_m * p.tiles_n;
@@ -58,34 +76,57 @@ __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, i
   nb = rr / gm;
 }
 
+// GeLU (tanh form) through the logistic identity 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)):
+// with s = 1 / (1 + e^(-2u)), GeLU(x) = x s and, since 1 - tanh^2 u = 4 s (1 - s),
+// GeLU'(x) = s (1 + 2 x (1 - s) u').  One exp2 and one reciprocal per element, and
+// no cancellation in 1 + tanh u for negative x.  The exponent is clamped so that
+// e^(-2u) stays finite (s then underflows towards 0 smoothly).
+__device__ __forceinline__ void gelu_logistic(float x, float& s, float& oms, float& du) {
+  const float x2 = x * x;
+  const float u = 0.7978845608028654f * fmaf(0.044715f * x2, x, x);
+  du = 0.7978845608028654f * fmaf(0.134145f, x2, 1.0f);
+  const float a = fminf(-2.8853900817779268f * u, 126.0f);  // -2u log2(e)
+  const float e = exp2f(a);
+  s = __frcp_rn(1.0f + e);
+  oms = e * s;  // 1 - s without cancellation
+}
+
 __device__ __forceinline__ float gelu_f(float x) {
-  const float u = 0.7978845608028654f * (x + 0.044715f * x * x * x);
-  return 0.5f * x * (1.0f + tanhf(u));
+  float s, oms, du;
+  gelu_logistic(x, s, oms, du);
+  return x * s;
 }
 
 __device__ __forceinline__ float gelu_grad_f(float x) {
-  const float x2 = x * x;
-  const float u = 0.7978845608028654f * (x + 0.044715f * x2 * x);
-  const float t = tanhf(u);
-  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * 0.7978845608028654f * (1.0f + 0.134145f * x2);
+  float s, oms, du;
+  gelu_logistic(x, s, oms, du);
+  return s * fmaf(2.0f * x * oms, du, 1.0f);
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, const GemmShape p) {
+  using C = Cfg<PAIR>;
+  constexpr int BM = C::BM, STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
+  constexpr int BAR_FULL = C::BAR_FULL, BAR_EMPTY = C::BAR_EMPTY, BAR_TFULL = C::BAR_TFULL;
+  constexpr int BAR_TEMPTY = C::BAR_TEMPTY, BAR_Y = C::BAR_Y, BAR_DRAIN = C::BAR_DRAIN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const uint32_t sbase = raw + pad;
-  const uint32_t bar0 = sbase + SMEM_BAR_OFF;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_MISC_OFF);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC_OFF + 4);
-  volatile int* never_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC_OFF + 8);
+  const uint32_t bar0 = sbase + C::SMEM_BAR_OFF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SMEM_MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC_OFF + 4);
+  volatile int* never_flag = reinterpret_cast<volatile int*>(smem + C::SMEM_MISC_OFF + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -94,7 +135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar0 + 8u * (BAR_TFULL + i), 1);
-      mbar_init(bar0 + 8u * (BAR_TEMPTY + i), EPI_WARPS);
+      mbar_init(bar0 + 8u * (BAR_TEMPTY + i), PAIR ? 2 * EPI_WARPS : EPI_WARPS);
     }
     for (int i = 0; i < 2 * EPI_WARPS; ++i) mbar_init(bar0 + 8u * (BAR_Y + i), 1);
     mbar_init(bar0 + 8u * BAR_DRAIN, 1);
@@ -102,18 +143,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     *never_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == WARP_PRODUCER && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
     if (EPI != kEpiStore) prefetch_tmap(&tmY);
   }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+  if (warp == WARP_MMA) {
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -122,15 +169,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int total = p.G * p.tiles_m * p.tiles_n;
   const int nk = p.S * p.kb_per_seg;
 
-  if (warp == 4) {
+  if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
         decode_tile(t, p, g, mb, nb);
+        const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
+        const int bcol = nb * BN + static_cast<int>(rank) * C::BN_CTA;
         for (int s = 0; s < p.S && ok; ++s) {
           const int az = g * p.a_zg + s * p.a_zs;
           const int bz = g * p.b_zg + s * p.b_zs;
@@ -139,22 +188,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ok = false;
               break;
             }
-            const uint32_t fb = bar0 + 8u * (BAR_FULL + stage);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            const uint32_t fb_local = bar0 + 8u * (BAR_FULL + stage);
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
             const int kc = kb * BK;
-            if (A_MN) {
+            if (PAIR) {
+              const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's full barrier counts both
+              if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
+              if (A_MN) {
 #pragma unroll
-              for (int j = 0; j < BM / 64; ++j) tma_load_3d(sa + j * (BK * 128), &tmA, fb, mb * BM + j * 64, kc, az);
-            } else {
-              tma_load_3d(sa, &tmA, fb, kc, mb * BM, az);
-            }
-            if (B_MN) {
+                for (int j = 0; j < BM / 64; ++j) tma_load_3d_pair(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az);
+              } else {
+                tma_load_3d_pair(sa, &tmA, fb, kc, arow, az);
+              }
+              if (B_MN) {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * (BK * 128), &tmB, fb, nb * BN + j * 64, kc, bz);
+                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                  tma_load_3d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz);
+              } else {
+                tma_load_3d_pair(sb, &tmB, fb, kc, bcol, bz);
+              }
             } else {
-              tma_load_3d(sb, &tmB, fb, kc, nb * BN, bz);
+              mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
+              if (A_MN) {
+#pragma unroll
+                for (int j = 0; j < BM / 64; ++j) tma_load_3d(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az);
+              } else {
+                tma_load_3d(sa, &tmA, fb_local, kc, arow, az);
+              }
+              if (B_MN) {
+#pragma unroll
+                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                  tma_load_3d(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz);
+              } else {
+                tma_load_3d(sb, &tmB, fb_local, kc, bcol, bz);
+              }
             }
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -165,18 +233,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      // every issued copy must land before the CTA may exit
+      // every issued copy must land before the CTA may exit: the even CTA watches
+      // its full barriers; the odd CTA the empty barriers the even CTA's MMAs
+      // release after consuming those copies
       for (int s2 = 0; s2 < STAGES; ++s2)
-        if (issued & (1u << s2)) mbar_wait(bar0 + 8u * (BAR_FULL + s2), (last_par >> s2) & 1u, wdrain);
+        if (issued & (1u << s2)) {
+          const uint32_t par = (last_par >> s2) & 1u;
+          if (!PAIR || leader)
+            mbar_wait(bar0 + 8u * (BAR_FULL + s2), par, wdrain);
+          else
+            mbar_wait(bar0 + 8u * (BAR_EMPTY + s2), par, wdrain);
+        }
     }
-  } else if (warp == 5) {
-    if (lane == 0) {
+  } else if (warp == WARP_MMA) {
+    if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t IDESC = idesc_bf16(BM, BN, A_MN, B_MN);
+      constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, BN, A_MN, B_MN);
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+      for (int t = unit; t < total && ok; t += nunits, ++it) {
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
         if (!mbar_wait(bar0 + 8u * (BAR_TEMPTY + buf), tph ^ 1u, wc)) {
@@ -197,27 +273,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
-            tc_mma_bf16(dt, ad, bd, IDESC, (k | kk) != 0 ? 1u : 0u);
+            if (PAIR)
+              tc_mma_bf16_pair(dt, ad, bd, IDESC, (k | kk) != 0 ? 1u : 0u);
+            else
+              tc_mma_bf16(dt, ad, bd, IDESC, (k | kk) != 0 ? 1u : 0u);
           }
           any = true;
-          tc_commit(bar0 + 8u * (BAR_EMPTY + stage));
+          if (PAIR)
+            tc_commit_pair(bar0 + 8u * (BAR_EMPTY + stage), 3);
+          else
+            tc_commit(bar0 + 8u * (BAR_EMPTY + stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(bar0 + 8u * (BAR_TFULL + buf));
+        if (PAIR)
+          tc_commit_pair(bar0 + 8u * (BAR_TFULL + buf), 3);
+        else
+          tc_commit(bar0 + 8u * (BAR_TFULL + buf));
       }
       if (any) {
-        tc_commit(bar0 + 8u * BAR_DRAIN);
+        if (PAIR)
+          tc_commit_pair(bar0 + 8u * BAR_DRAIN, 1);
+        else
+          tc_commit(bar0 + 8u * BAR_DRAIN);
         mbar_wait(bar0 + 8u * BAR_DRAIN, 0, wdrain);
       }
     }
   } else {
     // ------------------------------------------------------------------ epilogue
-    const int ew = warp;  // TMEM lanes 32*ew .. 32*ew+31
-    const uint32_t ebuf[2] = {sbase + SMEM_EPI_OFF + ew * 2 * EPI_BUF, sbase + SMEM_EPI_OFF + ew * 2 * EPI_BUF + EPI_BUF};
+    const int ew = warp;                 // staging buffers and Y barriers
+    const int quad = warp & 3;           // TMEM lanes 32*quad .. 32*quad+31
+    const int half = warp >> 2;          // tile columns 128*half .. 128*half+127
+    const uint32_t ebuf[2] = {sbase + C::SMEM_EPI_OFF + ew * 2 * EPI_BUF,
+                              sbase + C::SMEM_EPI_OFF + ew * 2 * EPI_BUF + EPI_BUF};
     const uint32_t ybar[2] = {bar0 + 8u * (BAR_Y + 2 * ew), bar0 + 8u * (BAR_Y + 2 * ew + 1)};
     const uint32_t rsw = static_cast<uint32_t>(lane & 7);
     uint32_t yph = 0;      // bit b: parity of the next completion of ybar[b]
@@ -225,17 +316,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t ecount = 0;   // chunks staged so far (buffer alternation for kEpiStore / kEpiDGelu)
     int it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+    for (int t = unit; t < total && ok; t += nunits, ++it) {
       int g, mb, nb;
       decode_tile(t, p, g, mb, nb);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
-      const int row0 = mb * BM + ew * 32;
-      const int col0 = nb * BN;
-      int nch = (p.N - col0 + 63) / 64;
-      if (nch > BN / 64) nch = BN / 64;
-      const bool rows_valid = row0 < p.M;
-
+      const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
+      const int col0 = nb * BN + half * (BN / 2);
+      int nch = col0 < p.N ? (p.N - col0 + 63) / 64 : 0;
+      if (nch > BN / 128) nch = BN / 128;
+      const bool rows_valid = row0 < p.M && nch > 0;
       if (EPI == kEpiDGelu && rows_valid) {
         const uint32_t b = ecount & 1u;
         if (lane == 0) {
@@ -249,18 +339,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (BAR_TFULL + buf), tph, wc));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tl = tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                          static_cast<uint32_t>(buf * BN + half * (BN / 2));
 
       if (rows_valid) {
         for (int j = 0; j < nch && ok; ++j) {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(tl + j * 64, r0);
-          tmem_ld32(tl + j * 64 + 32, r1);
-          tmem_ld_wait(r0);
-          tmem_ld_wait(r1);
           const int ccol = col0 + j * 64;
-
+          const uint32_t tcol = tl + j * 64;
+          // The fused epilogues run as a rolled loop of 16-column TMEM loads: a
+          // fully unrolled 64-column body is large enough to evict the MMA
+          // warp's instructions from the cache the SM sub-partition shares.
           if (EPI == kEpiStore) {
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tcol, r0);
+            tmem_ld32(tcol + 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
             const uint32_t sb = ebuf[ecount & 1u];
             if (lane == 0) bulk_wait_read1();
             __syncwarp();
@@ -284,19 +378,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool with_lo = ccol < p.split_cols;
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[16];
+              tmem_ld16(tcol + q * 16, v);
+              tmem_ld_wait16(v);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t* v = (c < 4) ? &r0[8 * c] : &r1[8 * (c - 4)];
-              uint32_t hi[4], lo[4];
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                uint32_t hi[4], lo[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-                hi[e] = pack_bf16x2(x0, x1);
-                lo[e] = pack_bf16x2(x0 - bf16lo_to_f32(hi[e]), x1 - bf16hi_to_f32(hi[e]));
+                for (int e = 0; e < 4; ++e) {
+                  const float x0 = __uint_as_float(v[8 * hh + 2 * e]), x1 = __uint_as_float(v[8 * hh + 2 * e + 1]);
+                  hi[e] = pack_bf16x2(x0, x1);
+                  lo[e] = pack_bf16x2(x0 - bf16lo_to_f32(hi[e]), x1 - bf16hi_to_f32(hi[e]));
+                }
+                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                st_shared_v4(ebuf[0] + off, hi[0], hi[1], hi[2], hi[3]);
+                if (with_lo) st_shared_v4(ebuf[1] + off, lo[0], lo[1], lo[2], lo[3]);
               }
-              const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
-              st_shared_v4(ebuf[0] + off, hi[0], hi[1], hi[2], hi[3]);
-              if (with_lo) st_shared_v4(ebuf[1] + off, lo[0], lo[1], lo[2], lo[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -308,19 +408,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else if (EPI == kEpiGelu) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[16];
+              tmem_ld16(tcol + q * 16, v);
+              tmem_ld_wait16(v);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t* v = (c < 4) ? &r0[8 * c] : &r1[8 * (c - 4)];
-              float x[8];
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                float x[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[e]);
-              const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
-              st_shared_v4(ebuf[0] + off, pack_bf16x2(gelu_f(x[0]), gelu_f(x[1])),
-                           pack_bf16x2(gelu_f(x[2]), gelu_f(x[3])), pack_bf16x2(gelu_f(x[4]), gelu_f(x[5])),
-                           pack_bf16x2(gelu_f(x[6]), gelu_f(x[7])));
-              if (p.store_y)
-                st_shared_v4(ebuf[1] + off, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+                for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * hh + e]);
+                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                st_shared_v4(ebuf[0] + off, pack_bf16x2(gelu_f(x[0]), gelu_f(x[1])),
+                             pack_bf16x2(gelu_f(x[2]), gelu_f(x[3])), pack_bf16x2(gelu_f(x[4]), gelu_f(x[5])),
+                             pack_bf16x2(gelu_f(x[6]), gelu_f(x[7])));
+                if (p.store_y)
+                  st_shared_v4(ebuf[1] + off, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                               pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+              }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -343,21 +449,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
             yph ^= 1u << cb;
             ypend &= ~(1u << cb);
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[16];
+              tmem_ld16(tcol + q * 16, v);
+              tmem_ld_wait16(v);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t* v = (c < 4) ? &r0[8 * c] : &r1[8 * (c - 4)];
-              const uint32_t addr = ebuf[cb] + lane * 128 + ((c ^ rsw) << 4);
-              uint32_t y0, y1, y2, y3;
-              ld_shared_v4(addr, y0, y1, y2, y3);
-              const uint32_t yy[4] = {y0, y1, y2, y3};
-              uint32_t o[4];
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                const uint32_t addr = ebuf[cb] + lane * 128 + ((c ^ rsw) << 4);
+                uint32_t y0, y1, y2, y3;
+                ld_shared_v4(addr, y0, y1, y2, y3);
+                const uint32_t yy[4] = {y0, y1, y2, y3};
+                uint32_t o[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = __uint_as_float(v[2 * e]) * gelu_grad_f(bf16lo_to_f32(yy[e]));
-                const float hi = __uint_as_float(v[2 * e + 1]) * gelu_grad_f(bf16hi_to_f32(yy[e]));
-                o[e] = pack_bf16x2(lo, hi);
+                for (int e = 0; e < 4; ++e) {
+                  const float lo = __uint_as_float(v[8 * hh + 2 * e]) * gelu_grad_f(bf16lo_to_f32(yy[e]));
+                  const float hi = __uint_as_float(v[8 * hh + 2 * e + 1]) * gelu_grad_f(bf16hi_to_f32(yy[e]));
+                  o[e] = pack_bf16x2(lo, hi);
+                }
+                st_shared_v4(addr, o[0], o[1], o[2], o[3]);
               }
-              st_shared_v4(addr, o[0], o[1], o[2], o[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -371,7 +483,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar0 + 8u * (BAR_TEMPTY + buf));
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(mapa_shared(bar0 + 8u * (BAR_TEMPTY + buf), 0));
+        else
+          mbar_arrive(bar0 + 8u * (BAR_TEMPTY + buf));
+      }
     }
     // drain: Y loads still in flight (only after an abort), then the stores
     if (EPI == kEpiDGelu) {
@@ -385,44 +502,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (PAIR) cluster_sync();  // neither CTA leaves while the pair's MMAs or signals may touch it
+  if (warp == WARP_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, GemmShape);
 
-template <bool A_MN, bool B_MN, int EPI>
+constexpr int kMaxDev = 64;
+
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 KernelFn get_kernel() {
-  static bool configured = false;
-  auto fn = &k_gemm<A_MN, B_MN, EPI>;
-  if (!configured) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC) != cudaSuccess)
+  static bool configured[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI>;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR>::SMEM_ALLOC) != cudaSuccess)
       return nullptr;
-    configured = true;
+    configured[dev] = true;
   }
-  return reinterpret_cast<KernelFn>(fn);
+  return fn;
 }
 
+template <bool PAIR>
 KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
-  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<false, true, kEpiGelu>();
-  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<false, true, kEpiStore>();
-  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<false, true, kEpiSplit>();
-  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<false, false, kEpiDGelu>();
-  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<false, false, kEpiStore>();
-  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<true, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<PAIR, false, true, kEpiGelu>();
+  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, false, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<PAIR, false, true, kEpiSplit>();
+  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu>();
+  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore>();
+  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore>();
   return nullptr;
 }
 
-bool operand_map(CUtensorMap* m, const GemmOperand& o, bool is_a) {
+bool operand_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
   const uint64_t dims[3] = {static_cast<uint64_t>(o.d0), static_cast<uint64_t>(o.d1), static_cast<uint64_t>(o.d2)};
-  const uint32_t rows = is_a ? BM : BN;
   const uint32_t box[3] = {64u, o.mn_major ? static_cast<uint32_t>(BK) : rows, 1u};
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o.ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pair per tile
+
 }  // namespace
+
+void set_gemm_tiling_mode(int mode) { g_tiling_mode = mode; }
 
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
                      bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,
@@ -434,10 +563,17 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (ldc != N && (N % 64)) return 1;  // a partial last chunk would not be clipped at N
   if (epi == kEpiSplit && ((extra.split_cols % 64) || extra.lo_off < N || extra.lo_off + extra.split_cols > ldc))
     return 1;
-  KernelFn fn = pick_kernel(A.mn_major, B.mn_major, epi);
+  const int sms = device_sm_count();
+  if (sms <= 0) return 2;
+  // pair tiles when there are enough 256 x 256 tiles to give every SM pair work
+  const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + BN - 1) / BN);
+  bool pair = g_tiling_mode == 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
+  if (sms < 2) pair = false;
+  KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
   if (!fn) return 2;
+  const uint32_t a_rows = 128, b_rows = pair ? Cfg<true>::BN_CTA : Cfg<false>::BN_CTA;
   CUtensorMap ta, tb, tc, ty;
-  if (!operand_map(&ta, A, true) || !operand_map(&tb, B, false)) return 2;
+  if (!operand_map(&ta, A, a_rows) || !operand_map(&tb, B, b_rows)) return 2;
   const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
   const uint32_t cbox[3] = {64u, 32u, 1u};
   if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
@@ -453,7 +589,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.G = G;
   p.S = S;
   p.kb_per_seg = static_cast<int>((Ks + BK - 1) / BK);
-  p.tiles_m = static_cast<int>((M + BM - 1) / BM);
+  p.tiles_m = static_cast<int>((M + (pair ? 255 : 127)) / (pair ? 256 : 128));
   p.tiles_n = static_cast<int>((N + BN - 1) / BN);
   p.a_zg = A.zg;
   p.a_zs = A.zs;
@@ -465,12 +601,28 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.err = err;
   p.timeout_ns = timeout_ns;
   const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;
-  const int sms = device_sm_count();
-  if (sms <= 0) return 2;
-  const int grid = static_cast<int>(total < sms ? total : sms);
   const int slot = timing_begin(kind, stream);
-  fn<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ta, tb, tc, ty, p);
-  const bool ok = cudaGetLastError() == cudaSuccess;
+  bool ok;
+  if (pair) {
+    const long long units = total < sms / 2 ? total : sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<true>::SMEM_ALLOC;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ok = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, ty, p) == cudaSuccess;
+  } else {
+    const int grid = static_cast<int>(total < sms ? total : sms);
+    fn<<<grid, NUM_THREADS, Cfg<false>::SMEM_ALLOC, stream>>>(ta, tb, tc, ty, p);
+    ok = cudaGetLastError() == cudaSuccess;
+  }
   timing_end(slot, stream);
   return ok ? 0 : 2;
 }

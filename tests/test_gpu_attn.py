@@ -160,3 +160,14 @@ def test_layer_full_config_sampled():
                        fro_tol=tol2)
     for k in ("dX", "dWqkv", "dWo"):
         assert torch.isfinite(ga[k].float()).all(), k
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_attention_block_each_tiling(mode):
+    """The attention projections (split-residual epilogue, shard-sum output GEMM,
+    backward GEMMs) under both GEMM tilings."""
+    tp.tp_set_gemm_tiling(mode)
+    try:
+        _check(2, 256, 512, 8, 64, 4, True, backward=True, seed=mode)
+    finally:
+        tp.tp_set_gemm_tiling(0)

@@ -131,3 +131,16 @@ def test_mlp_bf16_h4096_sampled():
     got2 = np.stack([dW2[c // fN, c % fN, :] for c in cols], axis=0)
     assert_bf16_parity(got1, gc["dW1_cols"], "dW1 cols")
     assert_bf16_parity(got2, gc["dW2_rows"], "dW2 rows")
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("T,h,f,N", [(333, 200, 264, 3), (2048, 1024, 4096, 4), (600, 520, 1040, 5), (1, 64, 64, 8)])
+def test_mlp_bf16_each_tiling(mode, T, h, f, N):
+    """Both GEMM tilings (one CTA per 128x256 tile; a CTA pair per 256x256 tile,
+    cta_group::2) against the oracle, including tails in M, N and K."""
+    import tensor_transformer_block_gb300 as tp
+    tp.tp_set_gemm_tiling(mode)
+    try:
+        _check_mlp(T, h, f, N, seed=T + mode)
+    finally:
+        tp.tp_set_gemm_tiling(0)
