@@ -141,16 +141,19 @@ def test_layer_full_config_sampled():
     assert_attn_parity(_np(a["Z"])[rows], Hs[rows], "attention output rows")
     cols = np.sort(np.concatenate([[0, f - 1], rng.choice(f, 30, replace=False)]))
     gc = O.mlp_backward_weight_columns(Hs, r["W1s"], r["W2s"], r["dZ"], cols)
-    # The MLP consumes the attention output H in bf16 (the block boundary).  At this
-    # size H's RMS is ~10 and the pre-activations' ~18, so GeLU'' turns H's
-    # rounding alone into a weight-gradient error near 5e-3: the oracle measures
-    # that floor here (its own H rounded to bf16, everything else exact) and the
-    # gradients are held to max(5e-3, 2 x floor).
+    # The MLP consumes the attention output H, which the attention block delivers
+    # in bf16 and within its own 5e-3 relative tolerance.  At this size H's RMS is
+    # ~10 and the pre-activations' ~18, so GeLU'' amplifies any error in H into the
+    # weight gradients.  The oracle measures that amplification on the same inputs:
+    # the gradient error caused by rounding its own H to bf16 (everything else
+    # exact), scaled linearly from that rounding's size to the 5e-3 the attention
+    # output is allowed.  The gradients are held to max(5e-3, that bound).
     Hb = torch.from_numpy(Hs).to(torch.bfloat16).to(torch.float64).numpy()
     gb = O.mlp_backward_weight_columns(Hb, r["W1s"], r["W2s"], r["dZ"], cols)
     rel = lambda x, y: float(np.linalg.norm(x - y) / np.linalg.norm(y))
-    tol1 = max(5e-3, 2 * rel(gb["dW1_cols"], gc["dW1_cols"]))
-    tol2 = max(5e-3, 2 * rel(gb["dW2_rows"], gc["dW2_rows"]))
+    per_unit = 5e-3 / rel(Hb, Hs)
+    tol1 = max(5e-3, per_unit * rel(gb["dW1_cols"], gc["dW1_cols"]))
+    tol2 = max(5e-3, per_unit * rel(gb["dW2_rows"], gc["dW2_rows"]))
     fN = f // N
     dW1 = _np(gm["dW1s"])
     dW2 = _np(gm["dW2s"])
