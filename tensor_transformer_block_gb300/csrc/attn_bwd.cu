@@ -54,13 +54,6 @@ struct BwdCommon {
   __device__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
 };
 
-// Row r of a [128 x 128] bf16 tile in the K-major 128-byte-swizzle layout
-// (two 64-column chunks of 16 KB): 16-byte group g (8 columns) of chunk kc.
-__device__ __forceinline__ uint32_t tile128_addr(uint32_t base, int r, int col8) {
-  const uint32_t kc = static_cast<uint32_t>(col8 >> 3), g = static_cast<uint32_t>(col8 & 7);
-  return base + kc * 16384u + static_cast<uint32_t>(r) * 128u + ((g ^ static_cast<uint32_t>(r & 7)) << 4);
-}
-
 // Writes a warp's 32 accumulator rows x D columns (fp32 in TMEM, times ``mul``)
 // as bf16 into a staging area laid out as D/64 boxes of 32 x 64 (swizzled).
 template <int D>
@@ -96,9 +89,15 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint32_t sa, uint32_
 }
 
 // ------------------------------------------------------------------ dK / dV
-// One CTA per (128-key block, head, batch); loops over 64-query blocks.
+// One CTA per (128-key block, head, batch); loops over 64-query blocks whose
+// Qh, Ql, dO tiles and LSE / Dsum rows are double-buffered, as are the S^T and
+// dP^T tiles in TMEM, so block i+1's products run while the key-row threads turn
+// block i's scores into P^T and dS^T.
 constexpr int QB = 64;
-enum : int { K_KVF = 0, K_QF = 1, K_QE = 2, K_STF = 3, K_PSF = 4, K_PSE = 5, K_ACC = 6, K_DR = 7, K_NB = 8 };
+enum : int {
+  K_KVF = 0, K_QF = 1 /* 2 */, K_QE = 3 /* 2 */, K_STF = 5 /* 2 */, K_STE = 7 /* 2 */,
+  K_PSF = 9, K_PSE = 10, K_ACC = 11, K_DR = 12, K_NB = 13
+};
 
 template <int D>
 struct DkdvCfg {
@@ -106,15 +105,16 @@ struct DkdvCfg {
   static constexpr int KTILE = CH * 16384;  // 128 key rows x D
   static constexpr int QTILE = CH * 8192;   // 64 query rows x D
   static constexpr int OFF_KH = 0, OFF_KL = KTILE, OFF_V = 2 * KTILE;
-  static constexpr int OFF_QH = 3 * KTILE, OFF_QL = 3 * KTILE + QTILE, OFF_DO = 3 * KTILE + 2 * QTILE;
-  static constexpr int OFF_P = 3 * KTILE + 3 * QTILE;  // [128 keys][64 queries] bf16, 16 KB
+  static constexpr int OFF_Q = 3 * KTILE;   // [stage][Qh, Ql, dO]
+  static constexpr int OFF_P = OFF_Q + 6 * QTILE;  // [128 keys][64 queries] bf16, 16 KB
   static constexpr int OFF_DS = OFF_P + 16384;
-  static constexpr int OFF_LSE = OFF_DS + 16384;        // [64] fp32
-  static constexpr int OFF_DD = OFF_LSE + 512;          // [64] fp32
+  static constexpr int OFF_LSE = OFF_DS + 16384;   // [2][64] fp32
+  static constexpr int OFF_DD = OFF_LSE + 512;     // [2][64] fp32
   static constexpr int OFF_BAR = OFF_DD + 512;
   static constexpr int OFF_MISC = OFF_BAR + K_NB * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
+  static_assert(USED + 1024 <= 232448, "shared memory budget");
 };
 
 template <int D>
@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const BwdCommon cm{raw + pad, raw + pad + C::OFF_BAR};
   const uint32_t sKh = cm.sb + C::OFF_KH, sKl = cm.sb + C::OFF_KL, sV = cm.sb + C::OFF_V;
-  const uint32_t sQh = cm.sb + C::OFF_QH, sQl = cm.sb + C::OFF_QL, sDO = cm.sb + C::OFF_DO;
+  auto sQh = [&](int st) { return cm.sb + C::OFF_Q + static_cast<uint32_t>((3 * st + 0) * C::QTILE); };
+  auto sQl = [&](int st) { return cm.sb + C::OFF_Q + static_cast<uint32_t>((3 * st + 1) * C::QTILE); };
+  auto sDO = [&](int st) { return cm.sb + C::OFF_Q + static_cast<uint32_t>((3 * st + 2) * C::QTILE); };
   const uint32_t sP = cm.sb + C::OFF_P, sDS = cm.sb + C::OFF_DS;
   float* lse_s = reinterpret_cast<float*>(smem + C::OFF_LSE);
   float* dd_s = reinterpret_cast<float*>(smem + C::OFF_DD);
@@ -150,7 +152,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int cQl = (3 * a.hN + jj) * D, cKl = (4 * a.hN + jj) * D;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < K_NB; ++i) mbar_init(cm.bar(i), i == K_PSF ? 4 : 1);
+    for (int i = 0; i < K_NB; ++i) {
+      const bool by_warps = i == K_PSF || i == K_STE || i == K_STE + 1;
+      mbar_init(cm.bar(i), by_warps ? 4 : 1);
+    }
     *abort_flag = 0;
     *never_flag = 0;
     fence_mbar_init();
@@ -165,12 +170,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
-  // TMEM: S^T [0,64), dP^T [64,128), dV [128,128+D), dK [128+D,128+2D)
-  const uint32_t tST = tmem, tDPT = tmem + 64, tDV = tmem + 128, tDK = tmem + 128 + D;
-
+  // TMEM: S^T [s*64, +64), dP^T [128 + s*64, +64), dV [256, +D), dK [256+D, +D)
+  const uint32_t tDV = tmem + 256, tDK = tmem + 256 + D;
   const size_t row_base = (static_cast<size_t>(b) * a.H + j) * a.S;
+
   if (warp == 4) {
-    // producer warp: lane 0 issues the TMA copies; all lanes stage the block's
+    // producer warp: lane 0 issues the TMA copies; all lanes stage each block's
     // LSE and Dsum rows (plain loads: any S), published by the same barrier
     if (lane == 0) {
       mbar_arrive_expect_tx(cm.bar(K_KVF), 3 * C::KTILE);
@@ -183,47 +188,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     int issued = 0;
     for (int it = 0; it < nq; ++it) {
+      const int st = it & 1;
+      const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
       const int q0 = (q_start + it) * QB;
-      if (!__all_sync(0xffffffffu, mbar_wait(cm.bar(K_QE), (it & 1) ^ 1, wc))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(cm.bar(K_QE + st), ph ^ 1u, wc))) break;
       for (int t = lane; t < QB; t += 32) {
         const int q = q0 + t;
-        lse_s[t] = q < a.S ? lse[row_base + q] : 0.0f;
-        dd_s[t] = q < a.S ? dsum[row_base + q] : 0.0f;
+        lse_s[st * QB + t] = q < a.S ? lse[row_base + q] : 0.0f;
+        dd_s[st * QB + t] = q < a.S ? dsum[row_base + q] : 0.0f;
       }
       __threadfence_block();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(cm.bar(K_QF), 3 * C::QTILE);
+        const uint32_t fb = cm.bar(K_QF + st);
+        mbar_arrive_expect_tx(fb, 3 * C::QTILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_4d(sQh + c * 8192, &tmQKV64, cm.bar(K_QF), cQh + 64 * c, q0, b, shard);
-          tma_load_4d(sQl + c * 8192, &tmQKV64, cm.bar(K_QF), cQl + 64 * c, q0, b, shard);
-          tma_load_4d(sDO + c * 8192, &tmDO64, cm.bar(K_QF), jj * D + 64 * c, q0, b, shard);
+          tma_load_4d(sQh(st) + c * 8192, &tmQKV64, fb, cQh + 64 * c, q0, b, shard);
+          tma_load_4d(sQl(st) + c * 8192, &tmQKV64, fb, cQl + 64 * c, q0, b, shard);
+          tma_load_4d(sDO(st) + c * 8192, &tmDO64, fb, jj * D + 64 * c, q0, b, shard);
         }
       }
       issued = it + 1;
     }
     if (lane == 0) {
       mbar_wait(cm.bar(K_KVF), 0, wdrain);
-      if (issued > 0) mbar_wait(cm.bar(K_QF), (issued - 1) & 1, wdrain);
+      for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
+        mbar_wait(cm.bar(K_QF + (it & 1)), (it >> 1) & 1, wdrain);
     }
   } else if (warp == 5) {
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_bf16(128, QB, false, false);
       constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(cm.bar(K_KVF), 0, wc), any = false;
+      auto issue_sd = [&](int it) -> bool {
+        const int st = it & 1;
+        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(cm.bar(K_QF + st), ph, wc) || !mbar_wait(cm.bar(K_STE + st), ph ^ 1u, wc)) return false;
+        tc_fence_after();
+        const uint32_t tS = tmem + static_cast<uint32_t>(st * 64), tP = tmem + 128 + static_cast<uint32_t>(st * 64);
+        mma_kmajor<D>(tS, sKh, sQh(st), 8192, ID_S, false);
+        mma_kmajor<D>(tS, sKl, sQh(st), 8192, ID_S, true);
+        mma_kmajor<D>(tS, sKh, sQl(st), 8192, ID_S, true);
+        mma_kmajor<D>(tP, sV, sDO(st), 8192, ID_S, false);
+        any = true;
+        tc_commit(cm.bar(K_STF + st));
+        return true;
+      };
+      if (ok && nq > 0) ok = issue_sd(0);
       for (int it = 0; it < nq && ok; ++it) {
-        if (!mbar_wait(cm.bar(K_QF), it & 1, wc)) {
+        const int st = it & 1;
+        if (it + 1 < nq && !issue_sd(it + 1)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        mma_kmajor<D>(tST, sKh, sQh, 8192, ID_S, false);
-        mma_kmajor<D>(tST, sKl, sQh, 8192, ID_S, true);
-        mma_kmajor<D>(tST, sKh, sQl, 8192, ID_S, true);
-        mma_kmajor<D>(tDPT, sV, sDO, 8192, ID_S, false);
-        any = true;
-        tc_commit(cm.bar(K_STF));
         if (!mbar_wait(cm.bar(K_PSF), it & 1, wc)) {
           ok = false;
           break;
@@ -233,10 +251,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < QB / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           // A: P^T / dS^T [128 keys][64 queries] K-major; B: dO / Qh tiles read MN-major (N = d)
-          tc_mma_bf16(tDV, sdesc_sw128(sP + kk * 32, 16, 1024), sdesc_sw128(sDO + kk * 2048, 8192, 1024), ID_G, acc);
-          tc_mma_bf16(tDK, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(sQh + kk * 2048, 8192, 1024), ID_G, acc);
+          tc_mma_bf16(tDV, sdesc_sw128(sP + kk * 32, 16, 1024), sdesc_sw128(sDO(st) + kk * 2048, 8192, 1024), ID_G,
+                      acc);
+          tc_mma_bf16(tDK, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(sQh(st) + kk * 2048, 8192, 1024), ID_G,
+                      acc);
         }
-        tc_commit(cm.bar(K_QE));
+        tc_commit(cm.bar(K_QE + st));
         tc_commit(cm.bar(K_PSE));
       }
       if (ok) tc_commit(cm.bar(K_ACC));
@@ -252,44 +272,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t rsw = static_cast<uint32_t>(r & 7);
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
-      const int qb = q_start + it;
-      const int q0 = qb * QB;
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_QF), it & 1, wc) && mbar_wait(cm.bar(K_STF), it & 1, wc) &&
-                                       mbar_wait(cm.bar(K_PSE), (it & 1) ^ 1, wc));
+      const int st = it & 1;
+      const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+      const int q0 = (q_start + it) * QB;
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_STF + st), ph, wc) && mbar_wait(cm.bar(K_QF + st), ph, wc));
       if (!ok) break;
       tc_fence_after();
-      const bool need_mask = (a.causal && q0 < k0 + BLK) || (q0 + QB > a.S) || (k0 + BLK > a.S);
-#pragma unroll
-      for (int c = 0; c < QB / 32; ++c) {
-        uint32_t vs[32], vp[32];
-        tmem_ld32(tST + trow + 32 * c, vs);
-        tmem_ld32(tDPT + trow + 32 * c, vp);
-        tmem_ld_wait(vs);
-        tmem_ld_wait(vp);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p2[2], d2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qc = 32 * c + e + u;
-            const int q = q0 + qc;
-            float p = exp2f(__uint_as_float(vs[e + u]) * scale_log2 - lse_s[qc] * kLog2e);
-            if (need_mask && (q >= a.S || key >= a.S || (a.causal && key > q))) p = 0.0f;
-            p2[u] = p;
-            d2[u] = p * (__uint_as_float(vp[e + u]) - dd_s[qc]);
-          }
-          pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
-          dk[e >> 1] = pack_bf16x2(d2[0], d2[1]);
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const uint32_t ad = static_cast<uint32_t>(r) * 128u + (((static_cast<uint32_t>(4 * c + g)) ^ rsw) << 4);
-          st_shared_v4(sP + ad, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-          st_shared_v4(sDS + ad, dk[4 * g], dk[4 * g + 1], dk[4 * g + 2], dk[4 * g + 3]);
-        }
-      }
+      uint32_t vs0[32], vs1[32], vp0[32], vp1[32];
+      tmem_ld32(tmem + trow + st * 64, vs0);
+      tmem_ld32(tmem + trow + st * 64 + 32, vs1);
+      tmem_ld32(tmem + trow + 128 + st * 64, vp0);
+      tmem_ld32(tmem + trow + 128 + st * 64 + 32, vp1);
+      tmem_ld_wait(vs0);
+      tmem_ld_wait(vs1);
+      tmem_ld_wait(vp0);
+      tmem_ld_wait(vp1);
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cm.bar(K_STE + st));  // the S^T / dP^T buffers may be refilled
+      const bool need_mask = (a.causal && q0 < k0 + BLK) || (q0 + QB > a.S) || (k0 + BLK > a.S);
+      const float* ls = lse_s + st * QB;
+      const float* ds = dd_s + st * QB;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        float p2[2], d2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int qc = e + u;
+          const int q = q0 + qc;
+          const float sv = __uint_as_float(qc < 32 ? vs0[qc] : vs1[qc - 32]);
+          const float dpv = __uint_as_float(qc < 32 ? vp0[qc] : vp1[qc - 32]);
+          float p = exp2f(sv * scale_log2 - ls[qc] * kLog2e);
+          if (need_mask && (q >= a.S || key >= a.S || (a.causal && key > q))) p = 0.0f;
+          p2[u] = p;
+          d2[u] = p * (dpv - ds[qc]);
+        }
+        pk[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+        dk[e >> 1] = pack_bf16x2(d2[0], d2[1]);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_PSE), (it & 1) ^ 1, wc));
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t ad = static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(g) ^ rsw) << 4);
+        st_shared_v4(sP + ad, pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+        st_shared_v4(sDS + ad, dk[4 * g], dk[4 * g + 1], dk[4 * g + 2], dk[4 * g + 3]);
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(cm.bar(K_PSF));
@@ -297,9 +326,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_ACC), 0, wc));
     if (ok) {
       tc_fence_after();
-      // all MMAs are complete: the Q/dO tiles are free for staging (2 x 4 warps x CH x 4 KB)
-      const uint32_t stV = sQh + static_cast<uint32_t>(warp * C::CH * 4096);
-      const uint32_t stK = sQh + static_cast<uint32_t>((4 + warp) * C::CH * 4096);
+      // all MMAs are complete: the Q/dO stages are free for staging (2 x 4 warps x CH x 4 KB)
+      const uint32_t stV = cm.sb + C::OFF_Q + static_cast<uint32_t>(warp * C::CH * 4096);
+      const uint32_t stK = cm.sb + C::OFF_Q + static_cast<uint32_t>((4 + warp) * C::CH * 4096);
       stage_rows_from_tmem<D>(tDV + trow, stV, lane, 1.0f);
       stage_rows_from_tmem<D>(tDK + trow, stK, lane, scale);
       fence_proxy_async_smem();
@@ -327,27 +356,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------------- dQ
-// One CTA per (128-query block, head, batch); loops over 128-key blocks.
-enum : int { Q_QF = 0, Q_KVF = 1, Q_KVE = 2, Q_SF = 3, Q_DSF = 4, Q_DSE = 5, Q_ACC = 6, Q_DR = 7, Q_NB = 8 };
+// One CTA per (128-query block, head, batch); loops over 64-key blocks whose
+// Kh, Kl, V tiles are double-buffered, as are the S and dP tiles in TMEM.
+constexpr int KBQ = 64;
+enum : int {
+  Q_QF = 0, Q_KF = 1 /* 2 */, Q_KE = 3 /* 2 */, Q_SF = 5 /* 2 */, Q_SE = 7 /* 2 */,
+  Q_DSF = 9, Q_DSE = 10, Q_ACC = 11, Q_DR = 12, Q_NB = 13
+};
 
 template <int D>
 struct DqCfg {
   static constexpr int CH = D / 64;
-  static constexpr int TILE = CH * 16384;
-  static constexpr int OFF_QH = 0, OFF_QL = TILE, OFF_DO = 2 * TILE, OFF_KH = 3 * TILE, OFF_KL = 4 * TILE;
-  static constexpr int OFF_V = 5 * TILE, OFF_DS = 6 * TILE;
-  static constexpr int OFF_BAR = OFF_DS + 32768;
+  static constexpr int QTILE = CH * 16384;  // 128 query rows x D
+  static constexpr int KTILE = CH * 8192;   // 64 key rows x D
+  static constexpr int OFF_QH = 0, OFF_QL = QTILE, OFF_DO = 2 * QTILE;
+  static constexpr int OFF_K = 3 * QTILE;   // [stage][Kh, Kl, V]
+  static constexpr int OFF_DS = OFF_K + 6 * KTILE;  // [128 queries][64 keys] bf16, 16 KB
+  static constexpr int OFF_BAR = OFF_DS + 16384;
   static constexpr int OFF_MISC = OFF_BAR + Q_NB * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
+  static_assert(USED + 1024 <= 232448, "shared memory budget");
 };
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    k_attn_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
-              const float* __restrict__ dsum, const AttnDims a, const float scale_log2, const float scale,
-              unsigned* err, const unsigned long long timeout_ns) {
+    k_attn_dq(const __grid_constant__ CUtensorMap tmQKV128, const __grid_constant__ CUtensorMap tmQKV64,
+              const __grid_constant__ CUtensorMap tmDO128, const __grid_constant__ CUtensorMap tmDQKV,
+              const float* __restrict__ lse, const float* __restrict__ dsum, const AttnDims a, const float scale_log2,
+              const float scale, unsigned* err, const unsigned long long timeout_ns) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -355,7 +392,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const BwdCommon cm{raw + pad, raw + pad + C::OFF_BAR};
   const uint32_t sQh = cm.sb + C::OFF_QH, sQl = cm.sb + C::OFF_QL, sDO = cm.sb + C::OFF_DO;
-  const uint32_t sKh = cm.sb + C::OFF_KH, sKl = cm.sb + C::OFF_KL, sV = cm.sb + C::OFF_V;
+  auto sKh = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>((3 * st + 0) * C::KTILE); };
+  auto sKl = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>((3 * st + 1) * C::KTILE); };
+  auto sV = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>((3 * st + 2) * C::KTILE); };
   const uint32_t sDS = cm.sb + C::OFF_DS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -367,12 +406,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int j = blockIdx.y, b = blockIdx.z;
   const int shard = j / a.hN, jj = j % a.hN;
   const int q0 = qb * BLK;
-  const int nkv = a.causal ? qb + 1 : nb;
+  const int nkb = (a.S + KBQ - 1) / KBQ;
+  const int nkv = a.causal ? min((min(q0 + BLK, a.S) - 1) / KBQ + 1, nkb) : nkb;
   const int cQh = jj * D, cKh = (a.hN + jj) * D, cV = (2 * a.hN + jj) * D;
   const int cQl = (3 * a.hN + jj) * D, cKl = (4 * a.hN + jj) * D;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q_NB; ++i) mbar_init(cm.bar(i), i == Q_DSF ? 4 : 1);
+    for (int i = 0; i < Q_NB; ++i) {
+      const bool by_warps = i == Q_DSF || i == Q_SE || i == Q_SE + 1;
+      mbar_init(cm.bar(i), by_warps ? 4 : 1);
+    }
     *abort_flag = 0;
     *never_flag = 0;
     fence_mbar_init();
@@ -387,60 +430,72 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
+  // TMEM: S [s*64, +64), dP [128 + s*64, +64), dQ [256, +D)
 
   if (warp == 4) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(cm.bar(Q_QF), 3 * C::TILE);
+      mbar_arrive_expect_tx(cm.bar(Q_QF), 3 * C::QTILE);
 #pragma unroll
       for (int c = 0; c < C::CH; ++c) {
-        tma_load_4d(sQh + c * 16384, &tmQKV, cm.bar(Q_QF), cQh + 64 * c, q0, b, shard);
-        tma_load_4d(sQl + c * 16384, &tmQKV, cm.bar(Q_QF), cQl + 64 * c, q0, b, shard);
-        tma_load_4d(sDO + c * 16384, &tmDO, cm.bar(Q_QF), jj * D + 64 * c, q0, b, shard);
+        tma_load_4d(sQh + c * 16384, &tmQKV128, cm.bar(Q_QF), cQh + 64 * c, q0, b, shard);
+        tma_load_4d(sQl + c * 16384, &tmQKV128, cm.bar(Q_QF), cQl + 64 * c, q0, b, shard);
+        tma_load_4d(sDO + c * 16384, &tmDO128, cm.bar(Q_QF), jj * D + 64 * c, q0, b, shard);
       }
       int issued = 0;
       for (int it = 0; it < nkv; ++it) {
-        if (!mbar_wait(cm.bar(Q_KVE), (it & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(cm.bar(Q_KVF), 3 * C::TILE);
+        const int st = it & 1;
+        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(cm.bar(Q_KE + st), ph ^ 1u, wc)) break;
+        const uint32_t fb = cm.bar(Q_KF + st);
+        mbar_arrive_expect_tx(fb, 3 * C::KTILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_4d(sKh + c * 16384, &tmQKV, cm.bar(Q_KVF), cKh + 64 * c, it * BLK, b, shard);
-          tma_load_4d(sKl + c * 16384, &tmQKV, cm.bar(Q_KVF), cKl + 64 * c, it * BLK, b, shard);
-          tma_load_4d(sV + c * 16384, &tmQKV, cm.bar(Q_KVF), cV + 64 * c, it * BLK, b, shard);
+          tma_load_4d(sKh(st) + c * 8192, &tmQKV64, fb, cKh + 64 * c, it * KBQ, b, shard);
+          tma_load_4d(sKl(st) + c * 8192, &tmQKV64, fb, cKl + 64 * c, it * KBQ, b, shard);
+          tma_load_4d(sV(st) + c * 8192, &tmQKV64, fb, cV + 64 * c, it * KBQ, b, shard);
         }
         issued = it + 1;
       }
       mbar_wait(cm.bar(Q_QF), 0, wdrain);
-      if (issued > 0) mbar_wait(cm.bar(Q_KVF), (issued - 1) & 1, wdrain);
+      for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
+        mbar_wait(cm.bar(Q_KF + (it & 1)), (it >> 1) & 1, wdrain);
     }
   } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t ID_S = idesc_bf16(128, KBQ, false, false);
       constexpr uint32_t ID_G = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(cm.bar(Q_QF), 0, wc), any = false;
+      auto issue_sp = [&](int it) -> bool {
+        const int st = it & 1;
+        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+        if (!mbar_wait(cm.bar(Q_KF + st), ph, wc) || !mbar_wait(cm.bar(Q_SE + st), ph ^ 1u, wc)) return false;
+        tc_fence_after();
+        const uint32_t tS = tmem + static_cast<uint32_t>(st * 64), tP = tmem + 128 + static_cast<uint32_t>(st * 64);
+        mma_kmajor<D>(tS, sQh, sKh(st), 8192, ID_S, false);
+        mma_kmajor<D>(tS, sQh, sKl(st), 8192, ID_S, true);
+        mma_kmajor<D>(tS, sQl, sKh(st), 8192, ID_S, true);
+        mma_kmajor<D>(tP, sDO, sV(st), 8192, ID_S, false);
+        any = true;
+        tc_commit(cm.bar(Q_SF + st));
+        return true;
+      };
+      if (ok && nkv > 0) ok = issue_sp(0);
       for (int it = 0; it < nkv && ok; ++it) {
-        if (!mbar_wait(cm.bar(Q_KVF), it & 1, wc)) {
+        const int st = it & 1;
+        if (it + 1 < nkv && !issue_sp(it + 1)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        mma_kmajor<D>(tmem, sQh, sKh, 16384, ID_S, false);
-        mma_kmajor<D>(tmem, sQh, sKl, 16384, ID_S, true);
-        mma_kmajor<D>(tmem, sQl, sKh, 16384, ID_S, true);
-        mma_kmajor<D>(tmem + 128, sDO, sV, 16384, ID_S, false);
-        any = true;
-        tc_commit(cm.bar(Q_SF));
         if (!mbar_wait(cm.bar(Q_DSF), it & 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BLK / 16; ++kk) {
-          const uint32_t aoff = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
-          tc_mma_bf16(tmem + 256, sdesc_sw128(sDS + aoff, 16, 1024), sdesc_sw128(sKh + kk * 2048, 16384, 1024), ID_G,
-                      (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(cm.bar(Q_KVE));
+        for (int kk = 0; kk < KBQ / 16; ++kk)
+          tc_mma_bf16(tmem + 256, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(sKh(st) + kk * 2048, 8192, 1024),
+                      ID_G, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(cm.bar(Q_KE + st));
         tc_commit(cm.bar(Q_DSE));
       }
       if (ok) tc_commit(cm.bar(Q_ACC));
@@ -453,43 +508,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int r = warp * 32 + lane;
     const int q = q0 + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t rsw = static_cast<uint32_t>(r & 7);
     const bool qvalid = q < a.S;
     const size_t ridx = (static_cast<size_t>(b) * a.H + j) * a.S + q;
     const float lse2 = qvalid ? lse[ridx] * kLog2e : 0.0f;
     const float dd = qvalid ? dsum[ridx] : 0.0f;
     bool ok = true;
     for (int it = 0; it < nkv; ++it) {
-      const int kbase = it * BLK;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(cm.bar(Q_SF), it & 1, wc) && mbar_wait(cm.bar(Q_DSE), (it & 1) ^ 1, wc));
+      const int st = it & 1;
+      const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
+      const int kbase = it * KBQ;
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_SF + st), ph, wc));
       if (!ok) break;
       tc_fence_after();
-      const bool need_mask = (a.causal && it == qb) || (kbase + BLK > a.S) || !qvalid;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t vs[32], vp[32];
-        tmem_ld32(trow + 32 * c, vs);
-        tmem_ld32(trow + 128 + 32 * c, vp);
-        tmem_ld_wait(vs);
-        tmem_ld_wait(vp);
-        uint32_t dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float d2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = kbase + 32 * c + e + u;
-            float p = exp2f(__uint_as_float(vs[e + u]) * scale_log2 - lse2);
-            if (need_mask && (!qvalid || key >= a.S || (a.causal && key > q))) p = 0.0f;
-            d2[u] = p * (__uint_as_float(vp[e + u]) - dd);
-          }
-          dk[e >> 1] = pack_bf16x2(d2[0], d2[1]);
-        }
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-          st_shared_v4(sDS + tile128_addr(0, r, 4 * c + g), dk[4 * g], dk[4 * g + 1], dk[4 * g + 2], dk[4 * g + 3]);
-      }
+      uint32_t vs0[32], vs1[32], vp0[32], vp1[32];
+      tmem_ld32(trow + st * 64, vs0);
+      tmem_ld32(trow + st * 64 + 32, vs1);
+      tmem_ld32(trow + 128 + st * 64, vp0);
+      tmem_ld32(trow + 128 + st * 64 + 32, vp1);
+      tmem_ld_wait(vs0);
+      tmem_ld_wait(vs1);
+      tmem_ld_wait(vp0);
+      tmem_ld_wait(vp1);
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cm.bar(Q_SE + st));
+      const bool need_mask = (a.causal && kbase + KBQ > q0) || (kbase + KBQ > a.S) || !qvalid;
+      uint32_t dk[32];
+#pragma unroll
+      for (int e = 0; e < 64; e += 2) {
+        float d2[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int kc = e + u;
+          const int key = kbase + kc;
+          const float sv = __uint_as_float(kc < 32 ? vs0[kc] : vs1[kc - 32]);
+          const float dpv = __uint_as_float(kc < 32 ? vp0[kc] : vp1[kc - 32]);
+          float p = exp2f(sv * scale_log2 - lse2);
+          if (need_mask && (!qvalid || key >= a.S || (a.causal && key > q))) p = 0.0f;
+          d2[u] = p * (dpv - dd);
+        }
+        dk[e >> 1] = pack_bf16x2(d2[0], d2[1]);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DSE), (it & 1) ^ 1, wc));
+      if (!ok) break;
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        st_shared_v4(sDS + static_cast<uint32_t>(r) * 128u + ((static_cast<uint32_t>(g) ^ rsw) << 4), dk[4 * g],
+                     dk[4 * g + 1], dk[4 * g + 2], dk[4 * g + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(cm.bar(Q_DSF));
@@ -497,7 +563,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_ACC), 0, wc));
     if (ok) {
       tc_fence_after();
-      const uint32_t stQ = sDS + static_cast<uint32_t>(warp * C::CH * 4096);
+      // all MMAs are complete: the Qh tile is free for staging
+      const uint32_t stQ = sQh + static_cast<uint32_t>(warp * C::CH * 4096);
       stage_rows_from_tmem<D>(trow + 256, stQ, lane, scale);
       fence_proxy_async_smem();
       __syncwarp();
@@ -567,8 +634,8 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   timing_end(slot, st);
   if (!ok) return 2;
   slot = timing_begin(kKAttnDq, st);
-  k_attn_dq<D><<<grid, NTHREADS, DqCfg<D>::SMEM, st>>>(tq128, tdo128, tdq, lse, dsum, a, scale_log2, scale, err,
-                                                      timeout_ns);
+  k_attn_dq<D><<<grid, NTHREADS, DqCfg<D>::SMEM, st>>>(tq128, tq64, tdo128, tdq, lse, dsum, a, scale_log2, scale,
+                                                      err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
