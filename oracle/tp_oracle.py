@@ -51,6 +51,7 @@ __all__ = [
     "attention_forward", "attention_backward", "attention_forward_sharded",
     "layer_forward", "layer_backward",
     "mlp_backward_weight_columns", "attention_forward_rows",
+    "silu", "silu_grad", "gated_mlp_forward", "gated_mlp_backward", "gated_mlp_forward_sharded",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -437,3 +438,86 @@ def attention_forward_rows(X, Wqkv, Wo, B: int, S: int, rows, causal: bool = Tru
             O[ri, c] = matmul(P, V[kr, c])[0]
             LSE[ri, j] = lse[0]
     return {"Z": matmul(O, Wo_full), "O": O, "LSE": LSE}
+
+
+# --------------------------------------------------------------------------
+# Gated MLP (the Qwen3-style MLP of wangyu 张量并行 §多层感知机（MLP）中的张量并行)
+# --------------------------------------------------------------------------
+def silu(x: np.ndarray) -> np.ndarray:
+    """silu(x) = x * sigmoid(x) = x / (1 + e^-x)."""
+    x = _f64(x)
+    return x / (1.0 + np.exp(-x))
+
+
+def silu_grad(x: np.ndarray) -> np.ndarray:
+    """d/dx silu(x) = s (1 + x (1 - s)) with s = sigmoid(x)."""
+    x = _f64(x)
+    s = 1.0 / (1.0 + np.exp(-x))
+    return s * (1.0 + x * (1.0 - s))
+
+
+def _split_gate_up(Wgus):
+    """Shard-major [N][h][2][f/N] (shard i = [W_gate_i | W_up_i], the page's fused
+    column concatenation) -> unsharded W_gate, W_up, each [h][f]."""
+    W = _f64(Wgus)
+    n, h, two, fn = W.shape
+    assert two == 2
+    Wg = np.concatenate([W[i, :, 0, :] for i in range(n)], axis=1)
+    Wu = np.concatenate([W[i, :, 1, :] for i in range(n)], axis=1)
+    return Wg, Wu
+
+
+def gated_mlp_forward(X, Wgus, Wds) -> dict:
+    """gate = X W_gate, up = X W_up, x = silu(gate) * up, down = x W_down (wangyu
+    张量并行 §多层感知机: the Qwen3 MLP; W_gate and W_up concatenated by columns so
+    gate and up come from one GEMM).  Unsharded; returns GU in shard layout
+    [N][T][2][f/N] (gate block then up block per shard), A = x [N][T][f/N], Z."""
+    X = _f64(X)
+    n = Wgus.shape[0]
+    Wg, Wu = _split_gate_up(Wgus)
+    Wd = stack_rows(Wds)
+    G = matmul(X, Wg)
+    U = matmul(X, Wu)
+    A = silu(G) * U
+    Z = matmul(A, Wd)
+    GU = np.stack([split_columns_like(G, n), split_columns_like(U, n)], axis=2)  # [N][T][2][f/N]
+    return {"GU": GU, "A": split_columns_like(A, n), "Z": Z}
+
+
+def gated_mlp_backward(X, Wgus, Wds, dZ) -> dict:
+    """Gradients of <dZ, Z>: dA = dZ W_down^T, dG = dA * up * silu'(gate),
+    dU = dA * silu(gate), dW_down = A^T dZ, dW_gate = X^T dG, dW_up = X^T dU,
+    dX = dG W_gate^T + dU W_up^T.  Weight gradients in shard layout."""
+    X, dZ = _f64(X), _f64(dZ)
+    n = Wgus.shape[0]
+    Wg, Wu = _split_gate_up(Wgus)
+    Wd = stack_rows(Wds)
+    G = matmul(X, Wg)
+    U = matmul(X, Wu)
+    A = silu(G) * U
+    dA = matmul(dZ, Wd.T)
+    dG = dA * U * silu_grad(G)
+    dU = dA * silu(G)
+    dWd = matmul(A.T, dZ)
+    dWg = matmul(X.T, dG)
+    dWu = matmul(X.T, dU)
+    dX = matmul(dG, Wg.T) + matmul(dU, Wu.T)
+    dWgus = np.stack([split_columns_like(dWg, n), split_columns_like(dWu, n)], axis=2)  # [N][h][2][f/N]
+    return {"dX": dX, "dWgus": dWgus, "dWds": split_rows_like(dWd, n)}
+
+
+def gated_mlp_forward_sharded(X, Wgus, Wds) -> np.ndarray:
+    """Shard by shard: shard i computes [gate_i | up_i] = X [W_gate_i | W_up_i] in one
+    product, x_i = silu(gate_i) * up_i locally, then x_i W_down_i; the all-reduce
+    sums the partial products."""
+    X = _f64(X)
+    n = Wgus.shape[0]
+    Z = None
+    for i in range(n):
+        Wi = _f64(Wgus[i])
+        h, _, fn = Wi.shape
+        GUi = matmul(X, Wi.reshape(h, 2 * fn))
+        xi = silu(GUi[:, :fn]) * GUi[:, fn:]
+        part = matmul(xi, Wds[i])
+        Z = part if Z is None else Z + part
+    return Z

@@ -430,3 +430,70 @@ def test_planted_mistakes_are_caught(monkeypatch):
         np.tril(np.ones((q.shape[0], k.shape[0]), bool)), 0.0, -np.inf)
     monkeypatch.setattr(O, "_causal_scores", bad_scores)
     assert rel(O.attention_forward(X, Wqkv, Wos, B, S, True)["Z"], good) > 1e-3
+
+
+# ---------------------------------------------------------------- gated MLP
+def _gmlp_inputs(T, h, f, n, seed=0):
+    r = np.random.default_rng(seed)
+    X = r.standard_normal((T, h))
+    Wg, Wu = r.standard_normal((h, f)) * 0.3, r.standard_normal((h, f)) * 0.3
+    Wd = r.standard_normal((f, h)) * 0.3
+    dZ = r.standard_normal((T, h))
+    c = f // n
+    Wgus = np.stack([np.stack([Wg[:, i * c:(i + 1) * c], Wu[:, i * c:(i + 1) * c]], axis=1) for i in range(n)])
+    Wds = np.stack([Wd[i * c:(i + 1) * c] for i in range(n)])
+    return X, Wg, Wu, Wd, Wgus, Wds, dZ
+
+
+def test_silu_vs_torch_and_closed_forms():
+    x = RNG.standard_normal(2048) * 6
+    ref = torch.nn.functional.silu(torch.from_numpy(x)).numpy()
+    assert np.max(np.abs(O.silu(x) - ref)) < 1e-13
+    assert O.silu(np.array([0.0]))[0] == 0.0
+    assert np.allclose(O.silu(np.array([40.0])), 40.0)
+    t = torch.from_numpy(x.copy()).requires_grad_(True)
+    torch.nn.functional.silu(t).sum().backward()
+    assert np.max(np.abs(O.silu_grad(x) - t.grad.numpy())) < 1e-13
+
+
+def test_gated_mlp_vs_brute_force_and_sharded():
+    X, Wg, Wu, Wd, Wgus, Wds, _ = _gmlp_inputs(4, 6, 8, 2)
+    T, h = X.shape
+    f = Wg.shape[1]
+    ref = np.zeros((T, h))
+    for t in range(T):
+        xs = []
+        for c in range(f):
+            g = sum(X[t, k] * Wg[k, c] for k in range(h))
+            u = sum(X[t, k] * Wu[k, c] for k in range(h))
+            xs.append(g / (1.0 + math.exp(-g)) * u)
+        for o in range(h):
+            ref[t, o] = sum(xs[c] * Wd[c, o] for c in range(f))
+    assert rel(O.gated_mlp_forward(X, Wgus, Wds)["Z"], ref) < 1e-13
+    for n in divisors(8):
+        X, Wg, Wu, Wd, Wgus, Wds, _ = _gmlp_inputs(5, 6, 8, n, seed=n)
+        assert rel(O.gated_mlp_forward_sharded(X, Wgus, Wds), O.gated_mlp_forward(X, Wgus, Wds)["Z"]) < 1e-13
+
+
+def test_gated_mlp_backward_vs_autograd_and_fd():
+    X, Wg, Wu, Wd, Wgus, Wds, dZ = _gmlp_inputs(5, 6, 8, 2, seed=4)
+    tX, tg, tu, td = (torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, Wg, Wu, Wd))
+    Z = (torch.nn.functional.silu(tX @ tg) * (tX @ tu)) @ td
+    (Z * torch.from_numpy(dZ)).sum().backward()
+    g = O.gated_mlp_backward(X, Wgus, Wds, dZ)
+    assert rel(g["dX"], tX.grad.numpy()) < 1e-13
+    assert rel(np.concatenate([g["dWgus"][i, :, 0] for i in range(2)], axis=1), tg.grad.numpy()) < 1e-13
+    assert rel(np.concatenate([g["dWgus"][i, :, 1] for i in range(2)], axis=1), tu.grad.numpy()) < 1e-13
+    assert rel(O.stack_rows(g["dWds"]), td.grad.numpy()) < 1e-13
+    # finite differences on a few entries of every input
+    loss = lambda: float(np.sum(dZ * O.gated_mlp_forward(X, Wgus, Wds)["Z"]))
+    eps = 1e-6
+    for arr, grad in ((X, g["dX"]), (Wgus, g["dWgus"]), (Wds, g["dWds"])):
+        for idx in [tuple(RNG.integers(0, s) for s in arr.shape) for _ in range(6)]:
+            old = arr[idx]
+            arr[idx] = old + eps
+            lp = loss()
+            arr[idx] = old - eps
+            lm = loss()
+            arr[idx] = old
+            assert abs((lp - lm) / (2 * eps) - grad[idx]) < 1e-6 * max(1.0, abs(grad[idx]))
