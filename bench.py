@@ -57,6 +57,11 @@ def kernel_flops(w) -> dict:
         out.update({"mlp.fc1_col_gemm_gelu": g, "mlp.fc2_row_gemm_shard_sum": g, "mlp.bwd_dA_gemm_dgelu": g,
                     "mlp.bwd_dW2_gemm": g, "mlp.bwd_dW1_gemm": g, "mlp.bwd_dX_row_gemm_shard_sum": g,
                     "mlp.f32_fc1_col_gemm_gelu": g, "mlp.f32_fc2_row_gemm": g})
+    if w.kind == "gmlp":
+        g = 2.0 * T * h * f
+        out.update({"gmlp.fc1_col_gemm_swiglu": 2 * g, "gmlp.fc2_row_gemm_shard_sum": g,
+                    "gmlp.bwd_dA_gemm_dswiglu": g, "gmlp.bwd_dWd_gemm": g, "gmlp.bwd_dWgu_gemm": 2 * g,
+                    "gmlp.bwd_dX_row_gemm_shard_sum": 2 * g})
     if w.kind in ("attn", "layer"):
         Hd = w.H * w.d
         pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d  # (causal half) x d
@@ -73,6 +78,8 @@ def step_flops(w) -> float:
     tot = 0.0
     if w.kind in ("mlp", "layer"):
         tot += (12.0 if w.backward else 4.0) * T * h * f
+    if w.kind == "gmlp":
+        tot += (18.0 if w.backward else 6.0) * T * h * f
     if w.kind in ("attn", "layer"):
         Hd = w.H * w.d
         core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
@@ -86,6 +93,9 @@ def describe(w) -> str:
     if w.kind == "mlp":
         return (f"MLP block {'fwd+bwd' if w.backward else 'fwd'}, {w.dtype}, T={w.T} tokens, h={w.h}, f={w.f}, "
                 f"N={w.N} logical shards")
+    if w.kind == "gmlp":
+        return (f"gated (SwiGLU) MLP block {'fwd+bwd' if w.backward else 'fwd'}, {w.dtype}, T={w.T} tokens, "
+                f"h={w.h}, f={w.f} (gate and up each), N={w.N} logical shards")
     if w.kind == "attn":
         return (f"self-attention block fwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
                 f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
@@ -184,6 +194,12 @@ def oracle_step(w, inp_np: dict, rows: int) -> float:
         if w.backward:
             O.mlp_backward(X, inp_np["W1s"], inp_np["W2s"], dZ[:rows])
         return (12.0 if w.backward else 4.0) * rows * w.h * w.f
+    if w.kind == "gmlp":
+        X, dZ = inp_np["X"][:rows], inp_np.get("dZ")
+        O.gated_mlp_forward(X, inp_np["Wgus"], inp_np["Wds"])
+        if w.backward:
+            O.gated_mlp_backward(X, inp_np["Wgus"], inp_np["Wds"], dZ[:rows])
+        return (18.0 if w.backward else 6.0) * rows * w.h * w.f
     import dataclasses
     sub = dataclasses.replace(w, B=1, S=rows, T=rows)
     X = inp_np["X"][:rows]
@@ -211,11 +227,11 @@ def oracle_cores() -> int:
 
 
 def calibrate_rows(w, inp_np, target_s: float) -> int:
-    rows = 128 if w.kind != "mlp" else 256
+    rows = 128 if w.kind not in ("mlp", "gmlp") else 256
     t0 = time.perf_counter()
     oracle_step(w, inp_np, rows)
     dt = max(time.perf_counter() - t0, 1e-3)
-    limit = w.T if w.kind == "mlp" else w.S
+    limit = w.T if w.kind in ("mlp", "gmlp") else w.S
     return int(max(64, min(limit, rows * target_s / dt)))
 
 
@@ -224,7 +240,7 @@ def cpu_baseline(w, inp_np, target_s: float = 15.0) -> dict:
     t0 = time.perf_counter()
     fl = oracle_step(w, inp_np, rows)
     dt = time.perf_counter() - t0
-    unit = "tokens" if w.kind == "mlp" else "sequence positions of batch 0"
+    unit = "tokens" if w.kind in ("mlp", "gmlp") else "sequence positions of batch 0"
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_cores(), "kind": "oracle",
             "sample": f"fp64 oracle on the first {rows} {unit} of the same workload ({dt:.1f} s)",
             "seconds": dt}
@@ -244,7 +260,7 @@ def run_reference(args, w) -> None:
         fl += oracle_step(w, inp_np, rows)
     dt = time.perf_counter() - t0
     value = fl / dt / 1e12
-    unit = "tokens" if w.kind == "mlp" else "sequence positions of batch 0"
+    unit = "tokens" if w.kind in ("mlp", "gmlp") else "sequence positions of batch 0"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -299,6 +315,15 @@ def run_gpu(args, w) -> None:
         buf["dW1s"] = torch.empty_like(d["W1s"])
         buf["dW2s"] = torch.empty_like(d["W2s"])
         buf["mws"] = block.workspace(tp.tp_mlp_workspace_bytes(dt, T, h, f, N), dev)
+    if w.kind == "gmlp":
+        fN = f // N
+        buf["GU"] = torch.empty(N, T, 2, fN, dtype=torch.bfloat16, device=dev)
+        buf["A"] = torch.empty(N, T, fN, dtype=torch.bfloat16, device=dev)
+        buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["dX"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["dWgus"] = torch.empty_like(d["Wgus"])
+        buf["dWds"] = torch.empty_like(d["Wds"])
+        buf["gws"] = block.workspace(tp.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
     if w.kind in ("attn", "layer"):
         hN = w.H // N
         buf["QKV"] = torch.empty(N, T, tp.QKV_PLANES * hN * w.d, dtype=torch.bfloat16, device=dev)
@@ -318,6 +343,12 @@ def run_gpu(args, w) -> None:
             if w.backward:
                 tp.tp_mlp_bwd(dt, T, h, f, N, X, d["W1s"], d["W2s"], buf["Y"], buf["A"], dZ, buf["dX"], buf["dW1s"],
                               buf["dW2s"], buf["mws"], stream)
+            return buf["Z"], buf["dX"] if w.backward else None
+        if w.kind == "gmlp":
+            tp.tp_gmlp_fwd(dt, T, h, f, N, X, d["Wgus"], d["Wds"], buf["GU"], buf["A"], buf["Z"], buf["gws"], stream)
+            if w.backward:
+                tp.tp_gmlp_bwd(dt, T, h, f, N, X, d["Wgus"], d["Wds"], buf["GU"], buf["A"], dZ, buf["dX"],
+                               buf["dWgus"], buf["dWds"], buf["gws"], stream)
             return buf["Z"], buf["dX"] if w.backward else None
         if w.kind == "attn":
             tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
@@ -405,7 +436,7 @@ def run_gpu(args, w) -> None:
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
-    if w.kind in ("mlp", "layer") or w.kind == "attn":
+    if w.kind in ("mlp", "gmlp", "layer", "attn"):
         hX = inp["X"].pin_memory()
         hdZ = inp["dZ"].pin_memory() if "dZ" in inp and w.backward else None
         dX_in = torch.empty_like(d["X"])

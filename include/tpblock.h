@@ -34,7 +34,7 @@
  *    Errors detected on the device (a bounded wait that ran out) are latched in a
  *    device error word and surface through tp_sync_status().
  *  - dtype: TP_BF16 (bf16 storage, fp32 accumulation) everywhere; TP_F32 (fp32
- *    FFMA, no TF32) is accepted by tp_mlp_fwd only.
+ *    FFMA, no TF32) is accepted by tp_mlp_fwd (and tp_mlp_fwd_noalloc) only.
  */
 #ifndef TPBLOCK_H
 #define TPBLOCK_H
@@ -145,6 +145,49 @@ TP_API int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
  *    kernels overlap on the GPU, such as calls on two streams at once, race on it. */
 TP_API int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N,
                               const void* X, const void* W1s, const void* W2s, void* Z, void* stream);
+
+/* ------------------------------------------------------ gated MLP block */
+
+/* Bytes of scratch tp_gmlp_fwd (with A_save == NULL) and tp_gmlp_bwd need: one
+ * [N][T][2][f/N] buffer (the backward's dG, dU) plus alignment.  0 for invalid
+ * sizes or a dtype other than TP_BF16. */
+TP_API size_t tp_gmlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N);
+
+/* Gated (SwiGLU) MLP block forward (bf16), Z = sum_i (silu(X Wg_i) * (X Wu_i)) Wd_i.
+ * (wangyu.me 张量并行 §多层感知机（MLP）中的张量并行: the Qwen3 MLP, gate and up
+ *  projections fused by concatenating their columns so that one product gives
+ *  both; both split by columns, the down projection by rows, one all-reduce.)
+ *   X       [T][h]              input (read)
+ *   Wgus    [N][h][2][f/N]      shard i = [Wg_i | Wu_i]: columns i*f/N..(i+1)*f/N-1
+ *                               of W_gate, then the same columns of W_up (read)
+ *   Wds     [N][f/N][h]         row blocks of W_down (read)
+ *   GU_save [N][T][2][f/N] or NULL  G_i = X Wg_i and U_i = X Wu_i (written if not
+ *                               NULL; tp_gmlp_bwd needs it)
+ *   A_save  [N][T][f/N] or NULL A_i = silu(G_i) * U_i (written; if NULL it lives in ws)
+ *   Z       [T][h]              output, shard partial sums added on the device in
+ *                               order i = 0..N-1 in one fp32 accumulator
+ * silu(x) = x / (1 + e^-x) in fp32 on the fp32 accumulators; f is the width of
+ * each of the gate and up projections.  TP_ERR_DTYPE for TP_F32. */
+TP_API int tp_gmlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
+                       const void* X, const void* Wgus, const void* Wds,
+                       void* GU_save, void* A_save, void* Z,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Gated MLP block backward for an upstream gradient dZ (bf16).  The pages give
+ * no backward for this block; this is the chain rule through the forward:
+ *   dA_i  = dZ Wd_i^T
+ *   dG_i  = dA_i * U_i * silu'(G_i),  dU_i = dA_i * silu(G_i)   kept in ws [N][T][2][f/N]
+ *   dWd_i = A_i^T dZ                       -> dWds  [N][f/N][h]
+ *   [dWg_i | dWu_i] = X^T [dG_i | dU_i]    -> dWgus [N][h][2][f/N]
+ *   dX    = sum_i [dG_i | dU_i] [Wg_i | Wu_i]^T -> dX [T][h], shard sum on the
+ *           device, order 0..N-1 (the column split's backward all-reduce)
+ * silu'(x) = s (1 + x (1 - s)) with s = 1 / (1 + e^-x).  GU_save and A_save are
+ * what tp_gmlp_fwd wrote for the same X, Wgus. */
+TP_API int tp_gmlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
+                       const void* X, const void* Wgus, const void* Wds,
+                       const void* GU_save, const void* A_save, const void* dZ,
+                       void* dX, void* dWgus, void* dWds,
+                       void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------- attention block */
 

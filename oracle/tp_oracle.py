@@ -52,6 +52,7 @@ __all__ = [
     "layer_forward", "layer_backward",
     "mlp_backward_weight_columns", "attention_forward_rows",
     "silu", "silu_grad", "gated_mlp_forward", "gated_mlp_backward", "gated_mlp_forward_sharded",
+    "gated_mlp_backward_weight_columns",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -484,20 +485,31 @@ def gated_mlp_forward(X, Wgus, Wds) -> dict:
     return {"GU": GU, "A": split_columns_like(A, n), "Z": Z}
 
 
-def gated_mlp_backward(X, Wgus, Wds, dZ) -> dict:
+def _keep(x):
+    return x
+
+
+def gated_mlp_backward(X, Wgus, Wds, dZ, store=None) -> dict:
     """Gradients of <dZ, Z>: dA = dZ W_down^T, dG = dA * up * silu'(gate),
     dU = dA * silu(gate), dW_down = A^T dZ, dW_gate = X^T dG, dW_up = X^T dU,
-    dX = dG W_gate^T + dU W_up^T.  Weight gradients in shard layout."""
+    dX = dG W_gate^T + dU W_up^T.  Weight gradients in shard layout.
+
+    ``store`` (default: none) is applied to each intermediate a tensor-parallel
+    implementation keeps in memory between its products (gate, up, A, dG, dU);
+    the tests pass a rounding to the storage type to measure the error that
+    storage alone causes.  Without it this is the exact definition."""
+    st = store or _keep
     X, dZ = _f64(X), _f64(dZ)
     n = Wgus.shape[0]
     Wg, Wu = _split_gate_up(Wgus)
     Wd = stack_rows(Wds)
-    G = matmul(X, Wg)
-    U = matmul(X, Wu)
-    A = silu(G) * U
+    G0 = matmul(X, Wg)
+    U0 = matmul(X, Wu)
+    A = st(silu(G0) * U0)
+    G, U = st(G0), st(U0)
     dA = matmul(dZ, Wd.T)
-    dG = dA * U * silu_grad(G)
-    dU = dA * silu(G)
+    dG = st(dA * U * silu_grad(G))
+    dU = st(dA * silu(G))
     dWd = matmul(A.T, dZ)
     dWg = matmul(X.T, dG)
     dWu = matmul(X.T, dU)
@@ -521,3 +533,23 @@ def gated_mlp_forward_sharded(X, Wgus, Wds) -> np.ndarray:
         part = matmul(xi, Wds[i])
         Z = part if Z is None else Z + part
     return Z
+
+
+def gated_mlp_backward_weight_columns(X, Wgus, Wds, dZ, cols, store=None) -> dict:
+    """dW_gate[:, cols], dW_up[:, cols] and dW_down[cols, :] of
+    :func:`gated_mlp_backward` for global FFN column indices ``cols``.  Column c of
+    dG and dU needs only column c of gate, up and dA: dA[:, c] = dZ W_down[c, :]^T,
+    dG[:, c] = dA[:, c] up[:, c] silu'(gate[:, c]), dU[:, c] = dA[:, c] silu(gate[:, c]).
+    ``store`` as in :func:`gated_mlp_backward`."""
+    st = store or _keep
+    X, dZ = _f64(X), _f64(dZ)
+    cols = np.asarray(cols, dtype=np.int64)
+    Wg, Wu = _split_gate_up(Wgus)
+    Wd = stack_rows(Wds)[cols, :]
+    G0 = matmul(X, Wg[:, cols])
+    U0 = matmul(X, Wu[:, cols])
+    A = st(silu(G0) * U0)
+    G, U = st(G0), st(U0)
+    dA = matmul(dZ, Wd.T)
+    return {"dWg_cols": matmul(X.T, st(dA * U * silu_grad(G))), "dWu_cols": matmul(X.T, st(dA * silu(G))),
+            "dWd_rows": matmul(A.T, dZ)}

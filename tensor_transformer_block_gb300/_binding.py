@@ -42,6 +42,9 @@ _SIGS = {
     "tp_attn_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                      vp], i32),
     "tp_mlp_fwd_noalloc": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp], i32),
+    "tp_gmlp_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
+    "tp_gmlp_fwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_gmlp_bwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
     "tp_set_gemm_tiling": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
@@ -185,6 +188,31 @@ def tp_mlp_fwd_noalloc(dtype, T, h, f, N, X, W1s, W2s, Z, stream=None) -> int:
     return _check(load_library().tp_mlp_fwd_noalloc(
         dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
         _p(Z, "Z", dt, T * h), _stream(stream)), "tp_mlp_fwd_noalloc")
+
+
+# ---------------------------------------------------------------- gated MLP block
+def tp_gmlp_workspace_bytes(dtype: int, T: int, h: int, f: int, N: int) -> int:
+    return load_library().tp_gmlp_workspace_bytes(dtype, T, h, f, N)
+
+
+def tp_gmlp_fwd(dtype, T, h, f, N, X, Wgus, Wds, GU_save, A_save, Z, ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    wptr, wbytes = _ws(ws, tp_gmlp_workspace_bytes(dtype, T, h, f, N))
+    return _check(load_library().tp_gmlp_fwd(
+        dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(Wgus, "Wgus", dt, 2 * h * f), _p(Wds, "Wds", dt, f * h),
+        _p(GU_save, "GU_save", dt, 2 * T * f, False), _p(A_save, "A_save", dt, T * f, False),
+        _p(Z, "Z", dt, T * h), wptr, wbytes, _stream(stream)), "tp_gmlp_fwd")
+
+
+def tp_gmlp_bwd(dtype, T, h, f, N, X, Wgus, Wds, GU_save, A_save, dZ, dX, dWgus, dWds, ws=None,
+                stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    wptr, wbytes = _ws(ws, tp_gmlp_workspace_bytes(dtype, T, h, f, N))
+    return _check(load_library().tp_gmlp_bwd(
+        dtype, T, h, f, N, _p(X, "X", dt, T * h), _p(Wgus, "Wgus", dt, 2 * h * f), _p(Wds, "Wds", dt, f * h),
+        _p(GU_save, "GU_save", dt, 2 * T * f), _p(A_save, "A_save", dt, T * f), _p(dZ, "dZ", dt, T * h),
+        _p(dX, "dX", dt, T * h), _p(dWgus, "dWgus", dt, 2 * h * f), _p(dWds, "dWds", dt, f * h),
+        wptr, wbytes, _stream(stream)), "tp_gmlp_bwd")
 
 
 # ---------------------------------------------------------------- attention block

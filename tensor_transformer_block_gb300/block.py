@@ -55,6 +55,41 @@ def mlp_backward(X, W1s, W2s, Y, A, dZ, ws=None, stream=None, out=None) -> dict:
     return out
 
 
+def gmlp_forward(X, Wgus, Wds, save: bool = True, ws=None, stream=None) -> dict:
+    """Z = sum_i (silu(X Wg_i) * (X Wu_i)) Wd_i.  With ``save`` the gate and up
+    pre-activations GU ([N][T][2][f/N]) and the activation A ([N][T][f/N]) are
+    returned for the backward."""
+    N, h, two, fN = Wgus.shape
+    assert two == 2
+    T = X.shape[0]
+    f = N * fN
+    dt = _dtype(X)
+    dev = X.device
+    Z = torch.empty(T, h, dtype=X.dtype, device=dev)
+    GU = torch.empty(N, T, 2, fN, dtype=X.dtype, device=dev) if save else None
+    A = torch.empty(N, T, fN, dtype=X.dtype, device=dev) if save else None
+    if A is None and ws is None:
+        ws = workspace(B.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
+    B.tp_gmlp_fwd(dt, T, h, f, N, X, Wgus, Wds, GU, A, Z, ws, stream)
+    return {"Z": Z, "GU": GU, "A": A}
+
+
+def gmlp_backward(X, Wgus, Wds, GU, A, dZ, ws=None, stream=None, out=None) -> dict:
+    """dX, dWgus, dWds of L = <dZ, Z> for the gated block whose forward saved GU and A."""
+    N, h, _, fN = Wgus.shape
+    T = X.shape[0]
+    f = N * fN
+    dt = _dtype(X)
+    dev = X.device
+    if out is None:
+        out = {"dX": torch.empty(T, h, dtype=X.dtype, device=dev),
+               "dWgus": torch.empty_like(Wgus), "dWds": torch.empty_like(Wds)}
+    if ws is None:
+        ws = workspace(B.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
+    B.tp_gmlp_bwd(dt, T, h, f, N, X, Wgus, Wds, GU, A, dZ, out["dX"], out["dWgus"], out["dWds"], ws, stream)
+    return out
+
+
 def attn_forward(X, Wqkv, Wo, B_: int, S: int, causal: bool = True, save: bool = True, ws=None,
                  stream=None) -> dict:
     """Z = sum_i O_i Wo_i with O the per-head causal attention of X Wqkv_i."""

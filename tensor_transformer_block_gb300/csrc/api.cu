@@ -111,7 +111,7 @@ AttnWs attn_ws(int64_t B, int64_t S, int H, int d) {
 
 extern "C" {
 
-int tp_version(void) { return (0 << 16) | 3; }
+int tp_version(void) { return (0 << 16) | 4; }
 
 const char* tp_status_string(int s) {
   switch (s) {
@@ -273,6 +273,98 @@ int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
   const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
                              st, tpb::kKMlpDx);
+  return gemm_status(rc);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------- gated MLP block
+namespace {
+int gmlp_shape_check(int dtype, int64_t T, int64_t h, int64_t f, int N) {
+  if (dtype != TP_BF16) return TP_ERR_DTYPE;
+  return mlp_shape_check(dtype, T, h, f, N);
+}
+}  // namespace
+
+extern "C" {
+
+size_t tp_gmlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N) {
+  if (gmlp_shape_check(dtype, T, h, f, N) != TP_OK) return 0;
+  return round_up(static_cast<size_t>(T) * static_cast<size_t>(f) * 2 * 2, 256);
+}
+
+int tp_gmlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* Wgus,
+                const void* Wds, void* GU_save, void* A_save, void* Z, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = gmlp_shape_check(dtype, T, h, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wgus || !Wds || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wgus) || !al16(Wds) || !al16(Z) || !al16(GU_save) || !al16(A_save)) return TP_ERR_ALIGN;
+  void* Abuf = A_save;
+  if (!Abuf) {
+    if (!ws || ws_bytes < tp_gmlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+    if (!al256(ws)) return TP_ERR_ALIGN;
+    Abuf = ws;
+  }
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t fN = f / N;
+  // [G_i U_i] = X [Wg_i Wu_i] in one product per shard; A_i = silu(G_i) * U_i in the epilogue
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opWgu{Wgus, fN, h, N, true, 1, 0, 2};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiSwiGLU, opX, opWgu, Abuf, GU_save, GU_save != nullptr, T, fN, N, 1, h,
+                                 err, kWaitTimeoutNs, st, tpb::kKGmlpFc1);
+  if (rc) return gemm_status(rc);
+  // Z = sum_i A_i Wd_i  (row-parallel, shard sum in the accumulator, order 0..N-1)
+  const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opWd{Wds, h, fN, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opWd, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st,
+                             tpb::kKGmlpFc2);
+  return gemm_status(rc);
+}
+
+int tp_gmlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* Wgus,
+                const void* Wds, const void* GU_save, const void* A_save, const void* dZ, void* dX, void* dWgus,
+                void* dWds, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = gmlp_shape_check(dtype, T, h, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wgus || !Wds || !GU_save || !A_save || !dZ || !dX || !dWgus || !dWds) return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wgus) || !al16(Wds) || !al16(GU_save) || !al16(A_save) || !al16(dZ) || !al16(dX) ||
+      !al16(dWgus) || !al16(dWds))
+    return TP_ERR_ALIGN;
+  if (!ws || ws_bytes < tp_gmlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+  if (!al256(ws)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t fN = f / N;
+  void* dGU = ws;  // [N][T][2][f/N]
+
+  // dA_i = dZ Wd_i^T; epilogue: dG_i = dA_i * U_i * silu'(G_i), dU_i = dA_i * silu(G_i)
+  const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opWdk{Wds, h, fN, N, false, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiDSwiGLU, opdZk, opWdk, dGU, GU_save, false, T, fN, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKGmlpDswiglu);
+  if (rc) return gemm_status(rc);
+  // dWd_i = A_i^T dZ
+  const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
+  const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opAt, opdZn, dWds, nullptr, false, fN, h, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKGmlpDwd);
+  if (rc) return gemm_status(rc);
+  // [dWg_i dWu_i] = X^T [dG_i dU_i]  (one product per shard over the fused columns)
+  const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
+  const tpb::GemmOperand opdGUn{dGU, 2 * fN, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdGUn, dWgus, nullptr, false, h, 2 * fN, N, 1, T, err,
+                             kWaitTimeoutNs, st, tpb::kKGmlpDwgu);
+  if (rc) return gemm_status(rc);
+  // dX = sum_i [dG_i dU_i] [Wg_i Wu_i]^T  (the column split's backward all-reduce, in the accumulator)
+  const tpb::GemmOperand opdGUk{dGU, 2 * fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opWguk{Wgus, 2 * fN, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdGUk, opWguk, dX, nullptr, false, T, h, 1, N, 2 * fN, err,
+                             kWaitTimeoutNs, st, tpb::kKGmlpDx);
   return gemm_status(rc);
 }
 

@@ -103,11 +103,24 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
   return s * fmaf(2.0f * x * oms, du, 1.0f);
 }
 
+// Logistic sigmoid s = 1 / (1 + e^(-x)) and 1 - s = e^(-x) s (no cancellation);
+// silu(x) = x s, silu'(x) = s (1 + x (1 - s)).  The exponent is clamped as above.
+__device__ __forceinline__ void sigmoid_parts(float x, float& s, float& oms) {
+  const float a = fminf(-1.4426950408889634f * x, 126.0f);  // -x log2(e)
+  const float e = exp2f(a);
+  s = __frcp_rn(1.0f + e);
+  oms = e * s;
+}
+
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, const GemmShape p) {
   using C = Cfg<PAIR>;
+  // output columns per tile: the gated forward spends half the MMA's N on the up part
+  constexpr int TILE_N = EPI == kEpiSwiGLU ? BN / 2 : BN;
+  constexpr int WARP_COLS = TILE_N / 2;  // output columns per epilogue warp
+  constexpr bool LOADS_Y = EPI == kEpiDGelu || EPI == kEpiDSwiGLU;
   constexpr int BM = C::BM, STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
   constexpr int BAR_FULL = C::BAR_FULL, BAR_EMPTY = C::BAR_EMPTY, BAR_TFULL = C::BAR_TFULL;
   constexpr int BAR_TEMPTY = C::BAR_TEMPTY, BAR_Y = C::BAR_Y, BAR_DRAIN = C::BAR_DRAIN;
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    if (EPI != kEpiStore) prefetch_tmap(&tmY);
+    if (EPI != kEpiStore && EPI != kEpiSplit) prefetch_tmap(&tmY);
   }
   if (warp == WARP_MMA) {
     if (PAIR) {
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int g, mb, nb;
         decode_tile(t, p, g, mb, nb);
         const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
-        const int bcol = nb * BN + static_cast<int>(rank) * C::BN_CTA;
+        const int bcol = EPI == kEpiSwiGLU ? nb * TILE_N : nb * BN + static_cast<int>(rank) * C::BN_CTA;
         for (int s = 0; s < p.S && ok; ++s) {
           const int az = g * p.a_zg + s * p.a_zs;
           const int bz = g * p.b_zg + s * p.b_zs;
@@ -201,7 +214,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else {
                 tma_load_3d_pair(sa, &tmA, fb, kc, arow, az);
               }
-              if (B_MN) {
+              if (EPI == kEpiSwiGLU) {
+                // the even CTA stages the tile's gate columns, the odd CTA its up columns
+#pragma unroll
+                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                  tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz);
+              } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
                   tma_load_3d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz);
@@ -216,7 +234,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else {
                 tma_load_3d(sa, &tmA, fb_local, kc, arow, az);
               }
-              if (B_MN) {
+              if (EPI == kEpiSwiGLU) {
+                // atoms 0-1: gate columns, atoms 2-3: the same columns of the up part
+#pragma unroll
+                for (int j = 0; j < C::BN_CTA / 64; ++j)
+                  tma_load_4d(sb + j * (BK * 128), &tmB, fb_local, bcol + (j & 1) * 64, j >> 1, kc, bz);
+              } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
                   tma_load_3d(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz);
@@ -322,9 +345,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
-      const int col0 = nb * BN + half * (BN / 2);
+      const int col0 = nb * TILE_N + half * WARP_COLS;
       int nch = col0 < p.N ? (p.N - col0 + 63) / 64 : 0;
-      if (nch > BN / 128) nch = BN / 128;
+      if (nch > WARP_COLS / 64) nch = WARP_COLS / 64;
       const bool rows_valid = row0 < p.M && nch > 0;
       if (EPI == kEpiDGelu && rows_valid) {
         const uint32_t b = ecount & 1u;
@@ -335,12 +358,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ypend |= 1u << b;
       }
+      if (EPI == kEpiDSwiGLU && rows_valid) {
+        // G and U of the warp's first chunk, fetched while the main loop runs
+        if (lane == 0) {
+          bulk_wait_read0();
+          mbar_arrive_expect_tx(ybar[0], 2 * EPI_BUF);
+          tma_load_4d(ebuf[0], &tmY, ybar[0], col0, 0, row0, g);
+          tma_load_4d(ebuf[1], &tmY, ybar[0], col0, 1, row0, g);
+        }
+        ypend |= 1u;
+      }
 
       ok = __all_sync(0xffffffffu, mbar_wait(bar0 + 8u * (BAR_TFULL + buf), tph, wc));
       if (!ok) break;
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                          static_cast<uint32_t>(buf * BN + half * (BN / 2));
+                          static_cast<uint32_t>(buf * BN + half * WARP_COLS);
 
       if (rows_valid) {
         for (int j = 0; j < nch && ok; ++j) {
@@ -435,6 +468,127 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (p.store_y) tma_store_3d(&tmY, ebuf[1], ccol, row0, g);
               bulk_commit();
             }
+          } else if (EPI == kEpiSwiGLU) {
+            // gate at TMEM columns tcol.., up at tcol + 128..
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t vg[16], vu[16];
+              tmem_ld16(tcol + q * 16, vg);
+              tmem_ld16(tcol + 128 + q * 16, vu);
+              tmem_ld_wait16(vg);
+              tmem_ld_wait16(vu);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                uint32_t a[4], gg[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float s0, o0, s1, o1;
+                  const float g0 = __uint_as_float(vg[8 * hh + 2 * e]), g1 = __uint_as_float(vg[8 * hh + 2 * e + 1]);
+                  sigmoid_parts(g0, s0, o0);
+                  sigmoid_parts(g1, s1, o1);
+                  a[e] = pack_bf16x2(g0 * s0 * __uint_as_float(vu[8 * hh + 2 * e]),
+                                     g1 * s1 * __uint_as_float(vu[8 * hh + 2 * e + 1]));
+                  gg[e] = pack_bf16x2(g0, g1);
+                }
+                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                st_shared_v4(ebuf[0] + off, a[0], a[1], a[2], a[3]);
+                if (p.store_y) st_shared_v4(ebuf[1] + off, gg[0], gg[1], gg[2], gg[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, ebuf[0], ccol, row0, g);
+              bulk_commit();
+              if (p.store_y) {
+                tma_store_4d(&tmY, ebuf[1], ccol, 0, row0, g);
+                bulk_commit();
+              }
+            }
+            if (p.store_y) {
+              // the up part goes out through ebuf[0] once the activation store has read it
+              if (lane == 0) bulk_wait_read1();
+              __syncwarp();
+#pragma unroll 1
+              for (int q = 0; q < 4; ++q) {
+                uint32_t vu[16];
+                tmem_ld16(tcol + 128 + q * 16, vu);
+                tmem_ld_wait16(vu);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                  const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                  const uint32_t* v = &vu[8 * hh];
+                  st_shared_v4(ebuf[0] + lane * 128 + ((c ^ rsw) << 4),
+                               pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                               pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                               pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                               pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_4d(&tmY, ebuf[0], ccol, 1, row0, g);
+                bulk_commit();
+              }
+            }
+          } else if (EPI == kEpiDSwiGLU) {
+            // ebuf[0] <- G, ebuf[1] <- U of this chunk; dG, dU written over them in place
+            if (j > 0) {
+              if (lane == 0) {
+                bulk_wait_read0();
+                mbar_arrive_expect_tx(ybar[0], 2 * EPI_BUF);
+                tma_load_4d(ebuf[0], &tmY, ybar[0], ccol, 0, row0, g);
+                tma_load_4d(ebuf[1], &tmY, ybar[0], ccol, 1, row0, g);
+              }
+              ypend |= 1u;
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(ybar[0], yph & 1u, wc));
+            if (!ok) break;
+            yph ^= 1u;
+            ypend &= ~1u;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+              uint32_t v[16];
+              tmem_ld16(tcol + q * 16, v);
+              tmem_ld_wait16(v);
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
+                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                uint32_t gq[4], uq[4], dg[4], du[4];
+                ld_shared_v4(ebuf[0] + off, gq[0], gq[1], gq[2], gq[3]);
+                ld_shared_v4(ebuf[1] + off, uq[0], uq[1], uq[2], uq[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float r[2][2];
+#pragma unroll
+                  for (int k2 = 0; k2 < 2; ++k2) {
+                    const float gv = k2 ? bf16hi_to_f32(gq[e]) : bf16lo_to_f32(gq[e]);
+                    const float uv = k2 ? bf16hi_to_f32(uq[e]) : bf16lo_to_f32(uq[e]);
+                    const float da = __uint_as_float(v[8 * hh + 2 * e + k2]);
+                    float sg, om;
+                    sigmoid_parts(gv, sg, om);
+                    r[0][k2] = da * uv * (sg * fmaf(gv, om, 1.0f));  // dG = dA U silu'(G)
+                    r[1][k2] = da * gv * sg;                         // dU = dA silu(G)
+                  }
+                  dg[e] = pack_bf16x2(r[0][0], r[0][1]);
+                  du[e] = pack_bf16x2(r[1][0], r[1][1]);
+                }
+                st_shared_v4(ebuf[0] + off, dg[0], dg[1], dg[2], dg[3]);
+                st_shared_v4(ebuf[1] + off, du[0], du[1], du[2], du[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_4d(&tmC, ebuf[0], ccol, 0, row0, g);
+              tma_store_4d(&tmC, ebuf[1], ccol, 1, row0, g);
+              bulk_commit();
+            }
           } else {  // kEpiDGelu
             const uint32_t cb = ecount & 1u, nb2 = cb ^ 1u;
             if (j + 1 < nch) {
@@ -491,7 +645,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     // drain: Y loads still in flight (only after an abort), then the stores
-    if (EPI == kEpiDGelu) {
+    if (LOADS_Y) {
       for (int b = 0; b < 2; ++b)
         if (ypend & (1u << b)) mbar_wait(ybar[b], (yph >> b) & 1u, wdrain);
     }
@@ -538,13 +692,29 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
   if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu>();
   if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore>();
   if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU>();
+  if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
   return nullptr;
 }
 
 bool operand_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
+  const uint32_t r = o.mn_major ? static_cast<uint32_t>(BK) : rows;
+  if (o.parts == 2) {  // [d2][d1][2][d0]: the part is the second coordinate
+    const uint64_t dims[4] = {static_cast<uint64_t>(o.d0), 2u, static_cast<uint64_t>(o.d1),
+                              static_cast<uint64_t>(o.d2)};
+    const uint32_t box[4] = {64u, 1u, r, 1u};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, o.ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   const uint64_t dims[3] = {static_cast<uint64_t>(o.d0), static_cast<uint64_t>(o.d1), static_cast<uint64_t>(o.d2)};
-  const uint32_t box[3] = {64u, o.mn_major ? static_cast<uint32_t>(BK) : rows, 1u};
+  const uint32_t box[3] = {64u, r, 1u};
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o.ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// [G][M][2][N] output or auxiliary tensor of the gated epilogues, 32 x 64 boxes
+bool two_part_map(CUtensorMap* m, const void* ptr, int64_t N, int64_t M, int G) {
+  const uint64_t dims[4] = {static_cast<uint64_t>(N), 2u, static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
+  const uint32_t box[4] = {64u, 1u, 32u, 1u};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pair per tile
@@ -563,10 +733,16 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (ldc != N && (N % 64)) return 1;  // a partial last chunk would not be clipped at N
   if (epi == kEpiSplit && ((extra.split_cols % 64) || extra.lo_off < N || extra.lo_off + extra.split_cols > ldc))
     return 1;
+  const bool gated = epi == kEpiSwiGLU || epi == kEpiDSwiGLU;
+  if (gated && ldc != N) return 1;
+  if ((epi == kEpiSwiGLU) != (B.parts == 2) || A.parts != 1) return 1;
+  if (epi == kEpiSwiGLU && !B.mn_major) return 1;
+  if (epi == kEpiDSwiGLU && !Yaux) return 1;
+  const int64_t tile_n = epi == kEpiSwiGLU ? BN / 2 : BN;
   const int sms = device_sm_count();
   if (sms <= 0) return 2;
   // pair tiles when there are enough 256 x 256 tiles to give every SM pair work
-  const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + BN - 1) / BN);
+  const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
   bool pair = g_tiling_mode == 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
   if (sms < 2) pair = false;
   KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
@@ -576,8 +752,14 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (!operand_map(&ta, A, a_rows) || !operand_map(&tb, B, b_rows)) return 2;
   const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
   const uint32_t cbox[3] = {64u, 32u, 1u};
-  if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
-  if (Yaux) {
+  if (epi == kEpiDSwiGLU) {
+    if (!two_part_map(&tc, C, N, M, G)) return 2;
+  } else if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B)) {
+    return 2;
+  }
+  if (Yaux && gated) {
+    if (!two_part_map(&ty, Yaux, N, M, G)) return 2;
+  } else if (Yaux) {
     if (!encode_tmap(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, Yaux, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
       return 2;
   } else {
@@ -590,7 +772,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.S = S;
   p.kb_per_seg = static_cast<int>((Ks + BK - 1) / BK);
   p.tiles_m = static_cast<int>((M + (pair ? 255 : 127)) / (pair ? 256 : 128));
-  p.tiles_n = static_cast<int>((N + BN - 1) / BN);
+  p.tiles_n = static_cast<int>((N + tile_n - 1) / tile_n);
   p.a_zg = A.zg;
   p.a_zs = A.zs;
   p.b_zg = B.zg;

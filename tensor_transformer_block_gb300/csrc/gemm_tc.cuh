@@ -27,6 +27,12 @@ enum GemmEpi : int {
   kEpiDGelu = 2,  // C = bf16(acc * GeLU_tanh'(Yin)), Yin read through a TMA map
   kEpiSplit = 3,  // C = bf16(acc); for columns < split_cols also the residual
                   // bf16(acc - bf16(acc)) at column + lo_off of the same row
+  // Gated (SwiGLU) MLP.  B is a two-part operand [G][K][2][N] (gate columns, then
+  // up columns); one tile computes 128 output columns n: the MMA's 256 accumulator
+  // columns hold gate(n) in 0..127 and up(n) in 128..255.
+  kEpiSwiGLU = 4,   // C = bf16(silu(gate) * up); optionally Yaux [G][M][2][N] = bf16(gate), bf16(up)
+  kEpiDSwiGLU = 5,  // Yaux [G][M][2][N] holds G, U; C [G][M][2][N] gets
+                    // C(.,0,.) = bf16(acc * U * silu'(G)), C(.,1,.) = bf16(acc * silu(G))
 };
 
 struct GemmShape {
@@ -50,10 +56,12 @@ struct GemmOperand {
   int64_t d0, d1, d2;
   bool mn_major;
   int zg, zs;
+  int parts = 1;  // 2: the tensor is [d2][d1][2][d0] (kEpiSwiGLU's B: gate, up)
 };
 
 // Host launcher (gemm_tc.cu).  C and Yaux are [G][M][ldc] bf16 tensors of which
-// columns 0..N-1 are computed (ldc = 0 means ldc = N).
+// columns 0..N-1 are computed (ldc = 0 means ldc = N); for the gated epilogues
+// the two-part tensors are [G][M][2][N] and ldc must be 0.
 struct GemmExtra {
   int64_t ldc = 0;
   int64_t split_cols = 0;  // kEpiSplit

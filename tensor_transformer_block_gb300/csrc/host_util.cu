@@ -75,7 +75,9 @@ const char* const kKindNames[kNumKernelKinds] = {
     "mlp.bwd_dW1_gemm", "mlp.bwd_dX_row_gemm_shard_sum", "mlp.f32_fc1_col_gemm_gelu", "mlp.f32_fc2_row_gemm",
     "attn.qkv_col_gemm", "attn.core_fwd", "attn.out_row_gemm_shard_sum", "attn.bwd_dO_gemm", "attn.bwd_dWo_gemm",
     "attn.bwd_dsum", "attn.bwd_core_dkdv", "attn.bwd_core_dq", "attn.bwd_dWqkv_gemm",
-    "attn.bwd_dX_row_gemm_shard_sum", "debug.timeout_probe"};
+    "attn.bwd_dX_row_gemm_shard_sum", "gmlp.fc1_col_gemm_swiglu", "gmlp.fc2_row_gemm_shard_sum",
+    "gmlp.bwd_dA_gemm_dswiglu", "gmlp.bwd_dWd_gemm", "gmlp.bwd_dWgu_gemm", "gmlp.bwd_dX_row_gemm_shard_sum",
+    "debug.timeout_probe"};
 
 struct Slot {
   int kind;

@@ -44,6 +44,12 @@ enum KernelKind : int {
   kKAttnDq,         // dQ per query block
   kKAttnDwqkv,      // dWqkv_i = X^T dQKV_i
   kKAttnDx,         // dX = sum_i dQKV_i Wqkv_i^T
+  kKGmlpFc1,        // [G_i U_i] = X Wgu_i, A_i = silu(G_i) * U_i
+  kKGmlpFc2,        // Z = sum_i A_i Wd_i
+  kKGmlpDswiglu,    // dA_i = dZ Wd_i^T -> dG_i, dU_i
+  kKGmlpDwd,        // dWd_i = A_i^T dZ
+  kKGmlpDwgu,       // dWgu_i = X^T [dG_i dU_i]
+  kKGmlpDx,         // dX = sum_i [dG_i dU_i] Wgu_i^T
   kKProbe,          // timeout probe
   kNumKernelKinds
 };

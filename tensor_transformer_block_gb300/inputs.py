@@ -4,7 +4,8 @@ tests/benchmark and by the fp64 oracle.
 This module draws random numbers and arranges them in the shard-major layouts of
 the boundary; it contains none of the block's arithmetic.  Draws are fp32 normals
 from a CPU ``torch.Generator`` seeded once, in a fixed order (MLP: X, W1, W2, dZ;
-attention: X, Wqkv, Wo, dZ; layer: X, Wqkv, Wo, W1, W2, dZ), scaled by the stated
+gated MLP: X, W_gate, W_up, W_down, dZ; attention: X, Wqkv, Wo, dZ; layer: X, Wqkv,
+Wo, W1, W2, dZ), scaled by the stated
 standard deviation and cast to the workload's dtype once.  The GPU and the oracle
 then consume the identical values (the oracle upcasts them to float64).
 
@@ -12,6 +13,9 @@ Weights are drawn unsharded in the pages' [in x out] orientation and then cut th
 way the pages cut them:
   * W1 [h x f] -> W1s [N][h][f/N]           (column split)
   * W2 [f x h] -> W2s [N][f/N][h]           (row split; bit-identical to W2)
+  * W_gate, W_up [h x f] -> Wgus [N][h][2][f/N]  (both split by columns; shard i
+    holds its gate columns, then the same columns of W_up)
+  * W_down [f x h] -> Wds [N][f/N][h]       (row split)
   * Wqkv [h x 3*H*d] (Q heads | K heads | V heads) -> [N][h][3][H/N][d]
   * Wo [H*d x h] -> [N][H/N*d][h]           (row split by head)
 """
@@ -21,7 +25,7 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "mlp_inputs", "attn_inputs", "layer_inputs",
+__all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", "layer_inputs",
            "split_columns", "split_rows", "split_qkv_heads"]
 
 
@@ -29,7 +33,7 @@ __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "attn_inputs", "layer_inputs",
 class Workload:
     """One of the synthetic workloads the block is checked and measured on."""
     name: str
-    kind: str            # "mlp", "attn" or "layer"
+    kind: str            # "mlp", "gmlp" (gated MLP), "attn" or "layer"
     dtype: str           # "f32" or "bf16"
     backward: bool
     T: int = 0           # tokens = B*S
@@ -49,8 +53,8 @@ class Workload:
         return {k: getattr(self, k) for k in self.__dataclass_fields__}
 
 
-# The five workloads: MLP fp32 forward; MLP bf16 fwd+bwd (small and h=4096);
-# attention bf16 forward; full layer bf16 fwd+bwd.
+# The workloads: MLP fp32 forward; MLP bf16 fwd+bwd (small and h=4096);
+# attention bf16 forward; full layer bf16 fwd+bwd; gated MLP bf16 fwd+bwd.
 WORKLOADS = {
     "mlp_f32_T64_h256_f1024_N2": Workload("mlp_f32_T64_h256_f1024_N2", "mlp", "f32", False,
                                           T=64, h=256, f=1024, N=2),
@@ -64,6 +68,8 @@ WORKLOADS = {
     "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
         "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "layer", "bf16", True,
         T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
+    "gmlp_bf16_T8192_h4096_f12288_N8": Workload("gmlp_bf16_T8192_h4096_f12288_N8", "gmlp", "bf16", True,
+                                                T=8192, h=4096, f=12288, N=8),
 }
 
 _DT = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -110,6 +116,24 @@ def mlp_inputs(T: int, h: int, f: int, N: int, dtype: str = "bf16", seed: int = 
     return out
 
 
+def gmlp_inputs(T: int, h: int, f: int, N: int, dtype: str = "bf16", seed: int = 0,
+                x_std: float = 1.0, w_std: float = 0.02, backward: bool = True) -> dict:
+    """Gated MLP: X [T][h], Wgus [N][h][2][f/N], Wds [N][f/N][h] and (if
+    ``backward``) dZ [T][h]; f is the width of each of the gate and up projections."""
+    if N < 1 or f % N:
+        raise ValueError("N must divide f")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (T, h), x_std, dtype)
+    Wg = _draw(gen, (h, f), w_std, dtype)
+    Wu = _draw(gen, (h, f), w_std, dtype)
+    Wd = _draw(gen, (f, h), w_std, dtype)
+    out = {"X": X, "Wgus": torch.stack([split_columns(Wg, N), split_columns(Wu, N)], dim=2).contiguous(),
+           "Wds": split_rows(Wd, N)}
+    if backward:
+        out["dZ"] = _draw(gen, (T, h), 1.0, dtype)
+    return out
+
+
 def attn_inputs(B: int, S: int, h: int, H: int, d: int, N: int, dtype: str = "bf16",
                 seed: int = 0, x_std: float = 1.0, w_std: float = 0.02,
                 backward: bool = True) -> dict:
@@ -148,6 +172,9 @@ def workload_inputs(w: Workload, **overrides) -> dict:
     if p["kind"] == "mlp":
         return mlp_inputs(p["T"], p["h"], p["f"], p["N"], p["dtype"], p["seed"], p["x_std"],
                           p["w_std"], p["backward"])
+    if p["kind"] == "gmlp":
+        return gmlp_inputs(p["T"], p["h"], p["f"], p["N"], p["dtype"], p["seed"], p["x_std"],
+                           p["w_std"], p["backward"])
     if p["kind"] == "attn":
         return attn_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["N"], p["dtype"], p["seed"],
                            p["x_std"], p["w_std"], p["backward"])

@@ -41,17 +41,32 @@ def errors(gpu, ref, floor: float = 0.0) -> dict:
     return {"rel_fro": fro, "col_ratio": col, "finite": bool(np.all(np.isfinite(g)))}
 
 
-def assert_bf16_parity(gpu, ref, name: str = "", floor: float = 0.0) -> dict:
+def assert_bf16_parity(gpu, ref, name: str = "", floor: float = 0.0, col_tol: float = BF16_COL_MAXABS) -> dict:
     """North-star criteria for bf16 outputs (floor = 0): rel Frobenius <= 5e-3 and
     per-column max-abs <= 2e-2 x column RMS.  ``floor`` adds floor x |oracle| per
     element: the bf16 storage floor of outputs that pass through several bf16
-    intermediates (attention); it is stated next to each use."""
+    intermediates (attention); it is stated next to each use.  ``col_tol`` replaces
+    the 2e-2 column bound where a measured storage floor says so (stated at each use)."""
     e = errors(gpu, ref, floor)
     assert e["finite"], f"{name}: non-finite values"
     assert e["rel_fro"] <= BF16_REL_FRO, f"{name}: rel Frobenius {e['rel_fro']:.3e} > {BF16_REL_FRO}"
-    assert e["col_ratio"] <= BF16_COL_MAXABS, (f"{name}: column max-abs/(RMS-scaled bound) {e['col_ratio']:.3e} > "
-                                               f"{BF16_COL_MAXABS} (floor {floor})")
+    assert e["col_ratio"] <= col_tol, (f"{name}: column max-abs/(RMS-scaled bound) {e['col_ratio']:.3e} > "
+                                       f"{col_tol} (floor {floor})")
     return e
+
+
+def bf16_round(x) -> np.ndarray:
+    """x rounded to bf16 (round to nearest even) and back to float64."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def storage_col_tol(rounded, exact) -> float:
+    """Column bound for an output whose inputs pass through bf16 intermediates:
+    twice the column ratio that the oracle itself reaches when those intermediates
+    and the output are rounded to bf16 (``rounded``: the oracle run with its
+    storage hook), and never below the 2e-2 bound."""
+    return max(BF16_COL_MAXABS, 2.0 * errors(bf16_round(rounded), exact)["col_ratio"])
 
 
 def assert_f32_parity(gpu, ref, name: str = "") -> dict:

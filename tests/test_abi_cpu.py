@@ -69,6 +69,22 @@ def test_mlp_validation_before_cuda(lib):
     assert bwd == 3                                     # fp32 backward is not provided
 
 
+def test_gmlp_validation_before_cuda(lib):
+    g = lambda **k: lib.tp_gmlp_fwd(k.get("dt", 1), k.get("T", 64), k.get("h", 256), k.get("f", 1024),
+                                    k.get("N", 2), k.get("X", 16), 16, 16, None, None, 16, k.get("ws", None),
+                                    k.get("wsb", 0), None)
+    assert g(N=3, f=1000) == 2                          # N does not divide f
+    assert g(dt=0) == 3                                 # bf16 only
+    assert g(h=250) == 2
+    assert g(X=None) == 1
+    assert g(X=8) == 7
+    assert g() == 4                                     # A_save NULL needs a workspace
+    assert tp.tp_gmlp_workspace_bytes(tp.TP_BF16, 64, 256, 1024, 2) == 2 * 64 * 1024 * 2
+    assert tp.tp_gmlp_workspace_bytes(tp.TP_F32, 64, 256, 1024, 2) == 0
+    bwd = lib.tp_gmlp_bwd(1, 64, 256, 1024, 2, 16, 16, 16, None, 16, 16, 16, 16, 16, 256, 1 << 30, None)
+    assert bwd == 1                                     # GU_save is required
+
+
 def test_attention_validation_before_cuda(lib):
     f = lambda **k: lib.tp_attn_fwd(k.get("dt", 1), k.get("B", 2), k.get("S", 128), k.get("h", 512),
                                     k.get("H", 8), k.get("d", 64), k.get("N", 2), 1, k.get("X", 16), 16, 16,

@@ -497,3 +497,39 @@ def test_gated_mlp_backward_vs_autograd_and_fd():
             lm = loss()
             arr[idx] = old
             assert abs((lp - lm) / (2 * eps) - grad[idx]) < 1e-6 * max(1.0, abs(grad[idx]))
+
+
+def test_gated_mlp_weight_column_restriction():
+    X, Wg, Wu, Wd, Wgus, Wds, dZ = _gmlp_inputs(9, 8, 12, 3, seed=5)
+    g = O.gated_mlp_backward(X, Wgus, Wds, dZ)
+    cols = np.array([0, 3, 4, 11])
+    r = O.gated_mlp_backward_weight_columns(X, Wgus, Wds, dZ, cols)
+    dWg = np.concatenate([g["dWgus"][i, :, 0, :] for i in range(3)], axis=1)
+    dWu = np.concatenate([g["dWgus"][i, :, 1, :] for i in range(3)], axis=1)
+    assert rel(r["dWg_cols"], dWg[:, cols]) < 1e-13
+    assert rel(r["dWu_cols"], dWu[:, cols]) < 1e-13
+    assert rel(r["dWd_rows"], O.stack_rows(g["dWds"])[cols, :]) < 1e-13
+
+
+def test_gated_mlp_store_hook():
+    """The storage hook: the identity reproduces the exact gradients bit for bit, and
+    a rounding hook touches exactly the five stored intermediates (gate, up, A, dG,
+    dU), whose rounding moves the gradients by about the rounding's own size."""
+    X, Wg, Wu, Wd, Wgus, Wds, dZ = _gmlp_inputs(16, 8, 12, 3, seed=9)
+    exact = O.gated_mlp_backward(X, Wgus, Wds, dZ)
+    same = O.gated_mlp_backward(X, Wgus, Wds, dZ, store=lambda x: x)
+    for k in exact:
+        assert np.array_equal(exact[k], same[k]), k
+    seen = []
+    O.gated_mlp_backward(X, Wgus, Wds, dZ, store=lambda x: seen.append(x.shape) or x)
+    assert sorted(seen) == sorted([(16, 12)] * 5)
+    q = lambda x: np.round(x * 2.0 ** 10) / 2.0 ** 10     # a coarse fixed-point storage
+    rounded = O.gated_mlp_backward(X, Wgus, Wds, dZ, store=q)
+    for k in exact:
+        d = rel(rounded[k], exact[k])
+        assert 0 < d < 1e-2, (k, d)
+    cols = np.array([1, 5, 11])
+    rc = O.gated_mlp_backward_weight_columns(X, Wgus, Wds, dZ, cols, store=q)
+    dWg = np.concatenate([rounded["dWgus"][i, :, 0, :] for i in range(3)], axis=1)
+    assert rel(rc["dWg_cols"], dWg[:, cols]) < 1e-13
+    assert rel(rc["dWd_rows"], O.stack_rows(rounded["dWds"])[cols, :]) < 1e-13
