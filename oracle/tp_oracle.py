@@ -53,6 +53,7 @@ __all__ = [
     "mlp_backward_weight_columns", "attention_forward_rows",
     "silu", "silu_grad", "gated_mlp_forward", "gated_mlp_backward", "gated_mlp_forward_sharded",
     "gated_mlp_backward_weight_columns",
+    "LN_EPS", "layer_norm", "layer_norm_backward", "prenorm_layer_forward", "prenorm_layer_backward",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -553,3 +554,67 @@ def gated_mlp_backward_weight_columns(X, Wgus, Wds, dZ, cols, store=None) -> dic
     dA = matmul(dZ, Wd.T)
     return {"dWg_cols": matmul(X.T, st(dA * U * silu_grad(G))), "dWu_cols": matmul(X.T, st(dA * silu(G))),
             "dWd_rows": matmul(A.T, dZ)}
+
+
+# --------------------------------------------------------------------------
+# LayerNorm and residuals around the two blocks
+# --------------------------------------------------------------------------
+LN_EPS = 1e-5  # the pages leave epsilon open ("a very small value"); 1e-5 is the reading taken
+
+
+def layer_norm(x, gamma, beta, eps: float = LN_EPS) -> dict:
+    """Per row (one hidden state of d_model = h values): mu = mean(h_i),
+    sigma^2 = mean((h_i - mu)^2), h_hat = (h - mu) / sqrt(sigma^2 + eps),
+    h' = gamma * h_hat + beta (zouht 张量并行 §2.2.2, LayerNorm).  Returns y = h'
+    and the per-row mean and 1 / sqrt(sigma^2 + eps) a backward needs."""
+    x = _f64(x)
+    mu = x.mean(axis=1)
+    var = ((x - mu[:, None]) ** 2).mean(axis=1)
+    rstd = 1.0 / np.sqrt(var + eps)
+    xhat = (x - mu[:, None]) * rstd[:, None]
+    return {"y": xhat * _f64(gamma)[None, :] + _f64(beta)[None, :], "mean": mu, "rstd": rstd}
+
+
+def layer_norm_backward(x, gamma, dy, eps: float = LN_EPS) -> dict:
+    """Gradients of <dy, layer_norm(x)["y"]>.  The pages give no backward; by the
+    chain rule through the definition above, with g = dy * gamma and h the row
+    length: dx = rstd (g - mean(g) - h_hat mean(g h_hat)) per row,
+    dgamma = sum over rows of dy * h_hat, dbeta = sum over rows of dy."""
+    x, dy = _f64(x), _f64(dy)
+    f = layer_norm(x, np.ones(x.shape[1]), np.zeros(x.shape[1]), eps)
+    xhat, rstd = f["y"], f["rstd"]
+    g = dy * _f64(gamma)[None, :]
+    dx = rstd[:, None] * (g - g.mean(axis=1, keepdims=True) - xhat * (g * xhat).mean(axis=1, keepdims=True))
+    return {"dx": dx, "dgamma": (dy * xhat).sum(axis=0), "dbeta": dy.sum(axis=0)}
+
+
+def prenorm_layer_forward(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, B: int, S: int,
+                          causal: bool = True, eps: float = LN_EPS) -> dict:
+    """The layer with LayerNorm and residuals in the replicated (non-TP) region
+    (zouht 张量并行 §2.2.2; sunjinbo 并行方式 §SP: LayerNorm, dropout and the
+    residual sit outside the tensor-parallel blocks).  The pages give no placement;
+    the reading taken is the pre-norm layer, dropout off:
+        H1 = X + Attn(LN1(X)),   Z = H1 + MLP(LN2(H1))."""
+    X = _f64(X)
+    l1 = layer_norm(X, ln1_g, ln1_b, eps)
+    a = attention_forward(l1["y"], Wqkv, Wo, B, S, causal)
+    H1 = X + a["Z"]
+    l2 = layer_norm(H1, ln2_g, ln2_b, eps)
+    m = mlp_forward(l2["y"], W1s, W2s)
+    return {"Z": H1 + m["Z"], "H1": H1, "LN1": l1, "LN2": l2, "attn": a, "mlp": m}
+
+
+def prenorm_layer_backward(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, dZ, B: int, S: int,
+                           causal: bool = True, eps: float = LN_EPS) -> dict:
+    """Gradients of <dZ, prenorm_layer_forward(...)["Z"]>: each residual passes its
+    gradient through unchanged and adds the gradient through its block."""
+    dZ = _f64(dZ)
+    f = prenorm_layer_forward(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, B, S, causal, eps)
+    gm = mlp_backward(f["LN2"]["y"], W1s, W2s, dZ)
+    g2 = layer_norm_backward(f["H1"], ln2_g, gm["dX"], eps)
+    dH1 = dZ + g2["dx"]
+    ga = attention_backward(f["LN1"]["y"], Wqkv, Wo, dH1, B, S, causal)
+    g1 = layer_norm_backward(_f64(X), ln1_g, ga["dX"], eps)
+    return {"dX": dH1 + g1["dx"], "dln1_g": g1["dgamma"], "dln1_b": g1["dbeta"], "dWqkv": ga["dWqkv"],
+            "dWo": ga["dWo"], "dln2_g": g2["dgamma"], "dln2_b": g2["dbeta"], "dW1s": gm["dW1s"],
+            "dW2s": gm["dW2s"], "dH1": dH1}

@@ -533,3 +533,107 @@ def test_gated_mlp_store_hook():
     dWg = np.concatenate([rounded["dWgus"][i, :, 0, :] for i in range(3)], axis=1)
     assert rel(rc["dWg_cols"], dWg[:, cols]) < 1e-13
     assert rel(rc["dWd_rows"], O.stack_rows(rounded["dWds"])[cols, :]) < 1e-13
+
+
+# ---------------------------------------------------------------- LayerNorm + residual
+def test_layer_norm_brute_force_and_torch():
+    """The page's three formulas written as loops on a tiny case, and
+    torch.nn.functional.layer_norm (fp64, eps = 1e-5)."""
+    x = RNG.standard_normal((5, 7)) * 3 + 1.5
+    g, b = RNG.standard_normal(7), RNG.standard_normal(7)
+    y = O.layer_norm(x, g, b)["y"]
+    ref = np.zeros_like(x)
+    for t in range(5):
+        mu = sum(x[t]) / 7
+        var = sum((v - mu) ** 2 for v in x[t]) / 7
+        for i in range(7):
+            ref[t, i] = g[i] * (x[t, i] - mu) / math.sqrt(var + 1e-5) + b[i]
+    assert rel(y, ref) < 1e-14
+    tl = torch.nn.functional.layer_norm(torch.from_numpy(x), (7,), torch.from_numpy(g), torch.from_numpy(b), 1e-5)
+    assert rel(y, tl.numpy()) < 1e-14
+
+
+def test_layer_norm_invariants():
+    """With gamma = 1, beta = 0 each output row has mean 0 and variance
+    var / (var + eps); the output ignores a constant added to a row; scaling a row
+    by c changes it only through eps."""
+    x = RNG.standard_normal((6, 64)) * 2
+    one, zero = np.ones(64), np.zeros(64)
+    f = O.layer_norm(x, one, zero)
+    var = x.var(axis=1)
+    assert np.abs(f["y"].mean(axis=1)).max() < 1e-14
+    assert np.allclose(f["y"].var(axis=1), var / (var + 1e-5), rtol=0, atol=1e-13)
+    assert rel(O.layer_norm(x + 7.25, one, zero)["y"], f["y"]) < 1e-13
+    assert rel(O.layer_norm(x * 3.0, one, zero, eps=0.0)["y"], O.layer_norm(x, one, zero, eps=0.0)["y"]) < 1e-13
+
+
+def test_layer_norm_backward_vs_autograd_and_fd():
+    x = RNG.standard_normal((4, 9)) * 2 + 0.5
+    g, b, dy = RNG.standard_normal(9), RNG.standard_normal(9), RNG.standard_normal((4, 9))
+    tx, tg, tb = (torch.from_numpy(a.copy()).requires_grad_(True) for a in (x, g, b))
+    (torch.nn.functional.layer_norm(tx, (9,), tg, tb, 1e-5) * torch.from_numpy(dy)).sum().backward()
+    r = O.layer_norm_backward(x, g, dy)
+    assert rel(r["dx"], tx.grad.numpy()) < 1e-12
+    assert rel(r["dgamma"], tg.grad.numpy()) < 1e-12
+    assert rel(r["dbeta"], tb.grad.numpy()) < 1e-12
+    loss = lambda xx: float((O.layer_norm(xx, g, b)["y"] * dy).sum())
+    fd = np.zeros_like(x)
+    for idx in itertools.product(range(4), range(9)):
+        xp, xm = x.copy(), x.copy()
+        xp[idx] += 1e-6
+        xm[idx] -= 1e-6
+        fd[idx] = (loss(xp) - loss(xm)) / 2e-6
+    assert rel(r["dx"], fd) < 1e-7
+
+
+def _prenorm_inputs(seed=21):
+    B, S, H, d, n, f = 2, 4, 2, 4, 2, 12
+    X, Wq, Wk, Wv, Wo, Wqkv, Wos, dZ = _attn_inputs(B, S, H, d, n, seed=seed)
+    h = X.shape[1]
+    r = np.random.default_rng(seed + 1)
+    W1, W2 = r.standard_normal((h, f)) * 0.3, r.standard_normal((f, h)) * 0.3
+    ln = [r.standard_normal(h) * 0.5 + 1.0, r.standard_normal(h) * 0.1, r.standard_normal(h) * 0.5 + 1.0,
+          r.standard_normal(h) * 0.1]
+    return (B, S, H, d, n, X, Wq, Wk, Wv, Wo, Wqkv, Wos, W1, W2,
+            np.stack(np.split(W1, n, axis=1)), np.stack(np.split(W2, n, axis=0)), ln, dZ)
+
+
+def test_prenorm_layer_vs_torch_autograd():
+    """The pre-norm layer written with torch's own LayerNorm, SDPA and tanh-GeLU
+    (fp64): forward and every gradient."""
+    B, S, H, d, n, X, Wq, Wk, Wv, Wo, Wqkv, Wos, W1, W2, W1s, W2s, ln, dZ = _prenorm_inputs()
+    h = X.shape[1]
+    F = torch.nn.functional
+    t = [torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, Wq, Wk, Wv, Wo, W1, W2, *ln)]
+    tX, tq, tk, tv, to, t1, t2, g1, b1, g2, b2 = t
+    shp = lambda a: a.reshape(B, S, H, d).transpose(1, 2)
+    l1 = F.layer_norm(tX, (h,), g1, b1, 1e-5)
+    o = F.scaled_dot_product_attention(shp(l1 @ tq), shp(l1 @ tk), shp(l1 @ tv), is_causal=True)
+    H1 = tX + o.transpose(1, 2).reshape(B * S, H * d) @ to
+    Z = H1 + F.gelu(F.layer_norm(H1, (h,), g2, b2, 1e-5) @ t1, approximate="tanh") @ t2
+    (Z * torch.from_numpy(dZ)).sum().backward()
+    fw = O.prenorm_layer_forward(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S)
+    assert rel(fw["Z"], Z.detach().numpy()) < 1e-13
+    assert rel(fw["H1"], H1.detach().numpy()) < 1e-13
+    g = O.prenorm_layer_backward(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, dZ, B, S)
+    assert rel(g["dX"], tX.grad.numpy()) < 1e-12
+    q, k, v = O.unpack_qkv(g["dWqkv"])
+    for a, b in ((q, tq), (k, tk), (v, tv)):
+        assert rel(a, b.grad.numpy()) < 1e-12
+    assert rel(O.stack_rows(g["dWo"]), to.grad.numpy()) < 1e-12
+    assert rel(O.concat_columns(g["dW1s"]), t1.grad.numpy()) < 1e-12
+    assert rel(O.stack_rows(g["dW2s"]), t2.grad.numpy()) < 1e-12
+    for name, tt in (("dln1_g", g1), ("dln1_b", b1), ("dln2_g", g2), ("dln2_b", b2)):
+        assert rel(g[name], tt.grad.numpy()) < 1e-12, name
+
+
+def test_prenorm_layer_residual_structure():
+    """Zero output projections make both blocks vanish: Z = H1 = X exactly, and the
+    input gradient is dZ itself (the residual path alone)."""
+    B, S, H, d, n, X, Wq, Wk, Wv, Wo, Wqkv, Wos, W1, W2, W1s, W2s, ln, dZ = _prenorm_inputs(seed=5)
+    fw = O.prenorm_layer_forward(X, ln[0], ln[1], Wqkv, np.zeros_like(Wos), ln[2], ln[3], W1s,
+                                 np.zeros_like(W2s), B, S)
+    assert np.array_equal(fw["Z"], X) and np.array_equal(fw["H1"], X)
+    g = O.prenorm_layer_backward(X, ln[0], ln[1], Wqkv, np.zeros_like(Wos), ln[2], ln[3], W1s,
+                                 np.zeros_like(W2s), dZ, B, S)
+    assert np.array_equal(g["dX"], dZ)
