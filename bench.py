@@ -52,7 +52,7 @@ def kernel_flops(w) -> dict:
     """Algorithmic flops per launch of each kernel kind of the workload."""
     T, h, f = w.T, w.h, w.f
     out = {}
-    if w.kind in ("mlp", "layer"):
+    if w.kind in ("mlp", "layer", "lnlayer"):
         g = 2.0 * T * h * f
         out.update({"mlp.fc1_col_gemm_gelu": g, "mlp.fc2_row_gemm_shard_sum": g, "mlp.bwd_dA_gemm_dgelu": g,
                     "mlp.bwd_dW2_gemm": g, "mlp.bwd_dW1_gemm": g, "mlp.bwd_dX_row_gemm_shard_sum": g,
@@ -62,7 +62,7 @@ def kernel_flops(w) -> dict:
         out.update({"gmlp.fc1_col_gemm_swiglu": 2 * g, "gmlp.fc2_row_gemm_shard_sum": g,
                     "gmlp.bwd_dA_gemm_dswiglu": g, "gmlp.bwd_dWd_gemm": g, "gmlp.bwd_dWgu_gemm": 2 * g,
                     "gmlp.bwd_dX_row_gemm_shard_sum": 2 * g})
-    if w.kind in ("attn", "layer"):
+    if w.kind in ("attn", "layer", "lnlayer"):
         Hd = w.H * w.d
         pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d  # (causal half) x d
         out.update({"attn.qkv_col_gemm": 2.0 * T * h * 3 * Hd, "attn.core_fwd": 2.0 * pairs,
@@ -76,11 +76,11 @@ def kernel_flops(w) -> dict:
 def step_flops(w) -> float:
     T, h, f = w.T, w.h, w.f
     tot = 0.0
-    if w.kind in ("mlp", "layer"):
+    if w.kind in ("mlp", "layer", "lnlayer"):
         tot += (12.0 if w.backward else 4.0) * T * h * f
     if w.kind == "gmlp":
         tot += (18.0 if w.backward else 6.0) * T * h * f
-    if w.kind in ("attn", "layer"):
+    if w.kind in ("attn", "layer", "lnlayer"):
         Hd = w.H * w.d
         core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
         tot += 8.0 * T * h * Hd + core
@@ -99,6 +99,10 @@ def describe(w) -> str:
     if w.kind == "attn":
         return (f"self-attention block fwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
                 f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
+    if w.kind == "lnlayer":
+        return (f"pre-norm layer (LN, attention, residual, LN, MLP, residual) fwd+bwd, {w.dtype}, B={w.B} x "
+                f"S={w.S}, h={w.h}, {w.H} heads x d={w.d}, f={w.f}, causal, N={w.N} logical shards; LayerNorm and "
+                f"residual adds not counted in the flops")
     return (f"attention + MLP layer fwd+bwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
             f"f={w.f}, causal, N={w.N} logical shards")
 
@@ -205,6 +209,11 @@ def oracle_step(w, inp_np: dict, rows: int) -> float:
     X = inp_np["X"][:rows]
     if w.kind == "attn":
         O.attention_forward(X, inp_np["Wqkv"], inp_np["Wo"], 1, rows, w.causal)
+    elif w.kind == "lnlayer":
+        args = (X, inp_np["ln1_g"], inp_np["ln1_b"], inp_np["Wqkv"], inp_np["Wo"], inp_np["ln2_g"], inp_np["ln2_b"],
+                inp_np["W1s"], inp_np["W2s"])
+        O.prenorm_layer_forward(*args, 1, rows, True)
+        O.prenorm_layer_backward(*args, inp_np["dZ"][:rows], 1, rows, True)
     else:
         O.layer_forward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["W1s"], inp_np["W2s"], 1, rows, True)
         O.layer_backward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["W1s"], inp_np["W2s"], inp_np["dZ"][:rows], 1,
@@ -324,6 +333,13 @@ def run_gpu(args, w) -> None:
         buf["dWgus"] = torch.empty_like(d["Wgus"])
         buf["dWds"] = torch.empty_like(d["Wds"])
         buf["gws"] = block.workspace(tp.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
+    if w.kind == "lnlayer":
+        p = {k: d[k] for k in ("ln1_g", "ln1_b", "Wqkv", "Wo", "ln2_g", "ln2_b", "W1s", "W2s")}
+        buf["save"] = block.workspace(tp.tp_layer_save_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
+        buf["lws"] = block.workspace(tp.tp_layer_workspace_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
+        buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["grads"] = {"dX": torch.empty(T, h, dtype=torch.bfloat16, device=dev),
+                        **{"d" + k: torch.empty_like(v) for k, v in p.items()}}
     if w.kind in ("attn", "layer"):
         hN = w.H // N
         buf["QKV"] = torch.empty(N, T, tp.QKV_PLANES * hN * w.d, dtype=torch.bfloat16, device=dev)
@@ -350,6 +366,14 @@ def run_gpu(args, w) -> None:
                 tp.tp_gmlp_bwd(dt, T, h, f, N, X, d["Wgus"], d["Wds"], buf["GU"], buf["A"], dZ, buf["dX"],
                                buf["dWgus"], buf["dWds"], buf["gws"], stream)
             return buf["Z"], buf["dX"] if w.backward else None
+        if w.kind == "lnlayer":
+            gr = buf["grads"]
+            tp.tp_layer_fwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, 1e-5, X, p["ln1_g"], p["ln1_b"], p["Wqkv"],
+                            p["Wo"], p["ln2_g"], p["ln2_b"], p["W1s"], p["W2s"], buf["save"], buf["Z"], stream)
+            tp.tp_layer_bwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"],
+                            p["W1s"], p["W2s"], buf["save"], dZ, gr["dX"], gr["dln1_g"], gr["dln1_b"], gr["dWqkv"],
+                            gr["dWo"], gr["dln2_g"], gr["dln2_b"], gr["dW1s"], gr["dW2s"], buf["lws"], stream)
+            return buf["Z"], gr["dX"]
         if w.kind == "attn":
             tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
                            buf["LSE"], buf["H"], buf["aws"], stream)
@@ -364,7 +388,8 @@ def run_gpu(args, w) -> None:
         return buf["Z"], buf["dXa"]
 
     # L2: flush between steps unless one step's working set is far above L2
-    work_bytes = sum(t.numel() * t.element_size() for t in list(d.values()) + list(buf.values()))
+    work_bytes = sum(t.numel() * t.element_size() for t in list(d.values()) + list(buf.values())
+                     if isinstance(t, torch.Tensor))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if work_bytes < 4 * (129 << 20) else None
 
     def barrier():
@@ -436,7 +461,7 @@ def run_gpu(args, w) -> None:
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
-    if w.kind in ("mlp", "gmlp", "layer", "attn"):
+    if w.kind in ("mlp", "gmlp", "layer", "lnlayer", "attn"):
         hX = inp["X"].pin_memory()
         hdZ = inp["dZ"].pin_memory() if "dZ" in inp and w.backward else None
         dX_in = torch.empty_like(d["X"])

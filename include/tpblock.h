@@ -228,6 +228,72 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
                 const void* dZ, void* dX, void* dWqkv, void* dWo,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------ LayerNorm and residuals */
+
+/* The pages keep LayerNorm, dropout and the residual connections outside the
+ * tensor-parallel blocks, replicated on every shard (io.zouht.com 张量并行 §2.2.2;
+ * sunjinbo.space 并行方式 §SP).  LayerNorm of one hidden state h of d_model values
+ * (io.zouht.com 张量并行 §2.2.2, LayerNorm):
+ *   mu = mean_i h_i,  sigma^2 = mean_i (h_i - mu)^2,
+ *   h_hat = (h - mu) / sqrt(sigma^2 + eps),  h' = gamma * h_hat + beta.
+ * Rows are bf16 [T][h] with h a multiple of 8 and h <= 16384; gamma, beta bf16 [h];
+ * statistics fp32, computed on the device in fp32. */
+
+/* Scratch of tp_layernorm_bwd (fp32 partial column sums).  0 for invalid sizes. */
+TP_API size_t tp_layernorm_workspace_bytes(int dtype, int64_t T, int64_t h);
+
+/* Y = LayerNorm(X) per row; mean [T] and rstd [T] = 1 / sqrt(sigma^2 + eps) are
+ * written for the backward.  eps >= 0 (TP_ERR_SHAPE otherwise). */
+TP_API int tp_layernorm_fwd(int dtype, int64_t T, int64_t h, float eps,
+                            const void* X, const void* gamma, const void* beta,
+                            void* Y, float* mean, float* rstd, void* stream);
+
+/* Backward of Y = LayerNorm(X) for an upstream dY, plus an optional residual
+ * gradient dR [T][h] (NULL = none).  The pages give no backward; by the chain
+ * rule, with g = dY * gamma and x_hat = (X - mean) * rstd per row:
+ *   dX = rstd (g - mean(g) - x_hat mean(g x_hat)) + dR
+ *   dgamma = sum over rows of dY * x_hat,  dbeta = sum over rows of dY   (bf16 [h])
+ * The column sums are finished from per-CTA fp32 partials in a fixed order (the
+ * result does not vary run to run).  mean, rstd: what tp_layernorm_fwd wrote. */
+TP_API int tp_layernorm_bwd(int dtype, int64_t T, int64_t h,
+                            const void* X, const void* gamma, const float* mean, const float* rstd,
+                            const void* dY, const void* dR, void* dX, void* dgamma, void* dbeta,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Bytes of the ``save`` buffer tp_layer_fwd fills and tp_layer_bwd reads, and of
+ * tp_layer_bwd's scratch.  0 for invalid sizes (the attention and MLP rules
+ * above, plus the LayerNorm rules, apply). */
+TP_API size_t tp_layer_save_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N);
+TP_API size_t tp_layer_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N);
+
+/* Pre-norm transformer layer forward (bf16): the two tensor-parallel blocks with
+ * LayerNorm and a residual connection around each, dropout off.  The pages do not
+ * fix the order; the pre-norm placement is the reading taken:
+ *   H1 = X + Attn(LN1(X))      (the residual is added in the output projection's
+ *                               epilogue, after the shard sum)
+ *   Z  = H1 + MLP(LN2(H1))     (likewise in the second MLP GEMM's epilogue)
+ * Attn and MLP are exactly tp_attn_fwd and tp_mlp_fwd.  ``save`` (256-byte aligned,
+ * tp_layer_save_bytes) receives LN1(X), H1, LN2(H1), their row statistics and the
+ * blocks' saved tensors; its layout is private to the library. */
+TP_API int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N,
+                        int causal, float eps,
+                        const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                        const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s,
+                        void* save, size_t save_bytes, void* Z, void* stream);
+
+/* Pre-norm layer backward for an upstream dZ: the MLP block's backward on LN2(H1),
+ * dH1 = dZ + LN2'(.), the attention block's backward with upstream dH1, then
+ * dX = dH1 + LN1'(.).  Every gradient is written: dX [T][h], dln1_g, dln1_b,
+ * dln2_g, dln2_b [h], dWqkv, dWo, dW1s, dW2s in the forward's layouts.  ``save``
+ * is what tp_layer_fwd wrote for the same inputs; ws: tp_layer_workspace_bytes. */
+TP_API int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                        const void* X, const void* ln1_g, const void* Wqkv, const void* Wo,
+                        const void* ln2_g, const void* W1s, const void* W2s,
+                        const void* save, size_t save_bytes, const void* dZ,
+                        void* dX, void* dln1_g, void* dln1_b, void* dWqkv, void* dWo,
+                        void* dln2_g, void* dln2_b, void* dW1s, void* dW2s,
+                        void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /* Launches one block whose single thread waits on a shared-memory barrier that

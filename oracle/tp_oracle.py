@@ -54,6 +54,7 @@ __all__ = [
     "silu", "silu_grad", "gated_mlp_forward", "gated_mlp_backward", "gated_mlp_forward_sharded",
     "gated_mlp_backward_weight_columns",
     "LN_EPS", "layer_norm", "layer_norm_backward", "prenorm_layer_forward", "prenorm_layer_backward",
+    "prenorm_layer_forward_rows",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -618,3 +619,23 @@ def prenorm_layer_backward(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, dZ
     return {"dX": dH1 + g1["dx"], "dln1_g": g1["dgamma"], "dln1_b": g1["dbeta"], "dWqkv": ga["dWqkv"],
             "dWo": ga["dWo"], "dln2_g": g2["dgamma"], "dln2_b": g2["dbeta"], "dW1s": gm["dW1s"],
             "dW2s": gm["dW2s"], "dH1": dH1}
+
+
+def prenorm_layer_forward_rows(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, B: int, S: int, rows,
+                               causal: bool = True, eps: float = LN_EPS, store=None) -> dict:
+    """H1[rows] and Z[rows] of :func:`prenorm_layer_forward`: LayerNorm, the MLP and
+    the residuals act row by row; only the attention needs the other rows (its
+    keys and values), which :func:`attention_forward_rows` provides.
+
+    ``store`` (default: none) is applied to the tensors a layer implementation keeps
+    in memory between its kernels outside the attention core (LN1(X), H1, LN2(H1),
+    the MLP activation); the tests pass a rounding to the storage type to measure
+    the error that storage alone causes.  Without it this is the exact definition."""
+    st = store or _keep
+    X = _f64(X)
+    rows = np.asarray(rows, dtype=np.int64)
+    l1 = st(layer_norm(X, ln1_g, ln1_b, eps)["y"])
+    H1 = st(X[rows] + attention_forward_rows(l1, Wqkv, Wo, B, S, rows, causal)["Z"])
+    m = mlp_forward(st(layer_norm(H1, ln2_g, ln2_b, eps)["y"]), W1s, W2s)
+    Z = H1 + (matmul(st(concat_columns(m["A"])), stack_rows(W2s)) if store else m["Z"])
+    return {"H1": H1, "Z": Z}

@@ -45,6 +45,14 @@ _SIGS = {
     "tp_gmlp_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
     "tp_gmlp_fwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
     "tp_gmlp_bwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_layernorm_workspace_bytes": ([i32, i64, i64], sz),
+    "tp_layernorm_fwd": ([i32, i64, i64, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp], i32),
+    "tp_layernorm_bwd": ([i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_layer_save_bytes": ([i32, i64, i64, i64, i32, i32, i64, i32], sz),
+    "tp_layer_workspace_bytes": ([i32, i64, i64, i64, i32, i32, i64, i32], sz),
+    "tp_layer_fwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32, ctypes.c_float] + [vp] * 10 + [sz, vp, vp], i32),
+    "tp_layer_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 8 + [sz] + [vp] * 10 + [vp, sz, vp],
+                     i32),
     "tp_set_gemm_tiling": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
@@ -213,6 +221,65 @@ def tp_gmlp_bwd(dtype, T, h, f, N, X, Wgus, Wds, GU_save, A_save, dZ, dX, dWgus,
         _p(GU_save, "GU_save", dt, 2 * T * f), _p(A_save, "A_save", dt, T * f), _p(dZ, "dZ", dt, T * h),
         _p(dX, "dX", dt, T * h), _p(dWgus, "dWgus", dt, 2 * h * f), _p(dWds, "dWds", dt, f * h),
         wptr, wbytes, _stream(stream)), "tp_gmlp_bwd")
+
+
+# ---------------------------------------------------------------- LayerNorm, pre-norm layer
+def tp_layernorm_workspace_bytes(dtype: int, T: int, h: int) -> int:
+    return load_library().tp_layernorm_workspace_bytes(dtype, T, h)
+
+
+def tp_layernorm_fwd(dtype, T, h, eps, X, gamma, beta, Y, mean, rstd, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    return _check(load_library().tp_layernorm_fwd(
+        dtype, T, h, eps, _p(X, "X", dt, T * h), _p(gamma, "gamma", dt, h), _p(beta, "beta", dt, h),
+        _p(Y, "Y", dt, T * h), _p(mean, "mean", torch.float32, T), _p(rstd, "rstd", torch.float32, T),
+        _stream(stream)), "tp_layernorm_fwd")
+
+
+def tp_layernorm_bwd(dtype, T, h, X, gamma, mean, rstd, dY, dR, dX, dgamma, dbeta, ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    wptr, wbytes = _ws(ws, tp_layernorm_workspace_bytes(dtype, T, h))
+    return _check(load_library().tp_layernorm_bwd(
+        dtype, T, h, _p(X, "X", dt, T * h), _p(gamma, "gamma", dt, h), _p(mean, "mean", torch.float32, T),
+        _p(rstd, "rstd", torch.float32, T), _p(dY, "dY", dt, T * h), _p(dR, "dR", dt, T * h, False),
+        _p(dX, "dX", dt, T * h), _p(dgamma, "dgamma", dt, h), _p(dbeta, "dbeta", dt, h), wptr, wbytes,
+        _stream(stream)), "tp_layernorm_bwd")
+
+
+def tp_layer_save_bytes(dtype, B, S, h, H, d, f, N) -> int:
+    return load_library().tp_layer_save_bytes(dtype, B, S, h, H, d, f, N)
+
+
+def tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N) -> int:
+    return load_library().tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N)
+
+
+def tp_layer_fwd(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+                 save, Z, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    sptr, sbytes = _ws(save, tp_layer_save_bytes(dtype, B, S, h, H, d, f, N))
+    return _check(load_library().tp_layer_fwd(
+        dtype, B, S, h, H, d, f, N, 1 if causal else 0, eps, _p(X, "X", dt, T * h), _p(ln1_g, "ln1_g", dt, h),
+        _p(ln1_b, "ln1_b", dt, h), _p(Wqkv, "Wqkv", dt, 3 * h * H * d), _p(Wo, "Wo", dt, H * d * h),
+        _p(ln2_g, "ln2_g", dt, h), _p(ln2_b, "ln2_b", dt, h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
+        sptr, sbytes, _p(Z, "Z", dt, T * h), _stream(stream)), "tp_layer_fwd")
+
+
+def tp_layer_bwd(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, dZ, dX, dln1_g,
+                 dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    sptr, sbytes = _ws(save, tp_layer_save_bytes(dtype, B, S, h, H, d, f, N))
+    wptr, wbytes = _ws(ws, tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N))
+    return _check(load_library().tp_layer_bwd(
+        dtype, B, S, h, H, d, f, N, 1 if causal else 0, _p(X, "X", dt, T * h), _p(ln1_g, "ln1_g", dt, h),
+        _p(Wqkv, "Wqkv", dt, 3 * h * H * d), _p(Wo, "Wo", dt, H * d * h), _p(ln2_g, "ln2_g", dt, h),
+        _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h), sptr, sbytes, _p(dZ, "dZ", dt, T * h),
+        _p(dX, "dX", dt, T * h), _p(dln1_g, "dln1_g", dt, h), _p(dln1_b, "dln1_b", dt, h),
+        _p(dWqkv, "dWqkv", dt, 3 * h * H * d), _p(dWo, "dWo", dt, H * d * h), _p(dln2_g, "dln2_g", dt, h),
+        _p(dln2_b, "dln2_b", dt, h), _p(dW1s, "dW1s", dt, h * f), _p(dW2s, "dW2s", dt, f * h), wptr, wbytes,
+        _stream(stream)), "tp_layer_bwd")
 
 
 # ---------------------------------------------------------------- attention block

@@ -123,3 +123,65 @@ def attn_backward(X, Wqkv, Wo, QKV, O, LSE, dZ, B_: int, S: int, causal: bool = 
     B.tp_attn_bwd(dt, B_, S, h, H, d, N, causal, X, Wqkv, Wo, QKV, O, LSE, dZ, out["dX"], out["dWqkv"],
                   out["dWo"], ws, stream)
     return out
+
+
+LN_EPS = 1e-5
+
+
+def layernorm_forward(X, gamma, beta, eps: float = LN_EPS, stream=None) -> dict:
+    """Y = gamma * (X - mean) / sqrt(var + eps) + beta per row, with the row statistics."""
+    T, h = X.shape
+    dev = X.device
+    Y = torch.empty_like(X)
+    mean = torch.empty(T, dtype=torch.float32, device=dev)
+    rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    B.tp_layernorm_fwd(_dtype(X), T, h, eps, X, gamma, beta, Y, mean, rstd, stream)
+    return {"Y": Y, "mean": mean, "rstd": rstd}
+
+
+def layernorm_backward(X, gamma, mean, rstd, dY, dR=None, ws=None, stream=None) -> dict:
+    """dX (+ dR), dgamma, dbeta of the LayerNorm whose forward gave mean and rstd."""
+    T, h = X.shape
+    dev = X.device
+    dt = _dtype(X)
+    out = {"dX": torch.empty_like(X), "dgamma": torch.empty_like(gamma), "dbeta": torch.empty_like(gamma)}
+    if ws is None:
+        ws = workspace(B.tp_layernorm_workspace_bytes(dt, T, h), dev)
+    B.tp_layernorm_bwd(dt, T, h, X, gamma, mean, rstd, dY, dR, out["dX"], out["dgamma"], out["dbeta"], ws, stream)
+    return out
+
+
+def prenorm_layer_forward(X, p: dict, B_: int, S: int, causal: bool = True, eps: float = LN_EPS, save=None,
+                          stream=None) -> dict:
+    """H1 = X + Attn(LN1(X)), Z = H1 + MLP(LN2(H1)).  ``p`` holds ln1_g, ln1_b, Wqkv,
+    Wo, ln2_g, ln2_b, W1s, W2s; the returned ``save`` buffer feeds the backward."""
+    N, h, _, hN, d = p["Wqkv"].shape
+    H = N * hN
+    f = N * p["W1s"].shape[2]
+    dt = _dtype(X)
+    if save is None:
+        save = workspace(B.tp_layer_save_bytes(dt, B_, S, h, H, d, f, N), X.device)
+    Z = torch.empty_like(X)
+    B.tp_layer_fwd(dt, B_, S, h, H, d, f, N, causal, eps, X, p["ln1_g"], p["ln1_b"], p["Wqkv"], p["Wo"],
+                   p["ln2_g"], p["ln2_b"], p["W1s"], p["W2s"], save, Z, stream)
+    return {"Z": Z, "save": save}
+
+
+def prenorm_layer_backward(X, p: dict, save, dZ, B_: int, S: int, causal: bool = True, ws=None, stream=None,
+                           out=None) -> dict:
+    N, h, _, hN, d = p["Wqkv"].shape
+    H = N * hN
+    f = N * p["W1s"].shape[2]
+    dt = _dtype(X)
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dln1_g": torch.empty_like(p["ln1_g"]),
+               "dln1_b": torch.empty_like(p["ln1_b"]), "dWqkv": torch.empty_like(p["Wqkv"]),
+               "dWo": torch.empty_like(p["Wo"]), "dln2_g": torch.empty_like(p["ln2_g"]),
+               "dln2_b": torch.empty_like(p["ln2_b"]), "dW1s": torch.empty_like(p["W1s"]),
+               "dW2s": torch.empty_like(p["W2s"])}
+    if ws is None:
+        ws = workspace(B.tp_layer_workspace_bytes(dt, B_, S, h, H, d, f, N), X.device)
+    B.tp_layer_bwd(dt, B_, S, h, H, d, f, N, causal, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"], p["W1s"],
+                   p["W2s"], save, dZ, out["dX"], out["dln1_g"], out["dln1_b"], out["dWqkv"], out["dWo"],
+                   out["dln2_g"], out["dln2_b"], out["dW1s"], out["dW2s"], ws, stream)
+    return out

@@ -12,6 +12,7 @@
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
 #include "host_util.cuh"
+#include "ln.cuh"
 #include "ptx.cuh"
 
 // Device error word: kernels latch bits here (atomicOr); tp_sync_status reads and clears it.
@@ -111,7 +112,7 @@ AttnWs attn_ws(int64_t B, int64_t S, int H, int d) {
 
 extern "C" {
 
-int tp_version(void) { return (0 << 16) | 4; }
+int tp_version(void) { return (0 << 16) | 5; }
 
 const char* tp_status_string(int s) {
   switch (s) {
@@ -156,6 +157,61 @@ int tp_debug_timeout_probe(int64_t timeout_ns, void* stream) {
   tpb::timing_end(slot, static_cast<cudaStream_t>(stream));
   return ok ? TP_OK : TP_ERR_CUDA;
 }
+
+}  // extern "C"
+
+namespace {
+// bf16 MLP forward kernels: a1 then a2.  With ``residual`` (a [T][h] tensor) the
+// row-parallel GEMM's epilogue adds it: Z = residual + sum_i A_i W2_i.
+int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
+                void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st) {
+  const int64_t fN = f / N;
+  // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard)
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKMlpFc1);
+  if (rc) return gemm_status(rc);
+  // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
+  const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opA, opW2, Z, residual, false, T, h, 1,
+                             N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2);
+  return gemm_status(rc);
+}
+
+// Attention forward kernels: a7, a8, a9.  With ``residual`` ([T][h]) the output
+// projection's epilogue adds it: Z = residual + sum_i O_i Wo_i.
+int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X, const void* Wqkv,
+                 const void* Wo, void* QKV, void* Ob, float* LSE, void* Z, const void* residual, unsigned* err,
+                 cudaStream_t st) {
+  const int hN = H / N;
+  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
+  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
+  // writes the bf16 residuals of Q and K as planes 3 and 4 (split-bf16 scores)
+  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opW{Wqkv, 3 * hNd, h, N, true, 1, 0};
+  tpb::GemmExtra split;
+  split.ldc = tpb::kQkvPlanes * hNd;
+  split.split_cols = 2 * hNd;
+  split.lo_off = 3 * hNd;
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, 3 * hNd, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
+  if (rc) return gemm_status(rc);
+  // a8: per-head causal attention
+  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
+  rc = tpb::launch_attn_fwd(ad, QKV, Ob, LSE, err, kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // a9: Z = sum_i O_i Wo_i  (row-parallel, shard sum in the accumulator)
+  const tpb::GemmOperand opO{Ob, hNd, T, N, false, 0, 1};
+  const tpb::GemmOperand opWo{Wo, h, hNd, N, true, 0, 1};
+  rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opO, opWo, Z, residual, false, T, h, 1,
+                             N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut);
+  return gemm_status(rc);
+}
+}  // namespace
+
+extern "C" {
 
 // ------------------------------------------------------------------ MLP block
 size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N) {
@@ -218,17 +274,7 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
     return gemm_status(tpb::launch_gemm_f32(a2, st, tpb::kKMlpF32Fc2));
   }
 
-  // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard)
-  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
-  const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
-  int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKMlpFc1);
-  if (rc) return gemm_status(rc);
-  // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
-  const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
-  const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opA, opW2, Z, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2);
-  return gemm_status(rc);
+  return mlp_fwd_seq(T, h, f, N, X, W1s, W2s, Y_save, Abuf, Z, nullptr, err, st);
 }
 
 int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
@@ -396,32 +442,10 @@ int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int hN = H / N;
-  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
   void* QKV = QKV_save ? QKV_save : static_cast<void*>(wsb);
   void* Ob = O_save ? O_save : static_cast<void*>(wsb + w.qkv);
   float* LSE = LSE_save ? LSE_save : reinterpret_cast<float*>(wsb + w.qkv + w.o);
-
-  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
-  // writes the bf16 residuals of Q and K as planes 3 and 4 (split-bf16 scores)
-  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
-  const tpb::GemmOperand opW{Wqkv, 3 * hNd, h, N, true, 1, 0};
-  tpb::GemmExtra split;
-  split.ldc = tpb::kQkvPlanes * hNd;
-  split.split_cols = 2 * hNd;
-  split.lo_off = 3 * hNd;
-  int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, 3 * hNd, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
-  if (rc) return gemm_status(rc);
-  // a8: per-head causal attention
-  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
-  rc = tpb::launch_attn_fwd(ad, QKV, Ob, LSE, err, kWaitTimeoutNs, st);
-  if (rc) return gemm_status(rc);
-  // a9: Z = sum_i O_i Wo_i  (row-parallel, shard sum in the accumulator)
-  const tpb::GemmOperand opO{Ob, hNd, T, N, false, 0, 1};
-  const tpb::GemmOperand opWo{Wo, h, hNd, N, true, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opO, opWo, Z, nullptr, false, T, h, 1, N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut);
-  return gemm_status(rc);
+  return attn_fwd_seq(B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV, Ob, LSE, Z, nullptr, err, st);
 }
 
 int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
@@ -474,6 +498,194 @@ int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
   const tpb::GemmOperand opWk{Wqkv, 3 * hNd, h, N, false, 0, 1};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, 3 * hNd, err,
                              kWaitTimeoutNs, st, tpb::kKAttnDx);
+  return gemm_status(rc);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------ LayerNorm + residual
+namespace {
+constexpr float kEpsMin = 0.0f;
+
+// The pre-norm layer's saved tensors, carved from the caller's ``save`` buffer in
+// this order (each region 256-byte aligned).
+struct LayerSave {
+  size_t ln1, mean1, rstd1, qkv, o, lse, h1, ln2, mean2, rstd2, y, a, total;
+};
+LayerSave layer_save(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
+  const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  const size_t th = round_up(T * static_cast<size_t>(h) * 2, 256), tv = round_up(T * 4, 256);
+  const AttnWs aw = attn_ws(B, S, H, d);
+  LayerSave L;
+  size_t o = 0;
+  L.ln1 = o;   o += th;
+  L.mean1 = o; o += tv;
+  L.rstd1 = o; o += tv;
+  L.qkv = o;   o += aw.qkv;
+  L.o = o;     o += aw.o;
+  L.lse = o;   o += aw.lse;
+  L.h1 = o;    o += th;
+  L.ln2 = o;   o += th;
+  L.mean2 = o; o += tv;
+  L.rstd2 = o; o += tv;
+  L.y = o;     o += round_up(T * static_cast<size_t>(f) * 2, 256);
+  L.a = o;     o += round_up(T * static_cast<size_t>(f) * 2, 256);
+  L.total = o;
+  return L;
+}
+
+// Backward scratch: [block scratch (attention or MLP, used in turn) | dLN | dH1 | LN partials].
+struct LayerWs {
+  size_t blk, dln, dh1, part, total;
+};
+LayerWs layer_ws(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
+  const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  const size_t th = round_up(T * static_cast<size_t>(h) * 2, 256);
+  const size_t a = attn_ws(B, S, H, d).total, m = round_up(T * static_cast<size_t>(f) * 2, 256);
+  LayerWs w;
+  w.blk = 0;
+  w.dln = a > m ? a : m;
+  w.dh1 = w.dln + th;
+  w.part = w.dh1 + th;
+  w.total = w.part + round_up(tpb::ln_partial_bytes(static_cast<int64_t>(T), h), 256);
+  return w;
+}
+
+int layer_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  int c = attn_shape_check(dtype, B, S, h, H, d, N);
+  if (c != TP_OK) return c;
+  c = mlp_shape_check(dtype, B * S, h, f, N);
+  if (c != TP_OK) return c;
+  return tpb::ln_shape_ok(B * S, h) ? TP_OK : TP_ERR_SHAPE;
+}
+}  // namespace
+
+extern "C" {
+
+size_t tp_layernorm_workspace_bytes(int dtype, int64_t T, int64_t h) {
+  if (dtype != TP_BF16 || !tpb::ln_shape_ok(T, h)) return 0;
+  return round_up(tpb::ln_partial_bytes(T, h), 256);
+}
+
+int tp_layernorm_fwd(int dtype, int64_t T, int64_t h, float eps, const void* X, const void* gamma, const void* beta,
+                     void* Y, float* mean, float* rstd, void* stream) {
+  if (dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (!tpb::ln_shape_ok(T, h) || !(eps >= kEpsMin)) return TP_ERR_SHAPE;
+  if (!X || !gamma || !beta || !Y || !mean || !rstd) return TP_ERR_NULL;
+  if (!al16(X) || !al16(gamma) || !al16(beta) || !al16(Y) || !al16(mean) || !al16(rstd)) return TP_ERR_ALIGN;
+  const int dc = check_device(nullptr);
+  if (dc != TP_OK) return dc;
+  return gemm_status(tpb::launch_ln_fwd(X, gamma, beta, Y, mean, rstd, T, h, eps, static_cast<cudaStream_t>(stream)));
+}
+
+int tp_layernorm_bwd(int dtype, int64_t T, int64_t h, const void* X, const void* gamma, const float* mean,
+                     const float* rstd, const void* dY, const void* dR, void* dX, void* dgamma, void* dbeta, void* ws,
+                     size_t ws_bytes, void* stream) {
+  if (dtype != TP_BF16) return TP_ERR_DTYPE;
+  if (!tpb::ln_shape_ok(T, h)) return TP_ERR_SHAPE;
+  if (!X || !gamma || !mean || !rstd || !dY || !dX || !dgamma || !dbeta) return TP_ERR_NULL;
+  if (!al16(X) || !al16(gamma) || !al16(mean) || !al16(rstd) || !al16(dY) || !al16(dR) || !al16(dX) ||
+      !al16(dgamma) || !al16(dbeta))
+    return TP_ERR_ALIGN;
+  if (!ws || ws_bytes < tp_layernorm_workspace_bytes(dtype, T, h)) return TP_ERR_WORKSPACE;
+  if (!al256(ws)) return TP_ERR_ALIGN;
+  const int dc = check_device(nullptr);
+  if (dc != TP_OK) return dc;
+  return gemm_status(tpb::launch_ln_bwd(X, gamma, mean, rstd, dY, dR, dX, dgamma, dbeta, static_cast<float*>(ws), T,
+                                        h, static_cast<cudaStream_t>(stream)));
+}
+
+size_t tp_layer_save_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  if (layer_check(dtype, B, S, h, H, d, f, N) != TP_OK) return 0;
+  return layer_save(B, S, h, H, d, f).total;
+}
+
+size_t tp_layer_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  if (layer_check(dtype, B, S, h, H, d, f, N) != TP_OK) return 0;
+  return layer_ws(B, S, h, H, d, f).total;
+}
+
+int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal, float eps,
+                 const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                 const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
+                 size_t save_bytes, void* Z, void* stream) {
+  const int sc = layer_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (!(eps >= kEpsMin)) return TP_ERR_SHAPE;
+  if (!X || !ln1_g || !ln1_b || !Wqkv || !Wo || !ln2_g || !ln2_b || !W1s || !W2s || !save || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(ln1_g) || !al16(ln1_b) || !al16(Wqkv) || !al16(Wo) || !al16(ln2_g) || !al16(ln2_b) ||
+      !al16(W1s) || !al16(W2s) || !al16(Z))
+    return TP_ERR_ALIGN;
+  const LayerSave L = layer_save(B, S, h, H, d, f);
+  if (save_bytes < L.total) return TP_ERR_WORKSPACE;
+  if (!al256(save)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* sv = static_cast<char*>(save);
+  const int64_t T = B * S;
+  float* mean1 = reinterpret_cast<float*>(sv + L.mean1);
+  float* rstd1 = reinterpret_cast<float*>(sv + L.rstd1);
+  float* mean2 = reinterpret_cast<float*>(sv + L.mean2);
+  float* rstd2 = reinterpret_cast<float*>(sv + L.rstd2);
+  // LN1(X)
+  int rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st);
+  if (rc) return gemm_status(rc);
+  // H1 = X + Attn(LN1(X)): the residual is added in the output projection's epilogue
+  rc = attn_fwd_seq(B, S, h, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
+                    reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st);
+  if (rc) return rc;
+  // LN2(H1)
+  rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st);
+  if (rc) return gemm_status(rc);
+  // Z = H1 + MLP(LN2(H1)): the residual is added in the second GEMM's epilogue
+  return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st);
+}
+
+int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                 const void* X, const void* ln1_g, const void* Wqkv, const void* Wo, const void* ln2_g,
+                 const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
+                 void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
+                 void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = layer_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !ln1_g || !Wqkv || !Wo || !ln2_g || !W1s || !W2s || !save || !dZ || !dX || !dln1_g || !dln1_b ||
+      !dWqkv || !dWo || !dln2_g || !dln2_b || !dW1s || !dW2s)
+    return TP_ERR_NULL;
+  if (!al16(X) || !al16(ln1_g) || !al16(Wqkv) || !al16(Wo) || !al16(ln2_g) || !al16(W1s) || !al16(W2s) ||
+      !al16(dZ) || !al16(dX) || !al16(dln1_g) || !al16(dln1_b) || !al16(dWqkv) || !al16(dWo) || !al16(dln2_g) ||
+      !al16(dln2_b) || !al16(dW1s) || !al16(dW2s))
+    return TP_ERR_ALIGN;
+  const LayerSave L = layer_save(B, S, h, H, d, f);
+  const LayerWs W = layer_ws(B, S, h, H, d, f);
+  if (save_bytes < L.total || !ws || ws_bytes < W.total) return TP_ERR_WORKSPACE;
+  if (!al256(save) || !al256(ws)) return TP_ERR_ALIGN;
+  const int dc = check_device(nullptr);
+  if (dc != TP_OK) return dc;
+  const char* sv = static_cast<const char*>(save);
+  char* wb = static_cast<char*>(ws);
+  const int64_t T = B * S;
+  const size_t blk = W.dln - W.blk;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* dLN = wb + W.dln;
+  void* dH1 = wb + W.dh1;
+  float* part = reinterpret_cast<float*>(wb + W.part);
+  // MLP block backward on LN2(H1): dLN2 -> dLN
+  int rc = tp_mlp_bwd(dtype, T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, dZ, dLN, dW1s, dW2s, wb + W.blk,
+                      blk, stream);
+  if (rc) return rc;
+  // dH1 = dZ + LN2'(dLN2)   (the residual passes dZ through)
+  rc = tpb::launch_ln_bwd(sv + L.h1, ln2_g, reinterpret_cast<const float*>(sv + L.mean2),
+                          reinterpret_cast<const float*>(sv + L.rstd2), dLN, dZ, dH1, dln2_g, dln2_b, part, T, h, st);
+  if (rc) return gemm_status(rc);
+  // attention block backward on LN1(X) with upstream dH1: dLN1 -> dLN
+  rc = tp_attn_bwd(dtype, B, S, h, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
+                   reinterpret_cast<const float*>(sv + L.lse), dH1, dLN, dWqkv, dWo, wb + W.blk, blk, stream);
+  if (rc) return rc;
+  // dX = dH1 + LN1'(dLN1)
+  rc = tpb::launch_ln_bwd(X, ln1_g, reinterpret_cast<const float*>(sv + L.mean1),
+                          reinterpret_cast<const float*>(sv + L.rstd1), dLN, dH1, dX, dln1_g, dln1_b, part, T, h, st);
   return gemm_status(rc);
 }
 

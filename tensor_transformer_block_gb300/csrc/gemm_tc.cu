@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // output columns per tile: the gated forward spends half the MMA's N on the up part
   constexpr int TILE_N = EPI == kEpiSwiGLU ? BN / 2 : BN;
   constexpr int WARP_COLS = TILE_N / 2;  // output columns per epilogue warp
-  constexpr bool LOADS_Y = EPI == kEpiDGelu || EPI == kEpiDSwiGLU;
+  constexpr bool LOADS_Y = EPI == kEpiDGelu || EPI == kEpiDSwiGLU || EPI == kEpiResidual;
   constexpr int BM = C::BM, STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES;
   constexpr int BAR_FULL = C::BAR_FULL, BAR_EMPTY = C::BAR_EMPTY, BAR_TFULL = C::BAR_TFULL;
   constexpr int BAR_TEMPTY = C::BAR_TEMPTY, BAR_Y = C::BAR_Y, BAR_DRAIN = C::BAR_DRAIN;
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int nch = col0 < p.N ? (p.N - col0 + 63) / 64 : 0;
       if (nch > WARP_COLS / 64) nch = WARP_COLS / 64;
       const bool rows_valid = row0 < p.M && nch > 0;
-      if (EPI == kEpiDGelu && rows_valid) {
+      if ((EPI == kEpiDGelu || EPI == kEpiResidual) && rows_valid) {
         const uint32_t b = ecount & 1u;
         if (lane == 0) {
           bulk_wait_read0();
@@ -589,7 +589,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_store_4d(&tmC, ebuf[1], ccol, 1, row0, g);
               bulk_commit();
             }
-          } else {  // kEpiDGelu
+          } else {  // kEpiDGelu, kEpiResidual: Y / R chunks double-buffered through ebuf
             const uint32_t cb = ecount & 1u, nb2 = cb ^ 1u;
             if (j + 1 < nch) {
               if (lane == 0) {
@@ -618,9 +618,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  const float lo = __uint_as_float(v[8 * hh + 2 * e]) * gelu_grad_f(bf16lo_to_f32(yy[e]));
-                  const float hi = __uint_as_float(v[8 * hh + 2 * e + 1]) * gelu_grad_f(bf16hi_to_f32(yy[e]));
-                  o[e] = pack_bf16x2(lo, hi);
+                  const float a0 = __uint_as_float(v[8 * hh + 2 * e]), a1 = __uint_as_float(v[8 * hh + 2 * e + 1]);
+                  const float y0 = bf16lo_to_f32(yy[e]), y1 = bf16hi_to_f32(yy[e]);
+                  if (EPI == kEpiResidual)
+                    o[e] = pack_bf16x2(a0 + y0, a1 + y1);
+                  else
+                    o[e] = pack_bf16x2(a0 * gelu_grad_f(y0), a1 * gelu_grad_f(y1));
                 }
                 st_shared_v4(addr, o[0], o[1], o[2], o[3]);
               }
@@ -694,6 +697,7 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
   if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore>();
   if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU>();
   if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
+  if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual>();
   return nullptr;
 }
 
@@ -737,7 +741,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (gated && ldc != N) return 1;
   if ((epi == kEpiSwiGLU) != (B.parts == 2) || A.parts != 1) return 1;
   if (epi == kEpiSwiGLU && !B.mn_major) return 1;
-  if (epi == kEpiDSwiGLU && !Yaux) return 1;
+  if ((epi == kEpiDSwiGLU || epi == kEpiResidual || epi == kEpiDGelu) && !Yaux) return 1;
   const int64_t tile_n = epi == kEpiSwiGLU ? BN / 2 : BN;
   const int sms = device_sm_count();
   if (sms <= 0) return 2;

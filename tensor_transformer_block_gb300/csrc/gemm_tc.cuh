@@ -33,6 +33,7 @@ enum GemmEpi : int {
   kEpiSwiGLU = 4,   // C = bf16(silu(gate) * up); optionally Yaux [G][M][2][N] = bf16(gate), bf16(up)
   kEpiDSwiGLU = 5,  // Yaux [G][M][2][N] holds G, U; C [G][M][2][N] gets
                     // C(.,0,.) = bf16(acc * U * silu'(G)), C(.,1,.) = bf16(acc * silu(G))
+  kEpiResidual = 6,  // C = bf16(acc + R), R = Yaux [G][M][ldc] (a residual connection)
 };
 
 struct GemmShape {

@@ -50,6 +50,9 @@ enum KernelKind : int {
   kKGmlpDwd,        // dWd_i = A_i^T dZ
   kKGmlpDwgu,       // dWgu_i = X^T [dG_i dU_i]
   kKGmlpDx,         // dX = sum_i [dG_i dU_i] Wgu_i^T
+  kKLnFwd,          // LayerNorm forward
+  kKLnBwd,          // LayerNorm backward (+ residual gradient), per-CTA partial dgamma / dbeta
+  kKLnColsum,       // fixed-order sum of the partial rows -> dgamma, dbeta
   kKProbe,          // timeout probe
   kNumKernelKinds
 };

@@ -1,0 +1,309 @@
+// LayerNorm over the hidden dimension of bf16 rows (zouht 张量并行 §2.2.2:
+// mu = mean(h_i), sigma^2 = mean((h_i - mu)^2), h_hat = (h - mu) / sqrt(sigma^2 + eps),
+// h' = gamma * h_hat + beta), its backward with an optional residual gradient
+// added in, and the fixed-order column sums that finish dgamma and dbeta.
+//
+// Both row kernels are HBM-bound: every element is read once and written once.
+// A row is held in registers by one CTA of up to 1024 threads: thread t owns
+// the 16-byte vectors t, t + blockDim, ... (VPT <= 2 of them), so the loads of
+// a warp are contiguous 512-byte runs; h <= 8192 takes one vector per thread.
+// Statistics are fp32, taken in two passes over the registers (mean first,
+// then the centred sum of squares), so no cancellation.
+//
+// The backward is persistent over rows: CTA b takes rows b, b + grid, ... and,
+// because each thread always owns the same columns, accumulates its columns'
+// dgamma / dbeta partial sums in registers; each CTA writes one partial row and
+// k_ln_colsum adds the partial rows in CTA order.  Both kernels and their
+// launch geometry depend only on T and h, so the result is bit-reproducible.
+#include <cuda_bf16.h>
+
+#include "host_util.cuh"
+#include "ln.cuh"
+#include "ptx.cuh"
+
+namespace tpb {
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4& q, float (&v)[8]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = bf16lo_to_f32(w[e]);
+    v[2 * e + 1] = bf16hi_to_f32(w[e]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  return q;
+}
+
+// Sum of one value (or two) over the CTA; every thread gets the result.
+// ``red`` holds 2 x 32 floats; the leading barrier protects its previous use.
+__device__ __forceinline__ float2 block_sum2(float a, float b, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = (blockDim.x + 31) >> 5;
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = a;
+    red[32 + warp] = b;
+  }
+  __syncthreads();
+  a = lane < nw ? red[lane] : 0.0f;
+  b = lane < nw ? red[32 + lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  return make_float2(a, b);
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
+                                                 const uint4* __restrict__ beta, uint4* __restrict__ Y,
+                                                 float* __restrict__ mean, float* __restrict__ rstd, int T,
+                                                 int nvec, float inv_h, float eps) {
+  __shared__ float red[64];
+  const int64_t row = blockIdx.x;
+  if (row >= T) return;
+  const uint4* xr = X + row * nvec;
+  float v[VPT][8];
+  float s = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < nvec) {
+      unpack8(xr[i], v[k]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += v[k][e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[k][e] = 0.0f;
+    }
+  }
+  const float mu = block_sum2(s, 0.0f, red).x * inv_h;
+  float q = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    if (threadIdx.x + k * blockDim.x < nvec) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float dlt = v[k][e] - mu;
+        q = fmaf(dlt, dlt, q);
+      }
+    }
+  }
+  const float var = block_sum2(q, 0.0f, red).x * inv_h;
+  const float r = rsqrtf(var + eps);
+  uint4* yr = Y + row * nvec;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < nvec) {
+      float g[8], b[8], o[8];
+      unpack8(gamma[i], g);
+      unpack8(beta[i], b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[k][e] - mu) * r, g[e], b[e]);
+      yr[i] = pack8(o);
+    }
+  }
+  if (threadIdx.x == 0) {
+    mean[row] = mu;
+    rstd[row] = r;
+  }
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
+                                                 const float* __restrict__ mean, const float* __restrict__ rstd,
+                                                 const uint4* __restrict__ dY, const uint4* __restrict__ dR,
+                                                 uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec,
+                                                 float inv_h) {
+  __shared__ float red[64];
+  float gm[VPT][8], pg[VPT][8], pb[VPT][8];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < nvec) {
+      unpack8(gamma[i], gm[k]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gm[k][e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      pg[k][e] = 0.0f;
+      pb[k][e] = 0.0f;
+    }
+  }
+  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+    const float mu = mean[row], r = rstd[row];
+    float xh[VPT][8], g[VPT][8];
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < nvec) {
+        float xv[8], dy[8];
+        unpack8(X[row * nvec + i], xv);
+        unpack8(dY[row * nvec + i], dy);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xh[k][e] = (xv[e] - mu) * r;
+          g[k][e] = dy[e] * gm[k][e];
+          s1 += g[k][e];
+          s2 = fmaf(g[k][e], xh[k][e], s2);
+          pg[k][e] = fmaf(dy[e], xh[k][e], pg[k][e]);
+          pb[k][e] += dy[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          xh[k][e] = 0.0f;
+          g[k][e] = 0.0f;
+        }
+      }
+    }
+    const float2 c = block_sum2(s1, s2, red);
+    const float c1 = c.x * inv_h, c2 = c.y * inv_h;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < nvec) {
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = r * (g[k][e] - c1 - xh[k][e] * c2);
+        if (dR) {
+          float rr[8];
+          unpack8(dR[row * nvec + i], rr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[e] += rr[e];
+        }
+        dX[row * nvec + i] = pack8(o);
+      }
+    }
+  }
+  // partial row of this CTA: [2][h] fp32 (dgamma, then dbeta)
+  float* pr = part + static_cast<int64_t>(blockIdx.x) * 2 * nvec * 8;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int i = threadIdx.x + k * blockDim.x;
+    if (i < nvec) {
+      float4* a = reinterpret_cast<float4*>(pr + i * 8);
+      float4* b = reinterpret_cast<float4*>(pr + nvec * 8 + i * 8);
+      a[0] = make_float4(pg[k][0], pg[k][1], pg[k][2], pg[k][3]);
+      a[1] = make_float4(pg[k][4], pg[k][5], pg[k][6], pg[k][7]);
+      b[0] = make_float4(pb[k][0], pb[k][1], pb[k][2], pb[k][3]);
+      b[1] = make_float4(pb[k][4], pb[k][5], pb[k][6], pb[k][7]);
+    }
+  }
+}
+
+// out[c] = bf16(sum_{p=0}^{P-1} part[p][c]) for c < 2h (dgamma then dbeta), in order p.
+__global__ void k_ln_colsum(const float* __restrict__ part, int P, int two_h, int h, __nv_bfloat16* dgamma,
+                            __nv_bfloat16* dbeta) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= two_h) return;
+  float s = 0.0f;
+#pragma unroll 8
+  for (int p = 0; p < P; ++p) s += part[static_cast<int64_t>(p) * two_h + c];
+  if (c < h)
+    dgamma[c] = __float2bfloat16_rn(s);
+  else
+    dbeta[c - h] = __float2bfloat16_rn(s);
+}
+
+struct LnGeom {
+  int vpt, threads;
+};
+
+LnGeom ln_geom(int64_t h) {
+  const int64_t nvec = h / 8;
+  LnGeom g{1, 32};
+  g.vpt = nvec <= 1024 ? 1 : 2;
+  const int64_t t = (nvec + g.vpt - 1) / g.vpt;
+  g.threads = static_cast<int>((t + 31) / 32 * 32);
+  return g;
+}
+
+int ln_bwd_grid(int64_t T, int threads) {
+  const int sms = device_sm_count();
+  const int per_sm = threads > 0 ? 2048 / threads : 1;
+  int64_t g = static_cast<int64_t>(sms > 0 ? sms : 1) * (per_sm > 0 ? per_sm : 1);
+  if (g > T) g = T;
+  return static_cast<int>(g);
+}
+
+}  // namespace
+
+bool ln_shape_ok(int64_t T, int64_t h) { return T >= 1 && h >= 8 && h % 8 == 0 && h <= kLnMaxH && T < (1ll << 31); }
+
+size_t ln_partial_bytes(int64_t T, int64_t h) {
+  const LnGeom g = ln_geom(h);
+  return static_cast<size_t>(ln_bwd_grid(T, g.threads)) * 2 * static_cast<size_t>(h) * sizeof(float);
+}
+
+int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, float* mean, float* rstd, int64_t T,
+                  int64_t h, float eps, cudaStream_t st) {
+  if (!ln_shape_ok(T, h)) return 1;
+  const LnGeom g = ln_geom(h);
+  const int nvec = static_cast<int>(h / 8);
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const auto* x = static_cast<const uint4*>(X);
+  const auto* ga = static_cast<const uint4*>(gamma);
+  const auto* be = static_cast<const uint4*>(beta);
+  auto* y = static_cast<uint4*>(Y);
+  const int slot = timing_begin(kKLnFwd, st);
+  const dim3 grid(static_cast<unsigned>(T));
+  if (g.vpt == 1)
+    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+  else
+    k_ln_fwd<2><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  timing_end(slot, st);
+  return ok ? 0 : 2;
+}
+
+int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd, const void* dY,
+                  const void* dR, void* dX, void* dgamma, void* dbeta, float* part, int64_t T, int64_t h,
+                  cudaStream_t st) {
+  if (!ln_shape_ok(T, h)) return 1;
+  const LnGeom g = ln_geom(h);
+  const int nvec = static_cast<int>(h / 8);
+  const float inv_h = 1.0f / static_cast<float>(h);
+  const int grid = ln_bwd_grid(T, g.threads);
+  const auto* x = static_cast<const uint4*>(X);
+  const auto* ga = static_cast<const uint4*>(gamma);
+  const auto* dy = static_cast<const uint4*>(dY);
+  const auto* dr = static_cast<const uint4*>(dR);
+  auto* dx = static_cast<uint4*>(dX);
+  int slot = timing_begin(kKLnBwd, st);
+  if (g.vpt == 1)
+    k_ln_bwd<1><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec, inv_h);
+  else
+    k_ln_bwd<2><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec, inv_h);
+  bool ok = cudaGetLastError() == cudaSuccess;
+  timing_end(slot, st);
+  if (!ok) return 2;
+  slot = timing_begin(kKLnColsum, st);
+  const int two_h = static_cast<int>(2 * h);
+  k_ln_colsum<<<(two_h + 255) / 256, 256, 0, st>>>(part, grid, two_h, static_cast<int>(h),
+                                                    static_cast<__nv_bfloat16*>(dgamma),
+                                                    static_cast<__nv_bfloat16*>(dbeta));
+  ok = cudaGetLastError() == cudaSuccess;
+  timing_end(slot, st);
+  return ok ? 0 : 2;
+}
+
+}  // namespace tpb

@@ -5,7 +5,8 @@ This module draws random numbers and arranges them in the shard-major layouts of
 the boundary; it contains none of the block's arithmetic.  Draws are fp32 normals
 from a CPU ``torch.Generator`` seeded once, in a fixed order (MLP: X, W1, W2, dZ;
 gated MLP: X, W_gate, W_up, W_down, dZ; attention: X, Wqkv, Wo, dZ; layer: X, Wqkv,
-Wo, W1, W2, dZ), scaled by the stated
+Wo, W1, W2, dZ; pre-norm layer: X, ln1 gamma, ln1 beta, Wqkv, Wo, ln2 gamma, ln2
+beta, W1, W2, dZ), scaled by the stated
 standard deviation and cast to the workload's dtype once.  The GPU and the oracle
 then consume the identical values (the oracle upcasts them to float64).
 
@@ -25,7 +26,8 @@ from dataclasses import dataclass
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", "layer_inputs",
+__all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", "layer_inputs", "prenorm_inputs",
+           "ln_inputs",
            "split_columns", "split_rows", "split_qkv_heads"]
 
 
@@ -33,7 +35,7 @@ __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", 
 class Workload:
     """One of the synthetic workloads the block is checked and measured on."""
     name: str
-    kind: str            # "mlp", "gmlp" (gated MLP), "attn" or "layer"
+    kind: str            # "mlp", "gmlp" (gated MLP), "attn", "layer" or "lnlayer" (pre-norm layer)
     dtype: str           # "f32" or "bf16"
     backward: bool
     T: int = 0           # tokens = B*S
@@ -67,6 +69,9 @@ WORKLOADS = {
                                                      S=2048, H=32, d=128),
     "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
         "layer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "layer", "bf16", True,
+        T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
+    "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
+        "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "lnlayer", "bf16", True,
         T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
     "gmlp_bf16_T8192_h4096_f12288_N8": Workload("gmlp_bf16_T8192_h4096_f12288_N8", "gmlp", "bf16", True,
                                                 T=8192, h=4096, f=12288, N=8),
@@ -166,6 +171,41 @@ def layer_inputs(B: int, S: int, h: int, H: int, d: int, f: int, N: int, dtype: 
             "W1s": split_columns(W1, N), "W2s": split_rows(W2, N), "dZ": dZ}
 
 
+def ln_inputs(T: int, h: int, dtype: str = "bf16", seed: int = 0, x_std: float = 1.0, x_mean: float = 0.0,
+              ln_std: float = 0.1) -> dict:
+    """LayerNorm alone: X [T][h] ~ N(x_mean, x_std^2), gamma ~ 1 + N(0, ln_std^2),
+    beta ~ N(0, ln_std^2), upstream dY and residual gradient dR ~ N(0, 1)."""
+    gen = torch.Generator().manual_seed(seed)
+    X = (torch.randn(T, h, generator=gen) * x_std + x_mean).to(_DT[dtype])
+    g = (_draw(gen, (h,), ln_std, "f32") + 1.0).to(_DT[dtype])
+    b = _draw(gen, (h,), ln_std, dtype)
+    dY = _draw(gen, (T, h), 1.0, dtype)
+    dR = _draw(gen, (T, h), 1.0, dtype)
+    return {"X": X, "gamma": g, "beta": b, "dY": dY, "dR": dR}
+
+
+def prenorm_inputs(B: int, S: int, h: int, H: int, d: int, f: int, N: int, dtype: str = "bf16",
+                   seed: int = 0, x_std: float = 1.0, w_std: float = 0.02, ln_std: float = 0.1) -> dict:
+    """Inputs of the pre-norm layer: the layer's plus LayerNorm gamma ~ 1 + N(0, ln_std^2)
+    and beta ~ N(0, ln_std^2), each [h] (perturbed from the usual 1 / 0 start so that
+    they take part in every check)."""
+    if N < 1 or H % N or f % N:
+        raise ValueError("N must divide H and f")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (B * S, h), x_std, dtype)
+    g1 = (_draw(gen, (h,), ln_std, "f32") + 1.0).to(_DT[dtype])
+    b1 = _draw(gen, (h,), ln_std, dtype)
+    Wqkv = _draw(gen, (h, 3 * H * d), w_std, dtype)
+    Wo = _draw(gen, (H * d, h), w_std, dtype)
+    g2 = (_draw(gen, (h,), ln_std, "f32") + 1.0).to(_DT[dtype])
+    b2 = _draw(gen, (h,), ln_std, dtype)
+    W1 = _draw(gen, (h, f), w_std, dtype)
+    W2 = _draw(gen, (f, h), w_std, dtype)
+    dZ = _draw(gen, (B * S, h), 1.0, dtype)
+    return {"X": X, "ln1_g": g1, "ln1_b": b1, "Wqkv": split_qkv_heads(Wqkv, N, H, d), "Wo": split_rows(Wo, N),
+            "ln2_g": g2, "ln2_b": b2, "W1s": split_columns(W1, N), "W2s": split_rows(W2, N), "dZ": dZ}
+
+
 def workload_inputs(w: Workload, **overrides) -> dict:
     """Inputs for a :class:`Workload` (shape fields may be overridden)."""
     p = {**w.as_dict(), **overrides}
@@ -178,5 +218,8 @@ def workload_inputs(w: Workload, **overrides) -> dict:
     if p["kind"] == "attn":
         return attn_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["N"], p["dtype"], p["seed"],
                            p["x_std"], p["w_std"], p["backward"])
+    if p["kind"] == "lnlayer":
+        return prenorm_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["f"], p["N"], p["dtype"],
+                              p["seed"], p["x_std"], p["w_std"])
     return layer_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["f"], p["N"], p["dtype"],
                         p["seed"], p["x_std"], p["w_std"])

@@ -637,3 +637,19 @@ def test_prenorm_layer_residual_structure():
     g = O.prenorm_layer_backward(X, ln[0], ln[1], Wqkv, np.zeros_like(Wos), ln[2], ln[3], W1s,
                                  np.zeros_like(W2s), dZ, B, S)
     assert np.array_equal(g["dX"], dZ)
+
+
+def test_prenorm_layer_row_restriction():
+    B, S, H, d, n, X, Wq, Wk, Wv, Wo, Wqkv, Wos, W1, W2, W1s, W2s, ln, dZ = _prenorm_inputs(seed=8)
+    full = O.prenorm_layer_forward(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S)
+    rows = np.array([0, 3, 4, 7])
+    r = O.prenorm_layer_forward_rows(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S, rows)
+    assert rel(r["H1"], full["H1"][rows]) < 1e-13
+    assert rel(r["Z"], full["Z"][rows]) < 1e-13
+    same = O.prenorm_layer_forward_rows(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S, rows,
+                                        store=lambda x: x)
+    assert rel(same["Z"], full["Z"][rows]) < 1e-13
+    q = lambda x: np.round(x * 2.0 ** 10) / 2.0 ** 10
+    coarse = O.prenorm_layer_forward_rows(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S, rows, store=q)
+    assert 0 < rel(coarse["Z"], full["Z"][rows]) < 1e-2
+    assert np.array_equal(coarse["H1"], q(coarse["H1"]))
