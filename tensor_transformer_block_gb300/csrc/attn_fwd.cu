@@ -4,18 +4,28 @@
 // recurrence is the one sunjinbo 并行方式 §CP uses to combine per-block results).
 //
 // One CTA per (256 queries = two 128-query tiles, head, batch), heaviest causal
-// blocks first.  Keys are processed in blocks of 64.
+// blocks first.  Keys are processed in blocks of 64; K and V each have two
+// shared-memory stages, so the copies of block kv+1 overlap the work on block kv.
 //   warp 8: TMA producer: both tiles' Qh, Ql once; Kh, Kl and V per key block
-//   warp 9: MMA issuer: for each key block and tile, S = Qh Kh^T + Qh Kl^T + Ql Kh^T
-//           (split-bf16 scores) into one of the tile's two TMEM score buffers, then
-//           O_tile += P V (P from shared memory) into the tile's TMEM accumulator
+//   warp 9: MMA issuer: per key block, S = Qh Kh^T + Qh Kl^T + Ql Kh^T (split-bf16
+//           scores) for each tile into one of the tile's two TMEM score buffers,
+//           then O_tile += P V with P read from TMEM and V from shared memory
 //   warps 0-3 / 4-7: the softmax warpgroup of tile 0 / tile 1, one query row per
-//           thread: one TMEM read of the score block, masked row max, exp2, P (bf16)
-//           to shared memory.  The running max is only moved (and the row of O in
-//           TMEM rescaled) when a block's max exceeds it by more than 8 (log2
-//           units); otherwise the stale max stays, P <= 2^8, and the final O / l is
-//           unchanged because the max cancels.  While one warpgroup works on its
-//           softmax the tensor core works on the other tile.
+//           thread: one TMEM read of the score block, masked row max, exp2, and P
+//           (bf16) written over the first half of the same score buffer.  The
+//           running max is only moved (and the row of O in TMEM rescaled) when a
+//           block's max exceeds it by more than 8 (log2 units); otherwise the stale
+//           max stays, P <= 2^8, and the final O / l is unchanged because the max
+//           cancels.  Only a rescale waits for the previous block's P V, so the
+//           softmax of block kv+1 overlaps the P V of block kv, and while one
+//           warpgroup works on its softmax the tensor core works on the other tile.
+// TMEM (512 columns): tile t's score buffers at 128 t and 128 t + 64 (64 columns;
+// P, 64 bf16 per row, in their first 32), its O at 256 + 128 t.  A score buffer
+// is refilled (block kv+2) only once the P V that read its P (block kv) is done.
+// P ready / P V done for even and odd blocks go to separate barriers, and every
+// waiter observes block kv-2 before it waits for block kv, so a parity wait never
+// meets a barrier two phases away from it (the softmax of block kv+1 may finish
+// before the MMA warp has taken block kv's P).
 #include <cmath>
 
 #include "attn.cuh"
@@ -34,12 +44,15 @@ constexpr int WARP_MMA = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 
 enum : int {
-  B_QF = 0, B_KF, B_KE, B_VF, B_VE,
-  B_SF = 5,    // [tile][buf]: 5..8
-  B_SE = 9,    // [tile][buf]: 9..12
-  B_PF = 13,   // [tile]: 13, 14
-  B_PE = 15,   // [tile]: 15, 16
-  B_DR = 17, NBARS = 18
+  B_QF = 0,
+  B_KF = 1,   // [stage]: 1, 2
+  B_KE = 3,   // [stage]: 3, 4
+  B_VF = 5,   // [stage]: 5, 6
+  B_VE = 7,   // [stage]: 7, 8
+  B_SF = 9,   // [tile][buffer]: scores ready (9..12)
+  B_PF = 13,  // [tile][block parity]: P written to TMEM, 4 arrivals (13..16)
+  B_PE = 17,  // [tile][block parity]: P.V complete (17..20)
+  B_DR = 21, NBARS = 22
 };
 
 template <int D>
@@ -47,15 +60,16 @@ struct FwdCfg {
   static constexpr int CH = D / 64;
   static constexpr int QTILE = CH * 16384;   // 128 rows x D bf16 in 64-column swizzled chunks
   static constexpr int KTILE = CH * 8192;    // 64 rows x D
-  static constexpr int PTILE = BQ * BKV * 2; // 128 x 64 bf16, one swizzle atom wide
   static constexpr int OFF_Q = 0;            // [tile][hi, lo]
-  static constexpr int OFF_KH = 4 * QTILE, OFF_KL = OFF_KH + KTILE, OFF_V = OFF_KL + KTILE;
-  static constexpr int OFF_P = OFF_V + KTILE;  // [tile]
-  static constexpr int OFF_BAR = OFF_P + QT * PTILE;
+  static constexpr int OFF_K = 4 * QTILE;    // [stage][hi, lo]
+  static constexpr int OFF_V = OFF_K + 4 * KTILE;  // [stage]
+  static constexpr int OFF_BAR = OFF_V + 2 * KTILE;
   static constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
   static constexpr int USED = OFF_MISC + 16;
+  // at least 120 KB so that a second CTA (which would wait for the TMEM this one
+  // holds) never shares the SM
   static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
-  // TMEM: tile t scores in [t*128, t*128 + 128) as two 64-column buffers; O_t at 256 + t*128
+  static_assert(SMEM <= 232448, "shared memory budget");
   static_assert(D <= 128, "head dim");
 };
 
@@ -87,8 +101,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   auto sQ = [&](int t, int lo) { return sb + C::OFF_Q + static_cast<uint32_t>((2 * t + lo) * C::QTILE); };
-  const uint32_t sKh = sb + C::OFF_KH, sKl = sb + C::OFF_KL, sV = sb + C::OFF_V;
-  auto sP = [&](int t) { return sb + C::OFF_P + static_cast<uint32_t>(t * C::PTILE); };
+  auto sKh = [&](int st) { return sb + C::OFF_K + static_cast<uint32_t>(2 * st * C::KTILE); };
+  auto sKl = [&](int st) { return sb + C::OFF_K + static_cast<uint32_t>((2 * st + 1) * C::KTILE); };
+  auto sV = [&](int st) { return sb + C::OFF_V + static_cast<uint32_t>(st * C::KTILE); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (a.S + QT * BQ - 1) / (QT * BQ);
@@ -110,7 +125,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
-      const bool by_warps = (i >= B_SE && i < B_SE + 4) || i == B_PF || i == B_PF + 1;
+      const bool by_warps = i >= B_PF && i < B_PF + 2 * QT;
       mbar_init(bar(i), by_warps ? 4 : 1);
     }
     *abort_flag = 0;
@@ -136,7 +151,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      int kiss = 0, viss = 0;
+      int kiss = 0, viss = 0;  // key blocks whose K / V copies were issued
       mbar_arrive_expect_tx(bar(B_QF), 4 * C::QTILE);
 #pragma unroll
       for (int t = 0; t < QT; ++t)
@@ -146,24 +161,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_4d(sQ(t, 1) + c * 16384, &tmQ, bar(B_QF), cQl + 64 * c, q0 + t * BQ, b, shard);
         }
       for (int kv = 0; kv < nkv; ++kv) {
-        const uint32_t ph = static_cast<uint32_t>(kv & 1);
-        if (!mbar_wait(bar(B_KE), ph ^ 1u, wc)) break;
-        mbar_arrive_expect_tx(bar(B_KF), 2 * C::KTILE);
+        const int st = kv & 1;
+        const uint32_t ph = static_cast<uint32_t>((kv >> 1) & 1);
+        if (!mbar_wait(bar(B_KE + st), ph ^ 1u, wc)) break;
+        mbar_arrive_expect_tx(bar(B_KF + st), 2 * C::KTILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_4d(sKh + c * 8192, &tmKV, bar(B_KF), cKh + 64 * c, kv * BKV, b, shard);
-          tma_load_4d(sKl + c * 8192, &tmKV, bar(B_KF), cKl + 64 * c, kv * BKV, b, shard);
+          tma_load_4d(sKh(st) + c * 8192, &tmKV, bar(B_KF + st), cKh + 64 * c, kv * BKV, b, shard);
+          tma_load_4d(sKl(st) + c * 8192, &tmKV, bar(B_KF + st), cKl + 64 * c, kv * BKV, b, shard);
         }
         kiss = kv + 1;
-        if (!mbar_wait(bar(B_VE), ph ^ 1u, wc)) break;
-        mbar_arrive_expect_tx(bar(B_VF), C::KTILE);
+        if (!mbar_wait(bar(B_VE + st), ph ^ 1u, wc)) break;
+        mbar_arrive_expect_tx(bar(B_VF + st), C::KTILE);
 #pragma unroll
-        for (int c = 0; c < C::CH; ++c) tma_load_4d(sV + c * 8192, &tmKV, bar(B_VF), cV + 64 * c, kv * BKV, b, shard);
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_4d(sV(st) + c * 8192, &tmKV, bar(B_VF + st), cV + 64 * c, kv * BKV, b, shard);
         viss = kv + 1;
       }
+      // every issued copy lands before the CTA may exit
       mbar_wait(bar(B_QF), 0, wdrain);
-      if (kiss) mbar_wait(bar(B_KF), (kiss - 1) & 1, wdrain);
-      if (viss) mbar_wait(bar(B_VF), (viss - 1) & 1, wdrain);
+      for (int k = (kiss > 2 ? kiss - 2 : 0); k < kiss; ++k)
+        mbar_wait(bar(B_KF + (k & 1)), static_cast<uint32_t>((k >> 1) & 1), wdrain);
+      for (int k = (viss > 2 ? viss - 2 : 0); k < viss; ++k)
+        mbar_wait(bar(B_VF + (k & 1)), static_cast<uint32_t>((k >> 1) & 1), wdrain);
     }
   } else if (warp == WARP_MMA) {
     if (lane == 0) {
@@ -171,24 +191,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t ID_S = idesc_bf16(128, BKV, false, false);
       constexpr uint32_t ID_PV = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(bar(B_QF), 0, wc), any = false;
-      // scores of key block kv for every tile that needs it, then release K
+      // scores of key block kv for every tile that needs it, then release the K stage
       auto issue_s = [&](int kv) -> bool {
-        if (!mbar_wait(bar(B_KF), kv & 1, wc)) return false;
         const int st = kv & 1;
-        const uint32_t ph = static_cast<uint32_t>((kv >> 1) & 1);
+        if (!mbar_wait(bar(B_KF + st), static_cast<uint32_t>((kv >> 1) & 1), wc)) return false;
 #pragma unroll
         for (int t = 0; t < QT; ++t) {
           if (kv >= nkv_t[t]) continue;
-          if (!mbar_wait(bar(B_SE + 2 * t + st), ph ^ 1u, wc)) return false;
+          // the P V of block kv-2 has read the P this buffer held
+          if (kv >= 2 && !mbar_wait(bar(B_PE + 2 * t + st), static_cast<uint32_t>(((kv - 2) >> 1) & 1), wc))
+            return false;
           tc_fence_after();
           const uint32_t dt = tmem + static_cast<uint32_t>(t * 128 + st * BKV);
-          mma_scores<D>(dt, sQ(t, 0), sKh, ID_S, false);
-          mma_scores<D>(dt, sQ(t, 0), sKl, ID_S, true);
-          mma_scores<D>(dt, sQ(t, 1), sKh, ID_S, true);
+          mma_scores<D>(dt, sQ(t, 0), sKh(st), ID_S, false);
+          mma_scores<D>(dt, sQ(t, 0), sKl(st), ID_S, true);
+          mma_scores<D>(dt, sQ(t, 1), sKh(st), ID_S, true);
           tc_commit(bar(B_SF + 2 * t + st));
         }
         any = true;
-        tc_commit(bar(B_KE));
+        tc_commit(bar(B_KE + st));
         return true;
       };
       if (ok && nkv > 0) ok = issue_s(0);
@@ -197,28 +218,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ok = false;
           break;
         }
-        if (!mbar_wait(bar(B_VF), kv & 1, wc)) {
+        const int st = kv & 1;
+        if (!mbar_wait(bar(B_VF + st), static_cast<uint32_t>((kv >> 1) & 1), wc)) {
           ok = false;
           break;
         }
 #pragma unroll
         for (int t = 0; t < QT; ++t) {
           if (kv >= nkv_t[t]) continue;
-          if (!mbar_wait(bar(B_PF + t), kv & 1, wc)) {
+          if (!mbar_wait(bar(B_PF + 2 * t + st), static_cast<uint32_t>((kv >> 1) & 1), wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
-            const uint64_t ad = sdesc_sw128(sP(t) + kk * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sV + kk * 2048, 8192, 1024);
-            tc_mma_bf16(tmem + 256 + t * 128, ad, bd, ID_PV, (kv > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(sV(st) + kk * 2048, 8192, 1024);
+            tc_mma_bf16_ts(tmem + 256 + t * 128, tmem + t * 128 + st * BKV + kk * 8, bd, ID_PV,
+                           (kv > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(bar(B_PE + t));
+          tc_commit(bar(B_PE + 2 * t + st));
         }
         if (!ok) break;
-        tc_commit(bar(B_VE));
+        tc_commit(bar(B_VE + st));
       }
       if (any) {
         tc_commit(bar(B_DR));
@@ -235,23 +257,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * 128);
     const uint32_t tO = tmem + lane_off + static_cast<uint32_t>(256 + t * 128);
-    const uint32_t rsw = static_cast<uint32_t>(r & 7);
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int kv = 0; kv < nk; ++kv) {
       const int st = kv & 1;
-      const uint32_t ph = static_cast<uint32_t>((kv >> 1) & 1);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SF + 2 * t + st), ph, wc));
+      const uint32_t tSb = tS + static_cast<uint32_t>(st * BKV);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SF + 2 * t + st), static_cast<uint32_t>((kv >> 1) & 1), wc));
       if (!ok) break;
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      tmem_ld32(tS + st * BKV, v0);
-      tmem_ld32(tS + st * BKV + 32, v1);
+      tmem_ld32(tSb, v0);
+      tmem_ld32(tSb + 32, v1);
       tmem_ld_wait(v0);
       tmem_ld_wait(v1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SE + 2 * t + st));  // the score buffer may be refilled
+      // keep the P V completion barriers in step (block kv-2: long done)
+      if (kv >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PE + 2 * t + st), static_cast<uint32_t>(((kv - 2) >> 1) & 1), wc));
+        if (!ok) break;
+      }
       const int kbase = kv * BKV;
       const bool masked = (a.causal && kbase + BKV - 1 > q0 + t * BQ) || (kbase + BKV > a.S);
       float sv[64];
@@ -266,15 +289,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         sv[e] = s;
         bmax = fmaxf(bmax, s);
       }
-      // P buffer free and O quiescent once the previous block's P.V has completed
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PE + t), (kv & 1) ^ 1, wc));
-      if (!ok) break;
-      tc_fence_after();
       if (kv == 0) {
         m = bmax;
       } else {
         const bool need = bmax > m + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {
+          // O must be quiescent: wait for the previous block's P V
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PE + 2 * t + ((kv - 1) & 1)),
+                                                 static_cast<uint32_t>(((kv - 1) >> 1) & 1), wc));
+          if (!ok) break;
+          tc_fence_after();
           const float alpha = need ? exp2f(m - bmax) : 1.0f;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
@@ -285,31 +309,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tmem_st32(tO + 32 * c, o);
           }
-          tmem_st_wait();
           l *= alpha;
           if (need) m = bmax;
         }
       }
       const float m_use = (m == -INFINITY) ? 0.0f : m;
       float ls = 0.0f;
+      uint32_t pk[32];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t pp = pack_bf16x2(exp2f(sv[8 * g + 2 * e] - m_use), exp2f(sv[8 * g + 2 * e + 1] - m_use));
-          ls += bf16lo_to_f32(pp) + bf16hi_to_f32(pp);
-          pk[e] = pp;
-        }
-        st_shared_v4(sP(t) + r * 128 + ((static_cast<uint32_t>(g) ^ rsw) << 4), pk[0], pk[1], pk[2], pk[3]);
+      for (int c = 0; c < 32; ++c) {
+        const uint32_t pp = pack_bf16x2(exp2f(sv[2 * c] - m_use), exp2f(sv[2 * c + 1] - m_use));
+        ls += bf16lo_to_f32(pp) + bf16hi_to_f32(pp);
+        pk[c] = pp;
       }
+      tmem_st32(tSb, pk);  // P over the scores just read (this thread's row only)
+      tmem_st_wait();
       l += ls;
       tc_fence_before();
-      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PF + t));
+      if (lane == 0) mbar_arrive(bar(B_PF + 2 * t + st));
     }
-    if (ok && nk > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PE + t), (nk - 1) & 1, wc));
+    if (ok && nk > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PE + 2 * t + ((nk - 1) & 1)),
+                                             static_cast<uint32_t>(((nk - 1) >> 1) & 1), wc));
     if (ok && nk > 0) {
       tc_fence_after();
       // every P.V of this tile is complete (and every score product before it): the

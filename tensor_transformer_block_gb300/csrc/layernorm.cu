@@ -13,7 +13,7 @@
 // The backward is persistent over rows: CTA b takes rows b, b + grid, ... and,
 // because each thread always owns the same columns, accumulates its columns'
 // dgamma / dbeta partial sums in registers; each CTA writes one partial row and
-// k_ln_colsum adds the partial rows in CTA order.  Both kernels and their
+// k_ln_colsum adds the partial rows in a fixed order.  Both kernels and their
 // launch geometry depend only on T and h, so the result is bit-reproducible.
 #include <cuda_bf16.h>
 
@@ -210,18 +210,32 @@ __global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, co
   }
 }
 
-// out[c] = bf16(sum_{p=0}^{P-1} part[p][c]) for c < 2h (dgamma then dbeta), in order p.
-__global__ void k_ln_colsum(const float* __restrict__ part, int P, int two_h, int h, __nv_bfloat16* dgamma,
-                            __nv_bfloat16* dbeta) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= two_h) return;
+// out[c] = bf16(sum_{p=0}^{P-1} part[p][c]) for c < 2h (dgamma then dbeta).  A CTA
+// of 8 warps takes 32 columns: warp w adds rows w, w + 8, ... in order, then lane c
+// of warp 0 adds the 8 warp sums in order, so the sum's order is fixed by P alone.
+constexpr int kColsumWarps = 8;
+__global__ void __launch_bounds__(kColsumWarps * 32) k_ln_colsum(const float* __restrict__ part, int P, int two_h,
+                                                                   int h, __nv_bfloat16* dgamma,
+                                                                   __nv_bfloat16* dbeta) {
+  __shared__ float red[kColsumWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.0f;
-#pragma unroll 8
-  for (int p = 0; p < P; ++p) s += part[static_cast<int64_t>(p) * two_h + c];
-  if (c < h)
-    dgamma[c] = __float2bfloat16_rn(s);
-  else
-    dbeta[c - h] = __float2bfloat16_rn(s);
+  if (c < two_h) {
+#pragma unroll 4
+    for (int p = warp; p < P; p += kColsumWarps) s += part[static_cast<int64_t>(p) * two_h + c];
+  }
+  red[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && c < two_h) {
+    float t = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kColsumWarps; ++w) t += red[w][lane];
+    if (c < h)
+      dgamma[c] = __float2bfloat16_rn(t);
+    else
+      dbeta[c - h] = __float2bfloat16_rn(t);
+  }
 }
 
 struct LnGeom {
@@ -298,7 +312,7 @@ int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const flo
   if (!ok) return 2;
   slot = timing_begin(kKLnColsum, st);
   const int two_h = static_cast<int>(2 * h);
-  k_ln_colsum<<<(two_h + 255) / 256, 256, 0, st>>>(part, grid, two_h, static_cast<int>(h),
+  k_ln_colsum<<<(two_h + 31) / 32, kColsumWarps * 32, 0, st>>>(part, grid, two_h, static_cast<int>(h),
                                                     static_cast<__nv_bfloat16*>(dgamma),
                                                     static_cast<__nv_bfloat16*>(dbeta));
   ok = cudaGetLastError() == cudaSuccess;
