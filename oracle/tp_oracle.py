@@ -55,6 +55,8 @@ __all__ = [
     "gated_mlp_backward_weight_columns",
     "LN_EPS", "layer_norm", "layer_norm_backward", "prenorm_layer_forward", "prenorm_layer_backward",
     "prenorm_layer_forward_rows",
+    "unpack_qkv_gqa", "pack_qkv_gqa", "gqa_attention_forward", "gqa_attention_backward",
+    "gqa_attention_forward_sharded",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -639,3 +641,115 @@ def prenorm_layer_forward_rows(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s
     m = mlp_forward(st(layer_norm(H1, ln2_g, ln2_b, eps)["y"]), W1s, W2s)
     Z = H1 + (matmul(st(concat_columns(m["A"])), stack_rows(W2s)) if store else m["Z"])
     return {"H1": H1, "Z": Z}
+
+
+# --------------------------------------------------------------------------
+# Grouped-query attention (named on wangyu 张量并行 §注意力机制中的张量并行 next to
+# MHA; the page gives no formula).  Reading: H query heads share Hkv key/value
+# heads, query head j using key/value head j // (H / Hkv) (consecutive query
+# heads form a group); the head split of the same section puts query heads
+# i*H/N .. (i+1)*H/N-1 and key/value heads i*Hkv/N .. (i+1)*Hkv/N-1 on shard i,
+# which keeps every group on one shard when N divides Hkv.
+# --------------------------------------------------------------------------
+def unpack_qkv_gqa(Wqkv, Hkv: int, d: int) -> tuple:
+    """Shard-major [N][h][(H/N + 2 Hkv/N) d] (shard i: its query heads, then its
+    key heads, then its value heads, each head d columns) -> unsharded Wq [h][H d],
+    Wk [h][Hkv d], Wv [h][Hkv d]."""
+    W = _f64(Wqkv)
+    n, h, cols = W.shape
+    kvn = Hkv // n
+    hn = cols // d - 2 * kvn
+    Wq = np.concatenate([W[i, :, :hn * d] for i in range(n)], axis=1)
+    Wk = np.concatenate([W[i, :, hn * d:(hn + kvn) * d] for i in range(n)], axis=1)
+    Wv = np.concatenate([W[i, :, (hn + kvn) * d:] for i in range(n)], axis=1)
+    return Wq, Wk, Wv
+
+
+def pack_qkv_gqa(Wq, Wk, Wv, n: int, d: int) -> np.ndarray:
+    """Inverse of :func:`unpack_qkv_gqa`."""
+    qn, kn = Wq.shape[1] // n, Wk.shape[1] // n
+    return np.stack([np.concatenate([_f64(Wq)[:, i * qn:(i + 1) * qn], _f64(Wk)[:, i * kn:(i + 1) * kn],
+                                     _f64(Wv)[:, i * kn:(i + 1) * kn]], axis=1) for i in range(n)])
+
+
+def gqa_attention_forward(X, Wqkv, Wo, B: int, S: int, H: int, Hkv: int, causal: bool = True) -> dict:
+    """Per batch b and query head j, with c = j // (H / Hkv):
+        head_j = softmax(mask(Q_j K_c^T / sqrt(d))) V_c,  Z = concat_j(head_j) Wo.
+    Returns Z, O (shard layout [N][T][H/N d]), LSE [B][H][S] and Q, K, V unsharded."""
+    X = _f64(X)
+    n = Wqkv.shape[0]
+    d = Wo.shape[1] * n // H
+    g = H // Hkv
+    T = B * S
+    Wq, Wk, Wv = unpack_qkv_gqa(Wqkv, Hkv, d)
+    Q, K, V = matmul(X, Wq), matmul(X, Wk), matmul(X, Wv)
+    O = np.zeros((T, H * d))
+    LSE = np.zeros((B, H, S))
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        for j in range(H):
+            c, kc = slice(j * d, (j + 1) * d), slice((j // g) * d, (j // g + 1) * d)
+            P, lse = _softmax_rows(_causal_scores(Q[r, c], K[r, kc], d, causal))
+            O[r, c] = matmul(P, V[r, kc])
+            LSE[b, j] = lse
+    Z = matmul(O, stack_rows(Wo))
+    return {"Z": Z, "O": np.ascontiguousarray(O.reshape(T, n, -1).transpose(1, 0, 2)), "LSE": LSE,
+            "Q": Q, "K": K, "V": V}
+
+
+def gqa_attention_backward(X, Wqkv, Wo, dZ, B: int, S: int, H: int, Hkv: int, causal: bool = True) -> dict:
+    """Gradients of <dZ, Z> for :func:`gqa_attention_forward`: each query head's
+    softmax Jacobian as in :func:`attention_backward`; a key/value head's gradient
+    is the sum over the query heads of its group."""
+    X, dZ = _f64(X), _f64(dZ)
+    n = Wqkv.shape[0]
+    d = Wo.shape[1] * n // H
+    g = H // Hkv
+    T = B * S
+    Wq, Wk, Wv = unpack_qkv_gqa(Wqkv, Hkv, d)
+    Wo_full = stack_rows(Wo)
+    Q, K, V = matmul(X, Wq), matmul(X, Wk), matmul(X, Wv)
+    O = np.zeros((T, H * d))
+    dO = matmul(dZ, Wo_full.T)
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for b in range(B):
+        r = slice(b * S, (b + 1) * S)
+        for j in range(H):
+            c, kc = slice(j * d, (j + 1) * d), slice((j // g) * d, (j // g + 1) * d)
+            P, _ = _softmax_rows(_causal_scores(Q[r, c], K[r, kc], d, causal))
+            O[r, c] = matmul(P, V[r, kc])
+            dV[r, kc] += matmul(P.T, dO[r, c])
+            dP = matmul(dO[r, c], V[r, kc].T)
+            dS = P * (dP - np.sum(dP * P, axis=1, keepdims=True))
+            dQ[r, c] = matmul(dS, K[r, kc]) / math.sqrt(d)
+            dK[r, kc] += matmul(dS.T, Q[r, c]) / math.sqrt(d)
+    dWo = matmul(O.T, dZ)
+    dX = matmul(dQ, Wq.T) + matmul(dK, Wk.T) + matmul(dV, Wv.T)
+    return {"dX": dX, "dWqkv": pack_qkv_gqa(matmul(X.T, dQ), matmul(X.T, dK), matmul(X.T, dV), n, d),
+            "dWo": split_rows_like(dWo, n)}
+
+
+def gqa_attention_forward_sharded(X, Wqkv, Wo, B: int, S: int, H: int, Hkv: int, causal: bool = True) -> np.ndarray:
+    """Shard by shard: shard i projects its own query and key/value heads with its
+    column block of Wqkv, attends within its groups, multiplies by its row block of
+    Wo; the all-reduce sums the partial outputs."""
+    X = _f64(X)
+    n = Wqkv.shape[0]
+    d = Wo.shape[1] * n // H
+    hn, kvn = H // n, Hkv // n
+    g = H // Hkv
+    T = B * S
+    Z = None
+    for i in range(n):
+        qkv = matmul(X, _f64(Wqkv[i]))
+        q, k, v = qkv[:, :hn * d], qkv[:, hn * d:(hn + kvn) * d], qkv[:, (hn + kvn) * d:]
+        Oi = np.zeros((T, hn * d))
+        for b in range(B):
+            r = slice(b * S, (b + 1) * S)
+            for jj in range(hn):
+                c, kc = slice(jj * d, (jj + 1) * d), slice((jj // g) * d, (jj // g + 1) * d)
+                P, _ = _softmax_rows(_causal_scores(q[r, c], k[r, kc], d, causal))
+                Oi[r, c] = matmul(P, v[r, kc])
+        part = matmul(Oi, Wo[i])
+        Z = part if Z is None else Z + part
+    return Z

@@ -653,3 +653,84 @@ def test_prenorm_layer_row_restriction():
     coarse = O.prenorm_layer_forward_rows(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S, rows, store=q)
     assert 0 < rel(coarse["Z"], full["Z"][rows]) < 1e-2
     assert np.array_equal(coarse["H1"], q(coarse["H1"]))
+
+
+# ---------------------------------------------------------------- grouped-query attention
+def _gqa_inputs(B, S, H, Hkv, d, n, h=32, seed=0, wstd=0.3):
+    r = np.random.default_rng(seed)
+    X = r.standard_normal((B * S, h))
+    Wq = r.standard_normal((h, H * d)) * wstd
+    Wk, Wv = r.standard_normal((h, Hkv * d)) * wstd, r.standard_normal((h, Hkv * d)) * wstd
+    Wo = r.standard_normal((H * d, h)) * wstd
+    dZ = r.standard_normal((B * S, h))
+    return X, Wq, Wk, Wv, Wo, O.pack_qkv_gqa(Wq, Wk, Wv, n, d), O.split_rows_like(Wo, n), dZ
+
+
+def test_gqa_with_one_head_per_group_is_mha():
+    """Hkv = H: the GQA layout [N][h][(H/N + 2H/N) d] is the MHA layout
+    [N][h][3][H/N][d] byte for byte, and the results coincide."""
+    B, S, H, d, n = 2, 5, 4, 4, 2
+    X, Wq, Wk, Wv, Wo, Wg, Wos, dZ = _gqa_inputs(B, S, H, H, d, n, seed=3)
+    Wm = O.pack_qkv(Wq, Wk, Wv, n, d)
+    assert np.array_equal(Wm.reshape(Wg.shape), Wg)
+    a = O.gqa_attention_forward(X, Wg, Wos, B, S, H, H)
+    m = O.attention_forward(X, Wm, Wos, B, S)
+    assert rel(a["Z"], m["Z"]) < 1e-14 and rel(a["LSE"], m["LSE"]) < 1e-14
+    ga = O.gqa_attention_backward(X, Wg, Wos, dZ, B, S, H, H)
+    gm = O.attention_backward(X, Wm, Wos, dZ, B, S)
+    assert rel(ga["dX"], gm["dX"]) < 1e-13
+    assert rel(ga["dWqkv"], gm["dWqkv"].reshape(ga["dWqkv"].shape)) < 1e-13
+
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    """A group shares one K/V head: MHA whose K/V weights repeat each shared head
+    for every query head of its group gives the same Z, dX, dWq and dWo, and the
+    shared head's gradient is the sum of its copies' gradients."""
+    B, S, H, Hkv, d, n = 2, 6, 8, 2, 4, 2
+    g = H // Hkv
+    X, Wq, Wk, Wv, Wo, Wg, Wos, dZ = _gqa_inputs(B, S, H, Hkv, d, n, seed=4)
+    rep = lambda W: np.concatenate([W[:, (j // g) * d:(j // g + 1) * d] for j in range(H)], axis=1)
+    Wm = O.pack_qkv(Wq, rep(Wk), rep(Wv), n, d)
+    for causal in (True, False):
+        a = O.gqa_attention_forward(X, Wg, Wos, B, S, H, Hkv, causal)
+        m = O.attention_forward(X, Wm, Wos, B, S, causal)
+        assert rel(a["Z"], m["Z"]) < 1e-13
+        ga = O.gqa_attention_backward(X, Wg, Wos, dZ, B, S, H, Hkv, causal)
+        gm = O.attention_backward(X, Wm, Wos, dZ, B, S, causal)
+        assert rel(ga["dX"], gm["dX"]) < 1e-13 and rel(ga["dWo"], gm["dWo"]) < 1e-13
+        aq, ak, av = O.unpack_qkv_gqa(ga["dWqkv"], Hkv, d)
+        mq, mk, mv = O.unpack_qkv(gm["dWqkv"])
+        fold = lambda W: sum(W[:, [c * g * d + gi * d + e for c in range(Hkv) for e in range(d)]]
+                             for gi in range(g))
+        assert rel(aq, mq) < 1e-13
+        assert rel(ak, fold(mk)) < 1e-13 and rel(av, fold(mv)) < 1e-13
+
+
+def test_gqa_vs_torch_sdpa_autograd():
+    """torch's SDPA on K/V heads repeated per group (fp64), forward and autograd."""
+    B, S, H, Hkv, d, n = 2, 7, 6, 2, 4, 2
+    X, Wq, Wk, Wv, Wo, Wg, Wos, dZ = _gqa_inputs(B, S, H, Hkv, d, n, seed=5)
+    t = [torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, Wq, Wk, Wv, Wo)]
+    tX, tq, tk, tv, to = t
+    shp = lambda a, hh: a.reshape(B, S, hh, d).transpose(1, 2)
+    k = shp(tX @ tk, Hkv).repeat_interleave(H // Hkv, dim=1)
+    v = shp(tX @ tv, Hkv).repeat_interleave(H // Hkv, dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(shp(tX @ tq, H), k, v, is_causal=True)
+    Z = o.transpose(1, 2).reshape(B * S, H * d) @ to
+    (Z * torch.from_numpy(dZ)).sum().backward()
+    assert rel(O.gqa_attention_forward(X, Wg, Wos, B, S, H, Hkv)["Z"], Z.detach().numpy()) < 1e-13
+    g = O.gqa_attention_backward(X, Wg, Wos, dZ, B, S, H, Hkv)
+    assert rel(g["dX"], tX.grad.numpy()) < 1e-12
+    q_, k_, v_ = O.unpack_qkv_gqa(g["dWqkv"], Hkv, d)
+    for a, b in ((q_, tq), (k_, tk), (v_, tv)):
+        assert rel(a, b.grad.numpy()) < 1e-12
+    assert rel(O.stack_rows(g["dWo"]), to.grad.numpy()) < 1e-12
+
+
+def test_gqa_sharded_equals_unsharded():
+    """Every shard count N dividing Hkv (each shard holds whole groups)."""
+    B, S, H, Hkv, d = 1, 5, 8, 4, 4
+    for n in divisors(Hkv):
+        X, Wq, Wk, Wv, Wo, Wg, Wos, dZ = _gqa_inputs(B, S, H, Hkv, d, n, seed=6)
+        assert rel(O.gqa_attention_forward_sharded(X, Wg, Wos, B, S, H, Hkv),
+                   O.gqa_attention_forward(X, Wg, Wos, B, S, H, Hkv)["Z"]) < 1e-13, n
