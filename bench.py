@@ -62,6 +62,14 @@ def kernel_flops(w) -> dict:
         out.update({"gmlp.fc1_col_gemm_swiglu": 2 * g, "gmlp.fc2_row_gemm_shard_sum": g,
                     "gmlp.bwd_dA_gemm_dswiglu": g, "gmlp.bwd_dWd_gemm": g, "gmlp.bwd_dWgu_gemm": 2 * g,
                     "gmlp.bwd_dX_row_gemm_shard_sum": 2 * g})
+    if w.kind == "gqa":
+        Hd, qkv = w.H * w.d, (w.H + 2 * w.Hkv) * w.d
+        pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
+        out.update({"attn.qkv_col_gemm": 2.0 * T * h * qkv, "attn.core_fwd": 2.0 * pairs,
+                    "attn.out_row_gemm_shard_sum": 2.0 * T * Hd * h, "attn.bwd_dO_gemm": 2.0 * T * h * Hd,
+                    "attn.bwd_dWo_gemm": 2.0 * T * Hd * h, "attn.bwd_core_dkdv": 3.0 * pairs,
+                    "attn.bwd_core_dq": 1.0 * pairs, "attn.bwd_dWqkv_gemm": 2.0 * T * h * qkv,
+                    "attn.bwd_dX_row_gemm_shard_sum": 2.0 * T * qkv * h})
     if w.kind in ("attn", "layer", "lnlayer"):
         Hd = w.H * w.d
         pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d  # (causal half) x d
@@ -80,6 +88,12 @@ def step_flops(w) -> float:
         tot += (12.0 if w.backward else 4.0) * T * h * f
     if w.kind == "gmlp":
         tot += (18.0 if w.backward else 6.0) * T * h * f
+    if w.kind == "gqa":
+        Hd, qkv = w.H * w.d, (w.H + 2 * w.Hkv) * w.d
+        core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
+        tot += 2.0 * T * h * qkv + 2.0 * T * Hd * h + core
+        if w.backward:
+            tot += 4.0 * T * h * Hd + 4.0 * T * h * qkv + 2.0 * core
     if w.kind in ("attn", "layer", "lnlayer"):
         Hd = w.H * w.d
         core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
@@ -96,6 +110,10 @@ def describe(w) -> str:
     if w.kind == "gmlp":
         return (f"gated (SwiGLU) MLP block {'fwd+bwd' if w.backward else 'fwd'}, {w.dtype}, T={w.T} tokens, "
                 f"h={w.h}, f={w.f} (gate and up each), N={w.N} logical shards")
+    if w.kind == "gqa":
+        return (f"grouped-query attention block {'fwd+bwd' if w.backward else 'fwd'}, {w.dtype}, B={w.B} x S={w.S}, "
+                f"h={w.h}, {w.H} query heads over {w.Hkv} key/value heads x d={w.d}, "
+                f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
     if w.kind == "attn":
         return (f"self-attention block fwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
                 f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
@@ -209,6 +227,11 @@ def oracle_step(w, inp_np: dict, rows: int) -> float:
     X = inp_np["X"][:rows]
     if w.kind == "attn":
         O.attention_forward(X, inp_np["Wqkv"], inp_np["Wo"], 1, rows, w.causal)
+    elif w.kind == "gqa":
+        O.gqa_attention_forward(X, inp_np["Wqkv"], inp_np["Wo"], 1, rows, w.H, w.Hkv, w.causal)
+        if w.backward:
+            O.gqa_attention_backward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["dZ"][:rows], 1, rows, w.H, w.Hkv,
+                                     w.causal)
     elif w.kind == "lnlayer":
         args = (X, inp_np["ln1_g"], inp_np["ln1_b"], inp_np["Wqkv"], inp_np["Wo"], inp_np["ln2_g"], inp_np["ln2_b"],
                 inp_np["W1s"], inp_np["W2s"])
@@ -333,6 +356,16 @@ def run_gpu(args, w) -> None:
         buf["dWgus"] = torch.empty_like(d["Wgus"])
         buf["dWds"] = torch.empty_like(d["Wds"])
         buf["gws"] = block.workspace(tp.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
+    if w.kind == "gqa":
+        hN, kvN = w.H // N, w.Hkv // N
+        buf["QKV"] = torch.empty(N, T, (2 * hN + 3 * kvN) * w.d, dtype=torch.bfloat16, device=dev)
+        buf["O"] = torch.empty(N, T, hN * w.d, dtype=torch.bfloat16, device=dev)
+        buf["LSE"] = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
+        buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["dX"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["dWqkv"] = torch.empty_like(d["Wqkv"])
+        buf["dWo"] = torch.empty_like(d["Wo"])
+        buf["qws"] = block.workspace(tp.tp_gqa_workspace_bytes(dt, w.B, w.S, h, w.H, w.Hkv, w.d, N), dev)
     if w.kind == "lnlayer":
         p = {k: d[k] for k in ("ln1_g", "ln1_b", "Wqkv", "Wo", "ln2_g", "ln2_b", "W1s", "W2s")}
         buf["save"] = block.workspace(tp.tp_layer_save_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
@@ -365,6 +398,13 @@ def run_gpu(args, w) -> None:
             if w.backward:
                 tp.tp_gmlp_bwd(dt, T, h, f, N, X, d["Wgus"], d["Wds"], buf["GU"], buf["A"], dZ, buf["dX"],
                                buf["dWgus"], buf["dWds"], buf["gws"], stream)
+            return buf["Z"], buf["dX"] if w.backward else None
+        if w.kind == "gqa":
+            tp.tp_gqa_fwd(dt, w.B, w.S, h, w.H, w.Hkv, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
+                          buf["LSE"], buf["Z"], buf["qws"], stream)
+            if w.backward:
+                tp.tp_gqa_bwd(dt, w.B, w.S, h, w.H, w.Hkv, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"],
+                              buf["O"], buf["LSE"], dZ, buf["dX"], buf["dWqkv"], buf["dWo"], buf["qws"], stream)
             return buf["Z"], buf["dX"] if w.backward else None
         if w.kind == "lnlayer":
             gr = buf["grads"]
@@ -461,7 +501,7 @@ def run_gpu(args, w) -> None:
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
-    if w.kind in ("mlp", "gmlp", "layer", "lnlayer", "attn"):
+    if w.kind in ("mlp", "gmlp", "layer", "lnlayer", "attn", "gqa"):
         hX = inp["X"].pin_memory()
         hdZ = inp["dZ"].pin_memory() if "dZ" in inp and w.backward else None
         dX_in = torch.empty_like(d["X"])

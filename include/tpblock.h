@@ -228,6 +228,33 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
                 const void* dZ, void* dX, void* dWqkv, void* dWo,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------- grouped-query attention block */
+
+/* The attention block with H query heads sharing Hkv key/value heads
+ * (grouped-query attention, named on wangyu.me 张量并行 §注意力机制中的张量并行
+ * next to multi-head attention; the page gives no formula).  Reading: query head
+ * j uses key/value head j / (H/Hkv) (consecutive query heads form a group); the
+ * head split puts query heads i*H/N .. (i+1)*H/N-1 and key/value heads
+ * i*Hkv/N .. (i+1)*Hkv/N-1 on shard i, so N must divide Hkv (every group stays on
+ * one shard; TP_ERR_SHAPE otherwise) and Hkv must divide H.  Hkv = H is exactly
+ * tp_attn_fwd / tp_attn_bwd (the same bytes in every layout).
+ *   Wqkv     [N][h][(H/N + 2 Hkv/N) d]   shard i: its query heads, then its key
+ *                                        heads, then its value heads, d columns each
+ *   Wo       [N][(H/N) d][h]             as tp_attn_fwd
+ *   QKV_save [N][T][(2 H/N + 3 Hkv/N) d] Q, K, V, then Q - bf16(Q), K - bf16(K)
+ *   O_save, LSE_save, Z, dX, dWo         as tp_attn_fwd / tp_attn_bwd
+ *   dWqkv    Wqkv's layout; a key/value head's gradient sums its group's query heads */
+TP_API size_t tp_gqa_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N);
+TP_API int tp_gqa_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal,
+                      const void* X, const void* Wqkv, const void* Wo,
+                      void* QKV_save, void* O_save, float* LSE_save, void* Z,
+                      void* ws, size_t ws_bytes, void* stream);
+TP_API int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal,
+                      const void* X, const void* Wqkv, const void* Wo,
+                      const void* QKV_save, const void* O_save, const float* LSE_save,
+                      const void* dZ, void* dX, void* dWqkv, void* dWo,
+                      void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------ LayerNorm and residuals */
 
 /* The pages keep LayerNorm, dropout and the residual connections outside the

@@ -45,6 +45,9 @@ _SIGS = {
     "tp_gmlp_workspace_bytes": ([i32, i64, i64, i64, i32], sz),
     "tp_gmlp_fwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
     "tp_gmlp_bwd": ([i32, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_gqa_workspace_bytes": ([i32, i64, i64, i64, i32, i32, i32, i32], sz),
+    "tp_gqa_fwd": ([i32, i64, i64, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
+    "tp_gqa_bwd": ([i32, i64, i64, i64, i32, i32, i32, i32, i32] + [vp] * 11 + [sz, vp], i32),
     "tp_layernorm_workspace_bytes": ([i32, i64, i64], sz),
     "tp_layernorm_fwd": ([i32, i64, i64, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp], i32),
     "tp_layernorm_bwd": ([i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], i32),
@@ -221,6 +224,38 @@ def tp_gmlp_bwd(dtype, T, h, f, N, X, Wgus, Wds, GU_save, A_save, dZ, dX, dWgus,
         _p(GU_save, "GU_save", dt, 2 * T * f), _p(A_save, "A_save", dt, T * f), _p(dZ, "dZ", dt, T * h),
         _p(dX, "dX", dt, T * h), _p(dWgus, "dWgus", dt, 2 * h * f), _p(dWds, "dWds", dt, f * h),
         wptr, wbytes, _stream(stream)), "tp_gmlp_bwd")
+
+
+# ---------------------------------------------------------------- grouped-query attention
+def tp_gqa_workspace_bytes(dtype: int, B: int, S: int, h: int, H: int, Hkv: int, d: int, N: int) -> int:
+    return load_library().tp_gqa_workspace_bytes(dtype, B, S, h, H, Hkv, d, N)
+
+
+def tp_gqa_fwd(dtype, B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, Z, ws=None,
+               stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    wptr, wbytes = _ws(ws, tp_gqa_workspace_bytes(dtype, B, S, h, H, Hkv, d, N))
+    return _check(load_library().tp_gqa_fwd(
+        dtype, B, S, h, H, Hkv, d, N, 1 if causal else 0, _p(X, "X", dt, T * h),
+        _p(Wqkv, "Wqkv", dt, h * (H + 2 * Hkv) * d), _p(Wo, "Wo", dt, H * d * h),
+        _p(QKV_save, "QKV_save", dt, T * (2 * H + 3 * Hkv) * d, False), _p(O_save, "O_save", dt, T * H * d, False),
+        _p(LSE_save, "LSE_save", torch.float32, B * H * S, False), _p(Z, "Z", dt, T * h), wptr, wbytes,
+        _stream(stream)), "tp_gqa_fwd")
+
+
+def tp_gqa_bwd(dtype, B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, dZ, dX, dWqkv, dWo,
+               ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    wptr, wbytes = _ws(ws, tp_gqa_workspace_bytes(dtype, B, S, h, H, Hkv, d, N))
+    return _check(load_library().tp_gqa_bwd(
+        dtype, B, S, h, H, Hkv, d, N, 1 if causal else 0, _p(X, "X", dt, T * h),
+        _p(Wqkv, "Wqkv", dt, h * (H + 2 * Hkv) * d), _p(Wo, "Wo", dt, H * d * h),
+        _p(QKV_save, "QKV_save", dt, T * (2 * H + 3 * Hkv) * d), _p(O_save, "O_save", dt, T * H * d),
+        _p(LSE_save, "LSE_save", torch.float32, B * H * S), _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h),
+        _p(dWqkv, "dWqkv", dt, h * (H + 2 * Hkv) * d), _p(dWo, "dWo", dt, H * d * h), wptr, wbytes,
+        _stream(stream)), "tp_gqa_bwd")
 
 
 # ---------------------------------------------------------------- LayerNorm, pre-norm layer

@@ -108,6 +108,38 @@ def attn_forward(X, Wqkv, Wo, B_: int, S: int, causal: bool = True, save: bool =
     return {"Z": Z, "QKV": QKV, "O": O, "LSE": LSE}
 
 
+def gqa_forward(X, Wqkv, Wo, H: int, Hkv: int, d: int, B_: int, S: int, causal: bool = True, ws=None,
+                stream=None) -> dict:
+    """Grouped-query attention block: Wqkv [N][h][(H/N + 2 Hkv/N) d]."""
+    N, h, _ = Wqkv.shape
+    T = B_ * S
+    dt = _dtype(X)
+    dev = X.device
+    Z = torch.empty(T, h, dtype=X.dtype, device=dev)
+    QKV = torch.empty(N, T, (2 * H + 3 * Hkv) * d // N, dtype=X.dtype, device=dev)
+    O = torch.empty(N, T, H * d // N, dtype=X.dtype, device=dev)
+    LSE = torch.empty(B_, H, S, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(B.tp_gqa_workspace_bytes(dt, B_, S, h, H, Hkv, d, N), dev)
+    B.tp_gqa_fwd(dt, B_, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV, O, LSE, Z, ws, stream)
+    return {"Z": Z, "QKV": QKV, "O": O, "LSE": LSE}
+
+
+def gqa_backward(X, Wqkv, Wo, QKV, O, LSE, dZ, H: int, Hkv: int, d: int, B_: int, S: int, causal: bool = True,
+                 ws=None, stream=None) -> dict:
+    N, h, _ = Wqkv.shape
+    T = B_ * S
+    dt = _dtype(X)
+    dev = X.device
+    out = {"dX": torch.empty(T, h, dtype=X.dtype, device=dev), "dWqkv": torch.empty_like(Wqkv),
+           "dWo": torch.empty_like(Wo)}
+    if ws is None:
+        ws = workspace(B.tp_gqa_workspace_bytes(dt, B_, S, h, H, Hkv, d, N), dev)
+    B.tp_gqa_bwd(dt, B_, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV, O, LSE, dZ, out["dX"], out["dWqkv"], out["dWo"],
+                 ws, stream)
+    return out
+
+
 def attn_backward(X, Wqkv, Wo, QKV, O, LSE, dZ, B_: int, S: int, causal: bool = True, ws=None, stream=None,
                   out=None) -> dict:
     N, h, _, hN, d = Wqkv.shape

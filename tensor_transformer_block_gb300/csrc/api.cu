@@ -82,26 +82,26 @@ int mlp_shape_check(int dtype, int64_t T, int64_t h, int64_t f, int N) {
   return TP_OK;
 }
 
-// Shape rules of the attention block.
-int attn_shape_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N) {
+// Shape rules of the attention block (H query heads, Hkv key/value heads).
+int attn_shape_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N) {
   if (dtype != TP_BF16) return TP_ERR_DTYPE;
-  if (B < 1 || S < 1 || h < 1 || H < 1 || d < 1 || N < 1) return TP_ERR_SHAPE;
-  if (H % N) return TP_ERR_SHAPE;
+  if (B < 1 || S < 1 || h < 1 || H < 1 || Hkv < 1 || d < 1 || N < 1) return TP_ERR_SHAPE;
+  if (H % N || H % Hkv || Hkv % N) return TP_ERR_SHAPE;
   if (d != 64 && d != 128) return TP_ERR_SHAPE;
   if (h % 8) return TP_ERR_SHAPE;
   if (B > 65535 || H > 65535 || B * S > (1ll << 31) - 1 || h > (1ll << 31) - 1) return TP_ERR_SHAPE;
   return TP_OK;
 }
 
-// Workspace of the attention block: [QKV (5 planes) | O | LSE] in the forward;
-// [dQKV (3 planes) | dO | Dsum] in the backward fits the same regions.
+// Workspace of the attention block: [QKV (Q, K, V and the residual planes) | O |
+// LSE] in the forward; [dQKV | dO | Dsum] in the backward fits the same regions.
 struct AttnWs {
   size_t qkv, o, lse, total;
 };
-AttnWs attn_ws(int64_t B, int64_t S, int H, int d) {
+AttnWs attn_ws(int64_t B, int64_t S, int H, int Hkv, int d) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
   AttnWs w;
-  w.qkv = round_up(T * tpb::kQkvPlanes * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
+  w.qkv = round_up(T * (2 * static_cast<size_t>(H) + 3 * static_cast<size_t>(Hkv)) * static_cast<size_t>(d) * 2, 256);
   w.o = round_up(T * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
   w.lse = round_up(T * static_cast<size_t>(H) * 4, 256);
   w.total = w.qkv + w.o + w.lse;
@@ -112,7 +112,7 @@ AttnWs attn_ws(int64_t B, int64_t S, int H, int d) {
 
 extern "C" {
 
-int tp_version(void) { return (0 << 16) | 5; }
+int tp_version(void) { return (0 << 16) | 6; }
 
 const char* tp_status_string(int s) {
   switch (s) {
@@ -180,26 +180,30 @@ int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const voi
   return gemm_status(rc);
 }
 
-// Attention forward kernels: a7, a8, a9.  With ``residual`` ([T][h]) the output
-// projection's epilogue adds it: Z = residual + sum_i O_i Wo_i.
-int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X, const void* Wqkv,
-                 const void* Wo, void* QKV, void* Ob, float* LSE, void* Z, const void* residual, unsigned* err,
-                 cudaStream_t st) {
-  const int hN = H / N;
-  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
+tpb::AttnDims attn_dims(int64_t B, int64_t S, int H, int Hkv, int d, int N, int causal) {
+  return tpb::AttnDims{static_cast<int>(B), static_cast<int>(S), H, H / N, N, d, causal ? 1 : 0, Hkv, Hkv / N};
+}
+
+// Attention forward kernels: a7, a8, a9 (H query heads, Hkv key/value heads).
+// With ``residual`` ([T][h]) the output projection's epilogue adds it:
+// Z = residual + sum_i O_i Wo_i.
+int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
+                 const void* Wqkv, const void* Wo, void* QKV, void* Ob, float* LSE, void* Z, const void* residual,
+                 unsigned* err, cudaStream_t st) {
+  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+  const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, kvd = static_cast<int64_t>(ad.hkvN) * d;
   // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
-  // writes the bf16 residuals of Q and K as planes 3 and 4 (split-bf16 scores)
+  // writes the bf16 residuals of Q and K after them (split-bf16 scores)
   const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
-  const tpb::GemmOperand opW{Wqkv, 3 * hNd, h, N, true, 1, 0};
+  const tpb::GemmOperand opW{Wqkv, hNd + 2 * kvd, h, N, true, 1, 0};
   tpb::GemmExtra split;
-  split.ldc = tpb::kQkvPlanes * hNd;
-  split.split_cols = 2 * hNd;
-  split.lo_off = 3 * hNd;
-  int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, 3 * hNd, N, 1, h, err,
+  split.ldc = ad.qkv_width();
+  split.split_cols = hNd + kvd;
+  split.lo_off = hNd + 2 * kvd;
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, hNd + 2 * kvd, N, 1, h, err,
                                  kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
   if (rc) return gemm_status(rc);
   // a8: per-head causal attention
-  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
   rc = tpb::launch_attn_fwd(ad, QKV, Ob, LSE, err, kWaitTimeoutNs, st);
   if (rc) return gemm_status(rc);
   // a9: Z = sum_i O_i Wo_i  (row-parallel, shard sum in the accumulator)
@@ -419,20 +423,24 @@ int tp_gmlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X
 // ------------------------------------------------------------ attention block
 extern "C" {
 
-size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N) {
-  if (attn_shape_check(dtype, B, S, h, H, d, N) != TP_OK) return 0;
-  return attn_ws(B, S, H, d).total;
+size_t tp_gqa_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N) {
+  if (attn_shape_check(dtype, B, S, h, H, Hkv, d, N) != TP_OK) return 0;
+  return attn_ws(B, S, H, Hkv, d).total;
 }
 
-int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
-                const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
-                size_t ws_bytes, void* stream) {
-  const int sc = attn_shape_check(dtype, B, S, h, H, d, N);
+size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N) {
+  return tp_gqa_workspace_bytes(dtype, B, S, h, H, H, d, N);
+}
+
+int tp_gqa_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
+               const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
+               size_t ws_bytes, void* stream) {
+  const int sc = attn_shape_check(dtype, B, S, h, H, Hkv, d, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !Z) return TP_ERR_NULL;
   if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(Z) || !al16(QKV_save) || !al16(O_save) || !al16(LSE_save))
     return TP_ERR_ALIGN;
-  const AttnWs w = attn_ws(B, S, H, d);
+  const AttnWs w = attn_ws(B, S, H, Hkv, d);
   char* wsb = static_cast<char*>(ws);
   if (!QKV_save || !O_save || !LSE_save) {
     if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
@@ -445,27 +453,34 @@ int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
   void* QKV = QKV_save ? QKV_save : static_cast<void*>(wsb);
   void* Ob = O_save ? O_save : static_cast<void*>(wsb + w.qkv);
   float* LSE = LSE_save ? LSE_save : reinterpret_cast<float*>(wsb + w.qkv + w.o);
-  return attn_fwd_seq(B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV, Ob, LSE, Z, nullptr, err, st);
+  return attn_fwd_seq(B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV, Ob, LSE, Z, nullptr, err, st);
 }
 
-int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
-                const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
-                const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
-  const int sc = attn_shape_check(dtype, B, S, h, H, d, N);
+int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
+                const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
+                size_t ws_bytes, void* stream) {
+  return tp_gqa_fwd(dtype, B, S, h, H, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, Z, ws, ws_bytes,
+                    stream);
+}
+
+int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
+               const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
+               const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = attn_shape_check(dtype, B, S, h, H, Hkv, d, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !QKV_save || !O_save || !LSE_save || !dZ || !dX || !dWqkv || !dWo) return TP_ERR_NULL;
   if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(QKV_save) || !al16(O_save) || !al16(LSE_save) || !al16(dZ) ||
       !al16(dX) || !al16(dWqkv) || !al16(dWo))
     return TP_ERR_ALIGN;
-  const AttnWs w = attn_ws(B, S, H, d);
+  const AttnWs w = attn_ws(B, S, H, Hkv, d);
   if (!ws || ws_bytes < w.total) return TP_ERR_WORKSPACE;
   if (!al256(ws)) return TP_ERR_ALIGN;
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int hN = H / N;
-  const int64_t T = B * S, hNd = static_cast<int64_t>(hN) * d;
+  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+  const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, gw = ad.dqkv_width();
   char* wsb = static_cast<char*>(ws);
   void* dQKV = wsb;
   void* dO = wsb + w.qkv;
@@ -484,21 +499,27 @@ int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
                              st, tpb::kKAttnDwo);
   if (rc) return gemm_status(rc);
   // attention core backward -> dQKV
-  const tpb::AttnDims ad{static_cast<int>(B), static_cast<int>(S), H, hN, N, d, causal ? 1 : 0};
   rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
   if (rc) return gemm_status(rc);
   // dWqkv_i = X^T dQKV_i
   const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
-  const tpb::GemmOperand opdQn{dQKV, 3 * hNd, T, N, true, 1, 0};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, 3 * hNd, N, 1, T, err,
-                             kWaitTimeoutNs, st, tpb::kKAttnDwqkv);
+  const tpb::GemmOperand opdQn{dQKV, gw, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, gw, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKAttnDwqkv);
   if (rc) return gemm_status(rc);
   // dX = sum_i dQKV_i Wqkv_i^T  (the column split's backward all-reduce, in the accumulator)
-  const tpb::GemmOperand opdQk{dQKV, 3 * hNd, T, N, false, 0, 1};
-  const tpb::GemmOperand opWk{Wqkv, 3 * hNd, h, N, false, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, 3 * hNd, err,
-                             kWaitTimeoutNs, st, tpb::kKAttnDx);
+  const tpb::GemmOperand opdQk{dQKV, gw, T, N, false, 0, 1};
+  const tpb::GemmOperand opWk{Wqkv, gw, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, gw, err, kWaitTimeoutNs, st,
+                             tpb::kKAttnDx);
   return gemm_status(rc);
+}
+
+int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
+                const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
+                const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
+  return tp_gqa_bwd(dtype, B, S, h, H, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, dZ, dX, dWqkv, dWo,
+                    ws, ws_bytes, stream);
 }
 
 }  // extern "C"
@@ -515,7 +536,7 @@ struct LayerSave {
 LayerSave layer_save(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
   const size_t th = round_up(T * static_cast<size_t>(h) * 2, 256), tv = round_up(T * 4, 256);
-  const AttnWs aw = attn_ws(B, S, H, d);
+  const AttnWs aw = attn_ws(B, S, H, H, d);
   LayerSave L;
   size_t o = 0;
   L.ln1 = o;   o += th;
@@ -541,7 +562,7 @@ struct LayerWs {
 LayerWs layer_ws(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
   const size_t th = round_up(T * static_cast<size_t>(h) * 2, 256);
-  const size_t a = attn_ws(B, S, H, d).total, m = round_up(T * static_cast<size_t>(f) * 2, 256);
+  const size_t a = attn_ws(B, S, H, H, d).total, m = round_up(T * static_cast<size_t>(f) * 2, 256);
   LayerWs w;
   w.blk = 0;
   w.dln = a > m ? a : m;
@@ -552,7 +573,7 @@ LayerWs layer_ws(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
 }
 
 int layer_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
-  int c = attn_shape_check(dtype, B, S, h, H, d, N);
+  int c = attn_shape_check(dtype, B, S, h, H, H, d, N);
   if (c != TP_OK) return c;
   c = mlp_shape_check(dtype, B * S, h, f, N);
   if (c != TP_OK) return c;
@@ -633,7 +654,7 @@ int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64
   int rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st);
   if (rc) return gemm_status(rc);
   // H1 = X + Attn(LN1(X)): the residual is added in the output projection's epilogue
-  rc = attn_fwd_seq(B, S, h, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
+  rc = attn_fwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
                     reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st);
   if (rc) return rc;
   // LN2(H1)

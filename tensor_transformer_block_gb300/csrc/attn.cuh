@@ -1,12 +1,16 @@
 // Per-head fused causal attention on tcgen05 (forward and backward cores).
 //
-// Tensors are in the shard-major layouts of the boundary:
-//   QKV  [N][B][S][5][H/N][d]   planes: Q, K, V, then the bf16 residuals
-//                               Q - bf16(Q) and K - bf16(K) of the projection
-//   O    [N][B][S][H/N][d]
+// Tensors are in the shard-major layouts of the boundary.  H query heads share
+// Hkv key/value heads (grouped-query attention; Hkv = H is multi-head attention):
+// query head j uses key/value head j / (H/Hkv).  Per shard, hN = H/N query and
+// hkvN = Hkv/N key/value heads (io.zouht.com 张量并行 §2.2.1: each shard owns
+// whole heads; with GQA it owns whole groups):
+//   QKV  [N][B][S][W] with W = (2 hN + 3 hkvN) d: Q (hN heads), K (hkvN), V (hkvN),
+//        then the bf16 residuals Q - bf16(Q) (hN) and K - bf16(K) (hkvN)
+//   dQKV [N][B][S][(hN + 2 hkvN) d]: dQ, dK, dV
+//   O    [N][B][S][hN][d]
 //   LSE  [B][H][S] fp32          natural-log sum of exp of the scaled scores
-// Global head j lives in shard i = j / (H/N) as local head jj = j % (H/N)
-// (io.zouht.com 张量并行 §2.2.1: each shard owns whole heads).
+// Global query head j lives in shard i = j / hN as local head jj = j % hN.
 //
 // Scores are computed split-bf16: S = Qh Kh^T + Qh Kl^T + Ql Kh^T with Qh =
 // bf16(Q), Ql = bf16(Q - Qh) (same for K), which carries Q K^T to ~2^-16
@@ -23,17 +27,27 @@ namespace tpb {
 
 struct AttnDims {
   int B, S, H, hN, N, d, causal;
+  int Hkv, hkvN;  // key/value heads in total and per shard (= H, hN without grouping)
+  // column offsets (elements) of local head jj (query) or kv (key/value) in QKV
+  __host__ __device__ int qkv_width() const { return (2 * hN + 3 * hkvN) * d; }
+  __host__ __device__ int col_q(int jj) const { return jj * d; }
+  __host__ __device__ int col_k(int kv) const { return (hN + kv) * d; }
+  __host__ __device__ int col_v(int kv) const { return (hN + hkvN + kv) * d; }
+  __host__ __device__ int col_ql(int jj) const { return (hN + 2 * hkvN + jj) * d; }
+  __host__ __device__ int col_kl(int kv) const { return (2 * hN + 2 * hkvN + kv) * d; }
+  __host__ __device__ int dqkv_width() const { return (hN + 2 * hkvN) * d; }
+  __host__ __device__ int group() const { return hN / hkvN; }
 };
 
-// Number of d-wide planes per (token, local head) in QKV.
+// Number of d-wide planes per (token, local head) in QKV without grouping.
 constexpr int kQkvPlanes = 5;
 
 // Forward: O and LSE from QKV (returns 0, 1 bad arguments, 2 CUDA failure).
 int launch_attn_fwd(const AttnDims& a, const void* qkv, void* o, float* lse, unsigned* err,
                     unsigned long long timeout_ns, cudaStream_t st);
 
-// Backward cores.  Dsum[b][j][s] = sum_e dO * O over the head dim; dqkv
-// [N][B][S][3][H/N][d] gets dQ, dK, dV.
+// Backward cores.  Dsum[b][j][s] = sum_e dO * O over the head dim; dqkv gets dQ,
+// dK, dV (a key/value head's gradient summed over the query heads of its group).
 int launch_attn_bwd(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse,
                     float* dsum, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st);
 

@@ -2,7 +2,9 @@
 // these kernels differentiate the forward's definition (see include/tpblock.h):
 //   Dsum = rowsum(dO * O)                       (k_attn_dsum)
 //   P = exp(S/sqrt(d) - LSE), dS = P * (dP - Dsum), dP = dO V^T
-//   dV = P^T dO, dK = dS^T Q / sqrt(d)          (k_attn_dkdv: one CTA per key block)
+//   dV = P^T dO, dK = dS^T Q / sqrt(d)          (k_attn_dkdv: one CTA per key block of
+//                                                a key/value head, summing over the
+//                                                query heads of its group)
 //   dQ = dS K / sqrt(d)                         (k_attn_dq:   one CTA per query block)
 // Each CTA owns its output rows and loops over the blocks it needs, so results
 // are deterministic (no atomics).  P is recomputed from the saved LSE.
@@ -89,7 +91,8 @@ __device__ __forceinline__ void mma_kmajor(uint32_t d_tmem, uint32_t sa, uint32_
 }
 
 // ------------------------------------------------------------------ dK / dV
-// One CTA per (128-key block, head, batch); loops over 64-query blocks whose
+// One CTA per (128-key block, key/value head, batch); loops over the query heads
+// of the head's group and, for each, over the 64-query blocks whose
 // Qh, Ql, dO tiles and LSE / Dsum rows are double-buffered, as are the S^T and
 // dP^T tiles in TMEM, so block i+1's products run while the key-row threads turn
 // block i's scores into P^T and dS^T.
@@ -143,13 +146,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (a.S + QB - 1) / QB;
   const int kb = static_cast<int>(blockIdx.x);  // low key blocks have the most causal work: first
-  const int j = blockIdx.y, b = blockIdx.z;
-  const int shard = j / a.hN, jj = j % a.hN;
+  const int jkv = blockIdx.y, b = blockIdx.z;   // global key/value head
+  const int shard = jkv / a.hkvN, kvh = jkv % a.hkvN;
+  const int g = a.group();
   const int k0 = kb * BLK;
   const int q_start = a.causal ? (k0 / QB) : 0;
   const int nq = nqb - q_start;
-  const int cQh = jj * D, cKh = (a.hN + jj) * D, cV = (2 * a.hN + jj) * D;
-  const int cQl = (3 * a.hN + jj) * D, cKl = (4 * a.hN + jj) * D;
+  const int nit = nq * g;  // (query head of the group, query block) pairs
+  const int cKh = a.col_k(kvh), cV = a.col_v(kvh), cKl = a.col_kl(kvh);
+  const int dcK = a.hN * D + kvh * D, dcV = (a.hN + a.hkvN + kvh) * D;  // in dQKV
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < K_NB; ++i) {
@@ -172,7 +177,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const WaitCtx wdrain{err, never_flag, timeout_ns};
   // TMEM: S^T [s*64, +64), dP^T [128 + s*64, +64), dV [256, +D), dK [256+D, +D)
   const uint32_t tDV = tmem + 256, tDK = tmem + 256 + D;
-  const size_t row_base = (static_cast<size_t>(b) * a.H + j) * a.S;
+  // iteration it: local query head jq(it) of the group, query block q0(it)
+  auto jq_of = [&](int it) { return kvh * g + it / nq; };
+  auto q0_of = [&](int it) { return (q_start + it % nq) * QB; };
 
   if (warp == 4) {
     // producer warp: lane 0 issues the TMA copies; all lanes stage each block's
@@ -187,10 +194,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     int issued = 0;
-    for (int it = 0; it < nq; ++it) {
+    for (int it = 0; it < nit; ++it) {
       const int st = it & 1;
       const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
-      const int q0 = (q_start + it) * QB;
+      const int q0 = q0_of(it), jq = jq_of(it);
+      const size_t row_base = (static_cast<size_t>(b) * a.H + shard * a.hN + jq) * a.S;
       if (!__all_sync(0xffffffffu, mbar_wait(cm.bar(K_QE + st), ph ^ 1u, wc))) break;
       for (int t = lane; t < QB; t += 32) {
         const int q = q0 + t;
@@ -204,9 +212,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive_expect_tx(fb, 3 * C::QTILE);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          tma_load_4d(sQh(st) + c * 8192, &tmQKV64, fb, cQh + 64 * c, q0, b, shard);
-          tma_load_4d(sQl(st) + c * 8192, &tmQKV64, fb, cQl + 64 * c, q0, b, shard);
-          tma_load_4d(sDO(st) + c * 8192, &tmDO64, fb, jj * D + 64 * c, q0, b, shard);
+          tma_load_4d(sQh(st) + c * 8192, &tmQKV64, fb, a.col_q(jq) + 64 * c, q0, b, shard);
+          tma_load_4d(sQl(st) + c * 8192, &tmQKV64, fb, a.col_ql(jq) + 64 * c, q0, b, shard);
+          tma_load_4d(sDO(st) + c * 8192, &tmDO64, fb, jq * D + 64 * c, q0, b, shard);
         }
       }
       issued = it + 1;
@@ -235,10 +243,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_commit(cm.bar(K_STF + st));
         return true;
       };
-      if (ok && nq > 0) ok = issue_sd(0);
-      for (int it = 0; it < nq && ok; ++it) {
+      if (ok && nit > 0) ok = issue_sd(0);
+      for (int it = 0; it < nit && ok; ++it) {
         const int st = it & 1;
-        if (it + 1 < nq && !issue_sd(it + 1)) {
+        if (it + 1 < nit && !issue_sd(it + 1)) {
           ok = false;
           break;
         }
@@ -271,10 +279,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t trow = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t rsw = static_cast<uint32_t>(r & 7);
     bool ok = true;
-    for (int it = 0; it < nq; ++it) {
+    for (int it = 0; it < nit; ++it) {
       const int st = it & 1;
       const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
-      const int q0 = (q_start + it) * QB;
+      const int q0 = q0_of(it);
       ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_STF + st), ph, wc) && mbar_wait(cm.bar(K_QF + st), ph, wc));
       if (!ok) break;
       tc_fence_after();
@@ -336,8 +344,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0 && k0 + warp * 32 < a.S) {
 #pragma unroll
         for (int cb = 0; cb < C::CH; ++cb) {
-          tma_store_4d(&tmDQKV, stV + cb * 4096, cV + 64 * cb, k0 + warp * 32, b, shard);
-          tma_store_4d(&tmDQKV, stK + cb * 4096, cKh + 64 * cb, k0 + warp * 32, b, shard);
+          tma_store_4d(&tmDQKV, stV + cb * 4096, dcV + 64 * cb, k0 + warp * 32, b, shard);
+          tma_store_4d(&tmDQKV, stK + cb * 4096, dcK + 64 * cb, k0 + warp * 32, b, shard);
         }
         bulk_commit();
       }
@@ -404,12 +412,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nb = (a.S + BLK - 1) / BLK;
   const int qb = nb - 1 - static_cast<int>(blockIdx.x);
   const int j = blockIdx.y, b = blockIdx.z;
-  const int shard = j / a.hN, jj = j % a.hN;
+  const int shard = j / a.hN, jj = j % a.hN, kvh = jj / a.group();
   const int q0 = qb * BLK;
   const int nkb = (a.S + KBQ - 1) / KBQ;
   const int nkv = a.causal ? min((min(q0 + BLK, a.S) - 1) / KBQ + 1, nkb) : nkb;
-  const int cQh = jj * D, cKh = (a.hN + jj) * D, cV = (2 * a.hN + jj) * D;
-  const int cQl = (3 * a.hN + jj) * D, cKl = (4 * a.hN + jj) * D;
+  const int cQh = a.col_q(jj), cKh = a.col_k(kvh), cV = a.col_v(kvh);
+  const int cQl = a.col_ql(jj), cKl = a.col_kl(kvh);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Q_NB; ++i) {
@@ -570,7 +578,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0 && q0 + warp * 32 < a.S) {
 #pragma unroll
-        for (int cb = 0; cb < C::CH; ++cb) tma_store_4d(&tmDQKV, stQ + cb * 4096, cQh + 64 * cb, q0 + warp * 32, b, shard);
+        for (int cb = 0; cb < C::CH; ++cb) tma_store_4d(&tmDQKV, stQ + cb * 4096, jj * D + 64 * cb, q0 + warp * 32, b, shard);
         bulk_commit();
       }
     }
@@ -600,8 +608,8 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   }
   const uint64_t S = static_cast<uint64_t>(a.S), Bb = static_cast<uint64_t>(a.B), Nn = static_cast<uint64_t>(a.N);
   CUtensorMap tq128, tq64, tdo128, tdo64, tdq;
-  const uint64_t qd[4] = {static_cast<uint64_t>(kQkvPlanes) * a.hN * D, S, Bb, Nn};
-  const uint64_t gd[4] = {static_cast<uint64_t>(3) * a.hN * D, S, Bb, Nn};
+  const uint64_t qd[4] = {static_cast<uint64_t>(a.qkv_width()), S, Bb, Nn};
+  const uint64_t gd[4] = {static_cast<uint64_t>(a.dqkv_width()), S, Bb, Nn};
   const uint64_t od[4] = {static_cast<uint64_t>(a.hN) * D, S, Bb, Nn};
   const uint32_t box128[4] = {64, 128, 1, 1};
   const uint32_t box64[4] = {64, 64, 1, 1};
@@ -626,9 +634,9 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   const int nb = (a.S + BLK - 1) / BLK;
   const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   const float scale_log2 = scale * kLog2e;
-  dim3 grid(nb, a.H, a.B);
+  const dim3 grid(nb, a.H, a.B), grid_kv(nb, a.Hkv, a.B);
   slot = timing_begin(kKAttnDkdv, st);
-  k_attn_dkdv<D><<<grid, NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq128, tq64, tdo64, tdq, lse, dsum, a, scale_log2,
+  k_attn_dkdv<D><<<grid_kv, NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq128, tq64, tdo64, tdq, lse, dsum, a, scale_log2,
                                                           scale, err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
@@ -646,6 +654,7 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
 int launch_attn_bwd(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse,
                     float* dsum, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
   if (a.B < 1 || a.S < 1 || a.H < 1 || a.N < 1 || a.hN * a.N != a.H) return 1;
+  if (a.Hkv < 1 || a.hkvN * a.N != a.Hkv || a.H % a.Hkv || a.hN % a.hkvN) return 1;
   if (a.H > 65535 || a.B > 65535) return 1;
   if (a.d == 128) return launch_bwd_d<128>(a, qkv, o, dout, lse, dsum, dqkv, err, timeout_ns, st);
   if (a.d == 64) return launch_bwd_d<64>(a, qkv, o, dout, lse, dsum, dqkv, err, timeout_ns, st);

@@ -3,8 +3,8 @@
 // (damodev 3D并行 §1.2.2 per-head attention; the blockwise online-softmax
 // recurrence is the one sunjinbo 并行方式 §CP uses to combine per-block results).
 //
-// One CTA per (256 queries = two 128-query tiles, head, batch), heaviest causal
-// blocks first.  Keys are processed in blocks of 64; K and V each have two
+// One CTA per (256 queries = two 128-query tiles, query head, batch), heaviest
+// causal blocks first; the key/value tiles are those of the head's group.  Keys are processed in blocks of 64; K and V each have two
 // shared-memory stages, so the copies of block kv+1 overlap the work on block kv.
 //   warp 8: TMA producer: both tiles' Qh, Ql once; Kh, Kl and V per key block
 //   warp 9: MMA issuer: per key block, S = Qh Kh^T + Qh Kl^T + Ql Kh^T (split-bf16
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nqb = (a.S + QT * BQ - 1) / (QT * BQ);
   const int qb = nqb - 1 - static_cast<int>(blockIdx.x);
   const int j = blockIdx.y, b = blockIdx.z;
-  const int shard = j / a.hN, jj = j % a.hN;
+  const int shard = j / a.hN, jj = j % a.hN, kvh = jj / a.group();
   const int q0 = qb * QT * BQ;
   const int nkb = (a.S + BKV - 1) / BKV;
   // key blocks each tile needs (causal: up to its last query)
@@ -120,8 +120,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     nkv_t[t] = (q0 + t * BQ >= a.S) ? 0 : (a.causal ? min(qlast / BKV + 1, nkb) : nkb);
   }
   const int nkv = max(nkv_t[0], nkv_t[1]);
-  const int cQh = jj * D, cKh = (a.hN + jj) * D, cV = (2 * a.hN + jj) * D;
-  const int cQl = (3 * a.hN + jj) * D, cKl = (4 * a.hN + jj) * D;
+  const int cQh = a.col_q(jj), cKh = a.col_k(kvh), cV = a.col_v(kvh);
+  const int cQl = a.col_ql(jj), cKl = a.col_kl(kvh);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBARS; ++i) {
@@ -386,7 +386,7 @@ int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsign
     configured = true;
   }
   CUtensorMap tq, tkv, to;
-  const uint64_t qd[4] = {static_cast<uint64_t>(kQkvPlanes) * a.hN * D, static_cast<uint64_t>(a.S),
+  const uint64_t qd[4] = {static_cast<uint64_t>(a.qkv_width()), static_cast<uint64_t>(a.S),
                           static_cast<uint64_t>(a.B), static_cast<uint64_t>(a.N)};
   const uint32_t qbox[4] = {64, 128, 1, 1};
   const uint32_t kbox[4] = {64, BKV, 1, 1};
@@ -411,6 +411,7 @@ int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsign
 int launch_attn_fwd(const AttnDims& a, const void* qkv, void* o, float* lse, unsigned* err,
                     unsigned long long timeout_ns, cudaStream_t st) {
   if (a.B < 1 || a.S < 1 || a.H < 1 || a.N < 1 || a.hN * a.N != a.H) return 1;
+  if (a.Hkv < 1 || a.hkvN * a.N != a.Hkv || a.H % a.Hkv || a.hN % a.hkvN) return 1;
   if (a.H > 65535 || a.B > 65535) return 1;
   if (a.d == 128) return launch_fwd_d<128>(a, qkv, o, lse, err, timeout_ns, st);
   if (a.d == 64) return launch_fwd_d<64>(a, qkv, o, lse, err, timeout_ns, st);

@@ -27,7 +27,7 @@ from dataclasses import dataclass
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", "layer_inputs", "prenorm_inputs",
-           "ln_inputs",
+           "ln_inputs", "gqa_inputs", "split_qkv_gqa",
            "split_columns", "split_rows", "split_qkv_heads"]
 
 
@@ -35,7 +35,7 @@ __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", 
 class Workload:
     """One of the synthetic workloads the block is checked and measured on."""
     name: str
-    kind: str            # "mlp", "gmlp" (gated MLP), "attn", "layer" or "lnlayer" (pre-norm layer)
+    kind: str            # "mlp", "gmlp" (gated MLP), "attn", "gqa", "layer" or "lnlayer" (pre-norm layer)
     dtype: str           # "f32" or "bf16"
     backward: bool
     T: int = 0           # tokens = B*S
@@ -46,6 +46,7 @@ class Workload:
     S: int = 0
     H: int = 0
     d: int = 0
+    Hkv: int = 0         # key/value heads (grouped-query attention)
     causal: bool = True
     x_std: float = 1.0
     w_std: float = 0.02
@@ -73,6 +74,9 @@ WORKLOADS = {
     "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
         "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "lnlayer", "bf16", True,
         T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
+    "gqa_bf16_B2_S2048_h4096_H32_Hkv8_d128_N8": Workload("gqa_bf16_B2_S2048_h4096_H32_Hkv8_d128_N8", "gqa",
+                                                         "bf16", True, T=4096, h=4096, N=8, B=2, S=2048, H=32,
+                                                         d=128, Hkv=8),
     "gmlp_bf16_T8192_h4096_f12288_N8": Workload("gmlp_bf16_T8192_h4096_f12288_N8", "gmlp", "bf16", True,
                                                 T=8192, h=4096, f=12288, N=8),
 }
@@ -171,6 +175,31 @@ def layer_inputs(B: int, S: int, h: int, H: int, d: int, f: int, N: int, dtype: 
             "W1s": split_columns(W1, N), "W2s": split_rows(W2, N), "dZ": dZ}
 
 
+def split_qkv_gqa(Wq: torch.Tensor, Wk: torch.Tensor, Wv: torch.Tensor, n: int) -> torch.Tensor:
+    """[h][H d], [h][Hkv d], [h][Hkv d] -> [n][h][(H/n + 2 Hkv/n) d]: shard i holds its
+    query heads' columns, then its key heads', then its value heads'."""
+    q, k, v = (w.reshape(w.shape[0], n, w.shape[1] // n) for w in (Wq, Wk, Wv))
+    return torch.cat([q, k, v], dim=2).permute(1, 0, 2).contiguous()
+
+
+def gqa_inputs(B: int, S: int, h: int, H: int, Hkv: int, d: int, N: int, dtype: str = "bf16", seed: int = 0,
+               x_std: float = 1.0, w_std: float = 0.02, backward: bool = True) -> dict:
+    """Grouped-query attention: X [B*S][h], Wqkv [N][h][(H/N + 2 Hkv/N) d] (W_Q, W_K,
+    W_V drawn in that order), Wo [N][H/N*d][h], dZ [B*S][h]."""
+    if N < 1 or H % Hkv or Hkv % N:
+        raise ValueError("Hkv must divide H and N must divide Hkv")
+    gen = torch.Generator().manual_seed(seed)
+    X = _draw(gen, (B * S, h), x_std, dtype)
+    Wq = _draw(gen, (h, H * d), w_std, dtype)
+    Wk = _draw(gen, (h, Hkv * d), w_std, dtype)
+    Wv = _draw(gen, (h, Hkv * d), w_std, dtype)
+    Wo = _draw(gen, (H * d, h), w_std, dtype)
+    out = {"X": X, "Wqkv": split_qkv_gqa(Wq, Wk, Wv, N), "Wo": split_rows(Wo, N)}
+    if backward:
+        out["dZ"] = _draw(gen, (B * S, h), 1.0, dtype)
+    return out
+
+
 def ln_inputs(T: int, h: int, dtype: str = "bf16", seed: int = 0, x_std: float = 1.0, x_mean: float = 0.0,
               ln_std: float = 0.1) -> dict:
     """LayerNorm alone: X [T][h] ~ N(x_mean, x_std^2), gamma ~ 1 + N(0, ln_std^2),
@@ -215,6 +244,9 @@ def workload_inputs(w: Workload, **overrides) -> dict:
     if p["kind"] == "gmlp":
         return gmlp_inputs(p["T"], p["h"], p["f"], p["N"], p["dtype"], p["seed"], p["x_std"],
                            p["w_std"], p["backward"])
+    if p["kind"] == "gqa":
+        return gqa_inputs(p["B"], p["S"], p["h"], p["H"], p["Hkv"], p["d"], p["N"], p["dtype"], p["seed"],
+                          p["x_std"], p["w_std"], p["backward"])
     if p["kind"] == "attn":
         return attn_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["N"], p["dtype"], p["seed"],
                            p["x_std"], p["w_std"], p["backward"])

@@ -85,6 +85,18 @@ def test_gmlp_validation_before_cuda(lib):
     assert bwd == 1                                     # GU_save is required
 
 
+def test_gqa_validation_before_cuda(lib):
+    f = lambda **k: lib.tp_gqa_fwd(1, 2, 128, 512, k.get("H", 8), k.get("Hkv", 2), 64, k.get("N", 2), 1, 16, 16, 16,
+                                   None, None, None, 16, None, 0, None)
+    assert f(Hkv=3) == 2                                # Hkv does not divide H
+    assert f(Hkv=2, N=4) == 2                           # N does not divide Hkv
+    assert f() == 4                                     # valid: wants a workspace for the unsaved tensors
+    assert tp.tp_gqa_workspace_bytes(tp.TP_BF16, 2, 128, 512, 8, 8, 64, 2) == \
+        tp.tp_attn_workspace_bytes(tp.TP_BF16, 2, 128, 512, 8, 64, 2)
+    assert tp.tp_gqa_workspace_bytes(tp.TP_BF16, 2, 128, 512, 8, 2, 64, 2) < \
+        tp.tp_attn_workspace_bytes(tp.TP_BF16, 2, 128, 512, 8, 64, 2)
+
+
 def test_attention_validation_before_cuda(lib):
     f = lambda **k: lib.tp_attn_fwd(k.get("dt", 1), k.get("B", 2), k.get("S", 128), k.get("h", 512),
                                     k.get("H", 8), k.get("d", 64), k.get("N", 2), 1, k.get("X", 16), 16, 16,
