@@ -57,6 +57,7 @@ __all__ = [
     "prenorm_layer_forward_rows",
     "unpack_qkv_gqa", "pack_qkv_gqa", "gqa_attention_forward", "gqa_attention_backward",
     "gqa_attention_forward_sharded",
+    "to_seq_shards", "from_seq_shards", "sp_prenorm_layer_forward", "sp_prenorm_layer_backward",
 ]
 
 SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
@@ -753,3 +754,77 @@ def gqa_attention_forward_sharded(X, Wqkv, Wo, B: int, S: int, H: int, Hkv: int,
         part = matmul(Oi, Wo[i])
         Z = part if Z is None else Z + part
     return Z
+
+
+# --------------------------------------------------------------------------
+# Tensor + sequence parallelism (zouht 张量并行 §2.2.2 与序列并行结合, §2.3): outside
+# the TP blocks the activations are split along the sequence, (batch, seq, hidden)
+# -> N x (batch, seq/N, hidden); entering a block an all-gather (g) rebuilds the
+# full sequence, leaving it a reduce-scatter (g*) sums the shards' partial outputs
+# and hands each sequence shard its rows.
+# --------------------------------------------------------------------------
+def to_seq_shards(X, B: int, S: int, n: int) -> np.ndarray:
+    """[B*S][h] (token t = b*S + s) -> [n][B][S/n][h]: shard c holds positions
+    c*S/n .. (c+1)*S/n - 1 of every sequence."""
+    X = _f64(X)
+    return np.ascontiguousarray(X.reshape(B, n, S // n, -1).transpose(1, 0, 2, 3))
+
+
+def from_seq_shards(Xs) -> np.ndarray:
+    """Inverse of :func:`to_seq_shards`."""
+    Xs = _f64(Xs)
+    n, B, L, h = Xs.shape
+    return np.ascontiguousarray(Xs.transpose(1, 0, 2, 3).reshape(B * n * L, h))
+
+
+def _all_gather_seq(shards):
+    """g: every shard's rows, concatenated along the sequence."""
+    return from_seq_shards(np.stack(shards))
+
+
+def _reduce_scatter_seq(partials, B: int, S: int, n: int):
+    """g*: the sum of the tensor shards' partial outputs, each sequence shard
+    receiving its own rows."""
+    total = partials[0]
+    for p in partials[1:]:
+        total = total + p
+    return list(to_seq_shards(total, B, S, n))
+
+
+def sp_prenorm_layer_forward(Xs, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, B: int, S: int,
+                             causal: bool = True, eps: float = LN_EPS) -> dict:
+    """:func:`prenorm_layer_forward` in the sequence-parallel form, step by step:
+    LayerNorm and the residual on each sequence shard, g before each block, the
+    block's per-tensor-shard partial outputs, g* after it.  Xs is [N][B][S/N][h];
+    returns Z and H1 in the same layout."""
+    n = Wqkv.shape[0]
+    xs = [_f64(x) for x in Xs]
+    ln1 = [layer_norm(x.reshape(-1, x.shape[-1]), ln1_g, ln1_b, eps)["y"].reshape(x.shape) for x in xs]
+    full = _all_gather_seq(ln1)
+    # attention block: tensor shard i holds heads i*H/N .. and Wo's rows for them
+    a = attention_forward(full, Wqkv, Wo, B, S, causal)
+    Wo_rows = np.asarray(Wo)
+    parts = [matmul(a["O"][i], Wo_rows[i]) for i in range(n)]
+    h1 = [x + r for x, r in zip(xs, _reduce_scatter_seq(parts, B, S, n))]
+    ln2 = [layer_norm(x.reshape(-1, x.shape[-1]), ln2_g, ln2_b, eps)["y"].reshape(x.shape) for x in h1]
+    full2 = _all_gather_seq(ln2)
+    m = mlp_forward(full2, W1s, W2s)
+    parts2 = [matmul(m["A"][i], _f64(W2s[i])) for i in range(n)]
+    z = [x + r for x, r in zip(h1, _reduce_scatter_seq(parts2, B, S, n))]
+    return {"Z": np.stack(z), "H1": np.stack(h1)}
+
+
+def sp_prenorm_layer_backward(Xs, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, dZs, B: int, S: int,
+                              causal: bool = True, eps: float = LN_EPS) -> dict:
+    """Gradients of <dZs, Z> for the sequence-parallel form.  The form computes the
+    same function of the same parameters, only with the activations laid out by
+    sequence shard, so the weight and LayerNorm gradients are those of the plain
+    layer and dX comes back in the shard layout (in the backward, g becomes a
+    reduce-scatter and g* an all-gather, the transposes of the forward's)."""
+    X = from_seq_shards(Xs)
+    g = prenorm_layer_backward(X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s, from_seq_shards(dZs), B, S,
+                               causal, eps)
+    n = Wqkv.shape[0]
+    out = {k: v for k, v in g.items() if k not in ("dX", "dH1")}
+    out["dX"] = to_seq_shards(g["dX"], B, S, n)
+    return out

@@ -734,3 +734,43 @@ def test_gqa_sharded_equals_unsharded():
         X, Wq, Wk, Wv, Wo, Wg, Wos, dZ = _gqa_inputs(B, S, H, Hkv, d, n, seed=6)
         assert rel(O.gqa_attention_forward_sharded(X, Wg, Wos, B, S, H, Hkv),
                    O.gqa_attention_forward(X, Wg, Wos, B, S, H, Hkv)["Z"]) < 1e-13, n
+
+
+# ---------------------------------------------------------------- sequence parallelism
+def test_seq_shard_layout_roundtrip_and_split_direction():
+    """The page's split: TP cuts (batch, seq, hidden) along hidden, SP along seq:
+    shard c of the SP layout holds positions c*S/N .. of every sequence, whole
+    hidden vectors."""
+    B, S, n, h = 3, 8, 4, 5
+    X = np.arange(B * S * h, dtype=np.float64).reshape(B * S, h)
+    Xs = O.to_seq_shards(X, B, S, n)
+    assert Xs.shape == (n, B, S // n, h)
+    for c in range(n):
+        for b in range(B):
+            for sl in range(S // n):
+                assert np.array_equal(Xs[c, b, sl], X[b * S + c * (S // n) + sl])
+    assert np.array_equal(O.from_seq_shards(Xs), X)
+
+
+def test_sp_layer_equals_tp_layer():
+    """TP + SP computes the same layer: all-gather before each block and
+    reduce-scatter after it give the all-reduce's sums, row by row."""
+    B, S, H, d, n, X, Wq, Wk, Wv, Wo, Wqkv, Wos, W1, W2, W1s, W2s, ln, dZ = _prenorm_inputs(seed=11)
+    ref = O.prenorm_layer_forward(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S)
+    sp = O.sp_prenorm_layer_forward(O.to_seq_shards(X, B, S, n), ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, B, S)
+    assert rel(O.from_seq_shards(sp["Z"]), ref["Z"]) < 1e-13
+    assert rel(O.from_seq_shards(sp["H1"]), ref["H1"]) < 1e-13
+    g = O.sp_prenorm_layer_backward(O.to_seq_shards(X, B, S, n), ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s,
+                                    O.to_seq_shards(dZ, B, S, n), B, S)
+    gr = O.prenorm_layer_backward(X, ln[0], ln[1], Wqkv, Wos, ln[2], ln[3], W1s, W2s, dZ, B, S)
+    assert rel(O.from_seq_shards(g["dX"]), gr["dX"]) < 1e-13
+    assert rel(g["dW1s"], gr["dW1s"]) < 1e-13 and rel(g["dln2_g"], gr["dln2_g"]) < 1e-13
+
+
+def test_sp_reduce_scatter_then_all_gather_is_all_reduce():
+    """The page's cost argument rests on all-reduce = reduce-scatter + all-gather:
+    the composition gives every shard the full sum."""
+    B, S, n, h = 2, 8, 4, 3
+    parts = [RNG.standard_normal((B * S, h)) for _ in range(n)]
+    rs = O._reduce_scatter_seq(parts, B, S, n)
+    assert rel(O._all_gather_seq(rs), sum(parts)) < 1e-15
