@@ -52,7 +52,7 @@ def kernel_flops(w) -> dict:
     """Algorithmic flops per launch of each kernel kind of the workload."""
     T, h, f = w.T, w.h, w.f
     out = {}
-    if w.kind in ("mlp", "layer", "lnlayer"):
+    if w.kind in ("mlp", "layer", "lnlayer", "splayer"):
         g = 2.0 * T * h * f
         out.update({"mlp.fc1_col_gemm_gelu": g, "mlp.fc2_row_gemm_shard_sum": g, "mlp.bwd_dA_gemm_dgelu": g,
                     "mlp.bwd_dW2_gemm": g, "mlp.bwd_dW1_gemm": g, "mlp.bwd_dX_row_gemm_shard_sum": g,
@@ -70,7 +70,7 @@ def kernel_flops(w) -> dict:
                     "attn.bwd_dWo_gemm": 2.0 * T * Hd * h, "attn.bwd_core_dkdv": 3.0 * pairs,
                     "attn.bwd_core_dq": 1.0 * pairs, "attn.bwd_dWqkv_gemm": 2.0 * T * h * qkv,
                     "attn.bwd_dX_row_gemm_shard_sum": 2.0 * T * qkv * h})
-    if w.kind in ("attn", "layer", "lnlayer"):
+    if w.kind in ("attn", "layer", "lnlayer", "splayer"):
         Hd = w.H * w.d
         pairs = w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d  # (causal half) x d
         out.update({"attn.qkv_col_gemm": 2.0 * T * h * 3 * Hd, "attn.core_fwd": 2.0 * pairs,
@@ -84,7 +84,7 @@ def kernel_flops(w) -> dict:
 def step_flops(w) -> float:
     T, h, f = w.T, w.h, w.f
     tot = 0.0
-    if w.kind in ("mlp", "layer", "lnlayer"):
+    if w.kind in ("mlp", "layer", "lnlayer", "splayer"):
         tot += (12.0 if w.backward else 4.0) * T * h * f
     if w.kind == "gmlp":
         tot += (18.0 if w.backward else 6.0) * T * h * f
@@ -94,7 +94,7 @@ def step_flops(w) -> float:
         tot += 2.0 * T * h * qkv + 2.0 * T * Hd * h + core
         if w.backward:
             tot += 4.0 * T * h * Hd + 4.0 * T * h * qkv + 2.0 * core
-    if w.kind in ("attn", "layer", "lnlayer"):
+    if w.kind in ("attn", "layer", "lnlayer", "splayer"):
         Hd = w.H * w.d
         core = 2.0 * w.B * w.H * (w.S * w.S if w.causal else 2 * w.S * w.S) * w.d
         tot += 8.0 * T * h * Hd + core
@@ -117,6 +117,10 @@ def describe(w) -> str:
     if w.kind == "attn":
         return (f"self-attention block fwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
                 f"{'causal' if w.causal else 'full'}, N={w.N} logical shards")
+    if w.kind == "splayer":
+        return (f"pre-norm layer in the tensor + sequence parallel form (X, Z, dZ, dX in {w.N} sequence shards of "
+                f"{w.S // w.N} positions) fwd+bwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
+                f"f={w.f}, causal, N={w.N} logical shards; LayerNorm and residual adds not counted in the flops")
     if w.kind == "lnlayer":
         return (f"pre-norm layer (LN, attention, residual, LN, MLP, residual) fwd+bwd, {w.dtype}, B={w.B} x "
                 f"S={w.S}, h={w.h}, {w.H} heads x d={w.d}, f={w.f}, causal, N={w.N} logical shards; LayerNorm and "
@@ -232,7 +236,7 @@ def oracle_step(w, inp_np: dict, rows: int) -> float:
         if w.backward:
             O.gqa_attention_backward(X, inp_np["Wqkv"], inp_np["Wo"], inp_np["dZ"][:rows], 1, rows, w.H, w.Hkv,
                                      w.causal)
-    elif w.kind == "lnlayer":
+    elif w.kind in ("lnlayer", "splayer"):
         args = (X, inp_np["ln1_g"], inp_np["ln1_b"], inp_np["Wqkv"], inp_np["Wo"], inp_np["ln2_g"], inp_np["ln2_b"],
                 inp_np["W1s"], inp_np["W2s"])
         O.prenorm_layer_forward(*args, 1, rows, True)
@@ -332,6 +336,7 @@ def run_gpu(args, w) -> None:
     tp.tp_set_gemm_tiling(args.gemm_tiling)
 
     inp = inputs.workload_inputs(w)
+    inp_tok = inp  # token-major copies (the oracle's layout)
     d = {k: v.to(dev) for k, v in inp.items()}
     stream = torch.cuda.current_stream(dev)
     dt = tp.TP_BF16 if w.dtype == "bf16" else tp.TP_F32
@@ -366,7 +371,12 @@ def run_gpu(args, w) -> None:
         buf["dWqkv"] = torch.empty_like(d["Wqkv"])
         buf["dWo"] = torch.empty_like(d["Wo"])
         buf["qws"] = block.workspace(tp.tp_gqa_workspace_bytes(dt, w.B, w.S, h, w.H, w.Hkv, w.d, N), dev)
-    if w.kind == "lnlayer":
+    if w.kind == "splayer":
+        # the sequence-parallel layout of the inputs the step consumes
+        d["X"] = inputs.to_seq_shards(d["X"], w.B, w.S, N)
+        d["dZ"] = inputs.to_seq_shards(d["dZ"], w.B, w.S, N)
+        inp = dict(inp, X=inputs.to_seq_shards(inp["X"], w.B, w.S, N), dZ=inputs.to_seq_shards(inp["dZ"], w.B, w.S, N))
+    if w.kind in ("lnlayer", "splayer"):
         p = {k: d[k] for k in ("ln1_g", "ln1_b", "Wqkv", "Wo", "ln2_g", "ln2_b", "W1s", "W2s")}
         buf["save"] = block.workspace(tp.tp_layer_save_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
         buf["lws"] = block.workspace(tp.tp_layer_workspace_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
@@ -406,13 +416,15 @@ def run_gpu(args, w) -> None:
                 tp.tp_gqa_bwd(dt, w.B, w.S, h, w.H, w.Hkv, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"],
                               buf["O"], buf["LSE"], dZ, buf["dX"], buf["dWqkv"], buf["dWo"], buf["qws"], stream)
             return buf["Z"], buf["dX"] if w.backward else None
-        if w.kind == "lnlayer":
+        if w.kind in ("lnlayer", "splayer"):
             gr = buf["grads"]
-            tp.tp_layer_fwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, 1e-5, X, p["ln1_g"], p["ln1_b"], p["Wqkv"],
-                            p["Wo"], p["ln2_g"], p["ln2_b"], p["W1s"], p["W2s"], buf["save"], buf["Z"], stream)
-            tp.tp_layer_bwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"],
-                            p["W1s"], p["W2s"], buf["save"], dZ, gr["dX"], gr["dln1_g"], gr["dln1_b"], gr["dWqkv"],
-                            gr["dWo"], gr["dln2_g"], gr["dln2_b"], gr["dW1s"], gr["dW2s"], buf["lws"], stream)
+            fwd, bwd = (tp.tp_sp_layer_fwd, tp.tp_sp_layer_bwd) if w.kind == "splayer" else (tp.tp_layer_fwd,
+                                                                                            tp.tp_layer_bwd)
+            fwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, 1e-5, X, p["ln1_g"], p["ln1_b"], p["Wqkv"], p["Wo"],
+                p["ln2_g"], p["ln2_b"], p["W1s"], p["W2s"], buf["save"], buf["Z"], stream)
+            bwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"], p["W1s"],
+                p["W2s"], buf["save"], dZ, gr["dX"], gr["dln1_g"], gr["dln1_b"], gr["dWqkv"], gr["dWo"], gr["dln2_g"],
+                gr["dln2_b"], gr["dW1s"], gr["dW2s"], buf["lws"], stream)
             return buf["Z"], gr["dX"]
         if w.kind == "attn":
             tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
@@ -501,7 +513,7 @@ def run_gpu(args, w) -> None:
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
-    if w.kind in ("mlp", "gmlp", "layer", "lnlayer", "attn", "gqa"):
+    if w.kind in ("mlp", "gmlp", "layer", "lnlayer", "splayer", "attn", "gqa"):
         hX = inp["X"].pin_memory()
         hdZ = inp["dZ"].pin_memory() if "dZ" in inp and w.backward else None
         dX_in = torch.empty_like(d["X"])
@@ -546,7 +558,7 @@ def run_gpu(args, w) -> None:
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         import torch as _t  # noqa: F401
-        cpu = cpu_baseline(w, {k: v.to(torch.float64).numpy() for k, v in inp.items()}, args.cpu_seconds)
+        cpu = cpu_baseline(w, {k: v.to(torch.float64).numpy() for k, v in inp_tok.items()}, args.cpu_seconds)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

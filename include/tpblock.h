@@ -321,6 +321,32 @@ TP_API int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d
                         void* dln2_g, void* dln2_b, void* dW1s, void* dW2s,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* The same pre-norm layer in the tensor + sequence parallel form (io.zouht.com
+ * 张量并行 §2.2.2 与序列并行结合 and §2.3): outside the blocks, X, Z, dZ, dX (and the
+ * saved LayerNorm outputs and H1) are split along the sequence into N shards,
+ *   X, Z, dZ, dX   [N][B][S/N][h]   shard c holds positions c*S/N .. (c+1)*S/N-1
+ *                                   of every sequence
+ * LayerNorm and the residual adds work shard by shard.  Where the pages place an
+ * all-gather before a block (g) the column-parallel GEMM's TMA copies read the
+ * rows of every shard in sequence order; where they place a reduce-scatter after
+ * it (g*) the row-parallel GEMM sums the tensor shards in its accumulator and its
+ * stores put each row in its sequence shard.  No extra pass over memory is made.
+ * Requires S/N to be a multiple of 128 (no GEMM tile spans two shards; else
+ * TP_ERR_SHAPE); everything else as tp_layer_fwd / tp_layer_bwd, whose save
+ * buffer and workspace sizes apply. */
+TP_API int tp_sp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N,
+                           int causal, float eps,
+                           const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                           const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s,
+                           void* save, size_t save_bytes, void* Z, void* stream);
+TP_API int tp_sp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                           const void* X, const void* ln1_g, const void* Wqkv, const void* Wo,
+                           const void* ln2_g, const void* W1s, const void* W2s,
+                           const void* save, size_t save_bytes, const void* dZ,
+                           void* dX, void* dln1_g, void* dln1_b, void* dWqkv, void* dWo,
+                           void* dln2_g, void* dln2_b, void* dW1s, void* dW2s,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /* Launches one block whose single thread waits on a shared-memory barrier that

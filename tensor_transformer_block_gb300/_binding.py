@@ -56,6 +56,9 @@ _SIGS = {
     "tp_layer_fwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32, ctypes.c_float] + [vp] * 10 + [sz, vp, vp], i32),
     "tp_layer_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 8 + [sz] + [vp] * 10 + [vp, sz, vp],
                      i32),
+    "tp_sp_layer_fwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32, ctypes.c_float] + [vp] * 10 + [sz, vp, vp], i32),
+    "tp_sp_layer_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 8 + [sz] + [vp] * 10 + [vp, sz, vp],
+                        i32),
     "tp_set_gemm_tiling": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
@@ -289,32 +292,58 @@ def tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N) -> int:
     return load_library().tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N)
 
 
-def tp_layer_fwd(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
-                 save, Z, stream=None) -> int:
+def _layer_fwd(name, dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+               save, Z, stream):
     dt = _TORCH_DT.get(dtype)
     T = B * S
     sptr, sbytes = _ws(save, tp_layer_save_bytes(dtype, B, S, h, H, d, f, N))
-    return _check(load_library().tp_layer_fwd(
+    return _check(getattr(load_library(), name)(
         dtype, B, S, h, H, d, f, N, 1 if causal else 0, eps, _p(X, "X", dt, T * h), _p(ln1_g, "ln1_g", dt, h),
         _p(ln1_b, "ln1_b", dt, h), _p(Wqkv, "Wqkv", dt, 3 * h * H * d), _p(Wo, "Wo", dt, H * d * h),
         _p(ln2_g, "ln2_g", dt, h), _p(ln2_b, "ln2_b", dt, h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h),
-        sptr, sbytes, _p(Z, "Z", dt, T * h), _stream(stream)), "tp_layer_fwd")
+        sptr, sbytes, _p(Z, "Z", dt, T * h), _stream(stream)), name)
 
 
-def tp_layer_bwd(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, dZ, dX, dln1_g,
-                 dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws=None, stream=None) -> int:
+def _layer_bwd(name, dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, dZ, dX, dln1_g,
+               dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, stream):
     dt = _TORCH_DT.get(dtype)
     T = B * S
     sptr, sbytes = _ws(save, tp_layer_save_bytes(dtype, B, S, h, H, d, f, N))
     wptr, wbytes = _ws(ws, tp_layer_workspace_bytes(dtype, B, S, h, H, d, f, N))
-    return _check(load_library().tp_layer_bwd(
+    return _check(getattr(load_library(), name)(
         dtype, B, S, h, H, d, f, N, 1 if causal else 0, _p(X, "X", dt, T * h), _p(ln1_g, "ln1_g", dt, h),
         _p(Wqkv, "Wqkv", dt, 3 * h * H * d), _p(Wo, "Wo", dt, H * d * h), _p(ln2_g, "ln2_g", dt, h),
         _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h), sptr, sbytes, _p(dZ, "dZ", dt, T * h),
         _p(dX, "dX", dt, T * h), _p(dln1_g, "dln1_g", dt, h), _p(dln1_b, "dln1_b", dt, h),
         _p(dWqkv, "dWqkv", dt, 3 * h * H * d), _p(dWo, "dWo", dt, H * d * h), _p(dln2_g, "dln2_g", dt, h),
         _p(dln2_b, "dln2_b", dt, h), _p(dW1s, "dW1s", dt, h * f), _p(dW2s, "dW2s", dt, f * h), wptr, wbytes,
-        _stream(stream)), "tp_layer_bwd")
+        _stream(stream)), name)
+
+
+def tp_layer_fwd(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+                 save, Z, stream=None) -> int:
+    return _layer_fwd("tp_layer_fwd", dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g,
+                      ln2_b, W1s, W2s, save, Z, stream)
+
+
+def tp_layer_bwd(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, dZ, dX, dln1_g,
+                 dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws=None, stream=None) -> int:
+    return _layer_bwd("tp_layer_bwd", dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s,
+                      save, dZ, dX, dln1_g, dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, stream)
+
+
+def tp_sp_layer_fwd(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+                    save, Z, stream=None) -> int:
+    """The layer with X and Z sequence-sharded ([N][B][S/N][h])."""
+    return _layer_fwd("tp_sp_layer_fwd", dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g,
+                      ln2_b, W1s, W2s, save, Z, stream)
+
+
+def tp_sp_layer_bwd(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, dZ, dX, dln1_g,
+                    dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws=None, stream=None) -> int:
+    """The layer's backward with X, dZ and dX sequence-sharded."""
+    return _layer_bwd("tp_sp_layer_bwd", dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s,
+                      save, dZ, dX, dln1_g, dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, stream)
 
 
 # ---------------------------------------------------------------- attention block

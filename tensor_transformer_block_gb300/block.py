@@ -184,9 +184,10 @@ def layernorm_backward(X, gamma, mean, rstd, dY, dR=None, ws=None, stream=None) 
 
 
 def prenorm_layer_forward(X, p: dict, B_: int, S: int, causal: bool = True, eps: float = LN_EPS, save=None,
-                          stream=None) -> dict:
+                          stream=None, seq_sharded: bool = False) -> dict:
     """H1 = X + Attn(LN1(X)), Z = H1 + MLP(LN2(H1)).  ``p`` holds ln1_g, ln1_b, Wqkv,
-    Wo, ln2_g, ln2_b, W1s, W2s; the returned ``save`` buffer feeds the backward."""
+    Wo, ln2_g, ln2_b, W1s, W2s; the returned ``save`` buffer feeds the backward.
+    With ``seq_sharded`` X and Z are in the sequence-parallel layout [N][B][S/N][h]."""
     N, h, _, hN, d = p["Wqkv"].shape
     H = N * hN
     f = N * p["W1s"].shape[2]
@@ -194,13 +195,14 @@ def prenorm_layer_forward(X, p: dict, B_: int, S: int, causal: bool = True, eps:
     if save is None:
         save = workspace(B.tp_layer_save_bytes(dt, B_, S, h, H, d, f, N), X.device)
     Z = torch.empty_like(X)
-    B.tp_layer_fwd(dt, B_, S, h, H, d, f, N, causal, eps, X, p["ln1_g"], p["ln1_b"], p["Wqkv"], p["Wo"],
-                   p["ln2_g"], p["ln2_b"], p["W1s"], p["W2s"], save, Z, stream)
+    fn = B.tp_sp_layer_fwd if seq_sharded else B.tp_layer_fwd
+    fn(dt, B_, S, h, H, d, f, N, causal, eps, X, p["ln1_g"], p["ln1_b"], p["Wqkv"], p["Wo"], p["ln2_g"], p["ln2_b"],
+       p["W1s"], p["W2s"], save, Z, stream)
     return {"Z": Z, "save": save}
 
 
 def prenorm_layer_backward(X, p: dict, save, dZ, B_: int, S: int, causal: bool = True, ws=None, stream=None,
-                           out=None) -> dict:
+                           out=None, seq_sharded: bool = False) -> dict:
     N, h, _, hN, d = p["Wqkv"].shape
     H = N * hN
     f = N * p["W1s"].shape[2]
@@ -213,7 +215,8 @@ def prenorm_layer_backward(X, p: dict, save, dZ, B_: int, S: int, causal: bool =
                "dW2s": torch.empty_like(p["W2s"])}
     if ws is None:
         ws = workspace(B.tp_layer_workspace_bytes(dt, B_, S, h, H, d, f, N), X.device)
-    B.tp_layer_bwd(dt, B_, S, h, H, d, f, N, causal, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"], p["W1s"],
-                   p["W2s"], save, dZ, out["dX"], out["dln1_g"], out["dln1_b"], out["dWqkv"], out["dWo"],
-                   out["dln2_g"], out["dln2_b"], out["dW1s"], out["dW2s"], ws, stream)
+    fn = B.tp_sp_layer_bwd if seq_sharded else B.tp_layer_bwd
+    fn(dt, B_, S, h, H, d, f, N, causal, X, p["ln1_g"], p["Wqkv"], p["Wo"], p["ln2_g"], p["W1s"], p["W2s"], save, dZ,
+       out["dX"], out["dln1_g"], out["dln1_b"], out["dWqkv"], out["dWo"], out["dln2_g"], out["dln2_b"], out["dW1s"],
+       out["dW2s"], ws, stream)
     return out

@@ -57,6 +57,24 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int gemm_status(int rc) { return rc == 0 ? TP_OK : (rc == 1 ? TP_ERR_SHAPE : TP_ERR_CUDA); }
 
+// Sequence-sharded activations (zouht 张量并行 §2.2.2, 与序列并行结合): outside the
+// tensor-parallel blocks an activation of B x S tokens is split along the sequence
+// into N shards [N][B][S/N][h].  S = 0: the plain token-major [B*S][h] layout.
+struct Sp {
+  int S = 0, L = 0;
+};
+tpb::GemmOperand with_sp(tpb::GemmOperand o, Sp sp) {
+  o.sp_S = sp.S;
+  o.sp_L = sp.L;
+  return o;
+}
+tpb::GemmExtra out_sp(Sp sp) {
+  tpb::GemmExtra e;
+  e.c_sp_S = sp.S;
+  e.c_sp_L = sp.L;
+  return e;
+}
+
 __global__ void k_timeout_probe(unsigned* err, unsigned long long timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -112,7 +130,7 @@ AttnWs attn_ws(int64_t B, int64_t S, int H, int Hkv, int d) {
 
 extern "C" {
 
-int tp_version(void) { return (0 << 16) | 6; }
+int tp_version(void) { return (0 << 16) | 7; }
 
 const char* tp_status_string(int s) {
   switch (s) {
@@ -164,10 +182,11 @@ namespace {
 // bf16 MLP forward kernels: a1 then a2.  With ``residual`` (a [T][h] tensor) the
 // row-parallel GEMM's epilogue adds it: Z = residual + sum_i A_i W2_i.
 int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
-                void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st) {
+                void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st, Sp sp = Sp()) {
   const int64_t fN = f / N;
-  // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard)
-  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard; with
+  // sequence-sharded X the copies gather the shards: the pages' all-gather g)
+  const tpb::GemmOperand opX = with_sp(tpb::GemmOperand{X, h, T, 1, false, 0, 0}, sp);
   const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
   int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
                                  kWaitTimeoutNs, st, tpb::kKMlpFc1);
@@ -175,8 +194,10 @@ int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const voi
   // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
   const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
   const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
+  // (sequence-sharded Z: the stores scatter the summed rows to their shards, the
+  // pages' reduce-scatter g*)
   rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opA, opW2, Z, residual, false, T, h, 1,
-                             N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2);
+                             N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2, out_sp(sp));
   return gemm_status(rc);
 }
 
@@ -184,17 +205,52 @@ tpb::AttnDims attn_dims(int64_t B, int64_t S, int H, int Hkv, int d, int N, int 
   return tpb::AttnDims{static_cast<int>(B), static_cast<int>(S), H, H / N, N, d, causal ? 1 : 0, Hkv, Hkv / N};
 }
 
+// bf16 MLP backward kernels a3..a6 (dY in ``dY``, an activation-sized scratch).
+// With sequence-sharded X, dZ and dX (``sp``) the GEMMs read and write those
+// tensors in their shards.
+int mlp_bwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
+                const void* Y_save, const void* A_save, const void* dZ, void* dX, void* dW1s, void* dW2s, void* dY,
+                unsigned* err, cudaStream_t st, Sp sp) {
+  const int64_t fN = f / N;
+
+  // a3: dY_i = (dZ W2_i^T) * GeLU'(Y_i)   (the row-split backward needs no reduction)
+  const tpb::GemmOperand opdZk = with_sp(tpb::GemmOperand{dZ, h, T, 1, false, 0, 0}, sp);
+  const tpb::GemmOperand opW2k{W2s, h, fN, N, false, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiDGelu, opdZk, opW2k, dY, Y_save, false, T, fN, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKMlpDgelu);
+  if (rc) return gemm_status(rc);
+  // a4: dW2_i = A_i^T dZ
+  const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
+  const tpb::GemmOperand opdZn = with_sp(tpb::GemmOperand{dZ, h, T, 1, true, 0, 0}, sp);
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opAt, opdZn, dW2s, nullptr, false, fN, h, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKMlpDw2);
+  if (rc) return gemm_status(rc);
+  // a5: dW1_i = X^T dY_i
+  const tpb::GemmOperand opXt = with_sp(tpb::GemmOperand{X, h, T, 1, true, 0, 0}, sp);
+  const tpb::GemmOperand opdYn{dY, fN, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdYn, dW1s, nullptr, false, h, fN, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKMlpDw1);
+  if (rc) return gemm_status(rc);
+  // a6: dX = sum_i dY_i W1_i^T   (the column split's backward all-reduce, done in the accumulator)
+  const tpb::GemmOperand opdYk{dY, fN, T, N, false, 0, 1};
+  const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
+                             st, tpb::kKMlpDx, out_sp(sp));
+  return gemm_status(rc);
+}
+
+
 // Attention forward kernels: a7, a8, a9 (H query heads, Hkv key/value heads).
 // With ``residual`` ([T][h]) the output projection's epilogue adds it:
 // Z = residual + sum_i O_i Wo_i.
 int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
                  const void* Wqkv, const void* Wo, void* QKV, void* Ob, float* LSE, void* Z, const void* residual,
-                 unsigned* err, cudaStream_t st) {
+                 unsigned* err, cudaStream_t st, Sp sp = Sp()) {
   const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
   const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, kvd = static_cast<int64_t>(ad.hkvN) * d;
   // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
   // writes the bf16 residuals of Q and K after them (split-bf16 scores)
-  const tpb::GemmOperand opX{X, h, T, 1, false, 0, 0};
+  const tpb::GemmOperand opX = with_sp(tpb::GemmOperand{X, h, T, 1, false, 0, 0}, sp);
   const tpb::GemmOperand opW{Wqkv, hNd + 2 * kvd, h, N, true, 1, 0};
   tpb::GemmExtra split;
   split.ldc = ad.qkv_width();
@@ -210,9 +266,51 @@ int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
   const tpb::GemmOperand opO{Ob, hNd, T, N, false, 0, 1};
   const tpb::GemmOperand opWo{Wo, h, hNd, N, true, 0, 1};
   rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opO, opWo, Z, residual, false, T, h, 1,
-                             N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut);
+                             N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut, out_sp(sp));
   return gemm_status(rc);
 }
+// Attention backward kernels (scratch [dQKV | dO | Dsum] carved from ``wsb`` per
+// ``w``).  With sequence-sharded X, dZ and dX (``sp``) the GEMMs read and write
+// those tensors in their shards.
+int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
+                 const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
+                 const void* dZ, void* dX, void* dWqkv, void* dWo, char* wsb, const AttnWs& w, unsigned* err,
+                 cudaStream_t st, Sp sp) {
+  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+  const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, gw = ad.dqkv_width();
+  void* dQKV = wsb;
+  void* dO = wsb + w.qkv;
+  float* dsum = reinterpret_cast<float*>(wsb + w.qkv + w.o);
+
+  // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ)
+  const tpb::GemmOperand opdZk = with_sp(tpb::GemmOperand{dZ, h, T, 1, false, 0, 0}, sp);
+  const tpb::GemmOperand opWok{Wo, h, hNd, N, false, 1, 0};
+  int rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdZk, opWok, dO, nullptr, false, T, hNd, N, 1, h, err,
+                                 kWaitTimeoutNs, st, tpb::kKAttnDo);
+  if (rc) return gemm_status(rc);
+  // dWo_i = O_i^T dZ
+  const tpb::GemmOperand opOt{O_save, hNd, T, N, true, 1, 0};
+  const tpb::GemmOperand opdZn = with_sp(tpb::GemmOperand{dZ, h, T, 1, true, 0, 0}, sp);
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opOt, opdZn, dWo, nullptr, false, hNd, h, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKAttnDwo);
+  if (rc) return gemm_status(rc);
+  // attention core backward -> dQKV
+  rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
+  if (rc) return gemm_status(rc);
+  // dWqkv_i = X^T dQKV_i
+  const tpb::GemmOperand opXt = with_sp(tpb::GemmOperand{X, h, T, 1, true, 0, 0}, sp);
+  const tpb::GemmOperand opdQn{dQKV, gw, T, N, true, 1, 0};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, gw, N, 1, T, err, kWaitTimeoutNs,
+                             st, tpb::kKAttnDwqkv);
+  if (rc) return gemm_status(rc);
+  // dX = sum_i dQKV_i Wqkv_i^T  (the column split's backward all-reduce, in the accumulator)
+  const tpb::GemmOperand opdQk{dQKV, gw, T, N, false, 0, 1};
+  const tpb::GemmOperand opWk{Wqkv, gw, h, N, false, 0, 1};
+  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, gw, err, kWaitTimeoutNs, st,
+                             tpb::kKAttnDx, out_sp(sp));
+  return gemm_status(rc);
+}
+
 }  // namespace
 
 extern "C" {
@@ -296,34 +394,8 @@ int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t fN = f / N;
-  void* dY = ws;
-
-  // a3: dY_i = (dZ W2_i^T) * GeLU'(Y_i)   (the row-split backward needs no reduction)
-  const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
-  const tpb::GemmOperand opW2k{W2s, h, fN, N, false, 1, 0};
-  int rc = tpb::launch_gemm_bf16(tpb::kEpiDGelu, opdZk, opW2k, dY, Y_save, false, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKMlpDgelu);
-  if (rc) return gemm_status(rc);
-  // a4: dW2_i = A_i^T dZ
-  const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
-  const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opAt, opdZn, dW2s, nullptr, false, fN, h, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKMlpDw2);
-  if (rc) return gemm_status(rc);
-  // a5: dW1_i = X^T dY_i
-  const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
-  const tpb::GemmOperand opdYn{dY, fN, T, N, true, 1, 0};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdYn, dW1s, nullptr, false, h, fN, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKMlpDw1);
-  if (rc) return gemm_status(rc);
-  // a6: dX = sum_i dY_i W1_i^T   (the column split's backward all-reduce, done in the accumulator)
-  const tpb::GemmOperand opdYk{dY, fN, T, N, false, 0, 1};
-  const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
-                             st, tpb::kKMlpDx);
-  return gemm_status(rc);
+  return mlp_bwd_seq(T, h, f, N, X, W1s, W2s, Y_save, A_save, dZ, dX, dW1s, dW2s, ws, err,
+                     static_cast<cudaStream_t>(stream), Sp());
 }
 
 }  // extern "C"
@@ -478,41 +550,8 @@ int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
-  const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, gw = ad.dqkv_width();
-  char* wsb = static_cast<char*>(ws);
-  void* dQKV = wsb;
-  void* dO = wsb + w.qkv;
-  float* dsum = reinterpret_cast<float*>(wsb + w.qkv + w.o);
-
-  // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ)
-  const tpb::GemmOperand opdZk{dZ, h, T, 1, false, 0, 0};
-  const tpb::GemmOperand opWok{Wo, h, hNd, N, false, 1, 0};
-  int rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdZk, opWok, dO, nullptr, false, T, hNd, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKAttnDo);
-  if (rc) return gemm_status(rc);
-  // dWo_i = O_i^T dZ
-  const tpb::GemmOperand opOt{O_save, hNd, T, N, true, 1, 0};
-  const tpb::GemmOperand opdZn{dZ, h, T, 1, true, 0, 0};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opOt, opdZn, dWo, nullptr, false, hNd, h, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKAttnDwo);
-  if (rc) return gemm_status(rc);
-  // attention core backward -> dQKV
-  rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
-  if (rc) return gemm_status(rc);
-  // dWqkv_i = X^T dQKV_i
-  const tpb::GemmOperand opXt{X, h, T, 1, true, 0, 0};
-  const tpb::GemmOperand opdQn{dQKV, gw, T, N, true, 1, 0};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, gw, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKAttnDwqkv);
-  if (rc) return gemm_status(rc);
-  // dX = sum_i dQKV_i Wqkv_i^T  (the column split's backward all-reduce, in the accumulator)
-  const tpb::GemmOperand opdQk{dQKV, gw, T, N, false, 0, 1};
-  const tpb::GemmOperand opWk{Wqkv, gw, h, N, false, 0, 1};
-  rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, gw, err, kWaitTimeoutNs, st,
-                             tpb::kKAttnDx);
-  return gemm_status(rc);
+  return attn_bwd_seq(B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, dZ, dX, dWqkv, dWo,
+                      static_cast<char*>(ws), w, err, static_cast<cudaStream_t>(stream), Sp());
 }
 
 int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
@@ -626,10 +665,16 @@ size_t tp_layer_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int 
   return layer_ws(B, S, h, H, d, f).total;
 }
 
-int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal, float eps,
-                 const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
-                 const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
-                 size_t save_bytes, void* Z, void* stream) {
+}  // extern "C"
+
+namespace {
+// The pre-norm layer's forward and backward kernel sequences; ``sp`` selects
+// sequence-sharded X, Z, dZ, dX (and the saved LN outputs and H1, which stay in
+// the same row order).
+int layer_fwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal, float eps,
+                   const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                   const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
+                   size_t save_bytes, void* Z, void* stream, Sp sp) {
   const int sc = layer_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
   if (!(eps >= kEpsMin)) return TP_ERR_SHAPE;
@@ -650,25 +695,25 @@ int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64
   float* rstd1 = reinterpret_cast<float*>(sv + L.rstd1);
   float* mean2 = reinterpret_cast<float*>(sv + L.mean2);
   float* rstd2 = reinterpret_cast<float*>(sv + L.rstd2);
-  // LN1(X)
+  // LN1(X) (row by row, so in whatever row order X is stored)
   int rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st);
   if (rc) return gemm_status(rc);
   // H1 = X + Attn(LN1(X)): the residual is added in the output projection's epilogue
   rc = attn_fwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
-                    reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st);
+                    reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st, sp);
   if (rc) return rc;
   // LN2(H1)
   rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st);
   if (rc) return gemm_status(rc);
   // Z = H1 + MLP(LN2(H1)): the residual is added in the second GEMM's epilogue
-  return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st);
+  return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st, sp);
 }
 
-int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
-                 const void* X, const void* ln1_g, const void* Wqkv, const void* Wo, const void* ln2_g,
-                 const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
-                 void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
-                 void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+int layer_bwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                   const void* X, const void* ln1_g, const void* Wqkv, const void* Wo, const void* ln2_g,
+                   const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
+                   void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
+                   void* dW2s, void* ws, size_t ws_bytes, void* stream, Sp sp) {
   const int sc = layer_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !ln1_g || !Wqkv || !Wo || !ln2_g || !W1s || !W2s || !save || !dZ || !dX || !dln1_g || !dln1_b ||
@@ -682,32 +727,87 @@ int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64
   const LayerWs W = layer_ws(B, S, h, H, d, f);
   if (save_bytes < L.total || !ws || ws_bytes < W.total) return TP_ERR_WORKSPACE;
   if (!al256(save) || !al256(ws)) return TP_ERR_ALIGN;
-  const int dc = check_device(nullptr);
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
   const char* sv = static_cast<const char*>(save);
   char* wb = static_cast<char*>(ws);
   const int64_t T = B * S;
-  const size_t blk = W.dln - W.blk;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   void* dLN = wb + W.dln;
   void* dH1 = wb + W.dh1;
   float* part = reinterpret_cast<float*>(wb + W.part);
-  // MLP block backward on LN2(H1): dLN2 -> dLN
-  int rc = tp_mlp_bwd(dtype, T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, dZ, dLN, dW1s, dW2s, wb + W.blk,
-                      blk, stream);
+  // MLP block backward on LN2(H1): dLN2 -> dLN (dY in the block scratch)
+  int rc = mlp_bwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, dZ, dLN, dW1s, dW2s, wb + W.blk, err, st,
+                       sp);
   if (rc) return rc;
   // dH1 = dZ + LN2'(dLN2)   (the residual passes dZ through)
   rc = tpb::launch_ln_bwd(sv + L.h1, ln2_g, reinterpret_cast<const float*>(sv + L.mean2),
                           reinterpret_cast<const float*>(sv + L.rstd2), dLN, dZ, dH1, dln2_g, dln2_b, part, T, h, st);
   if (rc) return gemm_status(rc);
   // attention block backward on LN1(X) with upstream dH1: dLN1 -> dLN
-  rc = tp_attn_bwd(dtype, B, S, h, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
-                   reinterpret_cast<const float*>(sv + L.lse), dH1, dLN, dWqkv, dWo, wb + W.blk, blk, stream);
+  rc = attn_bwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
+                    reinterpret_cast<const float*>(sv + L.lse), dH1, dLN, dWqkv, dWo, wb + W.blk, attn_ws(B, S, H, H, d),
+                    err, st, sp);
   if (rc) return rc;
   // dX = dH1 + LN1'(dLN1)
   rc = tpb::launch_ln_bwd(X, ln1_g, reinterpret_cast<const float*>(sv + L.mean1),
                           reinterpret_cast<const float*>(sv + L.rstd1), dLN, dH1, dX, dln1_g, dln1_b, part, T, h, st);
   return gemm_status(rc);
+}
+
+// The sequence split of the layer: N shards of S/N tokens per sequence, each a
+// multiple of 128 so that no tile of a GEMM spans two shards.
+int sp_of(int64_t S, int N, Sp* sp) {
+  if (N < 1 || S % N || (S / N) % 128) return TP_ERR_SHAPE;
+  sp->S = static_cast<int>(S);
+  sp->L = static_cast<int>(S / N);
+  return TP_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal, float eps,
+                 const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                 const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
+                 size_t save_bytes, void* Z, void* stream) {
+  return layer_fwd_impl(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+                        save, save_bytes, Z, stream, Sp());
+}
+
+int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                 const void* X, const void* ln1_g, const void* Wqkv, const void* Wo, const void* ln2_g,
+                 const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
+                 void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
+                 void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  return layer_bwd_impl(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, save_bytes,
+                        dZ, dX, dln1_g, dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, ws_bytes, stream, Sp());
+}
+
+int tp_sp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                    float eps, const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
+                    const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
+                    size_t save_bytes, void* Z, void* stream) {
+  Sp sp;
+  const int sc = layer_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (sp_of(S, N, &sp) != TP_OK) return TP_ERR_SHAPE;
+  return layer_fwd_impl(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
+                        save, save_bytes, Z, stream, sp);
+}
+
+int tp_sp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                    const void* X, const void* ln1_g, const void* Wqkv, const void* Wo, const void* ln2_g,
+                    const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
+                    void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
+                    void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  Sp sp;
+  const int sc = layer_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (sp_of(S, N, &sp) != TP_OK) return TP_ERR_SHAPE;
+  return layer_bwd_impl(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, save_bytes,
+                        dZ, dX, dln1_g, dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, ws_bytes, stream, sp);
 }
 
 }  // extern "C"

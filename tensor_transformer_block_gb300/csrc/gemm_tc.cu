@@ -112,6 +112,42 @@ __device__ __forceinline__ void sigmoid_parts(float x, float& s, float& oms) {
   oms = e * s;
 }
 
+// Tile copies of an operand whose second coordinate c1 may be a token of a
+// sequence-sharded tensor (spS > 0): token b*spS + s lives at [s / spL][b][s % spL].
+// Tiles never straddle a shard or a batch (spL is a multiple of every box height).
+__device__ __forceinline__ void tok_coords(int t, int spS, int spL, int& sl, int& bb, int& cc) {
+  bb = t / spS;
+  const int s = t - bb * spS;
+  cc = s / spL;
+  sl = s - cc * spL;
+}
+template <bool PAIR>
+__device__ __forceinline__ void op_load(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int z, int spS,
+                                        int spL) {
+  if (spS > 0) {
+    int sl, bb, cc;
+    tok_coords(c1, spS, spL, sl, bb, cc);
+    if (PAIR)
+      tma_load_4d_pair(dst, m, bar, c0, sl, bb, cc);
+    else
+      tma_load_4d(dst, m, bar, c0, sl, bb, cc);
+  } else {
+    if (PAIR)
+      tma_load_3d_pair(dst, m, bar, c0, c1, z);
+    else
+      tma_load_3d(dst, m, bar, c0, c1, z);
+  }
+}
+__device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, int c0, int row, int z, int spS, int spL) {
+  if (spS > 0) {
+    int sl, bb, cc;
+    tok_coords(row, spS, spL, sl, bb, cc);
+    tma_store_4d(m, src, c0, sl, bb, cc);
+  } else {
+    tma_store_3d(m, src, c0, row, z);
+  }
+}
+
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -210,9 +246,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
               if (A_MN) {
 #pragma unroll
-                for (int j = 0; j < BM / 64; ++j) tma_load_3d_pair(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az);
+                for (int j = 0; j < BM / 64; ++j)
+                  op_load<true>(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az, p.a_spS, p.a_spL);
               } else {
-                tma_load_3d_pair(sa, &tmA, fb, kc, arow, az);
+                op_load<true>(sa, &tmA, fb, kc, arow, az, p.a_spS, p.a_spL);
               }
               if (EPI == kEpiSwiGLU) {
                 // the even CTA stages the tile's gate columns, the odd CTA its up columns
@@ -222,17 +259,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  tma_load_3d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz);
+                  op_load<true>(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, p.b_spS, p.b_spL);
               } else {
-                tma_load_3d_pair(sb, &tmB, fb, kc, bcol, bz);
+                op_load<true>(sb, &tmB, fb, kc, bcol, bz, p.b_spS, p.b_spL);
               }
             } else {
               mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
               if (A_MN) {
 #pragma unroll
-                for (int j = 0; j < BM / 64; ++j) tma_load_3d(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az);
+                for (int j = 0; j < BM / 64; ++j)
+                  op_load<false>(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az, p.a_spS, p.a_spL);
               } else {
-                tma_load_3d(sa, &tmA, fb_local, kc, arow, az);
+                op_load<false>(sa, &tmA, fb_local, kc, arow, az, p.a_spS, p.a_spL);
               }
               if (EPI == kEpiSwiGLU) {
                 // atoms 0-1: gate columns, atoms 2-3: the same columns of the up part
@@ -242,9 +280,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  tma_load_3d(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz);
+                  op_load<false>(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz, p.b_spS, p.b_spL);
               } else {
-                tma_load_3d(sb, &tmB, fb_local, kc, bcol, bz);
+                op_load<false>(sb, &tmB, fb_local, kc, bcol, bz, p.b_spS, p.b_spL);
               }
             }
             issued |= 1u << stage;
@@ -354,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) {
           bulk_wait_read0();
           mbar_arrive_expect_tx(ybar[b], EPI_BUF);
-          tma_load_3d(ebuf[b], &tmY, ybar[b], col0, row0, g);
+          op_load<false>(ebuf[b], &tmY, ybar[b], col0, row0, g, p.c_spS, p.c_spL);
         }
         ypend |= 1u << b;
       }
@@ -403,7 +441,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, sb, ccol, row0, g);
+              out_store(&tmC, sb, ccol, row0, g, p.c_spS, p.c_spL);
               bulk_commit();
             }
             ++ecount;
@@ -595,7 +633,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (lane == 0) {
                 bulk_wait_read0();
                 mbar_arrive_expect_tx(ybar[nb2], EPI_BUF);
-                tma_load_3d(ebuf[nb2], &tmY, ybar[nb2], ccol + 64, row0, g);
+                op_load<false>(ebuf[nb2], &tmY, ybar[nb2], ccol + 64, row0, g, p.c_spS, p.c_spL);
               }
               ypend |= 1u << nb2;
             }
@@ -631,7 +669,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&tmC, ebuf[cb], ccol, row0, g);
+              out_store(&tmC, ebuf[cb], ccol, row0, g, p.c_spS, p.c_spL);
               bulk_commit();
             }
             ++ecount;
@@ -703,6 +741,12 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
 
 bool operand_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
   const uint32_t r = o.mn_major ? static_cast<uint32_t>(BK) : rows;
+  if (o.sp_S > 0) {  // [S/L][B][L][d0]
+    const uint64_t dims[4] = {static_cast<uint64_t>(o.d0), static_cast<uint64_t>(o.sp_L),
+                              static_cast<uint64_t>(o.d1 / o.sp_S), static_cast<uint64_t>(o.sp_S / o.sp_L)};
+    const uint32_t box[4] = {64u, r, 1u, 1u};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, o.ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   if (o.parts == 2) {  // [d2][d1][2][d0]: the part is the second coordinate
     const uint64_t dims[4] = {static_cast<uint64_t>(o.d0), 2u, static_cast<uint64_t>(o.d1),
                               static_cast<uint64_t>(o.d2)};
@@ -738,6 +782,17 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (epi == kEpiSplit && ((extra.split_cols % 64) || extra.lo_off < N || extra.lo_off + extra.split_cols > ldc))
     return 1;
   const bool gated = epi == kEpiSwiGLU || epi == kEpiDSwiGLU;
+  // sequence-sharded operands: the token axis is d1 (A, B) or M (C), d2 = 1, and
+  // every box height (128, 64, 32 rows) divides the shard length L
+  auto sp_ok = [](int S, int L, int64_t rows, int64_t d2) {
+    return S == 0 || (L > 0 && L % 128 == 0 && S % L == 0 && rows % S == 0 && d2 == 1);
+  };
+  if (!sp_ok(A.sp_S, A.sp_L, A.d1, A.d2) || !sp_ok(B.sp_S, B.sp_L, B.d1, B.d2) ||
+      !sp_ok(extra.c_sp_S, extra.c_sp_L, M, G))
+    return 1;
+  if (B.sp_S > 0 && !B.mn_major) return 1;  // a K-major B operand's rows are not tokens
+  if (extra.c_sp_S > 0 && ((epi != kEpiStore && epi != kEpiResidual) || ldc != N)) return 1;
+  if ((A.sp_S > 0 && A.parts != 1) || (B.sp_S > 0 && B.parts != 1)) return 1;
   if (gated && ldc != N) return 1;
   if ((epi == kEpiSwiGLU) != (B.parts == 2) || A.parts != 1) return 1;
   if (epi == kEpiSwiGLU && !B.mn_major) return 1;
@@ -756,16 +811,24 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (!operand_map(&ta, A, a_rows) || !operand_map(&tb, B, b_rows)) return 2;
   const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
   const uint32_t cbox[3] = {64u, 32u, 1u};
+  const uint64_t sdims[4] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(extra.c_sp_L),
+                             static_cast<uint64_t>(extra.c_sp_S > 0 ? M / extra.c_sp_S : 1),
+                             static_cast<uint64_t>(extra.c_sp_S > 0 ? extra.c_sp_S / extra.c_sp_L : 1)};
+  const uint32_t sbox[4] = {64u, 32u, 1u, 1u};
+  auto out_map = [&](CUtensorMap* m, const void* ptr) {
+    if (extra.c_sp_S > 0)
+      return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, sdims, sbox, CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
   if (epi == kEpiDSwiGLU) {
     if (!two_part_map(&tc, C, N, M, G)) return 2;
-  } else if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, C, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B)) {
+  } else if (!out_map(&tc, C)) {
     return 2;
   }
   if (Yaux && gated) {
     if (!two_part_map(&ty, Yaux, N, M, G)) return 2;
   } else if (Yaux) {
-    if (!encode_tmap(&ty, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, Yaux, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B))
-      return 2;
+    if (!out_map(&ty, Yaux)) return 2;
   } else {
     ty = tc;
   }
@@ -784,6 +847,12 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.store_y = (store_y && Yaux) ? 1 : 0;
   p.split_cols = static_cast<int>(extra.split_cols);
   p.lo_off = static_cast<int>(extra.lo_off);
+  p.a_spS = A.sp_S;
+  p.a_spL = A.sp_L;
+  p.b_spS = B.sp_S;
+  p.b_spL = B.sp_L;
+  p.c_spS = extra.c_sp_S;
+  p.c_spL = extra.c_sp_L;
   p.err = err;
   p.timeout_ns = timeout_ns;
   const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;

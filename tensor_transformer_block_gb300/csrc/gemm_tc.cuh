@@ -45,6 +45,9 @@ struct GemmShape {
   int a_zg, a_zs, b_zg, b_zs;  // outer TMA coordinate = g*zg + s*zs
   int store_y;                 // kEpiGelu: also write the pre-activation
   int split_cols, lo_off;      // kEpiSplit
+  // token remaps (0 = off): the operand's row coordinate t (A, B: d1; C, Yaux: M)
+  // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
+  int a_spS, a_spL, b_spS, b_spL, c_spS, c_spL;
   unsigned* err;
   unsigned long long timeout_ns;
 };
@@ -58,6 +61,9 @@ struct GemmOperand {
   bool mn_major;
   int zg, zs;
   int parts = 1;  // 2: the tensor is [d2][d1][2][d0] (kEpiSwiGLU's B: gate, up)
+  // Sequence-sharded rows (d2 must be 1): row t = b*sp_S + s of the logical
+  // [d1][d0] tensor is stored at [s / sp_L][b][s % sp_L][d0] (sp_S = 0: plain).
+  int sp_S = 0, sp_L = 0;
 };
 
 // Host launcher (gemm_tc.cu).  C and Yaux are [G][M][ldc] bf16 tensors of which
@@ -67,6 +73,7 @@ struct GemmExtra {
   int64_t ldc = 0;
   int64_t split_cols = 0;  // kEpiSplit
   int64_t lo_off = 0;      // kEpiSplit
+  int c_sp_S = 0, c_sp_L = 0;  // sequence-sharded rows of C and Yaux (kEpiStore, kEpiResidual)
 };
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
                      bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,

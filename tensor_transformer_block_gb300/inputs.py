@@ -27,7 +27,7 @@ from dataclasses import dataclass
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", "layer_inputs", "prenorm_inputs",
-           "ln_inputs", "gqa_inputs", "split_qkv_gqa",
+           "ln_inputs", "gqa_inputs", "split_qkv_gqa", "to_seq_shards", "from_seq_shards",
            "split_columns", "split_rows", "split_qkv_heads"]
 
 
@@ -35,7 +35,8 @@ __all__ = ["Workload", "WORKLOADS", "mlp_inputs", "gmlp_inputs", "attn_inputs", 
 class Workload:
     """One of the synthetic workloads the block is checked and measured on."""
     name: str
-    kind: str            # "mlp", "gmlp" (gated MLP), "attn", "gqa", "layer" or "lnlayer" (pre-norm layer)
+    kind: str            # "mlp", "gmlp" (gated MLP), "attn", "gqa", "layer", "lnlayer" (pre-norm layer) or
+                         # "splayer" (the pre-norm layer with sequence-sharded activations)
     dtype: str           # "f32" or "bf16"
     backward: bool
     T: int = 0           # tokens = B*S
@@ -74,6 +75,9 @@ WORKLOADS = {
     "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8": Workload(
         "lnlayer_bf16_B1_S4096_h8192_H64_d128_f28672_N8", "lnlayer", "bf16", True,
         T=4096, h=8192, f=28672, N=8, B=1, S=4096, H=64, d=128),
+    "splayer_bf16_B2_S2048_h8192_H64_d128_f28672_N8": Workload(
+        "splayer_bf16_B2_S2048_h8192_H64_d128_f28672_N8", "splayer", "bf16", True,
+        T=4096, h=8192, f=28672, N=8, B=2, S=2048, H=64, d=128),
     "gqa_bf16_B2_S2048_h4096_H32_Hkv8_d128_N8": Workload("gqa_bf16_B2_S2048_h4096_H32_Hkv8_d128_N8", "gqa",
                                                          "bf16", True, T=4096, h=4096, N=8, B=2, S=2048, H=32,
                                                          d=128, Hkv=8),
@@ -200,6 +204,18 @@ def gqa_inputs(B: int, S: int, h: int, H: int, Hkv: int, d: int, N: int, dtype: 
     return out
 
 
+def to_seq_shards(X: torch.Tensor, B: int, S: int, n: int) -> torch.Tensor:
+    """[B*S][h] (token t = b*S + s) -> [n][B][S/n][h]: the sequence-parallel layout,
+    shard c holding positions c*S/n .. (c+1)*S/n - 1 of every sequence."""
+    return X.reshape(B, n, S // n, X.shape[-1]).permute(1, 0, 2, 3).contiguous()
+
+
+def from_seq_shards(Xs: torch.Tensor) -> torch.Tensor:
+    """Inverse of :func:`to_seq_shards`."""
+    n, B, L, h = Xs.shape
+    return Xs.permute(1, 0, 2, 3).reshape(B * n * L, h).contiguous()
+
+
 def ln_inputs(T: int, h: int, dtype: str = "bf16", seed: int = 0, x_std: float = 1.0, x_mean: float = 0.0,
               ln_std: float = 0.1) -> dict:
     """LayerNorm alone: X [T][h] ~ N(x_mean, x_std^2), gamma ~ 1 + N(0, ln_std^2),
@@ -250,7 +266,7 @@ def workload_inputs(w: Workload, **overrides) -> dict:
     if p["kind"] == "attn":
         return attn_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["N"], p["dtype"], p["seed"],
                            p["x_std"], p["w_std"], p["backward"])
-    if p["kind"] == "lnlayer":
+    if p["kind"] in ("lnlayer", "splayer"):
         return prenorm_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["f"], p["N"], p["dtype"],
                               p["seed"], p["x_std"], p["w_std"])
     return layer_inputs(p["B"], p["S"], p["h"], p["H"], p["d"], p["f"], p["N"], p["dtype"],

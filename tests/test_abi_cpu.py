@@ -97,6 +97,13 @@ def test_gqa_validation_before_cuda(lib):
         tp.tp_attn_workspace_bytes(tp.TP_BF16, 2, 128, 512, 8, 64, 2)
 
 
+def test_sp_layer_validation_before_cuda(lib):
+    f = lambda S, N: lib.tp_sp_layer_fwd(1, 2, S, 512, 4, 128, 1024, N, 1, 1e-5, *([16] * 9), 256, 0, 16, None)
+    assert f(384, 2) == 2                               # S/N = 192: not a multiple of 128
+    assert f(256, 3) == 2                               # N does not divide S
+    assert f(256, 2) == 4                               # valid shape: the empty save buffer is reported
+
+
 def test_attention_validation_before_cuda(lib):
     f = lambda **k: lib.tp_attn_fwd(k.get("dt", 1), k.get("B", 2), k.get("S", 128), k.get("h", 512),
                                     k.get("H", 8), k.get("d", 64), k.get("N", 2), 1, k.get("X", 16), 16, 16,
