@@ -63,17 +63,33 @@ struct Cfg {
   static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
+// Tile order: GROUP_M consecutive M tiles sweep the N tiles together, so the
+// operand panels they share are reused from L2.  With several output groups that
+// share the A operand the groups are folded into the N sweep (g_mode 1), so an A
+// panel is read once for all groups instead of once per group; g_mode 2 folds
+// them into M instead.
 __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, int& mb, int& nb) {
-  const int per_g = p.tiles_m * p.tiles_n;
-  g = t / per_g;
-  const int r = t - g * per_g;
-  const int span = GROUP_M * p.tiles_n;
+  const int tm = p.g_mode == 2 ? p.G * p.tiles_m : p.tiles_m;
+  const int tn = p.g_mode == 1 ? p.G * p.tiles_n : p.tiles_n;
+  const int per_g = tm * tn;
+  const int g0 = p.g_mode == 0 ? t / per_g : 0;
+  const int r = t - g0 * per_g;
+  const int span = GROUP_M * tn;
   const int grp = r / span;
   const int first_m = grp * GROUP_M;
-  const int gm = min(p.tiles_m - first_m, GROUP_M);
+  const int gm = min(tm - first_m, GROUP_M);
   const int rr = r - grp * span;
-  mb = first_m + rr % gm;
-  nb = rr / gm;
+  int m = first_m + rr % gm, n = rr / gm;
+  g = g0;
+  if (p.g_mode == 1) {
+    g = n / p.tiles_n;
+    n -= g * p.tiles_n;
+  } else if (p.g_mode == 2) {
+    g = m / p.tiles_m;
+    m -= g * p.tiles_m;
+  }
+  mb = m;
+  nb = n;
 }
 
 // GeLU (tanh form) through the logistic identity 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)):
@@ -121,22 +137,32 @@ __device__ __forceinline__ void tok_coords(int t, int spS, int spL, int& sl, int
   cc = s / spL;
   sl = s - cc * spL;
 }
+// Position of a token in the sequence-sharded layout (tracked incrementally by the
+// producer, so the K loop does no integer division).
+struct TokPos {
+  int sl, b, c;
+};
 template <bool PAIR>
-__device__ __forceinline__ void op_load(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int z, int spS,
-                                        int spL) {
-  if (spS > 0) {
-    int sl, bb, cc;
-    tok_coords(c1, spS, spL, sl, bb, cc);
+__device__ __forceinline__ void op_load_at(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int z,
+                                           bool sp, const TokPos& tp) {
+  if (sp) {
     if (PAIR)
-      tma_load_4d_pair(dst, m, bar, c0, sl, bb, cc);
+      tma_load_4d_pair(dst, m, bar, c0, tp.sl, tp.b, tp.c);
     else
-      tma_load_4d(dst, m, bar, c0, sl, bb, cc);
+      tma_load_4d(dst, m, bar, c0, tp.sl, tp.b, tp.c);
   } else {
     if (PAIR)
       tma_load_3d_pair(dst, m, bar, c0, c1, z);
     else
       tma_load_3d(dst, m, bar, c0, c1, z);
   }
+}
+template <bool PAIR>
+__device__ __forceinline__ void op_load(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int z, int spS,
+                                        int spL) {
+  TokPos tp{0, 0, 0};
+  if (spS > 0) tok_coords(c1, spS, spL, tp.sl, tp.b, tp.c);
+  op_load_at<PAIR>(dst, m, bar, c0, c1, z, spS > 0, tp);
 }
 __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, int c0, int row, int z, int spS, int spL) {
   if (spS > 0) {
@@ -224,14 +250,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_par = 0;
       bool ok = true;
+      // sequence-sharded token axes: the rows of a K-major A (one position per
+      // tile) and the K axis of MN-major A / B (advanced by 64 per k-block)
+      const bool a_rows_sp = !A_MN && p.a_spS > 0;
+      const bool a_k_sp = A_MN && p.a_spS > 0, b_k_sp = B_MN && p.b_spS > 0;
+      const int k_spL = a_k_sp ? p.a_spL : p.b_spL;
+      const int k_nc = (a_k_sp || b_k_sp) ? (a_k_sp ? p.a_spS : p.b_spS) / k_spL : 1;
       for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
         decode_tile(t, p, g, mb, nb);
         const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
         const int bcol = EPI == kEpiSwiGLU ? nb * TILE_N : nb * BN + static_cast<int>(rank) * C::BN_CTA;
+        TokPos apos{0, 0, 0};
+        if (a_rows_sp) tok_coords(arow, p.a_spS, p.a_spL, apos.sl, apos.b, apos.c);
         for (int s = 0; s < p.S && ok; ++s) {
           const int az = g * p.a_zg + s * p.a_zs;
           const int bz = g * p.b_zg + s * p.b_zs;
+          TokPos kpos{0, 0, 0};
           for (int kb = 0; kb < p.kb_per_seg; ++kb) {
             if (!mbar_wait(bar0 + 8u * (BAR_EMPTY + stage), phase ^ 1u, wc)) {
               ok = false;
@@ -247,9 +282,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (A_MN) {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
-                  op_load<true>(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az, p.a_spS, p.a_spL);
+                  op_load_at<true>(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az, a_k_sp, kpos);
               } else {
-                op_load<true>(sa, &tmA, fb, kc, arow, az, p.a_spS, p.a_spL);
+                op_load_at<true>(sa, &tmA, fb, kc, arow, az, a_rows_sp, apos);
               }
               if (EPI == kEpiSwiGLU) {
                 // the even CTA stages the tile's gate columns, the odd CTA its up columns
@@ -259,18 +294,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  op_load<true>(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, p.b_spS, p.b_spL);
+                  op_load_at<true>(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, b_k_sp, kpos);
               } else {
-                op_load<true>(sb, &tmB, fb, kc, bcol, bz, p.b_spS, p.b_spL);
+                tma_load_3d_pair(sb, &tmB, fb, kc, bcol, bz);
               }
             } else {
               mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
               if (A_MN) {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
-                  op_load<false>(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az, p.a_spS, p.a_spL);
+                  op_load_at<false>(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az, a_k_sp, kpos);
               } else {
-                op_load<false>(sa, &tmA, fb_local, kc, arow, az, p.a_spS, p.a_spL);
+                op_load_at<false>(sa, &tmA, fb_local, kc, arow, az, a_rows_sp, apos);
               }
               if (EPI == kEpiSwiGLU) {
                 // atoms 0-1: gate columns, atoms 2-3: the same columns of the up part
@@ -280,9 +315,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  op_load<false>(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz, p.b_spS, p.b_spL);
+                  op_load_at<false>(sb + j * (BK * 128), &tmB, fb_local, bcol + j * 64, kc, bz, b_k_sp, kpos);
               } else {
-                op_load<false>(sb, &tmB, fb_local, kc, bcol, bz, p.b_spS, p.b_spL);
+                tma_load_3d(sb, &tmB, fb_local, kc, bcol, bz);
+              }
+            }
+            if (a_k_sp || b_k_sp) {  // next 64 tokens of the K axis
+              kpos.sl += BK;
+              if (kpos.sl >= k_spL) {
+                kpos.sl = 0;
+                if (++kpos.c >= k_nc) {
+                  kpos.c = 0;
+                  ++kpos.b;
+                }
               }
             }
             issued |= 1u << stage;
@@ -791,6 +836,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
       !sp_ok(extra.c_sp_S, extra.c_sp_L, M, G))
     return 1;
   if (B.sp_S > 0 && !B.mn_major) return 1;  // a K-major B operand's rows are not tokens
+  if (A.sp_S > 0 && A.mn_major && B.sp_S > 0 && (A.sp_S != B.sp_S || A.sp_L != B.sp_L)) return 1;
   if (extra.c_sp_S > 0 && ((epi != kEpiStore && epi != kEpiResidual) || ldc != N)) return 1;
   if ((A.sp_S > 0 && A.parts != 1) || (B.sp_S > 0 && B.parts != 1)) return 1;
   if (gated && ldc != N) return 1;
@@ -853,6 +899,9 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.b_spL = B.sp_L;
   p.c_spS = extra.c_sp_S;
   p.c_spL = extra.c_sp_L;
+  // fold the groups into N when they share A (the column-parallel GEMMs' X or dZ);
+  // folding into M for a shared B measured slower (more L2 misses) and is not used
+  p.g_mode = (G > 1 && A.zg == 0) ? 1 : 0;
   p.err = err;
   p.timeout_ns = timeout_ns;
   const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;

@@ -48,6 +48,7 @@ struct GemmShape {
   // token remaps (0 = off): the operand's row coordinate t (A, B: d1; C, Yaux: M)
   // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
   int a_spS, a_spL, b_spS, b_spL, c_spS, c_spL;
+  int g_mode;  // tile order across groups (gemm_tc.cu decode_tile)
   unsigned* err;
   unsigned long long timeout_ns;
 };
