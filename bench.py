@@ -363,7 +363,7 @@ def run_gpu(args, w) -> None:
         buf["gws"] = block.workspace(tp.tp_gmlp_workspace_bytes(dt, T, h, f, N), dev)
     if w.kind == "gqa":
         hN, kvN = w.H // N, w.Hkv // N
-        buf["QKV"] = torch.empty(N, T, (2 * hN + 3 * kvN) * w.d, dtype=torch.bfloat16, device=dev)
+        buf["QKV"] = torch.empty(N, T, (hN + 2 * kvN) * w.d, dtype=torch.bfloat16, device=dev)
         buf["O"] = torch.empty(N, T, hN * w.d, dtype=torch.bfloat16, device=dev)
         buf["LSE"] = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
         buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)

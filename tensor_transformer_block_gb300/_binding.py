@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(HERE, "libtpblock.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "tpblock.h")
 
 TP_F32, TP_BF16 = 0, 1
-QKV_PLANES = 5  # Q, K, V, Q - bf16(Q), K - bf16(K) per (token, head)
+QKV_PLANES = 3  # Q (fp16), K (fp16), V (bf16) per (token, head)
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_WORKSPACE",
           5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE"}
 _TORCH_DT = {TP_F32: torch.float32, TP_BF16: torch.bfloat16}
@@ -242,7 +242,7 @@ def tp_gqa_fwd(dtype, B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV_save, O_sa
     return _check(load_library().tp_gqa_fwd(
         dtype, B, S, h, H, Hkv, d, N, 1 if causal else 0, _p(X, "X", dt, T * h),
         _p(Wqkv, "Wqkv", dt, h * (H + 2 * Hkv) * d), _p(Wo, "Wo", dt, H * d * h),
-        _p(QKV_save, "QKV_save", dt, T * (2 * H + 3 * Hkv) * d, False), _p(O_save, "O_save", dt, T * H * d, False),
+        _p(QKV_save, "QKV_save", dt, T * (H + 2 * Hkv) * d, False), _p(O_save, "O_save", dt, T * H * d, False),
         _p(LSE_save, "LSE_save", torch.float32, B * H * S, False), _p(Z, "Z", dt, T * h), wptr, wbytes,
         _stream(stream)), "tp_gqa_fwd")
 
@@ -255,7 +255,7 @@ def tp_gqa_bwd(dtype, B, S, h, H, Hkv, d, N, causal, X, Wqkv, Wo, QKV_save, O_sa
     return _check(load_library().tp_gqa_bwd(
         dtype, B, S, h, H, Hkv, d, N, 1 if causal else 0, _p(X, "X", dt, T * h),
         _p(Wqkv, "Wqkv", dt, h * (H + 2 * Hkv) * d), _p(Wo, "Wo", dt, H * d * h),
-        _p(QKV_save, "QKV_save", dt, T * (2 * H + 3 * Hkv) * d), _p(O_save, "O_save", dt, T * H * d),
+        _p(QKV_save, "QKV_save", dt, T * (H + 2 * Hkv) * d), _p(O_save, "O_save", dt, T * H * d),
         _p(LSE_save, "LSE_save", torch.float32, B * H * S), _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h),
         _p(dWqkv, "dWqkv", dt, h * (H + 2 * Hkv) * d), _p(dWo, "dWo", dt, H * d * h), wptr, wbytes,
         _stream(stream)), "tp_gqa_bwd")

@@ -116,7 +116,7 @@ def gqa_forward(X, Wqkv, Wo, H: int, Hkv: int, d: int, B_: int, S: int, causal: 
     dt = _dtype(X)
     dev = X.device
     Z = torch.empty(T, h, dtype=X.dtype, device=dev)
-    QKV = torch.empty(N, T, (2 * H + 3 * Hkv) * d // N, dtype=X.dtype, device=dev)
+    QKV = torch.empty(N, T, (H + 2 * Hkv) * d // N, dtype=X.dtype, device=dev)
     O = torch.empty(N, T, H * d // N, dtype=X.dtype, device=dev)
     LSE = torch.empty(B_, H, S, dtype=torch.float32, device=dev)
     if ws is None:

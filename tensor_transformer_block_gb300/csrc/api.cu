@@ -119,7 +119,7 @@ struct AttnWs {
 AttnWs attn_ws(int64_t B, int64_t S, int H, int Hkv, int d) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
   AttnWs w;
-  w.qkv = round_up(T * (2 * static_cast<size_t>(H) + 3 * static_cast<size_t>(Hkv)) * static_cast<size_t>(d) * 2, 256);
+  w.qkv = round_up(T * (static_cast<size_t>(H) + 2 * static_cast<size_t>(Hkv)) * static_cast<size_t>(d) * 2, 256);
   w.o = round_up(T * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
   w.lse = round_up(T * static_cast<size_t>(H) * 4, 256);
   w.total = w.qkv + w.o + w.lse;
@@ -248,14 +248,11 @@ int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
                  unsigned* err, cudaStream_t st, Sp sp = Sp()) {
   const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
   const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, kvd = static_cast<int64_t>(ad.hkvN) * d;
-  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); the epilogue also
-  // writes the bf16 residuals of Q and K after them (split-bf16 scores)
+  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); Q and K stored fp16
   const tpb::GemmOperand opX = with_sp(tpb::GemmOperand{X, h, T, 1, false, 0, 0}, sp);
   const tpb::GemmOperand opW{Wqkv, hNd + 2 * kvd, h, N, true, 1, 0};
   tpb::GemmExtra split;
-  split.ldc = ad.qkv_width();
   split.split_cols = hNd + kvd;
-  split.lo_off = hNd + 2 * kvd;
   int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, hNd + 2 * kvd, N, 1, h, err,
                                  kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
   if (rc) return gemm_status(rc);

@@ -5,18 +5,18 @@
 // query head j uses key/value head j / (H/Hkv).  Per shard, hN = H/N query and
 // hkvN = Hkv/N key/value heads (io.zouht.com 张量并行 §2.2.1: each shard owns
 // whole heads; with GQA it owns whole groups):
-//   QKV  [N][B][S][W] with W = (2 hN + 3 hkvN) d: Q (hN heads), K (hkvN), V (hkvN),
-//        then the bf16 residuals Q - bf16(Q) (hN) and K - bf16(K) (hkvN)
-//   dQKV [N][B][S][(hN + 2 hkvN) d]: dQ, dK, dV
+//   QKV  [N][B][S][W] with W = (hN + 2 hkvN) d: Q (hN heads) and K (hkvN) in fp16,
+//        V (hkvN) in bf16
+//   dQKV [N][B][S][W]: dQ, dK, dV (bf16)
 //   O    [N][B][S][hN][d]
 //   LSE  [B][H][S] fp32          natural-log sum of exp of the scaled scores
 // Global query head j lives in shard i = j / hN as local head jj = j % hN.
 //
-// Scores are computed split-bf16: S = Qh Kh^T + Qh Kl^T + Ql Kh^T with Qh =
-// bf16(Q), Ql = bf16(Q - Qh) (same for K), which carries Q K^T to ~2^-16
-// relative instead of bf16's 2^-9; the softmax exponentiates scores whose range
-// reaches tens of units, where bf16 Q and K would move the largest weights by
-// several percent.
+// Q and K are kept in fp16 (11 significant bits instead of bf16's 8): the softmax
+// exponentiates scores whose range reaches tens of units, where bf16 Q and K would
+// move the largest weights by several percent; fp16 puts the scores within ~2^-11
+// relative and the products Q K^T still run as single tensor-core MMAs (fp16 x
+// fp16, fp32 accumulation).  Entries of Q and K beyond +-65504 would overflow.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -29,18 +29,16 @@ struct AttnDims {
   int B, S, H, hN, N, d, causal;
   int Hkv, hkvN;  // key/value heads in total and per shard (= H, hN without grouping)
   // column offsets (elements) of local head jj (query) or kv (key/value) in QKV
-  __host__ __device__ int qkv_width() const { return (2 * hN + 3 * hkvN) * d; }
+  __host__ __device__ int qkv_width() const { return (hN + 2 * hkvN) * d; }
   __host__ __device__ int col_q(int jj) const { return jj * d; }
   __host__ __device__ int col_k(int kv) const { return (hN + kv) * d; }
   __host__ __device__ int col_v(int kv) const { return (hN + hkvN + kv) * d; }
-  __host__ __device__ int col_ql(int jj) const { return (hN + 2 * hkvN + jj) * d; }
-  __host__ __device__ int col_kl(int kv) const { return (2 * hN + 2 * hkvN + kv) * d; }
   __host__ __device__ int dqkv_width() const { return (hN + 2 * hkvN) * d; }
   __host__ __device__ int group() const { return hN / hkvN; }
 };
 
 // Number of d-wide planes per (token, local head) in QKV without grouping.
-constexpr int kQkvPlanes = 5;
+constexpr int kQkvPlanes = 3;
 
 // Forward: O and LSE from QKV (returns 0, 1 bad arguments, 2 CUDA failure).
 int launch_attn_fwd(const AttnDims& a, const void* qkv, void* o, float* lse, unsigned* err,

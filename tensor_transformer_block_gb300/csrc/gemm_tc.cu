@@ -465,7 +465,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // The fused epilogues run as a rolled loop of 16-column TMEM loads: a
           // fully unrolled 64-column body is large enough to evict the MMA
           // warp's instructions from the cache the SM sub-partition shares.
-          if (EPI == kEpiStore) {
+          if (EPI == kEpiStore || EPI == kEpiSplit) {
+            // kEpiSplit: fp16 for the columns before split_cols (whole 64-column chunks)
+            const bool f16 = EPI == kEpiSplit && ccol < p.split_cols;
             uint32_t r0[32], r1[32];
             tmem_ld32(tcol, r0);
             tmem_ld32(tcol + 32, r1);
@@ -477,11 +479,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint32_t* v = (c < 4) ? &r0[8 * c] : &r1[8 * (c - 4)];
-              st_shared_v4(sb + lane * 128 + ((c ^ rsw) << 4),
-                           pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[e] = f16 ? pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
+                           : pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+              st_shared_v4(sb + lane * 128 + ((c ^ rsw) << 4), w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -490,37 +493,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               bulk_commit();
             }
             ++ecount;
-          } else if (EPI == kEpiSplit) {
-            const bool with_lo = ccol < p.split_cols;
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-#pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              uint32_t v[16];
-              tmem_ld16(tcol + q * 16, v);
-              tmem_ld_wait16(v);
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t c = static_cast<uint32_t>(2 * q + hh);
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float x0 = __uint_as_float(v[8 * hh + 2 * e]), x1 = __uint_as_float(v[8 * hh + 2 * e + 1]);
-                  hi[e] = pack_bf16x2(x0, x1);
-                  lo[e] = pack_bf16x2(x0 - bf16lo_to_f32(hi[e]), x1 - bf16hi_to_f32(hi[e]));
-                }
-                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
-                st_shared_v4(ebuf[0] + off, hi[0], hi[1], hi[2], hi[3]);
-                if (with_lo) st_shared_v4(ebuf[1] + off, lo[0], lo[1], lo[2], lo[3]);
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_3d(&tmC, ebuf[0], ccol, row0, g);
-              if (with_lo) tma_store_3d(&tmC, ebuf[1], ccol + p.lo_off, row0, g);
-              bulk_commit();
-            }
           } else if (EPI == kEpiGelu) {
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
@@ -824,8 +796,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const int64_t ldc = extra.ldc > 0 ? extra.ldc : N;
   if ((A.d0 % 8) || (B.d0 % 8) || (N % 8) || (ldc % 8) || ldc < N) return 1;
   if (ldc != N && (N % 64)) return 1;  // a partial last chunk would not be clipped at N
-  if (epi == kEpiSplit && ((extra.split_cols % 64) || extra.lo_off < N || extra.lo_off + extra.split_cols > ldc))
-    return 1;
+  if (epi == kEpiSplit && (extra.split_cols % 64)) return 1;
   const bool gated = epi == kEpiSwiGLU || epi == kEpiDSwiGLU;
   // sequence-sharded operands: the token axis is d1 (A, B) or M (C), d2 = 1, and
   // every box height (128, 64, 32 rows) divides the shard length L
@@ -892,7 +863,6 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.b_zs = B.zs;
   p.store_y = (store_y && Yaux) ? 1 : 0;
   p.split_cols = static_cast<int>(extra.split_cols);
-  p.lo_off = static_cast<int>(extra.lo_off);
   p.a_spS = A.sp_S;
   p.a_spL = A.sp_L;
   p.b_spS = B.sp_S;

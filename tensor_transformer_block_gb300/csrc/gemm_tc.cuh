@@ -25,8 +25,7 @@ enum GemmEpi : int {
   kEpiStore = 0,  // C = bf16(acc)
   kEpiGelu = 1,   // C = bf16(GeLU_tanh(acc)); optionally Yout = bf16(acc)
   kEpiDGelu = 2,  // C = bf16(acc * GeLU_tanh'(Yin)), Yin read through a TMA map
-  kEpiSplit = 3,  // C = bf16(acc); for columns < split_cols also the residual
-                  // bf16(acc - bf16(acc)) at column + lo_off of the same row
+  kEpiSplit = 3,  // C = fp16(acc) for columns < split_cols (a multiple of 64), bf16(acc) after
   // Gated (SwiGLU) MLP.  B is a two-part operand [G][K][2][N] (gate columns, then
   // up columns); one tile computes 128 output columns n: the MMA's 256 accumulator
   // columns hold gate(n) in 0..127 and up(n) in 128..255.
@@ -44,7 +43,7 @@ struct GemmShape {
   int tiles_m, tiles_n;
   int a_zg, a_zs, b_zg, b_zs;  // outer TMA coordinate = g*zg + s*zs
   int store_y;                 // kEpiGelu: also write the pre-activation
-  int split_cols, lo_off;      // kEpiSplit
+  int split_cols;              // kEpiSplit
   // token remaps (0 = off): the operand's row coordinate t (A, B: d1; C, Yaux: M)
   // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
   int a_spS, a_spL, b_spS, b_spL, c_spS, c_spL;
@@ -73,7 +72,6 @@ struct GemmOperand {
 struct GemmExtra {
   int64_t ldc = 0;
   int64_t split_cols = 0;  // kEpiSplit
-  int64_t lo_off = 0;      // kEpiSplit
   int c_sp_S = 0, c_sp_L = 0;  // sequence-sharded rows of C and Yaux (kEpiStore, kEpiResidual)
 };
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,

@@ -28,16 +28,14 @@ def _attn(B, S, h, H, d, N, causal=True, backward=True, seed=0):
 
 
 def _check_qkv(qkv_gpu, qkv_ref, N, T, hN, d):
-    """Planes 0-2 (Q, K, V) are single roundings of the projection; planes 3-4
-    carry the residuals, so Q = plane0 + plane3 and K = plane1 + plane4 to ~2^-16."""
-    g = _np(qkv_gpu).reshape(N, T, 5, hN, d)
+    """Q and K are stored in fp16, V in bf16: each a single rounding of the fp32
+    projection (at most 2^-11 of the value for fp16, held to 2^-10; 2^-8 for bf16)."""
+    g = qkv_gpu.detach().reshape(N, T, 3, hN, d)
+    qk = g[:, :, :2].contiguous().view(torch.float16).to("cpu", torch.float64).numpy()
+    v = _np(g[:, :, 2])
     r = qkv_ref.reshape(N, T, 3, hN, d)
-    assert_bf16_rounded(g[:, :, :3], r, "QKV")
-    for p in (0, 1):
-        # ~2^-16 relative, plus the fp32 accumulator's own error (~2^-13 of the RMS
-        # at K = 4096); bf16 alone would be off by up to 2^-8 relative
-        assert_bf16_rounded(g[:, :, p] + g[:, :, 3 + p], r[:, :, p], f"split plane {p}", rel=2.0 ** -15,
-                            abs_rms=2.0 ** -13)
+    assert_bf16_rounded(qk, r[:, :, :2], "Q, K (fp16)", rel=2.0 ** -10)
+    assert_bf16_rounded(v, r[:, :, 2], "V")
 
 
 def _check(B, S, h, H, d, N, causal=True, backward=True, seed=0):
