@@ -177,27 +177,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t ID_S = idesc_f16(128, BKV, false, false);
       constexpr uint32_t ID_PV = idesc_bf16(128, D, false, true);
       bool ok = mbar_wait(bar(B_QF), 0, wc), any = false;
-      // scores of key block kv for every tile that needs it, then release the K stage
-      auto issue_s = [&](int kv) -> bool {
-        const int st = kv & 1;
-        if (!mbar_wait(bar(B_KF + st), static_cast<uint32_t>((kv >> 1) & 1), wc)) return false;
-#pragma unroll
-        for (int t = 0; t < QT; ++t) {
-          if (kv >= nkv_t[t]) continue;
-          // the previous block's P V has read the P these columns hold
-          if (kv > 0 && !mbar_wait(bar(B_PE + t), static_cast<uint32_t>((kv - 1) & 1), wc)) return false;
+      // scores of key block 0 for every tile
+      if (ok && nkv > 0) {
+        ok = mbar_wait(bar(B_KF), 0, wc);
+        if (ok) {
           tc_fence_after();
-          mma_scores<D>(tmem + static_cast<uint32_t>(t * 256), sQ(t), sK(st), ID_S);
-          tc_commit(bar(B_SF + t));
+#pragma unroll
+          for (int t = 0; t < QT; ++t) {
+            if (nkv_t[t] == 0) continue;
+            mma_scores<D>(tmem + static_cast<uint32_t>(t * 256), sQ(t), sK(0), ID_S);
+            tc_commit(bar(B_SF + t));
+          }
+          any = true;
+          tc_commit(bar(B_KE));
         }
-        any = true;
-        tc_commit(bar(B_KE + st));
-        return true;
-      };
-      if (ok && nkv > 0) ok = issue_s(0);
+      }
+      // per block kv and tile t: O_t += P_t V (once the softmax wrote P_t), then, as
+      // soon as that P V has read P_t, the tile's scores of block kv+1 into the same
+      // columns; the other tile's softmax runs meanwhile
       for (int kv = 0; kv < nkv && ok; ++kv) {
-        const int st = kv & 1;
+        const int st = kv & 1, st1 = (kv + 1) & 1;
+        const bool next = kv + 1 < nkv;
         if (!mbar_wait(bar(B_VF + st), static_cast<uint32_t>((kv >> 1) & 1), wc)) {
+          ok = false;
+          break;
+        }
+        if (next && !mbar_wait(bar(B_KF + st1), static_cast<uint32_t>(((kv + 1) >> 1) & 1), wc)) {
           ok = false;
           break;
         }
@@ -215,10 +220,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tc_mma_bf16_ts(tS + 128, tS + kk * 8, sdesc_sw128(sV(st) + kk * 2048, 16384, 1024), ID_PV,
                            (kv > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(B_PE + t));
+          if (kv + 1 < nkv_t[t]) {
+            // the P V just issued has read the P these columns hold
+            if (!mbar_wait(bar(B_PE + t), static_cast<uint32_t>(kv & 1), wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_scores<D>(tS, sQ(t), sK(st1), ID_S);
+            tc_commit(bar(B_SF + t));
+          }
         }
         if (!ok) break;
         tc_commit(bar(B_VE + st));
-        if (kv + 1 < nkv && !issue_s(kv + 1)) ok = false;
+        if (next) tc_commit(bar(B_KE + st1));
       }
       if (any) {
         tc_commit(bar(B_DR));
@@ -244,20 +259,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int kbase = kv * BKV;
       const bool masked = (a.causal && kbase + BKV - 1 > q0 + t * BQ) || (kbase + BKV > a.S);
       const int klim = a.causal ? min(q, a.S - 1) : a.S - 1;  // last visible key
-      // pass 1: the block's row max (raw scores; the scale is positive)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_ld_wait(v);
+      // the block's 128 raw scores of this row, in registers
+      uint32_t v[BKV / 32][32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(v[e]);
-          if (masked && kbase + 32 * c + e > klim) x = -INFINITY;
-          mx[e & 3] = fmaxf(mx[e & 3], x);
-        }
+      for (int c = 0; c < BKV / 32; ++c) tmem_ld32(tS + 32 * c, v[c]);
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c) tmem_ld_wait(v[c]);
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < BKV / 32; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (kbase + 32 * c + e > klim) v[c][e] = __float_as_uint(-INFINITY);
       }
+      // row max (raw scores; the scale is positive)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BKV / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[c][e]));
       const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
       if (kv == 0) {
         m = bmax;
@@ -280,27 +300,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      // pass 2: P = exp2(s * scale - m) as bf16 over the columns already read
+      // P = exp2(s * scale - m) as bf16 (masked scores are -inf: exp2 gives 0),
+      // written over the first 64 of the columns just read
       float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < BKV / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_ld_wait(v);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int k0 = kbase + 32 * c + 2 * e;
-          float x0 = __uint_as_float(v[2 * e]), x1 = __uint_as_float(v[2 * e + 1]);
-          float p0 = exp2f(fmaf(x0, scale_log2, -m_use)), p1 = exp2f(fmaf(x1, scale_log2, -m_use));
-          if (masked) {
-            if (k0 > klim) p0 = 0.0f;
-            if (k0 + 1 > klim) p1 = 0.0f;
-          }
+          const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e]), scale_log2, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e + 1]), scale_log2, -m_use));
           pk[e] = pack_bf16x2(p0, p1);
           ls[e & 3] += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
         }
-        tmem_st16(tS + 16 * c, pk);  // columns 16c.. were read by this thread already
+        tmem_st16(tS + 16 * c, pk);
       }
       tmem_st_wait();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
