@@ -102,9 +102,12 @@ __device__ __forceinline__ uint32_t half_packed_col(int kk) {
 // and LSE / Dsum rows are double-buffered.  Per block: S^T = K Q^T (fp16) and
 // dP^T = V dO^T into TMEM; the elementwise warps turn them into P^T (bf16) and
 // dS^T = P^T (dP^T - Dsum) (fp16) in place; dV += P^T dO and dK += dS^T Q with
-// A from TMEM.  The next block's products wait for this block's dV / dK products.
+// A from TMEM.  Each product has its own barrier so that the elementwise phases
+// overlap the tensor core: P^T is computed while dP^T is, dS^T while dV is, and the
+// next block's S^T (dP^T) starts as soon as this block's dV (dK) has read P^T (dS^T).
 enum : int {
-  K_KVF = 0, K_QF = 1 /* 2 */, K_QE = 3 /* 2 */, K_STF = 5, K_PF = 6, K_DSF = 7, K_ACC = 8, K_DR = 9, K_NB = 10
+  K_KVF = 0, K_QF = 1 /* 2 */, K_QE = 3 /* 2 */, K_SF = 5, K_DPF = 6, K_PF = 7, K_DSF = 8, K_DVD = 9, K_ACC = 10,
+  K_DR = 11, K_NB = 12
 };
 
 template <int D>
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(cm.bar(K_QE + st), ph ^ 1u, wc))) break;
       for (int t = lane; t < BLK; t += 32) {
         const int q = q0 + t;
-        lse_s[st * BLK + t] = q < a.S ? lse[row_base + q] : 0.0f;
+        lse_s[st * BLK + t] = q < a.S ? lse[row_base + q] * kLog2e : 0.0f;
         dd_s[st * BLK + t] = q < a.S ? dsum[row_base + q] : 0.0f;
       }
       __threadfence_block();
@@ -224,34 +227,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t ID_P = idesc_bf16(128, BLK, false, false);  // V dO^T
       constexpr uint32_t ID_DV = idesc_bf16(128, D, false, true);    // P^T dO
       constexpr uint32_t ID_DK = idesc_f16(128, D, false, true);     // dS^T Q
-      bool ok = mbar_wait(cm.bar(K_KVF), 0, wc), any = false;
-      for (int it = 0; it < nit && ok; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
-        if (!mbar_wait(cm.bar(K_QF + st), ph, wc)) {
-          ok = false;
-          break;
-        }
-        // the previous block's dV / dK products have read its P^T and dS^T
-        if (it > 0 && !mbar_wait(cm.bar(K_ACC), static_cast<uint32_t>((it - 1) & 1), wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      auto s_mmas = [&](int st) {  // S^T = K Q^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
           tc_mma_bf16(tmem, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ(st) + off, 16, 1024), ID_S,
                       kk > 0 ? 1u : 0u);
         }
+      };
+      auto dp_mmas = [&](int st) {  // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
           tc_mma_bf16(tmem + 128, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO(st) + off, 16, 1024), ID_P,
                       kk > 0 ? 1u : 0u);
         }
+      };
+      bool ok = mbar_wait(cm.bar(K_KVF), 0, wc) && (nit == 0 || mbar_wait(cm.bar(K_QF), 0, wc)), any = false;
+      if (ok && nit > 0) {
+        tc_fence_after();
+        s_mmas(0);
+        tc_commit(cm.bar(K_SF));
+        dp_mmas(0);
+        tc_commit(cm.bar(K_DPF));
         any = true;
-        tc_commit(cm.bar(K_STF));
+      }
+      for (int it = 0; it < nit && ok; ++it) {
+        const int st = it & 1, st1 = (it + 1) & 1;
+        const bool more = it + 1 < nit;
         if (!mbar_wait(cm.bar(K_PF), static_cast<uint32_t>(it & 1), wc)) {
           ok = false;
           break;
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < BLK / 16; ++kk)
           tc_mma_bf16_ts(tDV, tmem + half_packed_col(kk), sdesc_sw128(sDO(st) + kk * 2048, 16384, 1024), ID_DV,
                          (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(cm.bar(K_DVD));
         if (!mbar_wait(cm.bar(K_DSF), static_cast<uint32_t>(it & 1), wc)) {
           ok = false;
           break;
@@ -272,6 +276,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                          (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(cm.bar(K_QE + st));
         tc_commit(cm.bar(K_ACC));
+        if (more) {
+          // next block: S^T once this block's dV has read P^T, dP^T once its dK has read dS^T
+          if (!mbar_wait(cm.bar(K_QF + st1), static_cast<uint32_t>(((it + 1) >> 1) & 1), wc) ||
+              !mbar_wait(cm.bar(K_DVD), static_cast<uint32_t>(it & 1), wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          s_mmas(st1);
+          tc_commit(cm.bar(K_SF));
+          if (!mbar_wait(cm.bar(K_ACC), static_cast<uint32_t>(it & 1), wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          dp_mmas(st1);
+          tc_commit(cm.bar(K_DPF));
+        }
       }
       if (any) {
         tc_commit(cm.bar(K_DR));
@@ -289,26 +311,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int st = it & 1;
       const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
       const int q0 = q0_of(it) + 64 * half;
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_STF), static_cast<uint32_t>(it & 1), wc) &&
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_SF), static_cast<uint32_t>(it & 1), wc) &&
                                        mbar_wait(cm.bar(K_QF + st), ph, wc));
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = (a.causal && q0 < k0 + BLK) || (q0 + 64 > a.S) || (k0 + BLK > a.S);
-      const float* ls = lse_s + st * BLK + 64 * half;
-      const float* ds = dd_s + st * BLK + 64 * half;
+      const float4* ls4 = reinterpret_cast<const float4*>(lse_s + st * BLK + 64 * half);  // LSE * log2(e)
+      const float4* ds4 = reinterpret_cast<const float4*>(dd_s + st * BLK + 64 * half);
       float p[64];
       // P^T = exp(S^T / sqrt(d) - LSE), bf16, over the first half of these columns
+      {
+        uint32_t v[2][32];
+        tmem_ld32(tmem + trow + cS, v[0]);
+        tmem_ld32(tmem + trow + cS + 32, v[1]);
+        tmem_ld_wait(v[0]);
+        tmem_ld_wait(v[1]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + trow + cS + 32 * c, v);
-        tmem_ld_wait(v);
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = ls4[c4];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int qc = 32 * c + e;
-          float pv = exp2f(fmaf(__uint_as_float(v[e]), scale_log2, -ls[qc] * kLog2e));
-          if (need_mask && (q0 + qc >= a.S || key >= a.S || (a.causal && key > q0 + qc))) pv = 0.0f;
-          p[qc] = pv;
+          for (int u = 0; u < 4; ++u) {
+            const int qc = 4 * c4 + u;
+            float pv = ex2_approx(fmaf(__uint_as_float(v[qc >> 5][qc & 31]), scale_log2, -lv[u]));
+            if (need_mask && (q0 + qc >= a.S || key >= a.S || (a.causal && key > q0 + qc))) pv = 0.0f;
+            p[qc] = pv;
+          }
         }
       }
       {
@@ -322,17 +350,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(cm.bar(K_PF));
       // dS^T = P^T (dP^T - Dsum), fp16, over the first half of the dP^T columns
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_DPF), static_cast<uint32_t>(it & 1), wc));
+      if (!ok) break;
+      tc_fence_after();
       uint32_t dk[32];
+      {
+        uint32_t v[2][32];
+        tmem_ld32(tmem + trow + 128 + cS, v[0]);
+        tmem_ld32(tmem + trow + 128 + cS + 32, v[1]);
+        tmem_ld_wait(v[0]);
+        tmem_ld_wait(v[1]);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + trow + 128 + cS + 32 * c, v);
-        tmem_ld_wait(v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int qc = 32 * c + 2 * e;
-          dk[16 * c + e] = pack_f16x2(p[qc] * (__uint_as_float(v[2 * e]) - ds[qc]),
-                                      p[qc + 1] * (__uint_as_float(v[2 * e + 1]) - ds[qc + 1]));
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 d4 = ds4[c4];
+          const int qc = 4 * c4;
+          dk[2 * c4] = pack_f16x2(p[qc] * (__uint_as_float(v[qc >> 5][qc & 31]) - d4.x),
+                                  p[qc + 1] * (__uint_as_float(v[qc >> 5][(qc + 1) & 31]) - d4.y));
+          dk[2 * c4 + 1] = pack_f16x2(p[qc + 2] * (__uint_as_float(v[qc >> 5][(qc + 2) & 31]) - d4.z),
+                                      p[qc + 3] * (__uint_as_float(v[qc >> 5][(qc + 3) & 31]) - d4.w));
         }
       }
       tmem_st32(tmem + trow + 128 + cS, dk);
@@ -377,9 +412,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // of the head's group, K and V double-buffered.  Per block: S = Q K^T (fp16) and
 // dP = dO V^T; the elementwise warps turn them into dS = P (dP - Dsum) (fp16) over
 // the dP columns; dQ += dS K with A from TMEM.  The next block's S is computed as
-// soon as this block's S and dP have been read; its dP waits for this block's dQ.
+// soon as this block's S has been read, so that its P is computed while this
+// block's dQ and the next dP run; the next dP waits for this block's dQ.
 enum : int {
-  Q_QF = 0, Q_KF = 1 /* 2 */, Q_KE = 3 /* 2 */, Q_SF = 5, Q_SE = 6, Q_DSF = 7, Q_DQE = 8, Q_DR = 9, Q_NB = 10
+  Q_QF = 0, Q_KF = 1 /* 2 */, Q_KE = 3 /* 2 */, Q_SF = 5, Q_SE = 6, Q_DPF = 7, Q_DSF = 8, Q_DQE = 9, Q_DR = 10,
+  Q_NB = 11
 };
 
 template <int D>
@@ -494,8 +531,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (ok) {
           tc_fence_after();
           s_mmas(0);
-          dp_mmas(0);
           tc_commit(cm.bar(Q_SF));
+          dp_mmas(0);
+          tc_commit(cm.bar(Q_DPF));
           any = true;
         }
       }
@@ -512,6 +550,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           tc_fence_after();
           s_mmas(st1);
+          tc_commit(cm.bar(Q_SF));
         }
         if (!mbar_wait(cm.bar(Q_DSF), static_cast<uint32_t>(it & 1), wc)) {
           ok = false;
@@ -532,7 +571,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           tc_fence_after();
           dp_mmas(st1);
-          tc_commit(cm.bar(Q_SF));
+          tc_commit(cm.bar(Q_DPF));
         }
       }
       if (any) {
@@ -556,33 +595,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_SF), static_cast<uint32_t>(it & 1), wc));
       if (!ok) break;
       tc_fence_after();
-      uint32_t vs[64], vp[64];
-      tmem_ld32(trow + cS, *reinterpret_cast<uint32_t(*)[32]>(&vs[0]));
-      tmem_ld32(trow + cS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vs[32]));
-      tmem_ld32(trow + 128 + cS, *reinterpret_cast<uint32_t(*)[32]>(&vp[0]));
-      tmem_ld32(trow + 128 + cS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vp[32]));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&vs[0]));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&vs[32]));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&vp[0]));
-      tmem_ld_wait(*reinterpret_cast<uint32_t(*)[32]>(&vp[32]));
+      uint32_t vs[2][32];
+      tmem_ld32(trow + cS, vs[0]);
+      tmem_ld32(trow + cS + 32, vs[1]);
+      tmem_ld_wait(vs[0]);
+      tmem_ld_wait(vs[1]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cm.bar(Q_SE));  // S may be recomputed for the next block
       const bool need_mask = (a.causal && kbase + 64 > q0) || (kbase + 64 > a.S) || !qvalid;
+      float p[64];
+#pragma unroll
+      for (int kc = 0; kc < 64; ++kc) {
+        const int key = kbase + kc;
+        float pv = ex2_approx(fmaf(__uint_as_float(vs[kc >> 5][kc & 31]), scale_log2, -lse2));
+        if (need_mask && (!qvalid || key >= a.S || (a.causal && key > q))) pv = 0.0f;
+        p[kc] = pv;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DPF), static_cast<uint32_t>(it & 1), wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t vp[2][32];
+      tmem_ld32(trow + 128 + cS, vp[0]);
+      tmem_ld32(trow + 128 + cS + 32, vp[1]);
+      tmem_ld_wait(vp[0]);
+      tmem_ld_wait(vp[1]);
       uint32_t dk[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float d2[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int kc = 2 * e + u;
-          const int key = kbase + kc;
-          float p = exp2f(fmaf(__uint_as_float(vs[kc]), scale_log2, -lse2));
-          if (need_mask && (!qvalid || key >= a.S || (a.causal && key > q))) p = 0.0f;
-          d2[u] = p * (__uint_as_float(vp[kc]) - dd);
-        }
-        dk[e] = pack_f16x2(d2[0], d2[1]);
-      }
+      for (int e = 0; e < 32; ++e)
+        dk[e] = pack_f16x2(p[2 * e] * (__uint_as_float(vp[e >> 4][(2 * e) & 31]) - dd),
+                           p[2 * e + 1] * (__uint_as_float(vp[e >> 4][(2 * e + 1) & 31]) - dd));
       tmem_st32(trow + 128 + cS, dk);
       tmem_st_wait();
       tc_fence_before();
