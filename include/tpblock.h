@@ -198,11 +198,13 @@ TP_API size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h
  * (damodev 3D并行 §1.2.2; io.zouht.com 张量并行 §2.2.1 多头注意力机制: Q/K/V split
  *  by columns so each shard owns whole heads, W_O split by rows, one all-reduce;
  *  wangyu.me 张量并行 §注意力机制中的张量并行.)
- *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][5][H/N][d] (or ws): planes
- *                                             Q, K, V, then Q - bf16(Q) and K - bf16(K)
- *                                             (the scores are formed split-bf16,
- *                                             Qh Kh^T + Qh Kl^T + Ql Kh^T, so that Q K^T
- *                                             keeps ~16 bits before the softmax)
+ *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][3][H/N][d] (or ws): planes
+ *                                             Q, K, V; Q and K are stored as fp16 (11
+ *                                             significant bits, so that the scores
+ *                                             Q K^T, which the softmax exponentiates,
+ *                                             carry about 2^-11 relative error instead
+ *                                             of bf16's 2^-8; |Q|, |K| entries above
+ *                                             65504 overflow), V as bf16
  *   O_j   = softmax(mask(Q_j K_j^T / sqrt(d))) V_j, per batch and head j
  *                                          -> O_save [N][T][(H/N)*d] (or ws)
  *   LSE   = log sum_k exp(Q_j K_j^T/sqrt(d)) per query -> LSE_save [B][H][S] fp32 (or ws)
@@ -220,7 +222,8 @@ TP_API int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  *   per head: D = rowsum(dO * O), P = exp(S/sqrt(d) - LSE), dV = P^T dO,
  *             dP = dO V^T, dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
  *   dWqkv_i = X^T dQKV_i,  dX = sum_i dQKV_i Wqkv_i^T (shard sum on the device)
- *   (dQKV [N][T][3][H/N][d] lives in ws; P is recomputed with the same split scores)
+ *   (dQKV [N][T][3][H/N][d], all bf16, lives in ws; P is recomputed from the
+ *   saved fp16 Q, K and LSE)
  * QKV_save, O_save, LSE_save are what tp_attn_fwd wrote for the same inputs. */
 TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal,
                 const void* X, const void* Wqkv, const void* Wo,
@@ -241,7 +244,7 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  *   Wqkv     [N][h][(H/N + 2 Hkv/N) d]   shard i: its query heads, then its key
  *                                        heads, then its value heads, d columns each
  *   Wo       [N][(H/N) d][h]             as tp_attn_fwd
- *   QKV_save [N][T][(2 H/N + 3 Hkv/N) d] Q, K, V, then Q - bf16(Q), K - bf16(K)
+ *   QKV_save [N][T][(H/N + 2 Hkv/N) d]   Q, K (fp16), V (bf16) as tp_attn_fwd
  *   O_save, LSE_save, Z, dX, dWo         as tp_attn_fwd / tp_attn_bwd
  *   dWqkv    Wqkv's layout; a key/value head's gradient sums its group's query heads */
 TP_API size_t tp_gqa_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N);

@@ -111,7 +111,7 @@ int attn_shape_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv,
   return TP_OK;
 }
 
-// Workspace of the attention block: [QKV (Q, K, V and the residual planes) | O |
+// Workspace of the attention block: [QKV (fp16 Q, K; bf16 V) | O |
 // LSE] in the forward; [dQKV | dO | Dsum] in the backward fits the same regions.
 struct AttnWs {
   size_t qkv, o, lse, total;
