@@ -277,7 +277,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_commit(cm.bar(K_QE + st));
         tc_commit(cm.bar(K_ACC));
         if (more) {
-          // next block: S^T once this block's dV has read P^T, dP^T once its dK has read dS^T
+          // the next block's S^T once this block's dV has read P^T (dK keeps the tensor
+          // core busy meanwhile), its dP^T once dK has read dS^T
           if (!mbar_wait(cm.bar(K_QF + st1), static_cast<uint32_t>(((it + 1) >> 1) & 1), wc) ||
               !mbar_wait(cm.bar(K_DVD), static_cast<uint32_t>(it & 1), wc)) {
             ok = false;
@@ -333,11 +334,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int qc = 4 * c4 + u;
-            float pv = ex2_approx(fmaf(__uint_as_float(v[qc >> 5][qc & 31]), scale_log2, -lv[u]));
-            if (need_mask && (q0 + qc >= a.S || key >= a.S || (a.causal && key > q0 + qc))) pv = 0.0f;
-            p[qc] = pv;
+            p[qc] = ex2_approx(fmaf(__uint_as_float(v[qc >> 5][qc & 31]), scale_log2, -lv[u]));
           }
         }
+      }
+      if (need_mask) {  // warp-uniform: only diagonal and ragged blocks
+#pragma unroll
+        for (int qc = 0; qc < 64; ++qc)
+          if (q0 + qc >= a.S || key >= a.S || (a.causal && key > q0 + qc)) p[qc] = 0.0f;
       }
       {
         uint32_t pk[32];
@@ -409,14 +413,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 // ---------------------------------------------------------------------- dQ
 // One CTA per (128-query block, query head, batch); loops over the 128-key blocks
-// of the head's group, K and V double-buffered.  Per block: S = Q K^T (fp16) and
+// of the head's group, K in three shared-memory stages (a stage is free only once
+// the block's dQ product has read it, late in the block) and V in two (free once
+// the block's dP has).  Per block: S = Q K^T (fp16) and
 // dP = dO V^T; the elementwise warps turn them into dS = P (dP - Dsum) (fp16) over
-// the dP columns; dQ += dS K with A from TMEM.  The next block's S is computed as
-// soon as this block's S has been read, so that its P is computed while this
-// block's dQ and the next dP run; the next dP waits for this block's dQ.
+// the dP columns; dQ += dS K with A from TMEM.  dP / dS alternate between two TMEM
+// buffers, so the next block's S and dP are computed while this block's dS and dQ
+// are: S once this block's S has been read, dP once the dQ product two blocks back
+// has read the dS its buffer held.
+constexpr int kDqKStages = 3;
 enum : int {
-  Q_QF = 0, Q_KF = 1 /* 2 */, Q_KE = 3 /* 2 */, Q_SF = 5, Q_SE = 6, Q_DPF = 7, Q_DSF = 8, Q_DQE = 9, Q_DR = 10,
-  Q_NB = 11
+  Q_QF = 0, Q_KF = 1 /* 3 */, Q_KE = 4 /* 3 */, Q_VF = 7 /* 2 */, Q_VE = 9 /* 2 */, Q_SF = 11, Q_SE = 12,
+  Q_DPF = 13 /* 2 */, Q_DSF = 15 /* 2 */, Q_DQE = 17 /* 2 */, Q_DR = 19, Q_NB = 20
 };
 
 template <int D>
@@ -424,8 +432,9 @@ struct DqCfg {
   static constexpr int CH = D / 64;
   static constexpr int TILE = CH * 16384;  // 128 rows x D 16-bit values
   static constexpr int OFF_Q = 0, OFF_DO = TILE;
-  static constexpr int OFF_K = 2 * TILE;  // [stage][K, V]
-  static constexpr int OFF_BAR = OFF_K + 4 * TILE;
+  static constexpr int OFF_K = 2 * TILE;                     // [3 stages]
+  static constexpr int OFF_V = OFF_K + kDqKStages * TILE;    // [2 stages]
+  static constexpr int OFF_BAR = OFF_V + 2 * TILE;
   static constexpr int OFF_MISC = OFF_BAR + Q_NB * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
@@ -445,8 +454,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = smem_raw + pad;
   const BwdCommon cm{raw + pad, raw + pad + C::OFF_BAR};
   const uint32_t sQ = cm.sb + C::OFF_Q, sDO = cm.sb + C::OFF_DO;
-  auto sK = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>((2 * st) * C::TILE); };
-  auto sV = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>((2 * st + 1) * C::TILE); };
+  auto sK = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>(st * C::TILE); };
+  auto sV = [&](int st) { return cm.sb + C::OFF_V + static_cast<uint32_t>(st * C::TILE); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -461,7 +470,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int cQ = a.col_q(jj), cK = a.col_k(kvh), cV = a.col_v(kvh);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q_NB; ++i) mbar_init(cm.bar(i), (i == Q_SE || i == Q_DSF) ? 8 : 1);
+    for (int i = 0; i < Q_NB; ++i) mbar_init(cm.bar(i), (i == Q_SE || i == Q_DSF || i == Q_DSF + 1) ? 8 : 1);
     *abort_flag = 0;
     *never_flag = 0;
     fence_mbar_init();
@@ -476,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
-  // TMEM: S [0, 128), dP / dS [128, 256), dQ [256, +D)
+  // TMEM: S [0, 128), dP / dS buffer 0 [128, 256), dQ [256, +D), dP / dS buffer 1 [384, 512)
 
   if (warp == 8) {
     if (lane == 0) {
@@ -486,23 +495,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_4d(sQ + c * 16384, &tmQKV, cm.bar(Q_QF), cQ + 64 * c, q0, b, shard);
         tma_load_4d(sDO + c * 16384, &tmDO, cm.bar(Q_QF), jj * D + 64 * c, q0, b, shard);
       }
-      int issued = 0;
+      int kiss = 0, viss = 0;  // key blocks whose K / V copies were issued
       for (int it = 0; it < nkv; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = static_cast<uint32_t>((it >> 1) & 1);
-        if (!mbar_wait(cm.bar(Q_KE + st), ph ^ 1u, wc)) break;
-        const uint32_t fb = cm.bar(Q_KF + st);
-        mbar_arrive_expect_tx(fb, 2 * C::TILE);
+        const int sk = it % kDqKStages, sv = it & 1;
+        if (!mbar_wait(cm.bar(Q_KE + sk), static_cast<uint32_t>(((it / kDqKStages) & 1) ^ 1), wc)) break;
+        mbar_arrive_expect_tx(cm.bar(Q_KF + sk), C::TILE);
 #pragma unroll
-        for (int c = 0; c < C::CH; ++c) {
-          tma_load_4d(sK(st) + c * 16384, &tmQKV, fb, cK + 64 * c, it * BLK, b, shard);
-          tma_load_4d(sV(st) + c * 16384, &tmQKV, fb, cV + 64 * c, it * BLK, b, shard);
-        }
-        issued = it + 1;
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_4d(sK(sk) + c * 16384, &tmQKV, cm.bar(Q_KF + sk), cK + 64 * c, it * BLK, b, shard);
+        kiss = it + 1;
+        if (!mbar_wait(cm.bar(Q_VE + sv), static_cast<uint32_t>(((it >> 1) & 1) ^ 1), wc)) break;
+        mbar_arrive_expect_tx(cm.bar(Q_VF + sv), C::TILE);
+#pragma unroll
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_4d(sV(sv) + c * 16384, &tmQKV, cm.bar(Q_VF + sv), cV + 64 * c, it * BLK, b, shard);
+        viss = it + 1;
       }
+      // every issued copy lands before the CTA may exit
       mbar_wait(cm.bar(Q_QF), 0, wdrain);
-      for (int it = issued - 2 < 0 ? 0 : issued - 2; it < issued; ++it)
-        mbar_wait(cm.bar(Q_KF + (it & 1)), (it >> 1) & 1, wdrain);
+      for (int k = (kiss > kDqKStages ? kiss - kDqKStages : 0); k < kiss; ++k)
+        mbar_wait(cm.bar(Q_KF + k % kDqKStages), static_cast<uint32_t>((k / kDqKStages) & 1), wdrain);
+      for (int k = (viss > 2 ? viss - 2 : 0); k < viss; ++k)
+        mbar_wait(cm.bar(Q_VF + (k & 1)), static_cast<uint32_t>((k >> 1) & 1), wdrain);
     }
   } else if (warp == 9) {
     if (lane == 0) {
@@ -517,62 +531,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       kk > 0 ? 1u : 0u);
         }
       };
-      auto dp_mmas = [&](int st) {
+      auto dp_mmas = [&](int st, int buf) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
-          tc_mma_bf16(tmem + 128, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(sV(st) + off, 16, 1024), ID_P,
-                      kk > 0 ? 1u : 0u);
+          tc_mma_bf16(tmem + 128 + 256 * buf, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(sV(st) + off, 16, 1024),
+                      ID_P, kk > 0 ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(cm.bar(Q_QF), 0, wc), any = false;
       if (ok && nkv > 0) {
-        ok = mbar_wait(cm.bar(Q_KF), 0, wc);
+        ok = mbar_wait(cm.bar(Q_KF), 0, wc) && mbar_wait(cm.bar(Q_VF), 0, wc);
         if (ok) {
           tc_fence_after();
           s_mmas(0);
           tc_commit(cm.bar(Q_SF));
-          dp_mmas(0);
+          dp_mmas(0, 0);
           tc_commit(cm.bar(Q_DPF));
+          tc_commit(cm.bar(Q_VE));
           any = true;
         }
       }
       for (int it = 0; it < nkv && ok; ++it) {
-        const int st = it & 1;
-        const int st1 = (it + 1) & 1;
+        const int st = it & 1, st1 = (it + 1) & 1;  // V stage; also the dP / dS buffer
+        const int sk = it % kDqKStages, sk1 = (it + 1) % kDqKStages;
         const bool more = it + 1 < nkv;
-        // the next block's scores once this block's S and dP have been read
         if (more) {
-          if (!mbar_wait(cm.bar(Q_KF + st1), static_cast<uint32_t>(((it + 1) >> 1) & 1), wc) ||
+          // the next block's scores once this block's S has been read
+          if (!mbar_wait(cm.bar(Q_KF + sk1), static_cast<uint32_t>(((it + 1) / kDqKStages) & 1), wc) ||
               !mbar_wait(cm.bar(Q_SE), static_cast<uint32_t>(it & 1), wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          s_mmas(st1);
+          s_mmas(sk1);
           tc_commit(cm.bar(Q_SF));
+          // its dP into the other buffer once the dQ product of block it-1 has read it
+          if ((it >= 1 && !mbar_wait(cm.bar(Q_DQE + st1), static_cast<uint32_t>(((it - 1) >> 1) & 1), wc)) ||
+              !mbar_wait(cm.bar(Q_VF + st1), static_cast<uint32_t>(((it + 1) >> 1) & 1), wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          dp_mmas(st1, st1);
+          tc_commit(cm.bar(Q_DPF + st1));
+          tc_commit(cm.bar(Q_VE + st1));
         }
-        if (!mbar_wait(cm.bar(Q_DSF), static_cast<uint32_t>(it & 1), wc)) {
+        if (!mbar_wait(cm.bar(Q_DSF + st), static_cast<uint32_t>((it >> 1) & 1), wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BLK / 16; ++kk)
-          tc_mma_bf16_ts(tmem + 256, tmem + 128 + half_packed_col(kk), sdesc_sw128(sK(st) + kk * 2048, 16384, 1024),
-                         ID_DQ, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(cm.bar(Q_DQE));
-        tc_commit(cm.bar(Q_KE + st));
-        if (more) {
-          // the next dP overwrites this block's dS: wait for the dQ product
-          if (!mbar_wait(cm.bar(Q_DQE), static_cast<uint32_t>(it & 1), wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          dp_mmas(st1);
-          tc_commit(cm.bar(Q_DPF));
-        }
+          tc_mma_bf16_ts(tmem + 256, tmem + 128 + 256 * st + half_packed_col(kk),
+                         sdesc_sw128(sK(sk) + kk * 2048, 16384, 1024), ID_DQ, (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(cm.bar(Q_DQE + st));
+        tc_commit(cm.bar(Q_KE + sk));
       }
       if (any) {
         tc_commit(cm.bar(Q_DR));
@@ -606,18 +621,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool need_mask = (a.causal && kbase + 64 > q0) || (kbase + 64 > a.S) || !qvalid;
       float p[64];
 #pragma unroll
-      for (int kc = 0; kc < 64; ++kc) {
-        const int key = kbase + kc;
-        float pv = ex2_approx(fmaf(__uint_as_float(vs[kc >> 5][kc & 31]), scale_log2, -lse2));
-        if (need_mask && (!qvalid || key >= a.S || (a.causal && key > q))) pv = 0.0f;
-        p[kc] = pv;
+      for (int kc = 0; kc < 64; ++kc)
+        p[kc] = ex2_approx(fmaf(__uint_as_float(vs[kc >> 5][kc & 31]), scale_log2, -lse2));
+      if (need_mask) {  // warp-uniform: only diagonal and ragged blocks
+#pragma unroll
+        for (int kc = 0; kc < 64; ++kc) {
+          const int key = kbase + kc;
+          if (!qvalid || key >= a.S || (a.causal && key > q)) p[kc] = 0.0f;
+        }
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DPF), static_cast<uint32_t>(it & 1), wc));
+      const uint32_t tbuf = trow + 128 + 256 * static_cast<uint32_t>(it & 1);  // this block's dP / dS
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DPF + (it & 1)), static_cast<uint32_t>((it >> 1) & 1), wc));
       if (!ok) break;
       tc_fence_after();
       uint32_t vp[2][32];
-      tmem_ld32(trow + 128 + cS, vp[0]);
-      tmem_ld32(trow + 128 + cS + 32, vp[1]);
+      tmem_ld32(tbuf + cS, vp[0]);
+      tmem_ld32(tbuf + cS + 32, vp[1]);
       tmem_ld_wait(vp[0]);
       tmem_ld_wait(vp[1]);
       uint32_t dk[32];
@@ -625,15 +644,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int e = 0; e < 32; ++e)
         dk[e] = pack_f16x2(p[2 * e] * (__uint_as_float(vp[e >> 4][(2 * e) & 31]) - dd),
                            p[2 * e + 1] * (__uint_as_float(vp[e >> 4][(2 * e + 1) & 31]) - dd));
-      tmem_st32(trow + 128 + cS, dk);
+      tmem_st32(tbuf + cS, dk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(cm.bar(Q_DSF));
+      if (lane == 0) mbar_arrive(cm.bar(Q_DSF + (it & 1)));
     }
-    // the last dQ product (the previous ones completed before their next dP)
+    // the last dQ product (its commit covers every earlier MMA of the issuing thread)
     if (ok && nkv > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DQE), static_cast<uint32_t>((nkv - 1) & 1), wc));
+      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DQE + ((nkv - 1) & 1)), static_cast<uint32_t>(((nkv - 1) >> 1) & 1), wc));
     if (ok && half == 0) {
       tc_fence_after();
       // all MMAs are complete: the Q tile is free for staging
