@@ -33,8 +33,18 @@ DEFAULT_WORKLOAD = "mlp_bf16_T8192_h4096_f16384_N8"
 
 # DRAM bytes (read + write) per launch from one ncu capture of the kernel, with
 # the sha256 of the kernel source it was taken on; reported as null once the
-# source has changed.  Filled from the summaries under profiles/.
-NCU_TRAFFIC: dict = {}
+# source has changed (profiles/gemm_mlp_T8192_h4096_f16384_N8_dram.md).
+NCU_TRAFFIC: dict = {
+    k: {"bytes": v, "sha": "c910f35bd853d4a6", "workload": "mlp_bf16_T8192_h4096_f16384_N8"}
+    for k, v in {
+        "mlp.fc1_col_gemm_gelu": 1014514688,
+        "mlp.fc2_row_gemm_shard_sum": 1445998080,
+        "mlp.bwd_dA_gemm_dgelu": 1088027136,
+        "mlp.bwd_dW2_gemm": 1339154432,
+        "mlp.bwd_dW1_gemm": 1349822720,
+        "mlp.bwd_dX_row_gemm_shard_sum": 1445978368,
+    }.items()
+}
 
 
 def peaks() -> dict:
