@@ -10,11 +10,17 @@
 //           columns 128*(w/4).. (its half), so every SM sub-partition runs two
 //           epilogue warps to hide the latency of the fused math; fused GeLU /
 //           GeLU' in fp32, bf16 pack into a swizzled staging box, TMA store.
+// The main loop is fed by as many stages as shared memory holds next to the
+// epilogue's staging: a k-block's loads take microseconds to arrive from L2, and
+// with one stage fewer the MMA issuer measurably waits for data.  The plain-store
+// epilogues stage through one 4 KB box per warp (32 KB), the fused ones through two
+// (an input and an output, or two outputs; 64 KB).
 // Two tilings:
-//   single: one CTA per 128 x 256 tile (cta_group::1, M=128 N=256); 3 stages of 48 KB.
+//   single: one CTA per 128 x 256 tile (cta_group::1, M=128 N=256); 4 (fused: 3)
+//           stages of 48 KB.
 //   pair:   a cluster of two CTAs per 256 x 256 tile (cta_group::2, M=256 N=256):
 //           each CTA stages its 128 rows of A and half (128 columns) of B, so each
-//           SM moves 32 KB per k-block instead of 48; 5 stages.  The even CTA issues
+//           SM moves 32 KB per k-block instead of 48; 6 (fused: 5) stages.  The even CTA issues
 //           the MMAs; both CTAs' TMA loads count on its full barrier; its commits
 //           multicast to both CTAs' empty / accumulator-ready barriers; both CTAs'
 //           epilogue warps release an accumulator on the even CTA's barrier.
@@ -39,12 +45,13 @@ constexpr int WARP_MMA = 9;
 constexpr int TMEM_COLS = 512;
 constexpr int GROUP_M = 16;
 
-template <bool PAIR>
+template <bool PAIR, int EPI>
 struct Cfg {
+  static constexpr int EBUFS = (EPI == kEpiStore || EPI == kEpiSplit) ? 1 : 2;  // staging boxes per warp
   static constexpr int BM = 128;                      // accumulator rows per CTA
   static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per output tile
   static constexpr int BN_CTA = PAIR ? 128 : 256;     // B columns staged per CTA
-  static constexpr int STAGES = PAIR ? 5 : 3;
+  static constexpr int STAGES = PAIR ? (EBUFS == 1 ? 6 : 5) : (EBUFS == 1 ? 4 : 3);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -56,7 +63,7 @@ struct Cfg {
   static constexpr int BAR_DRAIN = BAR_Y + 2 * EPI_WARPS;
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int SMEM_EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * 2 * EPI_BUF;
+  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * EBUFS * EPI_BUF;
   static constexpr int SMEM_MISC_OFF = SMEM_BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_USED = SMEM_MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
@@ -164,6 +171,23 @@ __device__ __forceinline__ void op_load(uint32_t dst, const CUtensorMap* m, uint
   if (spS > 0) tok_coords(c1, spS, spL, tp.sl, tp.b, tp.c);
   op_load_at<PAIR>(dst, m, bar, c0, c1, z, spS > 0, tp);
 }
+// One copy of an MN-major operand's stage through a chunked map: {64, K, chunks, z}
+// (or {64, L, chunks, B, S/L} for sequence-sharded K); chunk0 = first 64-wide chunk.
+template <bool PAIR>
+__device__ __forceinline__ void mn_load(uint32_t dst, const CUtensorMap* m, uint32_t bar, int chunk0, int k, int z,
+                                        bool sp, const TokPos& tp) {
+  if (sp) {
+    if (PAIR)
+      tma_load_5d_pair(dst, m, bar, 0, tp.sl, chunk0, tp.b, tp.c);
+    else
+      tma_load_5d(dst, m, bar, 0, tp.sl, chunk0, tp.b, tp.c);
+  } else {
+    if (PAIR)
+      tma_load_4d_pair(dst, m, bar, 0, k, chunk0, z);
+    else
+      tma_load_4d(dst, m, bar, 0, k, chunk0, z);
+  }
+}
 __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, int c0, int row, int z, int spS, int spL) {
   if (spS > 0) {
     int sl, bb, cc;
@@ -178,7 +202,7 @@ template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, const GemmShape p) {
-  using C = Cfg<PAIR>;
+  using C = Cfg<PAIR, EPI>;
   // output columns per tile: the gated forward spends half the MMA's N on the up part
   constexpr int TILE_N = EPI == kEpiSwiGLU ? BN / 2 : BN;
   constexpr int WARP_COLS = TILE_N / 2;  // output columns per epilogue warp
@@ -279,7 +303,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (PAIR) {
               const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's full barrier counts both
               if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
-              if (A_MN) {
+              if (A_MN && p.a_chunked) {
+                mn_load<true>(sa, &tmA, fb, arow / 64, kc, az, a_k_sp, kpos);
+              } else if (A_MN) {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
                   op_load_at<true>(sa + j * (BK * 128), &tmA, fb, arow + j * 64, kc, az, a_k_sp, kpos);
@@ -288,9 +314,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               if (EPI == kEpiSwiGLU) {
                 // the even CTA stages the tile's gate columns, the odd CTA its up columns
+                if (p.b_chunked) {
+                  tma_load_5d_pair(sb, &tmB, fb, 0, kc, bcol / 64, static_cast<int>(rank), bz);
+                } else {
 #pragma unroll
-                for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz);
+                  for (int j = 0; j < C::BN_CTA / 64; ++j)
+                    tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz);
+                }
+              } else if (B_MN && p.b_chunked) {
+                mn_load<true>(sb, &tmB, fb, bcol / 64, kc, bz, b_k_sp, kpos);
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
@@ -300,7 +332,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             } else {
               mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
-              if (A_MN) {
+              if (A_MN && p.a_chunked) {
+                mn_load<false>(sa, &tmA, fb_local, arow / 64, kc, az, a_k_sp, kpos);
+              } else if (A_MN) {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
                   op_load_at<false>(sa + j * (BK * 128), &tmA, fb_local, arow + j * 64, kc, az, a_k_sp, kpos);
@@ -309,9 +343,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               if (EPI == kEpiSwiGLU) {
                 // atoms 0-1: gate columns, atoms 2-3: the same columns of the up part
+                if (p.b_chunked) {
+                  tma_load_5d(sb, &tmB, fb_local, 0, kc, bcol / 64, 0, bz);
+                  tma_load_5d(sb + 2 * (BK * 128), &tmB, fb_local, 0, kc, bcol / 64, 1, bz);
+                } else {
 #pragma unroll
-                for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  tma_load_4d(sb + j * (BK * 128), &tmB, fb_local, bcol + (j & 1) * 64, j >> 1, kc, bz);
+                  for (int j = 0; j < C::BN_CTA / 64; ++j)
+                    tma_load_4d(sb + j * (BK * 128), &tmB, fb_local, bcol + (j & 1) * 64, j >> 1, kc, bz);
+                }
+              } else if (B_MN && p.b_chunked) {
+                mn_load<false>(sb, &tmB, fb_local, bcol / 64, kc, bz, b_k_sp, kpos);
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j)
@@ -413,8 +454,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp;                 // staging buffers and Y barriers
     const int quad = warp & 3;           // TMEM lanes 32*quad .. 32*quad+31
     const int half = warp >> 2;          // tile columns 128*half .. 128*half+127
-    const uint32_t ebuf[2] = {sbase + C::SMEM_EPI_OFF + ew * 2 * EPI_BUF,
-                              sbase + C::SMEM_EPI_OFF + ew * 2 * EPI_BUF + EPI_BUF};
+    const uint32_t ebuf[2] = {sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EPI_BUF,
+                              sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EPI_BUF + (C::EBUFS - 1) * EPI_BUF};
     const uint32_t ybar[2] = {bar0 + 8u * (BAR_Y + 2 * ew), bar0 + 8u * (BAR_Y + 2 * ew + 1)};
     const uint32_t rsw = static_cast<uint32_t>(lane & 7);
     uint32_t yph = 0;      // bit b: parity of the next completion of ybar[b]
@@ -474,7 +515,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld_wait(r0);
             tmem_ld_wait(r1);
             const uint32_t sb = ebuf[ecount & 1u];
-            if (lane == 0) bulk_wait_read1();
+            // one staging box: the previous chunk's store must have read it
+            if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
@@ -735,7 +777,8 @@ KernelFn get_kernel() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
   auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI>;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR>::SMEM_ALLOC) != cudaSuccess)
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR, EPI>::SMEM_ALLOC) !=
+        cudaSuccess)
       return nullptr;
     configured[dev] = true;
   }
@@ -754,6 +797,32 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
   if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
   if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual>();
   return nullptr;
+}
+
+// An MN-major operand whose d0 is a multiple of 64: the 64-element chunks of a row
+// become an outer dimension, so a box {64, BK, chunks} lands in shared memory as the
+// chunk-major 128-byte-swizzled layout the MMA descriptors read (chunk c at c * 8 KB).
+bool chunked_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
+  const uint64_t d0 = static_cast<uint64_t>(o.d0), e = 2;
+  const uint32_t nch = o.parts == 2 ? 2u : rows / 64u;
+  if (o.sp_S > 0) {  // [S/L][B][L][d0] -> {64, L, d0/64, B, S/L}
+    const uint64_t L = static_cast<uint64_t>(o.sp_L), Bn = static_cast<uint64_t>(o.d1 / o.sp_S);
+    const uint64_t dims[5] = {64u, L, d0 / 64, Bn, static_cast<uint64_t>(o.sp_S / o.sp_L)};
+    const uint64_t gs[4] = {d0 * e, 128u, L * d0 * e, Bn * L * d0 * e};
+    const uint32_t box[5] = {64u, static_cast<uint32_t>(BK), nch, 1u, 1u};
+    return encode_tmap_strided(m, 5, o.ptr, dims, gs, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t d1 = static_cast<uint64_t>(o.d1), d2 = static_cast<uint64_t>(o.d2);
+  if (o.parts == 2) {  // [d2][d1][2][d0] -> {64, d1, d0/64, 2, d2}
+    const uint64_t dims[5] = {64u, d1, d0 / 64, 2u, d2};
+    const uint64_t gs[4] = {2 * d0 * e, 128u, d0 * e, d1 * 2 * d0 * e};
+    const uint32_t box[5] = {64u, static_cast<uint32_t>(BK), nch, 1u, 1u};
+    return encode_tmap_strided(m, 5, o.ptr, dims, gs, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  const uint64_t dims[4] = {64u, d1, d0 / 64, d2};  // [d2][d1][d0] -> {64, d1, d0/64, d2}
+  const uint64_t gs[3] = {d0 * e, 128u, d1 * d0 * e};
+  const uint32_t box[4] = {64u, static_cast<uint32_t>(BK), nch, 1u};
+  return encode_tmap_strided(m, 4, o.ptr, dims, gs, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool operand_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
@@ -823,9 +892,16 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (sms < 2) pair = false;
   KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
   if (!fn) return 2;
-  const uint32_t a_rows = 128, b_rows = pair ? Cfg<true>::BN_CTA : Cfg<false>::BN_CTA;
+  const uint32_t a_rows = 128, b_rows = pair ? Cfg<true, kEpiStore>::BN_CTA : Cfg<false, kEpiStore>::BN_CTA;
+  const bool one_box = epi == kEpiStore || epi == kEpiSplit;
+  const int smem = pair ? (one_box ? Cfg<true, kEpiStore>::SMEM_ALLOC : Cfg<true, kEpiGelu>::SMEM_ALLOC)
+                        : (one_box ? Cfg<false, kEpiStore>::SMEM_ALLOC : Cfg<false, kEpiGelu>::SMEM_ALLOC);
   CUtensorMap ta, tb, tc, ty;
-  if (!operand_map(&ta, A, a_rows) || !operand_map(&tb, B, b_rows)) return 2;
+  // MN-major operands with whole 64-element chunks: one copy per stage
+  const bool a_ch = A.mn_major && A.d0 % 64 == 0, b_ch = B.mn_major && B.d0 % 64 == 0;
+  if (!(a_ch ? chunked_map(&ta, A, a_rows) : operand_map(&ta, A, a_rows)) ||
+      !(b_ch ? chunked_map(&tb, B, b_rows) : operand_map(&tb, B, b_rows)))
+    return 2;
   const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
   const uint32_t cbox[3] = {64u, 32u, 1u};
   const uint64_t sdims[4] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(extra.c_sp_L),
@@ -872,6 +948,8 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   // fold the groups into N when they share A (the column-parallel GEMMs' X or dZ);
   // folding into M for a shared B measured slower (more L2 misses) and is not used
   p.g_mode = (G > 1 && A.zg == 0) ? 1 : 0;
+  p.a_chunked = a_ch ? 1 : 0;
+  p.b_chunked = b_ch ? 1 : 0;
   p.err = err;
   p.timeout_ns = timeout_ns;
   const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;
@@ -882,7 +960,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<true>::SMEM_ALLOC;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -894,7 +972,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
     ok = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, ty, p) == cudaSuccess;
   } else {
     const int grid = static_cast<int>(total < sms ? total : sms);
-    fn<<<grid, NUM_THREADS, Cfg<false>::SMEM_ALLOC, stream>>>(ta, tb, tc, ty, p);
+    fn<<<grid, NUM_THREADS, static_cast<size_t>(smem), stream>>>(ta, tb, tc, ty, p);
     ok = cudaGetLastError() == cudaSuccess;
   }
   timing_end(slot, stream);

@@ -48,6 +48,10 @@ struct GemmShape {
   // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
   int a_spS, a_spL, b_spS, b_spL, c_spS, c_spL;
   int g_mode;  // tile order across groups (gemm_tc.cu decode_tile)
+  // an MN-major operand whose rows are whole 64-element chunks is read through a map
+  // with the chunk as an outer dimension ({64, K, chunks, ...}), so one copy per
+  // stage brings all of its columns (the producer's issue time per copy is ~100 cycles)
+  int a_chunked, b_chunked;
   unsigned* err;
   unsigned long long timeout_ns;
 };

@@ -50,6 +50,24 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_strided(CUtensorMap* map, int rank, const void* base, const uint64_t* dims, const uint64_t* gstride,
+                         const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode || rank < 1 || rank > 5) return false;
+  cuuint64_t gdim[5], gs[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gs[i - 1] = gstride[i - 1];
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                        gdim, gs, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

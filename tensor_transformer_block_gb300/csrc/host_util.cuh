@@ -15,6 +15,10 @@ namespace tpb {
 // 128-byte swizzle.  Returns true on success.
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                  const uint64_t* dims, const uint32_t* box, CUtensorMapSwizzle swizzle);
+// The same for a bf16 tensor whose dimensions are not packed: gstride[i] is the
+// byte stride of dimension i+1 (a multiple of 16), dimension 0 being contiguous.
+bool encode_tmap_strided(CUtensorMap* map, int rank, const void* base, const uint64_t* dims, const uint64_t* gstride,
+                         const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
