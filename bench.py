@@ -318,6 +318,108 @@ def run_reference(args, w) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ library baseline
+def library_composition(w, d: dict):
+    """(forward function, unsharded weights) of the workload's step composed from
+    torch library calls: matmuls, torch's tanh GeLU, SiLU, LayerNorm and
+    scaled-dot-product attention.  The shard-major weights are viewed back as the
+    unsharded matrices the pages split."""
+    import torch.nn.functional as F
+
+    N, h, f, T = w.N, w.h, w.f, w.T
+
+    def cols(Ws):  # [N][rows][c] -> [rows][N*c]: shard i holds columns i*c..
+        return Ws.permute(1, 0, 2).reshape(Ws.shape[1], -1)
+
+    def heads(t, nh):  # [T][nh*d] -> [B][nh][S][d]
+        return t.view(w.B, w.S, nh, w.d).transpose(1, 2)
+
+    def attention(x, Wq, Wk, Wv, Wo, H, Hkv):
+        q, k, v = heads(x @ Wq, H), heads(x @ Wk, Hkv), heads(x @ Wv, Hkv)
+        if H != Hkv:
+            o = F.scaled_dot_product_attention(q, k, v, is_causal=bool(w.causal), enable_gqa=True)
+        else:
+            o = F.scaled_dot_product_attention(q, k, v, is_causal=bool(w.causal))
+        return o.transpose(1, 2).reshape(T, H * w.d) @ Wo
+
+    def mlp(x, W1, W2):
+        return F.gelu(x @ W1, approximate="tanh") @ W2
+
+    def qkv_mha(Wqkv):  # [N][h][3][H/N][d] (same bytes as [N][h][3 H/N d])
+        q = Wqkv.reshape(N, h, 3, -1)
+        return cols(q[:, :, 0]), cols(q[:, :, 1]), cols(q[:, :, 2])
+
+    p = {}
+    if w.kind == "mlp":
+        p = {"W1": cols(d["W1s"]), "W2": d["W2s"].reshape(f, h)}
+        fwd = lambda x, q: mlp(x, q["W1"], q["W2"])  # noqa: E731
+    elif w.kind == "gmlp":
+        p = {"Wg": cols(d["Wgus"][:, :, 0]), "Wu": cols(d["Wgus"][:, :, 1]), "Wd": d["Wds"].reshape(f, h)}
+        fwd = lambda x, q: (F.silu(x @ q["Wg"]) * (x @ q["Wu"])) @ q["Wd"]  # noqa: E731
+    elif w.kind == "gqa":
+        hN, kvN = w.H // N, w.Hkv // N
+        Wqkv = d["Wqkv"]
+        p = {"Wq": cols(Wqkv[:, :, :hN * w.d]), "Wk": cols(Wqkv[:, :, hN * w.d:(hN + kvN) * w.d]),
+             "Wv": cols(Wqkv[:, :, (hN + kvN) * w.d:]), "Wo": d["Wo"].reshape(w.H * w.d, h)}
+        fwd = lambda x, q: attention(x, q["Wq"], q["Wk"], q["Wv"], q["Wo"], w.H, w.Hkv)  # noqa: E731
+    else:
+        Wq, Wk, Wv = qkv_mha(d["Wqkv"])
+        p = {"Wq": Wq, "Wk": Wk, "Wv": Wv, "Wo": d["Wo"].reshape(w.H * w.d, h)}
+        if w.kind == "attn":
+            fwd = lambda x, q: attention(x, q["Wq"], q["Wk"], q["Wv"], q["Wo"], w.H, w.H)  # noqa: E731
+        else:
+            p.update({"W1": cols(d["W1s"]), "W2": d["W2s"].reshape(f, h)})
+            if w.kind == "layer":
+                def fwd(x, q):
+                    return mlp(attention(x, q["Wq"], q["Wk"], q["Wv"], q["Wo"], w.H, w.H), q["W1"], q["W2"])
+            else:
+                p.update({k: d[k] for k in ("ln1_g", "ln1_b", "ln2_g", "ln2_b")})
+
+                def fwd(x, q):
+                    a = F.layer_norm(x, (h,), q["ln1_g"], q["ln1_b"], 1e-5)
+                    h1 = x + attention(a, q["Wq"], q["Wk"], q["Wv"], q["Wo"], w.H, w.H)
+                    return h1 + mlp(F.layer_norm(h1, (h,), q["ln2_g"], q["ln2_b"], 1e-5), q["W1"], q["W2"])
+    return fwd, p
+
+
+def library_baseline(w, d: dict, X, dZ, steps: int, warmup: int, dev, gpu_id=None) -> dict:
+    """The same step composed from torch library calls on the unsharded weights
+    (cuBLAS matmuls, torch's elementwise ops and attention, autograd for the
+    backward), timed with CUDA events.  Reported beside the kernels' number as
+    context; it is not a product path and shares nothing with it but the inputs."""
+    import torch
+
+    fwd, p = library_composition(w, d)
+    p = {k: v.contiguous().detach().requires_grad_(w.backward) for k, v in p.items()}
+    x = X.detach().requires_grad_(w.backward)
+
+    def step():
+        if not w.backward:
+            with torch.no_grad():
+                return fwd(x, p)
+        z = fwd(x, p)
+        return torch.autograd.grad(z, [x] + list(p.values()), dZ)
+
+    try:
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_id) as cs:
+            e0.record()
+            for _ in range(steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+    except Exception as e:  # a backend torch lacks on this GPU: report, do not fail the run
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+    return {"value": step_flops(w) / (ms / 1e3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+            "clocks": cs.summary(),
+            "what": "torch library composition of the same step on the unsharded weights (cuBLAS matmuls, "
+                    "torch GeLU/SiLU/LayerNorm/scaled_dot_product_attention, autograd backward); context only"}
+
+
 # ------------------------------------------------------------------ GPU arm
 def source_sha(kind: str) -> str:
     f = "gemm_tc.cu" if "gemm" in kind else ("attn_fwd.cu" if kind == "attn.core_fwd" else "attn_bwd.cu")
@@ -452,7 +554,8 @@ def run_gpu(args, w) -> None:
     # L2: flush between steps unless one step's working set is far above L2
     work_bytes = sum(t.numel() * t.element_size() for t in list(d.values()) + list(buf.values())
                      if isinstance(t, torch.Tensor))
-    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev) if work_bytes < 4 * (129 << 20) else None
+    want_flush = {"auto": work_bytes < 4 * (129 << 20), "flush": True, "none": False}[args.l2]
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev) if want_flush else None
 
     def barrier():
         if world > 1:
@@ -473,18 +576,18 @@ def run_gpu(args, w) -> None:
 
     def timed_region():
         tp.tp_timing_enable(True)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(gpu_id) as cs:
             if flush is None:
-                e0.record(stream)
-                for _ in range(args.steps):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+                evs[0].record(stream)
+                for i in range(args.steps):
                     step(d["X"], d.get("dZ"))
-                e1.record(stream)
+                    evs[i + 1].record(stream)
                 torch.cuda.synchronize(dev)
-                ms = e0.elapsed_time(e1)
+                ms = evs[0].elapsed_time(evs[-1])
+                per = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
             else:
                 # L2 flushed before every step, outside the step's own events
                 evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -495,15 +598,16 @@ def run_gpu(args, w) -> None:
                     step(d["X"], d.get("dZ"))
                     b.record(stream)
                 torch.cuda.synchronize(dev)
-                ms = sum(a.elapsed_time(b) for a, b in evs)
+                per = [a.elapsed_time(b) for a, b in evs]
+                ms = sum(per)
         barrier()
         rep = tp.timing_report()
         tp.tp_timing_enable(False)
-        return ms, rep, cs.summary()
+        return ms, statistics.median(per), rep, cs.summary()
 
-    ms, rep, clocks = timed_region()
+    ms, ms_median, rep, clocks = timed_region()
     if clocks_rejected(clocks):
-        ms, rep, clocks = timed_region()  # re-measured once
+        ms, ms_median, rep, clocks = timed_region()  # re-measured once
     if tp.tp_sync_status(stream) != 0:
         raise RuntimeError("device error during the timed region")
     if world > 1:
@@ -575,6 +679,24 @@ def run_gpu(args, w) -> None:
                "path": "pinned host -> device copies, tp_* C-ABI calls, device -> pinned host copies of the block "
                        "outputs, one stream"}
 
+    lib = None
+    if world == 1 and not args.no_library_baseline:
+        Xt = inp_tok["X"].to(dev) if w.kind == "splayer" else d["X"]
+        dZt = (inp_tok["dZ"].to(dev) if w.kind == "splayer" else d.get("dZ")) if w.backward else None
+        lib = library_baseline(w, d, Xt, dZt, args.steps, args.warmup, dev, gpu_id)
+        torch.cuda.synchronize(dev)
+
+    # peaks: measured copies, NVIDIA's nominal dense figure, and the clock the run saw
+    nominal = 2250.0  # dense bf16 TFLOP/s per GB300 GPU (NVIDIA's nominal, not the 2:4-sparse figure)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clock_peak = None
+    if clocks and clocks.get("sm_mhz"):
+        # one M=128, N=256, K=16 bf16 tcgen05 MMA per 128 SM cycles = 8192 flop per clock per SM;
+        # at 152 SMs and ~1.81 GHz this is the nominal 2.25 PFLOP/s
+        tf = sms * 8192 * clocks["sm_mhz"] * 1e6 / 1e12
+        clock_peak = {"tflops": tf, "frac": value / world / tf, "sm_count": sms, "flop_per_clk_per_sm": 8192,
+                      "sm_mhz": clocks["sm_mhz"]}
+
     cpu = None
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         import torch as _t  # noqa: F401
@@ -592,8 +714,11 @@ def run_gpu(args, w) -> None:
                                   f"inputs larger than L2 (step working set {work_bytes / 2**30:.2f} GiB); no flush")},
                 "pct_of_peak": {"of_measured_burst": value / world / pk["bf16_tflops"],
                                 "of_measured_sustained": value / world / pk["bf16_tflops_sustained"],
-                                "peaks": pk["source"]},
+                                "peaks": pk["source"], "of_nominal_dense": value / world / nominal,
+                                "nominal_dense_tflops": nominal, "clock_based": clock_peak},
+                "ms_per_step_median": ms_median,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "library_baseline": lib,
                 "kernels": {k: {"launches": v[0], "ms_total": v[1]} for k, v in rep.items()},
                 "clocks": clocks}
         print(json.dumps(line), flush=True)
@@ -609,6 +734,10 @@ def main() -> None:
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="tpblock", choices=["tpblock", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-library-baseline", action="store_true",
+                    help="skip timing the torch library composition of the step")
+    ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
+                    help="L2 between timed steps: auto flushes when a step's working set is under 4x L2")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--gemm-tiling", type=int, default=0, choices=[0, 1, 2],
                     help="0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile")
