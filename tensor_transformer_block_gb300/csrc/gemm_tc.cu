@@ -1,26 +1,29 @@
 // tcgen05 GEMM with TMA multi-stage pipeline and fused epilogues (see gemm_tc.cuh).
 //
-// CTA = 6 warps, one CTA per SM, persistent over output tiles:
+// CTA = 10 warps, one CTA per SM, persistent over output tiles:
 //   warp 8  TMA producer: fills a ring of (A 128x64, B 64-deep) bf16 stages,
-//           128-byte swizzled, K-major or MN-major as the operand is stored;
+//           128-byte swizzled, K-major or MN-major as the operand is stored; an
+//           MN-major operand whose rows are whole 64-element chunks comes in one
+//           copy per stage through a map with the chunk as an outer dimension;
 //   warp 9  MMA issuer: 4 x tcgen05.mma (K=16) per stage into one of two TMEM
 //           accumulators (2 x 256 fp32 columns), so the epilogue of tile t
 //           overlaps the main loop of tile t+1;
 //   warps 0-7 epilogue: warp w reads TMEM lanes 32*(w%4).. (its row quadrant) and
 //           columns 128*(w/4).. (its half), so every SM sub-partition runs two
 //           epilogue warps to hide the latency of the fused math; fused GeLU /
-//           GeLU' in fp32, bf16 pack into a swizzled staging box, TMA store.
+//           GeLU' / SwiGLU / residual in fp32, bf16 pack into a swizzled staging
+//           box, TMA store.
 // The main loop is fed by as many stages as shared memory holds next to the
 // epilogue's staging: a k-block's loads take microseconds to arrive from L2, and
-// with one stage fewer the MMA issuer measurably waits for data.  The plain-store
-// epilogues stage through one 4 KB box per warp (32 KB), the fused ones through two
-// (an input and an output, or two outputs; 64 KB).
+// with one stage fewer the MMA issuer measurably waits for data.  The epilogue
+// stages 32 KB per CTA: the plain-store epilogues one box of 32 rows x 64 columns
+// per warp (128-byte swizzle), the fused ones two boxes of 32 rows x 32 columns
+// (64-byte swizzle; an input and an output, or two outputs).
 // Two tilings:
-//   single: one CTA per 128 x 256 tile (cta_group::1, M=128 N=256); 4 (fused: 3)
-//           stages of 48 KB.
+//   single: one CTA per 128 x 256 tile (cta_group::1, M=128 N=256); 4 stages of 48 KB.
 //   pair:   a cluster of two CTAs per 256 x 256 tile (cta_group::2, M=256 N=256):
 //           each CTA stages its 128 rows of A and half (128 columns) of B, so each
-//           SM moves 32 KB per k-block instead of 48; 6 (fused: 5) stages.  The even CTA issues
+//           SM moves 32 KB per k-block instead of 48; 6 stages.  The even CTA issues
 //           the MMAs; both CTAs' TMA loads count on its full barrier; its commits
 //           multicast to both CTAs' empty / accumulator-ready barriers; both CTAs'
 //           epilogue warps release an accumulator on the even CTA's barrier.
@@ -38,7 +41,6 @@ namespace {
 constexpr int BK = 64;
 constexpr int BN = 256;  // MMA N (tile columns)
 constexpr int EPI_WARPS = 8;
-constexpr int EPI_BUF = 32 * 128;  // one 32-row x 64-column bf16 box
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;
@@ -48,10 +50,15 @@ constexpr int GROUP_M = 16;
 template <bool PAIR, int EPI>
 struct Cfg {
   static constexpr int EBUFS = (EPI == kEpiStore || EPI == kEpiSplit) ? 1 : 2;  // staging boxes per warp
+  // epilogue chunk: 32 rows x CW columns of bf16 (one box): 64 columns with 128-byte
+  // swizzle for the one-box epilogues, 32 columns with 64-byte swizzle for the fused
+  // ones, so that either stages 32 KB per CTA
+  static constexpr int CW = EBUFS == 1 ? 64 : 32;
+  static constexpr int EBOX = 32 * CW * 2;
   static constexpr int BM = 128;                      // accumulator rows per CTA
   static constexpr int TILE_M = PAIR ? 256 : 128;     // rows per output tile
   static constexpr int BN_CTA = PAIR ? 128 : 256;     // B columns staged per CTA
-  static constexpr int STAGES = PAIR ? (EBUFS == 1 ? 6 : 5) : (EBUFS == 1 ? 4 : 3);
+  static constexpr int STAGES = PAIR ? 6 : 4;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN_CTA * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -63,7 +70,7 @@ struct Cfg {
   static constexpr int BAR_DRAIN = BAR_Y + 2 * EPI_WARPS;
   static constexpr int NUM_BARS = BAR_DRAIN + 1;
   static constexpr int SMEM_EPI_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * EBUFS * EPI_BUF;
+  static constexpr int SMEM_BAR_OFF = SMEM_EPI_OFF + EPI_WARPS * EBUFS * EBOX;
   static constexpr int SMEM_MISC_OFF = SMEM_BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_USED = SMEM_MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
@@ -454,10 +461,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int ew = warp;                 // staging buffers and Y barriers
     const int quad = warp & 3;           // TMEM lanes 32*quad .. 32*quad+31
     const int half = warp >> 2;          // tile columns 128*half .. 128*half+127
-    const uint32_t ebuf[2] = {sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EPI_BUF,
-                              sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EPI_BUF + (C::EBUFS - 1) * EPI_BUF};
+    constexpr int CW = C::CW, EBOX = C::EBOX;
+    const uint32_t ebuf[2] = {sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EBOX,
+                              sbase + C::SMEM_EPI_OFF + ew * C::EBUFS * EBOX + (C::EBUFS - 1) * EBOX};
     const uint32_t ybar[2] = {bar0 + 8u * (BAR_Y + 2 * ew), bar0 + 8u * (BAR_Y + 2 * ew + 1)};
-    const uint32_t rsw = static_cast<uint32_t>(lane & 7);
+    // byte offset of this lane's 16-byte unit c in a swizzled staging box (row = lane):
+    // 128-byte rows XOR row % 8, or 64-byte rows XOR (row / 2) % 4
+    auto soff = [lane](uint32_t c) -> uint32_t {
+      const uint32_t r = static_cast<uint32_t>(lane);
+      return CW == 64 ? r * 128 + ((c ^ (r & 7)) << 4) : r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+    };
     uint32_t yph = 0;      // bit b: parity of the next completion of ybar[b]
     uint32_t ypend = 0;    // bit b: a Y load into ebuf[b] is in flight
     uint32_t ecount = 0;   // chunks staged so far (buffer alternation for kEpiStore / kEpiDGelu)
@@ -470,14 +483,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tph = (it >> 1) & 1;
       const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
       const int col0 = nb * TILE_N + half * WARP_COLS;
-      int nch = col0 < p.N ? (p.N - col0 + 63) / 64 : 0;
-      if (nch > WARP_COLS / 64) nch = WARP_COLS / 64;
+      int nch = col0 < p.N ? (p.N - col0 + CW - 1) / CW : 0;
+      if (nch > WARP_COLS / CW) nch = WARP_COLS / CW;
       const bool rows_valid = row0 < p.M && nch > 0;
       if ((EPI == kEpiDGelu || EPI == kEpiResidual) && rows_valid) {
         const uint32_t b = ecount & 1u;
         if (lane == 0) {
           bulk_wait_read0();
-          mbar_arrive_expect_tx(ybar[b], EPI_BUF);
+          mbar_arrive_expect_tx(ybar[b], EBOX);
           op_load<false>(ebuf[b], &tmY, ybar[b], col0, row0, g, p.c_spS, p.c_spL);
         }
         ypend |= 1u << b;
@@ -486,7 +499,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // G and U of the warp's first chunk, fetched while the main loop runs
         if (lane == 0) {
           bulk_wait_read0();
-          mbar_arrive_expect_tx(ybar[0], 2 * EPI_BUF);
+          mbar_arrive_expect_tx(ybar[0], 2 * EBOX);
           tma_load_4d(ebuf[0], &tmY, ybar[0], col0, 0, row0, g);
           tma_load_4d(ebuf[1], &tmY, ybar[0], col0, 1, row0, g);
         }
@@ -501,8 +514,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       if (rows_valid) {
         for (int j = 0; j < nch && ok; ++j) {
-          const int ccol = col0 + j * 64;
-          const uint32_t tcol = tl + j * 64;
+          const int ccol = col0 + j * CW;
+          const uint32_t tcol = tl + j * CW;
           // The fused epilogues run as a rolled loop of 16-column TMEM loads: a
           // fully unrolled 64-column body is large enough to evict the MMA
           // warp's instructions from the cache the SM sub-partition shares.
@@ -526,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int e = 0; e < 4; ++e)
                 w[e] = f16 ? pack_f16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]))
                            : pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-              st_shared_v4(sb + lane * 128 + ((c ^ rsw) << 4), w[0], w[1], w[2], w[3]);
+              st_shared_v4(sb + soff(c), w[0], w[1], w[2], w[3]);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -539,7 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < CW / 16; ++q) {
               uint32_t v[16];
               tmem_ld16(tcol + q * 16, v);
               tmem_ld_wait16(v);
@@ -549,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 float x[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * hh + e]);
-                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                const uint32_t off = soff(c);
                 st_shared_v4(ebuf[0] + off, pack_bf16x2(gelu_f(x[0]), gelu_f(x[1])),
                              pack_bf16x2(gelu_f(x[2]), gelu_f(x[3])), pack_bf16x2(gelu_f(x[4]), gelu_f(x[5])),
                              pack_bf16x2(gelu_f(x[6]), gelu_f(x[7])));
@@ -570,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < CW / 16; ++q) {
               uint32_t vg[16], vu[16];
               tmem_ld16(tcol + q * 16, vg);
               tmem_ld16(tcol + 128 + q * 16, vu);
@@ -590,7 +603,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                      g1 * s1 * __uint_as_float(vu[8 * hh + 2 * e + 1]));
                   gg[e] = pack_bf16x2(g0, g1);
                 }
-                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                const uint32_t off = soff(c);
                 st_shared_v4(ebuf[0] + off, a[0], a[1], a[2], a[3]);
                 if (p.store_y) st_shared_v4(ebuf[1] + off, gg[0], gg[1], gg[2], gg[3]);
               }
@@ -610,7 +623,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (lane == 0) bulk_wait_read1();
               __syncwarp();
 #pragma unroll 1
-              for (int q = 0; q < 4; ++q) {
+              for (int q = 0; q < CW / 16; ++q) {
                 uint32_t vu[16];
                 tmem_ld16(tcol + 128 + q * 16, vu);
                 tmem_ld_wait16(vu);
@@ -618,7 +631,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int hh = 0; hh < 2; ++hh) {
                   const uint32_t c = static_cast<uint32_t>(2 * q + hh);
                   const uint32_t* v = &vu[8 * hh];
-                  st_shared_v4(ebuf[0] + lane * 128 + ((c ^ rsw) << 4),
+                  st_shared_v4(ebuf[0] + soff(c),
                                pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
                                pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
                                pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
@@ -637,7 +650,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (j > 0) {
               if (lane == 0) {
                 bulk_wait_read0();
-                mbar_arrive_expect_tx(ybar[0], 2 * EPI_BUF);
+                mbar_arrive_expect_tx(ybar[0], 2 * EBOX);
                 tma_load_4d(ebuf[0], &tmY, ybar[0], ccol, 0, row0, g);
                 tma_load_4d(ebuf[1], &tmY, ybar[0], ccol, 1, row0, g);
               }
@@ -648,14 +661,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             yph ^= 1u;
             ypend &= ~1u;
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < CW / 16; ++q) {
               uint32_t v[16];
               tmem_ld16(tcol + q * 16, v);
               tmem_ld_wait16(v);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const uint32_t c = static_cast<uint32_t>(2 * q + hh);
-                const uint32_t off = lane * 128 + ((c ^ rsw) << 4);
+                const uint32_t off = soff(c);
                 uint32_t gq[4], uq[4], dg[4], du[4];
                 ld_shared_v4(ebuf[0] + off, gq[0], gq[1], gq[2], gq[3]);
                 ld_shared_v4(ebuf[1] + off, uq[0], uq[1], uq[2], uq[3]);
@@ -691,8 +704,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (j + 1 < nch) {
               if (lane == 0) {
                 bulk_wait_read0();
-                mbar_arrive_expect_tx(ybar[nb2], EPI_BUF);
-                op_load<false>(ebuf[nb2], &tmY, ybar[nb2], ccol + 64, row0, g, p.c_spS, p.c_spL);
+                mbar_arrive_expect_tx(ybar[nb2], EBOX);
+                op_load<false>(ebuf[nb2], &tmY, ybar[nb2], ccol + CW, row0, g, p.c_spS, p.c_spL);
               }
               ypend |= 1u << nb2;
             }
@@ -701,14 +714,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             yph ^= 1u << cb;
             ypend &= ~(1u << cb);
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < CW / 16; ++q) {
               uint32_t v[16];
               tmem_ld16(tcol + q * 16, v);
               tmem_ld_wait16(v);
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
                 const uint32_t c = static_cast<uint32_t>(2 * q + hh);
-                const uint32_t addr = ebuf[cb] + lane * 128 + ((c ^ rsw) << 4);
+                const uint32_t addr = ebuf[cb] + soff(c);
                 uint32_t y0, y1, y2, y3;
                 ld_shared_v4(addr, y0, y1, y2, y3);
                 const uint32_t yy[4] = {y0, y1, y2, y3};
@@ -844,11 +857,11 @@ bool operand_map(CUtensorMap* m, const GemmOperand& o, uint32_t rows) {
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o.ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// [G][M][2][N] output or auxiliary tensor of the gated epilogues, 32 x 64 boxes
-bool two_part_map(CUtensorMap* m, const void* ptr, int64_t N, int64_t M, int G) {
+// [G][M][2][N] output or auxiliary tensor of the gated epilogues, 32-row x cw boxes
+bool two_part_map(CUtensorMap* m, const void* ptr, int64_t N, int64_t M, int G, uint32_t cw, CUtensorMapSwizzle swz) {
   const uint64_t dims[4] = {static_cast<uint64_t>(N), 2u, static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
-  const uint32_t box[4] = {64u, 1u, 32u, 1u};
-  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, box, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint32_t box[4] = {cw, 1u, 32u, 1u};
+  return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, box, swz);
 }
 
 int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pair per tile
@@ -903,23 +916,26 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
       !(b_ch ? chunked_map(&tb, B, b_rows) : operand_map(&tb, B, b_rows)))
     return 2;
   const uint64_t cdims[3] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(M), static_cast<uint64_t>(G)};
-  const uint32_t cbox[3] = {64u, 32u, 1u};
+  // staging boxes: 64 columns (128-byte swizzle) for one-box epilogues, 32 (64-byte) for fused ones
+  const uint32_t cw = one_box ? 64u : 32u;
+  const CUtensorMapSwizzle swz = one_box ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const uint32_t cbox[3] = {cw, 32u, 1u};
   const uint64_t sdims[4] = {static_cast<uint64_t>(ldc), static_cast<uint64_t>(extra.c_sp_L),
                              static_cast<uint64_t>(extra.c_sp_S > 0 ? M / extra.c_sp_S : 1),
                              static_cast<uint64_t>(extra.c_sp_S > 0 ? extra.c_sp_S / extra.c_sp_L : 1)};
-  const uint32_t sbox[4] = {64u, 32u, 1u, 1u};
+  const uint32_t sbox[4] = {cw, 32u, 1u, 1u};
   auto out_map = [&](CUtensorMap* m, const void* ptr) {
     if (extra.c_sp_S > 0)
-      return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, sdims, sbox, CU_TENSOR_MAP_SWIZZLE_128B);
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, cdims, cbox, CU_TENSOR_MAP_SWIZZLE_128B);
+      return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, sdims, sbox, swz);
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, cdims, cbox, swz);
   };
   if (epi == kEpiDSwiGLU) {
-    if (!two_part_map(&tc, C, N, M, G)) return 2;
+    if (!two_part_map(&tc, C, N, M, G, cw, swz)) return 2;
   } else if (!out_map(&tc, C)) {
     return 2;
   }
   if (Yaux && gated) {
-    if (!two_part_map(&ty, Yaux, N, M, G)) return 2;
+    if (!two_part_map(&ty, Yaux, N, M, G, cw, swz)) return 2;
   } else if (Yaux) {
     if (!out_map(&ty, Yaux)) return 2;
   } else {
