@@ -195,6 +195,28 @@ __device__ __forceinline__ void mn_load(uint32_t dst, const CUtensorMap* m, uint
       tma_load_4d(dst, m, bar, 0, k, chunk0, z);
   }
 }
+// Pair loads of the B operand, multicast to the CTAs of ``mc`` when it is not 0.
+__device__ __forceinline__ void pld3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2,
+                                     uint16_t mc) {
+  if (mc)
+    tma_load_3d_pair_mc(dst, m, bar, c0, c1, c2, mc);
+  else
+    tma_load_3d_pair(dst, m, bar, c0, c1, c2);
+}
+__device__ __forceinline__ void pld4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2, int c3,
+                                     uint16_t mc) {
+  if (mc)
+    tma_load_4d_pair_mc(dst, m, bar, c0, c1, c2, c3, mc);
+  else
+    tma_load_4d_pair(dst, m, bar, c0, c1, c2, c3);
+}
+__device__ __forceinline__ void pld5(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2, int c3,
+                                     int c4, uint16_t mc) {
+  if (mc)
+    tma_load_5d_pair_mc(dst, m, bar, c0, c1, c2, c3, c4, mc);
+  else
+    tma_load_5d_pair(dst, m, bar, c0, c1, c2, c3, c4);
+}
 __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, int c0, int row, int z, int spS, int spL) {
   if (spS > 0) {
     int sl, bb, cc;
@@ -205,7 +227,10 @@ __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, in
   }
 }
 
-template <bool PAIR, bool A_MN, bool B_MN, int EPI>
+// MC (pair mode only): a cluster of two CTA pairs on consecutive M tiles of the same
+// N tile; the even pair's CTAs load each B half once, multicast to the same position
+// in the odd pair, so L2 delivers 48 instead of 64 KB per pair and k-block.
+template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool MC>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, const GemmShape p) {
@@ -229,15 +254,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
+  static_assert(PAIR || !MC, "multicast clusters are made of CTA pairs");
+  constexpr int CL = MC ? 4 : (PAIR ? 2 : 1);             // CTAs per cluster
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;   // position in the cluster
+  const uint32_t rank = crank & 1u;                       // position in the CTA pair
+  const uint32_t pid = MC ? (crank >> 1) : 0u;            // pair within the cluster (its M tile)
+  const uint32_t lead = crank & ~1u;                      // the pair's even CTA
   const bool leader = rank == 0;
-  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int unit = static_cast<int>(blockIdx.x) / CL;
+  const int nunits = static_cast<int>(gridDim.x) / CL;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bar0 + 8u * (BAR_FULL + i), 1);
-      mbar_init(bar0 + 8u * (BAR_EMPTY + i), 1);
+      mbar_init(bar0 + 8u * (BAR_EMPTY + i), MC ? 2 : 1);  // MC: both pairs consumed the stage
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar0 + 8u * (BAR_TFULL + i), 1);
@@ -290,6 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
         decode_tile(t, p, g, mb, nb);
+        if (MC) mb = 2 * mb + static_cast<int>(pid);
         const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
         const int bcol = EPI == kEpiSwiGLU ? nb * TILE_N : nb * BN + static_cast<int>(rank) * C::BN_CTA;
         TokPos apos{0, 0, 0};
@@ -308,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sb = sa + A_BYTES;
             const int kc = kb * BK;
             if (PAIR) {
-              const uint32_t fb = mapa_shared(fb_local, 0);  // the even CTA's full barrier counts both
+              const uint32_t fb = mapa_shared(fb_local, lead);  // the even CTA's full barrier counts both
               if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
               if (A_MN && p.a_chunked) {
                 mn_load<true>(sa, &tmA, fb, arow / 64, kc, az, a_k_sp, kpos);
@@ -319,23 +350,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else {
                 op_load_at<true>(sa, &tmA, fb, kc, arow, az, a_rows_sp, apos);
               }
-              if (EPI == kEpiSwiGLU) {
+              // B: each CTA stages half of the tile's columns; with MC only the even
+              // pair's CTAs load, for both pairs
+              const uint16_t mcm = MC ? static_cast<uint16_t>((1u << rank) | (1u << (rank + 2))) : 0;
+              if (MC && pid != 0) {
+              } else if (EPI == kEpiSwiGLU) {
                 // the even CTA stages the tile's gate columns, the odd CTA its up columns
                 if (p.b_chunked) {
-                  tma_load_5d_pair(sb, &tmB, fb, 0, kc, bcol / 64, static_cast<int>(rank), bz);
+                  pld5(sb, &tmB, fb, 0, kc, bcol / 64, static_cast<int>(rank), bz, mcm);
                 } else {
 #pragma unroll
                   for (int j = 0; j < C::BN_CTA / 64; ++j)
-                    tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz);
+                    pld4(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz, mcm);
                 }
               } else if (B_MN && p.b_chunked) {
-                mn_load<true>(sb, &tmB, fb, bcol / 64, kc, bz, b_k_sp, kpos);
+                if (b_k_sp)
+                  pld5(sb, &tmB, fb, 0, kpos.sl, bcol / 64, kpos.b, kpos.c, mcm);
+                else
+                  pld4(sb, &tmB, fb, 0, kc, bcol / 64, bz, mcm);
               } else if (B_MN) {
 #pragma unroll
-                for (int j = 0; j < C::BN_CTA / 64; ++j)
-                  op_load_at<true>(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, b_k_sp, kpos);
+                for (int j = 0; j < C::BN_CTA / 64; ++j) {
+                  if (b_k_sp)
+                    pld4(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kpos.sl, kpos.b, kpos.c, mcm);
+                  else
+                    pld3(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, mcm);
+                }
               } else {
-                tma_load_3d_pair(sb, &tmB, fb, kc, bcol, bz);
+                pld3(sb, &tmB, fb, kc, bcol, bz, mcm);
               }
             } else {
               mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
@@ -434,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           any = true;
           if (PAIR)
-            tc_commit_pair(bar0 + 8u * (BAR_EMPTY + stage), 3);
+            tc_commit_pair(bar0 + 8u * (BAR_EMPTY + stage), MC ? 0xF : 3);  // MC: both pairs' stages
           else
             tc_commit(bar0 + 8u * (BAR_EMPTY + stage));
           if (++stage == STAGES) {
@@ -444,13 +486,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         if (PAIR)
-          tc_commit_pair(bar0 + 8u * (BAR_TFULL + buf), 3);
+          tc_commit_pair(bar0 + 8u * (BAR_TFULL + buf), static_cast<uint16_t>(3u << (2 * pid)));
         else
           tc_commit(bar0 + 8u * (BAR_TFULL + buf));
       }
       if (any) {
         if (PAIR)
-          tc_commit_pair(bar0 + 8u * BAR_DRAIN, 1);
+          tc_commit_pair(bar0 + 8u * BAR_DRAIN, static_cast<uint16_t>(1u << crank));
         else
           tc_commit(bar0 + 8u * BAR_DRAIN);
         mbar_wait(bar0 + 8u * BAR_DRAIN, 0, wdrain);
@@ -479,6 +521,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int t = unit; t < total && ok; t += nunits, ++it) {
       int g, mb, nb;
       decode_tile(t, p, g, mb, nb);
+      if (MC) mb = 2 * mb + static_cast<int>(pid);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
@@ -752,7 +795,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) {
         if (PAIR)
-          mbar_arrive_cluster(mapa_shared(bar0 + 8u * (BAR_TEMPTY + buf), 0));
+          mbar_arrive_cluster(mapa_shared(bar0 + 8u * (BAR_TEMPTY + buf), lead));
         else
           mbar_arrive(bar0 + 8u * (BAR_TEMPTY + buf));
       }
@@ -783,12 +826,12 @@ using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Ge
 
 constexpr int kMaxDev = 64;
 
-template <bool PAIR, bool A_MN, bool B_MN, int EPI>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool MC>
 KernelFn get_kernel() {
   static bool configured[kMaxDev] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI>;
+  auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI, MC>;
   if (!configured[dev]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR, EPI>::SMEM_ALLOC) !=
         cudaSuccess)
@@ -798,17 +841,17 @@ KernelFn get_kernel() {
   return fn;
 }
 
-template <bool PAIR>
+template <bool PAIR, bool MC>
 KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
-  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<PAIR, false, true, kEpiGelu>();
-  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, false, true, kEpiStore>();
-  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<PAIR, false, true, kEpiSplit>();
-  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu>();
-  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore>();
-  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore>();
-  if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU>();
-  if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
-  if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual>();
+  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<PAIR, false, true, kEpiGelu, MC>();
+  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, false, true, kEpiStore, MC>();
+  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<PAIR, false, true, kEpiSplit, MC>();
+  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu, MC>();
+  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore, MC>();
+  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore, MC>();
+  if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU, MC>();
+  if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU, MC>();
+  if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual, MC>();
   return nullptr;
 }
 
@@ -864,7 +907,7 @@ bool two_part_map(CUtensorMap* m, const void* ptr, int64_t N, int64_t M, int G, 
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, box, swz);
 }
 
-int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pair per tile
+int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pairs, 3 CTA pairs sharing B in clusters of 4
 
 }  // namespace
 
@@ -901,9 +944,16 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if (sms <= 0) return 2;
   // pair tiles when there are enough 256 x 256 tiles to give every SM pair work
   const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
-  bool pair = g_tiling_mode == 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
+  bool pair = g_tiling_mode >= 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
   if (sms < 2) pair = false;
-  KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
+  // two pairs per cluster sharing B (multicast) only on request: at full clock it
+  // measured slower (36 four-CTA clusters fit, 144 SMs, and a tile row of two pair
+  // tiles doubles the tail of the last wave)
+  const int64_t pair_rows = (M + 255) / 256;
+  const bool mc = pair && sms >= 4 && pair_rows >= 2 && g_tiling_mode == 3;
+  KernelFn fn = !pair ? pick_kernel<false, false>(A.mn_major, B.mn_major, epi)
+                      : (mc ? pick_kernel<true, true>(A.mn_major, B.mn_major, epi)
+                            : pick_kernel<true, false>(A.mn_major, B.mn_major, epi));
   if (!fn) return 2;
   const uint32_t a_rows = 128, b_rows = pair ? Cfg<true, kEpiStore>::BN_CTA : Cfg<false, kEpiStore>::BN_CTA;
   const bool one_box = epi == kEpiStore || epi == kEpiSplit;
@@ -948,6 +998,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.S = S;
   p.kb_per_seg = static_cast<int>((Ks + BK - 1) / BK);
   p.tiles_m = static_cast<int>((M + (pair ? 255 : 127)) / (pair ? 256 : 128));
+  if (mc) p.tiles_m = (p.tiles_m + 1) / 2;  // a cluster's tile row covers two pair tiles
   p.tiles_n = static_cast<int>((N + tile_n - 1) / tile_n);
   p.a_zg = A.zg;
   p.a_zs = A.zs;
@@ -972,19 +1023,29 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const int slot = timing_begin(kind, stream);
   bool ok;
   if (pair) {
-    const long long units = total < sms / 2 ? total : sms / 2;
+    const int cl = mc ? 4 : 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * units), 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // persistent clusters: as many as can be resident at once (4-CTA clusters need
+    // four free SMs in one GPC, so fewer than #SM/4 may fit)
+    long long units = sms / cl;
+    cfg.gridDim = dim3(static_cast<unsigned>(cl * units), 1, 1);
+    if (mc) {
+      int resident = 0;
+      if (cudaOccupancyMaxActiveClusters(&resident, fn, &cfg) == cudaSuccess && resident > 0 && resident < units)
+        units = resident;
+    }
+    if (units > total) units = total;
+    cfg.gridDim = dim3(static_cast<unsigned>(cl * units), 1, 1);
     ok = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, ty, p) == cudaSuccess;
   } else {
     const int grid = static_cast<int>(total < sms ? total : sms);
