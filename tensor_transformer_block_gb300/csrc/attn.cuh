@@ -37,6 +37,35 @@ struct AttnDims {
   __host__ __device__ int group() const { return hN / hkvN; }
 };
 
+// Order in which the CTAs of an attention core are launched.  A CTA covers one
+// (batch, head) unit and one block of it; with a causal mask the blocks carry
+// unequal work, ranked r = 0 (most) .. blocks-1 (least).  The hardware gives CTAs
+// to SMs in linear index order as SMs free up, so the units are taken in groups of
+// `group`, and inside a group every unit's rank-0 block comes first, then every
+// unit's rank-1 block, and so on (longest first within the group): the light
+// blocks of one group run beside the heavy blocks of the next, and the launch
+// ends on light blocks.  A group of about two waves of CTAs keeps the makespan
+// within a few percent of the average load while the key/value tiles in use stay
+// those of a few dozen heads.
+struct WorkOrder {
+  int units, blocks, group;
+  __host__ __device__ void decode(int idx, int& unit, int& rank) const {
+    const int per = group * blocks;
+    const int grp = idx / per;
+    const int within = idx - grp * per;
+    const int gsize = units - grp * group < group ? units - grp * group : group;
+    rank = within / gsize;
+    unit = grp * group + (within - rank * gsize);
+  }
+  int ctas() const { return units * blocks; }
+};
+inline WorkOrder make_work_order(int units, int blocks, int sms) {
+  int group = (2 * sms + blocks - 1) / blocks;
+  if (group > units) group = units;
+  if (group < 1) group = 1;
+  return WorkOrder{units, blocks, group};
+}
+
 // Number of d-wide planes per (token, local head) in QKV without grouping.
 constexpr int kQkvPlanes = 3;
 

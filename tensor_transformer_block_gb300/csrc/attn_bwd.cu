@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     k_attn_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
                 const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
                 const float* __restrict__ dsum, const AttnDims a, const float scale_log2, const float scale,
-                unsigned* err, const unsigned long long timeout_ns) {
+                const WorkOrder ord, unsigned* err, const unsigned long long timeout_ns) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -148,8 +148,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (a.S + BLK - 1) / BLK;
-  const int kb = static_cast<int>(blockIdx.x);  // low key blocks have the most causal work: first
-  const int jkv = blockIdx.y, b = blockIdx.z;   // global key/value head
+  int unit, rank;
+  ord.decode(static_cast<int>(blockIdx.x), unit, rank);
+  const int kb = rank;                             // low key blocks have the most causal work
+  const int jkv = unit % a.Hkv, b = unit / a.Hkv;  // global key/value head
   const int shard = jkv / a.hkvN, kvh = jkv % a.hkvN;
   const int g = a.group();
   const int k0 = kb * BLK;
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     k_attn_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
               const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
               const float* __restrict__ dsum, const AttnDims a, const float scale_log2, const float scale,
-              unsigned* err, const unsigned long long timeout_ns) {
+              const WorkOrder ord, unsigned* err, const unsigned long long timeout_ns) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -462,8 +464,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (a.S + BLK - 1) / BLK;
-  const int qb = nb - 1 - static_cast<int>(blockIdx.x);
-  const int j = blockIdx.y, b = blockIdx.z;
+  int unit, rank;
+  ord.decode(static_cast<int>(blockIdx.x), unit, rank);
+  const int qb = nb - 1 - rank;  // the last query blocks have the most causal work
+  const int j = unit % a.H, b = unit / a.H;
   const int shard = j / a.hN, jj = j % a.hN, kvh = jj / a.group();
   const int q0 = qb * BLK;
   const int nkv = a.causal ? min((min(q0 + BLK, a.S) - 1) / BLK + 1, nb) : nb;
@@ -720,16 +724,16 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   const int nb = (a.S + BLK - 1) / BLK;
   const float scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
   const float scale_log2 = scale * kLog2e;
-  const dim3 grid(nb, a.H, a.B), grid_kv(nb, a.Hkv, a.B);
+  const WorkOrder ord_q = make_work_order(a.B * a.H, nb, sms), ord_kv = make_work_order(a.B * a.Hkv, nb, sms);
   slot = timing_begin(kKAttnDkdv, st);
-  k_attn_dkdv<D><<<grid_kv, NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale, err,
-                                                             timeout_ns);
+  k_attn_dkdv<D><<<ord_kv.ctas(), NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale,
+                                                                   ord_kv, err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
   slot = timing_begin(kKAttnDq, st);
-  k_attn_dq<D><<<grid, NTHREADS, DqCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale, err,
-                                                      timeout_ns);
+  k_attn_dq<D><<<ord_q.ctas(), NTHREADS, DqCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale, ord_q,
+                                                             err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;

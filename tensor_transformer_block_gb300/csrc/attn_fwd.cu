@@ -84,7 +84,8 @@ __device__ __forceinline__ void mma_scores(uint32_t d_tmem, uint32_t sa, uint32_
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_attn_fwd(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmO, const AttnDims a,
-               float* __restrict__ lse, const float scale_log2, unsigned* err, const unsigned long long timeout_ns) {
+               float* __restrict__ lse, const float scale_log2, const WorkOrder ord, unsigned* err,
+               const unsigned long long timeout_ns) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -102,8 +103,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (a.S + QT * BQ - 1) / (QT * BQ);
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x);
-  const int j = blockIdx.y, b = blockIdx.z;
+  int unit, rank;
+  ord.decode(static_cast<int>(blockIdx.x), unit, rank);
+  const int qb = nqb - 1 - rank;  // the last query blocks have the most causal work
+  const int j = unit % a.H, b = unit / a.H;
   const int shard = j / a.hN, jj = j % a.hN, kvh = jj / a.group();
   const int q0 = qb * QT * BQ;
   const int nkb = (a.S + BKV - 1) / BKV;
@@ -387,9 +390,9 @@ int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsign
   if (!encode_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, o, od, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
   const int nqb = (a.S + QT * BQ - 1) / (QT * BQ);
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-  dim3 grid(nqb, a.H, a.B);
+  const WorkOrder ord = make_work_order(a.B * a.H, nqb, device_sm_count());
   const int slot = timing_begin(kKAttnCore, st);
-  k_attn_fwd<D><<<grid, NTHREADS, C::SMEM, st>>>(tqkv, to, a, lse, scale_log2, err, timeout_ns);
+  k_attn_fwd<D><<<ord.ctas(), NTHREADS, C::SMEM, st>>>(tqkv, to, a, lse, scale_log2, ord, err, timeout_ns);
   const bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
