@@ -43,21 +43,27 @@ struct AttnDims {
 // to SMs in linear index order as SMs free up, so the units are taken in groups of
 // `group`, and inside a group every unit's rank-0 block comes first, then every
 // unit's rank-1 block, and so on (longest first within the group): the light
-// blocks of one group run beside the heavy blocks of the next, and the launch
-// ends on light blocks.  A group of about two waves of CTAs keeps the makespan
-// within a few percent of the average load while the key/value tiles in use stay
-// those of a few dozen heads.
+// blocks of one group run beside the heavy blocks of the next.  The group left
+// over (units % group) goes first, so that the launch ends on the light blocks of
+// a full group.  A group of about two waves of CTAs keeps the makespan within a
+// few percent of the average load while the key/value tiles in use stay those of
+// a few dozen heads.
 struct WorkOrder {
   int units, blocks, group;
   __host__ __device__ void decode(int idx, int& unit, int& rank) const {
-    const int per = group * blocks;
-    const int grp = idx / per;
-    const int within = idx - grp * per;
-    const int gsize = units - grp * group < group ? units - grp * group : group;
+    const int first = units % group;  // size of the leading partial group (0: none)
+    int base = 0, gsize = first, within = idx;
+    if (idx >= first * blocks) {
+      const int i = idx - first * blocks;
+      const int grp = i / (group * blocks);
+      within = i - grp * group * blocks;
+      gsize = group;
+      base = first + grp * group;
+    }
     rank = within / gsize;
-    unit = grp * group + (within - rank * gsize);
+    unit = base + (within - rank * gsize);
   }
-  int ctas() const { return units * blocks; }
+  __host__ __device__ int ctas() const { return units * blocks; }
 };
 inline WorkOrder make_work_order(int units, int blocks, int sms) {
   int group = (2 * sms + blocks - 1) / blocks;

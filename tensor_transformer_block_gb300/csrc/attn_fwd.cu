@@ -282,24 +282,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[c][e]));
       const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+      // the running max moves only when the block's exceeds it by the threshold; O
+      // is then rescaled after P is written, when the score registers are dead
+      float alpha = 1.0f;
+      bool rescale = false;
       if (kv == 0) {
         m = bmax;
       } else {
         const bool need = bmax > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          // O is quiescent: this tile's previous P V completed before these scores
-          const float alpha = need ? exp2f(m - bmax) : 1.0f;
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + 32 * c, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + 32 * c, o);
-          }
-          l *= alpha;
-          if (need) m = bmax;
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = exp2f(m - bmax);
+          m = bmax;
         }
       }
       const float m_use = (m == -INFINITY) ? 0.0f : m;
@@ -318,8 +312,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_st16(tS + 16 * c, pk);
       }
+      if (rescale) {
+        // O is quiescent: this tile's previous P V completed before these scores, and
+        // the next one waits for the P arrival below
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
       tmem_st_wait();
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_PF + t));
