@@ -54,6 +54,14 @@ enum : int {
   B_DR = 15, NBARS = 16
 };
 
+// acc + lo + hi of a bf16 pair, each half widened exactly inside the add
+__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.f32.bf16 %0, lo, %0;\n\tadd.f32.bf16 %0, hi, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(pk));
+  return acc;
+}
+
 template <int D>
 struct FwdCfg {
   static constexpr int CH = D / 64;
@@ -308,7 +316,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e]), scale_log2, -m_use));
           const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e + 1]), scale_log2, -m_use));
           pk[e] = pack_bf16x2(p0, p1);
-          ls[e & 3] += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
+          ls[e & 3] = add_bf16x2_f32(ls[e & 3], pk[e]);
         }
         tmem_st16(tS + 16 * c, pk);
       }
