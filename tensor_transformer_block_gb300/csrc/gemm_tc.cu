@@ -110,14 +110,17 @@ __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, i
 // with s = 1 / (1 + e^(-2u)), GeLU(x) = x s and, since 1 - tanh^2 u = 4 s (1 - s),
 // GeLU'(x) = s (1 + 2 x (1 - s) u').  One exp2 and one reciprocal per element, and
 // no cancellation in 1 + tanh u for negative x.  The exponent is clamped so that
-// e^(-2u) stays finite (s then underflows towards 0 smoothly).
+// e^(-2u) stays finite (s then underflows towards 0 smoothly).  exp2 and the
+// reciprocal are the special-function unit's approximations (about 1 ulp of fp32):
+// the results are rounded to bf16, and the correctly rounded reciprocal cost ~2%
+// of the fused GEMMs' time.
 __device__ __forceinline__ void gelu_logistic(float x, float& s, float& oms, float& du) {
   const float x2 = x * x;
   const float u = 0.7978845608028654f * fmaf(0.044715f * x2, x, x);
   du = 0.7978845608028654f * fmaf(0.134145f, x2, 1.0f);
   const float a = fminf(-2.8853900817779268f * u, 126.0f);  // -2u log2(e)
-  const float e = exp2f(a);
-  s = __frcp_rn(1.0f + e);
+  const float e = ex2_approx(a);
+  s = rcp_approx(1.0f + e);
   oms = e * s;  // 1 - s without cancellation
 }
 
@@ -137,8 +140,8 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
 // silu(x) = x s, silu'(x) = s (1 + x (1 - s)).  The exponent is clamped as above.
 __device__ __forceinline__ void sigmoid_parts(float x, float& s, float& oms) {
   const float a = fminf(-1.4426950408889634f * x, 126.0f);  // -x log2(e)
-  const float e = exp2f(a);
-  s = __frcp_rn(1.0f + e);
+  const float e = ex2_approx(a);
+  s = rcp_approx(1.0f + e);
   oms = e * s;
 }
 
