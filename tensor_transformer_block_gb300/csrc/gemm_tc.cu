@@ -106,34 +106,35 @@ __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, i
   nb = n;
 }
 
-// GeLU (tanh form) through the logistic identity 0.5 (1 + tanh u) = 1 / (1 + e^(-2u)):
-// with s = 1 / (1 + e^(-2u)), GeLU(x) = x s and, since 1 - tanh^2 u = 4 s (1 - s),
-// GeLU'(x) = s (1 + 2 x (1 - s) u').  One exp2 and one reciprocal per element, and
-// no cancellation in 1 + tanh u for negative x.  The exponent is clamped so that
-// e^(-2u) stays finite (s then underflows towards 0 smoothly).  exp2 and the
-// reciprocal are the special-function unit's approximations (about 1 ulp of fp32):
-// the results are rounded to bf16, and the correctly rounded reciprocal cost ~2%
-// of the fused GEMMs' time.
-__device__ __forceinline__ void gelu_logistic(float x, float& s, float& oms, float& du) {
-  const float x2 = x * x;
-  const float u = 0.7978845608028654f * fmaf(0.044715f * x2, x, x);
-  du = 0.7978845608028654f * fmaf(0.134145f, x2, 1.0f);
-  const float a = fminf(-2.8853900817779268f * u, 126.0f);  // -2u log2(e)
+// GeLU (tanh form) through the logistic identity 0.5 (1 + tanh u) = 1 / (1 + e^(-2u))
+// with u = sqrt(2/pi) (x + 0.044715 x^3): with s = 1 / (1 + e^(-2u)), GeLU(x) = x s
+// and, since 1 - tanh^2 u = 4 s (1 - s), GeLU'(x) = s (1 + x (1 - s) 2u').  One exp2
+// and one reciprocal per element, no cancellation in 1 + tanh u for negative x.  The
+// constants are folded (x2 = x^2):
+//   -2u log2(e) = x (k1 + k3 x2),  k1 = -2 log2(e) sqrt(2/pi),  k3 = 0.044715 k1
+//   2u'         = d0 + d2 x2,      d0 = 2 sqrt(2/pi),           d2 = 3 * 0.044715 d0
+// The exponent is clamped so that e^(-2u) stays finite (s then underflows towards 0
+// smoothly).  exp2 and the reciprocal are the special-function unit's approximations
+// (about 1 ulp of fp32): the results are rounded to bf16, and the correctly rounded
+// reciprocal cost ~2% of the fused GEMMs' time.
+__device__ __forceinline__ float gelu_sigmoid(float x, float x2, float& oms) {
+  const float a = fminf(x * fmaf(-0.1029432395800235f, x2, -2.302208198144325f), 126.0f);
   const float e = ex2_approx(a);
-  s = rcp_approx(1.0f + e);
+  const float s = rcp_approx(1.0f + e);
   oms = e * s;  // 1 - s without cancellation
+  return s;
 }
 
 __device__ __forceinline__ float gelu_f(float x) {
-  float s, oms, du;
-  gelu_logistic(x, s, oms, du);
-  return x * s;
+  float oms;
+  return x * gelu_sigmoid(x, x * x, oms);
 }
 
 __device__ __forceinline__ float gelu_grad_f(float x) {
-  float s, oms, du;
-  gelu_logistic(x, s, oms, du);
-  return s * fmaf(2.0f * x * oms, du, 1.0f);
+  const float x2 = x * x;
+  float oms;
+  const float s = gelu_sigmoid(x, x2, oms);
+  return s * fmaf(x * oms, fmaf(0.21406444881780076f, x2, 1.5957691216057308f), 1.0f);
 }
 
 // Logistic sigmoid s = 1 / (1 + e^(-x)) and 1 - s = e^(-x) s (no cancellation);
