@@ -4,9 +4,13 @@
 // added in, and the fixed-order column sums that finish dgamma and dbeta.
 //
 // Both row kernels are HBM-bound: every element is read once and written once.
-// A row is held in registers by one CTA of up to 1024 threads: thread t owns
-// the 16-byte vectors t, t + blockDim, ... (VPT <= 2 of them), so the loads of
-// a warp are contiguous 512-byte runs; h <= 8192 takes one vector per thread.
+// A row is held in registers by one CTA: thread t owns the 16-byte vectors t,
+// t + blockDim, ... (VPT of them), so the loads of a warp are contiguous 512-byte
+// runs.  The forward is persistent over rows and loads the next row while it
+// reduces the current one, so that every SM keeps a row's worth of loads in
+// flight; from h = 4096 up it takes four vectors per thread (h = 8192: 256 threads,
+// four CTAs per SM), below that one.  The backward, which also keeps dgamma /
+// dbeta partials per thread, takes one or two (up to 1024 threads).
 // Statistics are fp32, taken in two passes over the registers (mean first,
 // then the centred sum of squares), so no cancellation.
 //
@@ -74,53 +78,63 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
                                                  float* __restrict__ mean, float* __restrict__ rstd, int T,
                                                  int nvec, float inv_h, float eps) {
   __shared__ float red[64];
-  const int64_t row = blockIdx.x;
+  int64_t row = blockIdx.x;
   if (row >= T) return;
-  const uint4* xr = X + row * nvec;
-  float v[VPT][8];
-  float s = 0.0f;
+  // persistent over rows: the next row's vectors are loaded while this one is reduced
+  uint4 cur[VPT], nxt[VPT];
+  auto load = [&](int64_t r, uint4 (&q)[VPT]) {
+    const uint4* xr = X + r * nvec;
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int i = threadIdx.x + k * blockDim.x;
-    if (i < nvec) {
-      unpack8(xr[i], v[k]);
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      q[k] = i < nvec ? xr[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load(row, cur);
+  for (; row < T; row += gridDim.x) {
+    const int64_t nrow = row + gridDim.x;
+    if (nrow < T) load(nrow, nxt);
+    float v[VPT][8];
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      unpack8(cur[k], v[k]);  // zero beyond the row: adds nothing
 #pragma unroll
       for (int e = 0; e < 8; ++e) s += v[k][e];
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[k][e] = 0.0f;
     }
-  }
-  const float mu = block_sum2(s, 0.0f, red).x * inv_h;
-  float q = 0.0f;
+    const float mu = block_sum2(s, 0.0f, red).x * inv_h;
+    float q = 0.0f;
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    if (threadIdx.x + k * blockDim.x < nvec) {
+    for (int k = 0; k < VPT; ++k) {
+      if (threadIdx.x + k * blockDim.x < nvec) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float dlt = v[k][e] - mu;
-        q = fmaf(dlt, dlt, q);
+        for (int e = 0; e < 8; ++e) {
+          const float dlt = v[k][e] - mu;
+          q = fmaf(dlt, dlt, q);
+        }
       }
     }
-  }
-  const float var = block_sum2(q, 0.0f, red).x * inv_h;
-  const float r = rsqrtf(var + eps);
-  uint4* yr = Y + row * nvec;
+    const float var = block_sum2(q, 0.0f, red).x * inv_h;
+    const float r = rsqrtf(var + eps);
+    uint4* yr = Y + row * nvec;
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int i = threadIdx.x + k * blockDim.x;
-    if (i < nvec) {
-      float g[8], b[8], o[8];
-      unpack8(gamma[i], g);
-      unpack8(beta[i], b);
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      if (i < nvec) {
+        float g[8], b[8], o[8];
+        unpack8(gamma[i], g);
+        unpack8(beta[i], b);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = fmaf((v[k][e] - mu) * r, g[e], b[e]);
-      yr[i] = pack8(o);
+        for (int e = 0; e < 8; ++e) o[e] = fmaf((v[k][e] - mu) * r, g[e], b[e]);
+        yr[i] = pack8(o);
+      }
     }
-  }
-  if (threadIdx.x == 0) {
-    mean[row] = mu;
-    rstd[row] = r;
+    if (threadIdx.x == 0) {
+      mean[row] = mu;
+      rstd[row] = r;
+    }
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) cur[k] = nxt[k];
   }
 }
 
@@ -242,6 +256,16 @@ struct LnGeom {
   int vpt, threads;
 };
 
+// forward: four vectors per thread from h = 4096 up (fewer threads per row, more
+// rows per SM), one below (a narrow row would leave a CTA one warp wide)
+LnGeom ln_fwd_geom(int64_t h) {
+  const int64_t nvec = h / 8;
+  LnGeom g{nvec >= 512 ? 4 : 1, 32};
+  const int64_t t = (nvec + g.vpt - 1) / g.vpt;
+  g.threads = static_cast<int>((t + 31) / 32 * 32);
+  return g;
+}
+
 LnGeom ln_geom(int64_t h) {
   const int64_t nvec = h / 8;
   LnGeom g{1, 32};
@@ -271,19 +295,27 @@ size_t ln_partial_bytes(int64_t T, int64_t h) {
 int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, float* mean, float* rstd, int64_t T,
                   int64_t h, float eps, cudaStream_t st) {
   if (!ln_shape_ok(T, h)) return 1;
-  const LnGeom g = ln_geom(h);
+  const LnGeom g = ln_fwd_geom(h);
   const int nvec = static_cast<int>(h / 8);
   const float inv_h = 1.0f / static_cast<float>(h);
   const auto* x = static_cast<const uint4*>(X);
   const auto* ga = static_cast<const uint4*>(gamma);
   const auto* be = static_cast<const uint4*>(beta);
   auto* y = static_cast<uint4*>(Y);
+  // resident CTAs per SM for this shape (the grid is what fits at once)
+  int per_sm = 0;
+  const cudaError_t oe = g.vpt == 4
+                             ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ln_fwd<4>, g.threads, 0)
+                             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ln_fwd<1>, g.threads, 0);
+  if (oe != cudaSuccess) return 2;
+  int64_t nb = static_cast<int64_t>(device_sm_count()) * (per_sm > 0 ? per_sm : 1);
+  if (nb > T) nb = T;
   const int slot = timing_begin(kKLnFwd, st);
-  const dim3 grid(static_cast<unsigned>(T));
-  if (g.vpt == 1)
-    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+  const dim3 grid(static_cast<unsigned>(nb));
+  if (g.vpt == 4)
+    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
   else
-    k_ln_fwd<2><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
   const bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
