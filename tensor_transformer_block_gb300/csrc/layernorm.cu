@@ -10,15 +10,19 @@
 // reduces the current one, so that every SM keeps a row's worth of loads in
 // flight; from h = 4096 up it takes four vectors per thread (h = 8192: 256 threads,
 // four CTAs per SM), below that one.  The backward, which also keeps dgamma /
-// dbeta partials per thread, takes one or two (up to 1024 threads).
+// dbeta partials per thread, loads a row's dR together with X and dY and the
+// next row while it reduces the current one, with at most 512 threads (two
+// vectors per thread from h = 4096 up); above h = 8192 a row needs more threads
+// than those registers allow, and it loads row by row.
 // Statistics are fp32, taken in two passes over the registers (mean first,
 // then the centred sum of squares), so no cancellation.
 //
 // The backward is persistent over rows: CTA b takes rows b, b + grid, ... and,
 // because each thread always owns the same columns, accumulates its columns'
 // dgamma / dbeta partial sums in registers; each CTA writes one partial row and
-// k_ln_colsum adds the partial rows in a fixed order.  Both kernels and their
-// launch geometry depend only on T and h, so the result is bit-reproducible.
+// k_ln_colsum adds the partial rows in a fixed order.  Both kernels' launch
+// geometry depends only on T, h and the device (the grids are the CTAs that fit
+// at once), so the result is bit-reproducible on a given GPU.
 #include <cuda_bf16.h>
 
 #include "host_util.cuh"
@@ -138,12 +142,13 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
   }
 }
 
-template <int VPT>
-__global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
-                                                 const float* __restrict__ mean, const float* __restrict__ rstd,
-                                                 const uint4* __restrict__ dY, const uint4* __restrict__ dR,
-                                                 uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec,
-                                                 float inv_h) {
+// PF: the row's dR is loaded with X and dY, and the next row's three vectors are
+// loaded while this row is reduced (more registers: at most 512 threads).
+template <int VPT, bool PF>
+__global__ void __launch_bounds__(PF ? 512 : 1024)
+    k_ln_bwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma, const float* __restrict__ mean,
+             const float* __restrict__ rstd, const uint4* __restrict__ dY, const uint4* __restrict__ dR,
+             uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h) {
   __shared__ float red[64];
   float gm[VPT][8], pg[VPT][8], pb[VPT][8];
 #pragma unroll
@@ -161,7 +166,28 @@ __global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, co
       pb[k][e] = 0.0f;
     }
   }
+  // raw vectors of X, dY, dR for one row (zero past the row, or dR absent)
+  struct RowIn {
+    uint4 x[VPT], dy[VPT], dr[VPT];
+  };
+  auto load = [&](int64_t row, RowIn& q) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int i = threadIdx.x + k * blockDim.x;
+      const bool in = i < nvec;
+      q.x[k] = in ? X[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u);
+      q.dy[k] = in ? dY[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u);
+      if (PF) q.dr[k] = (in && dR) ? dR[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  RowIn cur, nxt;
+  if (PF && blockIdx.x < T) load(blockIdx.x, cur);
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
+    if (PF) {
+      if (row + gridDim.x < T) load(row + gridDim.x, nxt);
+    } else {
+      load(row, cur);
+    }
     const float mu = mean[row], r = rstd[row];
     float xh[VPT][8], g[VPT][8];
     float s1 = 0.0f, s2 = 0.0f;
@@ -170,8 +196,8 @@ __global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, co
       const int i = threadIdx.x + k * blockDim.x;
       if (i < nvec) {
         float xv[8], dy[8];
-        unpack8(X[row * nvec + i], xv);
-        unpack8(dY[row * nvec + i], dy);
+        unpack8(cur.x[k], xv);
+        unpack8(cur.dy[k], dy);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           xh[k][e] = (xv[e] - mu) * r;
@@ -195,18 +221,15 @@ __global__ void __launch_bounds__(1024) k_ln_bwd(const uint4* __restrict__ X, co
     for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
       if (i < nvec) {
-        float o[8];
+        float o[8], rr[8];
+        // zero without a residual (without the prefetch, loaded only now)
+        unpack8(PF ? cur.dr[k] : (dR ? dR[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u)), rr);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = r * (g[k][e] - c1 - xh[k][e] * c2);
-        if (dR) {
-          float rr[8];
-          unpack8(dR[row * nvec + i], rr);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] += rr[e];
-        }
+        for (int e = 0; e < 8; ++e) o[e] = r * (g[k][e] - c1 - xh[k][e] * c2) + rr[e];
         dX[row * nvec + i] = pack8(o);
       }
     }
+    if (PF) cur = nxt;
   }
   // partial row of this CTA: [2][h] fp32 (dgamma, then dbeta)
   float* pr = part + static_cast<int64_t>(blockIdx.x) * 2 * nvec * 8;
@@ -254,6 +277,7 @@ __global__ void __launch_bounds__(kColsumWarps * 32) k_ln_colsum(const float* __
 
 struct LnGeom {
   int vpt, threads;
+  bool pf = false;  // backward: dR with X and dY, next row prefetched
 };
 
 // forward: four vectors per thread from h = 4096 up (fewer threads per row, more
@@ -266,10 +290,14 @@ LnGeom ln_fwd_geom(int64_t h) {
   return g;
 }
 
+// backward: up to h = 8192 the prefetching kernel with at most 512 threads (two
+// vectors per thread from h = 4096 up); above that two vectors per thread, no
+// prefetch (a row then needs up to 1024 threads, whose registers leave no room)
 LnGeom ln_geom(int64_t h) {
   const int64_t nvec = h / 8;
   LnGeom g{1, 32};
-  g.vpt = nvec <= 1024 ? 1 : 2;
+  g.pf = nvec <= 1024;
+  g.vpt = g.pf ? (nvec >= 512 ? 2 : 1) : 2;
   const int64_t t = (nvec + g.vpt - 1) / g.vpt;
   g.threads = static_cast<int>((t + 31) / 32 * 32);
   return g;
@@ -328,17 +356,33 @@ int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const flo
   const LnGeom g = ln_geom(h);
   const int nvec = static_cast<int>(h / 8);
   const float inv_h = 1.0f / static_cast<float>(h);
-  const int grid = ln_bwd_grid(T, g.threads);
+  // as many persistent CTAs as fit at once (never more than the partials allow)
+  int per_sm = 0;
+  cudaError_t oe;
+  if (g.pf)
+    oe = g.vpt == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ln_bwd<2, true>, g.threads, 0)
+                    : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ln_bwd<1, true>, g.threads, 0);
+  else
+    oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_ln_bwd<2, false>, g.threads, 0);
+  if (oe != cudaSuccess) return 2;
+  int grid = ln_bwd_grid(T, g.threads);
+  const int64_t fit = static_cast<int64_t>(device_sm_count()) * (per_sm > 0 ? per_sm : 1);
+  if (fit < grid) grid = static_cast<int>(fit);
   const auto* x = static_cast<const uint4*>(X);
   const auto* ga = static_cast<const uint4*>(gamma);
   const auto* dy = static_cast<const uint4*>(dY);
   const auto* dr = static_cast<const uint4*>(dR);
   auto* dx = static_cast<uint4*>(dX);
   int slot = timing_begin(kKLnBwd, st);
-  if (g.vpt == 1)
-    k_ln_bwd<1><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec, inv_h);
+  if (g.pf && g.vpt == 2)
+    k_ln_bwd<2, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
+                                                 inv_h);
+  else if (g.pf)
+    k_ln_bwd<1, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
+                                                 inv_h);
   else
-    k_ln_bwd<2><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec, inv_h);
+    k_ln_bwd<2, false><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
+                                                  inv_h);
   bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
