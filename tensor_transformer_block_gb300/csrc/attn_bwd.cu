@@ -28,30 +28,43 @@ constexpr int NTHREADS = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // -------------------------------------------------------------------- Dsum
+// One row (a token's d values of one head) per group of D/8 lanes: each lane loads
+// one 16-byte vector of O and of dO, so a warp's loads are contiguous, and the
+// group adds its partial dot products with shuffles.  The loop runs whole warps
+// (a group past the last row adds zeros and stores nothing), so every shuffle
+// has all 32 lanes.
 template <int D>
 __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict__ dout, float* __restrict__ dsum,
                             const AttnDims a) {
+  constexpr int LPR = D / 8;  // lanes (16-byte vectors) per row
+  static_assert(32 % LPR == 0, "a row's lanes lie in one warp");
   const long long T = static_cast<long long>(a.B) * a.S;
   const long long total = static_cast<long long>(a.N) * T * a.hN;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long base = idx * (D / 8);  // uint4 = 8 bf16
+  const int lane = threadIdx.x & 31, sub = lane % LPR;
+  const long long warp0 = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) / 32;
+  const long long nwarps = static_cast<long long>(gridDim.x) * blockDim.x / 32;
+  for (long long w = warp0; w * (32 / LPR) < total; w += nwarps) {
+    const long long idx = w * (32 / LPR) + lane / LPR;  // this lane's row
+    const bool valid = idx < total;
     float s = 0.0f;
-#pragma unroll 4
-    for (int v = 0; v < D / 8; ++v) {
-      const uint4 x = o[base + v], y = dout[base + v];
-      s += bf16lo_to_f32(x.x) * bf16lo_to_f32(y.x) + bf16hi_to_f32(x.x) * bf16hi_to_f32(y.x);
+    if (valid) {
+      const uint4 x = o[idx * LPR + sub], y = dout[idx * LPR + sub];
+      s = bf16lo_to_f32(x.x) * bf16lo_to_f32(y.x) + bf16hi_to_f32(x.x) * bf16hi_to_f32(y.x);
       s += bf16lo_to_f32(x.y) * bf16lo_to_f32(y.y) + bf16hi_to_f32(x.y) * bf16hi_to_f32(y.y);
       s += bf16lo_to_f32(x.z) * bf16lo_to_f32(y.z) + bf16hi_to_f32(x.z) * bf16hi_to_f32(y.z);
       s += bf16lo_to_f32(x.w) * bf16lo_to_f32(y.w) + bf16hi_to_f32(x.w) * bf16hi_to_f32(y.w);
     }
-    const long long shard = idx / (T * a.hN);
-    const long long rem = idx - shard * T * a.hN;
-    const long long t = rem / a.hN;
-    const int jj = static_cast<int>(rem - t * a.hN);
-    const long long bb = t / a.S, ss = t - bb * a.S;
-    const long long j = shard * a.hN + jj;
-    dsum[(bb * a.H + j) * a.S + ss] = s;
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (valid && sub == 0) {
+      const long long shard = idx / (T * a.hN);
+      const long long rem = idx - shard * T * a.hN;
+      const long long t = rem / a.hN;
+      const int jj = static_cast<int>(rem - t * a.hN);
+      const long long bb = t / a.S, ss = t - bb * a.S;
+      const long long j = shard * a.hN + jj;
+      dsum[(bb * a.H + j) * a.S + ss] = s;
+    }
   }
 }
 
@@ -713,7 +726,7 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
 
   const long long rows = static_cast<long long>(a.N) * a.B * a.S * a.hN;
   const int sms = device_sm_count();
-  long long blocks = (rows + 255) / 256;
+  long long blocks = (rows * (D / 8) + 255) / 256;  // D/8 lanes per row
   if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
   int slot = timing_begin(kKAttnDsum, st);
   k_attn_dsum<D><<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(o),
