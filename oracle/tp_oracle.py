@@ -24,7 +24,7 @@ Page short names used in the citations (the pages are Chinese web articles):
   * "guijiagi 张量并行"   guijiagi.com/tags/张量并行/
   * "sunjinbo 并行方式"   sunjinbo.space/document/parallelism.html (大模型分布式并行方式详解)
 
-Conventions (readings where the pages are silent; each is listed in the design doc):
+Conventions (readings where the pages are silent):
   * Y = X W with W stored [in x out] (wangyu 张量并行 §两种切分方式: X is B x M,
     W is M x N; guijiagi 张量并行 §线性层的切分: W in R^{d x h}).
   * No biases: none of the pages' split identities carries one.
