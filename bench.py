@@ -790,8 +790,8 @@ def main() -> None:
     ap.add_argument("--l2", default="auto", choices=["auto", "flush", "none"],
                     help="L2 between timed steps: auto flushes when a step's working set is under 4x L2")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--gemm-tiling", type=int, default=0, choices=[0, 1, 2, 3],
-                    help="0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile, 3 CTA pairs in clusters of two sharing B")
+    ap.add_argument("--gemm-tiling", type=int, default=0, choices=[0, 1, 2],
+                    help="0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile")
     ap.add_argument("--override", action="append", default=[],
                     help="KEY=VALUE shape override of the workload (a smaller case for profiling)")
     args = ap.parse_args()

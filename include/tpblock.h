@@ -362,13 +362,12 @@ TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
 /* ------------------------------------------------------------ GEMM tiling */
 
 /* Tiling of every GEMM the library launches (process-wide; for tests and
- * measurement): 0 = automatic (default: when there are at least #SM/2 tiles of
- * 256 x 256, a CTA pair per tile through tcgen05 cta_group::2, two pairs per
- * cluster on consecutive M tiles sharing the B tile through TMA multicast when
- * there are two or more such M tiles; else one CTA per 128 x 256 tile), 1 = always
- * one CTA per tile, 2 = always CTA pairs without multicast, 3 = CTA pairs, two per
- * cluster sharing B wherever there are two M tiles.  Every tiling computes the
- * same products; TP_ERR_SHAPE for another value. */
+ * measurement): 0 = automatic (default: a CTA pair per 256 x 256 tile through
+ * tcgen05 cta_group::2 when there are at least #SM/2 such tiles, else one CTA per
+ * 128 x 256 tile), 1 = always one CTA per tile, 2 = always CTA pairs.  Every
+ * tiling computes the same products; TP_ERR_SHAPE for another value (the setting
+ * is then unchanged).  Each CTA loads only its own tiles: no TMA load is
+ * multicast across a cluster. */
 TP_API int tp_set_gemm_tiling(int mode);
 
 /* ---------------------------------------------------------- kernel timing */

@@ -813,9 +813,7 @@ int tp_sp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, in
 extern "C" {
 
 int tp_set_gemm_tiling(int mode) {
-  if (mode < 0 || mode > 3) return TP_ERR_SHAPE;
-  tpb::set_gemm_tiling_mode(mode);
-  return TP_OK;
+  return tpb::set_gemm_tiling_mode(mode) ? TP_OK : TP_ERR_SHAPE;
 }
 
 int tp_timing_enable(int on) {

@@ -25,7 +25,7 @@
 //           each CTA stages its 128 rows of A and half (128 columns) of B, so each
 //           SM moves 32 KB per k-block instead of 48; 6 stages.  The even CTA issues
 //           the MMAs; both CTAs' TMA loads count on its full barrier; its commits
-//           multicast to both CTAs' empty / accumulator-ready barriers; both CTAs'
+//           arrive on both CTAs' empty / accumulator-ready barriers; both CTAs'
 //           epilogue warps release an accumulator on the even CTA's barrier.
 // Every wait is bounded; on a timeout the CTA latches an error, drains its own
 // copies and MMAs, frees TMEM and returns.
@@ -199,28 +199,6 @@ __device__ __forceinline__ void mn_load(uint32_t dst, const CUtensorMap* m, uint
       tma_load_4d(dst, m, bar, 0, k, chunk0, z);
   }
 }
-// Pair loads of the B operand, multicast to the CTAs of ``mc`` when it is not 0.
-__device__ __forceinline__ void pld3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2,
-                                     uint16_t mc) {
-  if (mc)
-    tma_load_3d_pair_mc(dst, m, bar, c0, c1, c2, mc);
-  else
-    tma_load_3d_pair(dst, m, bar, c0, c1, c2);
-}
-__device__ __forceinline__ void pld4(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2, int c3,
-                                     uint16_t mc) {
-  if (mc)
-    tma_load_4d_pair_mc(dst, m, bar, c0, c1, c2, c3, mc);
-  else
-    tma_load_4d_pair(dst, m, bar, c0, c1, c2, c3);
-}
-__device__ __forceinline__ void pld5(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2, int c3,
-                                     int c4, uint16_t mc) {
-  if (mc)
-    tma_load_5d_pair_mc(dst, m, bar, c0, c1, c2, c3, c4, mc);
-  else
-    tma_load_5d_pair(dst, m, bar, c0, c1, c2, c3, c4);
-}
 __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, int c0, int row, int z, int spS, int spL) {
   if (spS > 0) {
     int sl, bb, cc;
@@ -231,10 +209,7 @@ __device__ __forceinline__ void out_store(const CUtensorMap* m, uint32_t src, in
   }
 }
 
-// MC (pair mode only): a cluster of two CTA pairs on consecutive M tiles of the same
-// N tile; the even pair's CTAs load each B half once, multicast to the same position
-// in the odd pair, so L2 delivers 48 instead of 64 KB per pair and k-block.
-template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool MC>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
            const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmY, const GemmShape p) {
@@ -258,12 +233,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  static_assert(PAIR || !MC, "multicast clusters are made of CTA pairs");
-  constexpr int CL = MC ? 4 : (PAIR ? 2 : 1);             // CTAs per cluster
-  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;   // position in the cluster
-  const uint32_t rank = crank & 1u;                       // position in the CTA pair
-  const uint32_t pid = MC ? (crank >> 1) : 0u;            // pair within the cluster (its M tile)
-  const uint32_t lead = crank & ~1u;                      // the pair's even CTA
+  constexpr int CL = PAIR ? 2 : 1;                     // CTAs per cluster
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // position in the CTA pair
+  const uint32_t lead = 0u;                            // the pair's even CTA
   const bool leader = rank == 0;
   const int unit = static_cast<int>(blockIdx.x) / CL;
   const int nunits = static_cast<int>(gridDim.x) / CL;
@@ -271,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(bar0 + 8u * (BAR_FULL + i), 1);
-      mbar_init(bar0 + 8u * (BAR_EMPTY + i), MC ? 2 : 1);  // MC: both pairs consumed the stage
+      mbar_init(bar0 + 8u * (BAR_EMPTY + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar0 + 8u * (BAR_TFULL + i), 1);
@@ -324,7 +296,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
         decode_tile(t, p, g, mb, nb);
-        if (MC) mb = 2 * mb + static_cast<int>(pid);
         const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
         const int bcol = EPI == kEpiSwiGLU ? nb * TILE_N : nb * BN + static_cast<int>(rank) * C::BN_CTA;
         TokPos apos{0, 0, 0};
@@ -354,34 +325,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               } else {
                 op_load_at<true>(sa, &tmA, fb, kc, arow, az, a_rows_sp, apos);
               }
-              // B: each CTA stages half of the tile's columns; with MC only the even
-              // pair's CTAs load, for both pairs
-              const uint16_t mcm = MC ? static_cast<uint16_t>((1u << rank) | (1u << (rank + 2))) : 0;
-              if (MC && pid != 0) {
-              } else if (EPI == kEpiSwiGLU) {
+              // B: each CTA stages half of the tile's columns
+              if (EPI == kEpiSwiGLU) {
                 // the even CTA stages the tile's gate columns, the odd CTA its up columns
                 if (p.b_chunked) {
-                  pld5(sb, &tmB, fb, 0, kc, bcol / 64, static_cast<int>(rank), bz, mcm);
+                  tma_load_5d_pair(sb, &tmB, fb, 0, kc, bcol / 64, static_cast<int>(rank), bz);
                 } else {
 #pragma unroll
                   for (int j = 0; j < C::BN_CTA / 64; ++j)
-                    pld4(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz, mcm);
+                    tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, static_cast<int>(rank), kc, bz);
                 }
               } else if (B_MN && p.b_chunked) {
                 if (b_k_sp)
-                  pld5(sb, &tmB, fb, 0, kpos.sl, bcol / 64, kpos.b, kpos.c, mcm);
+                  tma_load_5d_pair(sb, &tmB, fb, 0, kpos.sl, bcol / 64, kpos.b, kpos.c);
                 else
-                  pld4(sb, &tmB, fb, 0, kc, bcol / 64, bz, mcm);
+                  tma_load_4d_pair(sb, &tmB, fb, 0, kc, bcol / 64, bz);
               } else if (B_MN) {
 #pragma unroll
                 for (int j = 0; j < C::BN_CTA / 64; ++j) {
                   if (b_k_sp)
-                    pld4(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kpos.sl, kpos.b, kpos.c, mcm);
+                    tma_load_4d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kpos.sl, kpos.b, kpos.c);
                   else
-                    pld3(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz, mcm);
+                    tma_load_3d_pair(sb + j * (BK * 128), &tmB, fb, bcol + j * 64, kc, bz);
                 }
               } else {
-                pld3(sb, &tmB, fb, kc, bcol, bz, mcm);
+                tma_load_3d_pair(sb, &tmB, fb, kc, bcol, bz);
               }
             } else {
               mbar_arrive_expect_tx(fb_local, STAGE_BYTES);
@@ -480,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           any = true;
           if (PAIR)
-            tc_commit_pair(bar0 + 8u * (BAR_EMPTY + stage), MC ? 0xF : 3);  // MC: both pairs' stages
+            tc_commit_pair(bar0 + 8u * (BAR_EMPTY + stage), 3);
           else
             tc_commit(bar0 + 8u * (BAR_EMPTY + stage));
           if (++stage == STAGES) {
@@ -490,13 +458,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         if (PAIR)
-          tc_commit_pair(bar0 + 8u * (BAR_TFULL + buf), static_cast<uint16_t>(3u << (2 * pid)));
+          tc_commit_pair(bar0 + 8u * (BAR_TFULL + buf), 3);
         else
           tc_commit(bar0 + 8u * (BAR_TFULL + buf));
       }
       if (any) {
         if (PAIR)
-          tc_commit_pair(bar0 + 8u * BAR_DRAIN, static_cast<uint16_t>(1u << crank));
+          tc_commit_pair(bar0 + 8u * BAR_DRAIN, 1);
         else
           tc_commit(bar0 + 8u * BAR_DRAIN);
         mbar_wait(bar0 + 8u * BAR_DRAIN, 0, wdrain);
@@ -525,7 +493,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int t = unit; t < total && ok; t += nunits, ++it) {
       int g, mb, nb;
       decode_tile(t, p, g, mb, nb);
-      if (MC) mb = 2 * mb + static_cast<int>(pid);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
@@ -830,12 +797,12 @@ using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, Ge
 
 constexpr int kMaxDev = 64;
 
-template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool MC>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 KernelFn get_kernel() {
   static bool configured[kMaxDev] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
-  auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI, MC>;
+  auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI>;
   if (!configured[dev]) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR, EPI>::SMEM_ALLOC) !=
         cudaSuccess)
@@ -845,17 +812,17 @@ KernelFn get_kernel() {
   return fn;
 }
 
-template <bool PAIR, bool MC>
+template <bool PAIR>
 KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
-  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<PAIR, false, true, kEpiGelu, MC>();
-  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, false, true, kEpiStore, MC>();
-  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<PAIR, false, true, kEpiSplit, MC>();
-  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu, MC>();
-  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore, MC>();
-  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore, MC>();
-  if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU, MC>();
-  if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU, MC>();
-  if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual, MC>();
+  if (!a_mn && b_mn && epi == kEpiGelu) return get_kernel<PAIR, false, true, kEpiGelu>();
+  if (!a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, false, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiSplit) return get_kernel<PAIR, false, true, kEpiSplit>();
+  if (!a_mn && !b_mn && epi == kEpiDGelu) return get_kernel<PAIR, false, false, kEpiDGelu>();
+  if (!a_mn && !b_mn && epi == kEpiStore) return get_kernel<PAIR, false, false, kEpiStore>();
+  if (a_mn && b_mn && epi == kEpiStore) return get_kernel<PAIR, true, true, kEpiStore>();
+  if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU>();
+  if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
+  if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual>();
   return nullptr;
 }
 
@@ -911,11 +878,15 @@ bool two_part_map(CUtensorMap* m, const void* ptr, int64_t N, int64_t M, int G, 
   return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, box, swz);
 }
 
-int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pairs, 3 CTA pairs sharing B in clusters of 4
+int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pairs
 
 }  // namespace
 
-void set_gemm_tiling_mode(int mode) { g_tiling_mode = mode; }
+bool set_gemm_tiling_mode(int mode) {
+  if (mode < 0 || mode > 2) return false;
+  g_tiling_mode = mode;
+  return true;
+}
 
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
                      bool store_y, int64_t M, int64_t N, int G, int S, int64_t Ks, unsigned* err,
@@ -950,14 +921,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
   bool pair = g_tiling_mode >= 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
   if (sms < 2) pair = false;
-  // two pairs per cluster sharing B (multicast) only on request: at full clock it
-  // measured slower (36 four-CTA clusters fit, 144 SMs, and a tile row of two pair
-  // tiles doubles the tail of the last wave)
-  const int64_t pair_rows = (M + 255) / 256;
-  const bool mc = pair && sms >= 4 && pair_rows >= 2 && g_tiling_mode == 3;
-  KernelFn fn = !pair ? pick_kernel<false, false>(A.mn_major, B.mn_major, epi)
-                      : (mc ? pick_kernel<true, true>(A.mn_major, B.mn_major, epi)
-                            : pick_kernel<true, false>(A.mn_major, B.mn_major, epi));
+  KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
   if (!fn) return 2;
   const uint32_t a_rows = 128, b_rows = pair ? Cfg<true, kEpiStore>::BN_CTA : Cfg<false, kEpiStore>::BN_CTA;
   const bool one_box = epi == kEpiStore || epi == kEpiSplit;
@@ -1002,7 +966,6 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.S = S;
   p.kb_per_seg = static_cast<int>((Ks + BK - 1) / BK);
   p.tiles_m = static_cast<int>((M + (pair ? 255 : 127)) / (pair ? 256 : 128));
-  if (mc) p.tiles_m = (p.tiles_m + 1) / 2;  // a cluster's tile row covers two pair tiles
   p.tiles_n = static_cast<int>((N + tile_n - 1) / tile_n);
   p.a_zg = A.zg;
   p.a_zs = A.zs;
@@ -1027,7 +990,7 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const int slot = timing_begin(kind, stream);
   bool ok;
   if (pair) {
-    const int cl = mc ? 4 : 2;
+    const int cl = 2;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
@@ -1039,15 +1002,8 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // persistent clusters: as many as can be resident at once (4-CTA clusters need
-    // four free SMs in one GPC, so fewer than #SM/4 may fit)
+    // persistent pairs: one per two SMs
     long long units = sms / cl;
-    cfg.gridDim = dim3(static_cast<unsigned>(cl * units), 1, 1);
-    if (mc) {
-      int resident = 0;
-      if (cudaOccupancyMaxActiveClusters(&resident, fn, &cfg) == cudaSuccess && resident > 0 && resident < units)
-        units = resident;
-    }
     if (units > total) units = total;
     cfg.gridDim = dim3(static_cast<unsigned>(cl * units), 1, 1);
     ok = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, ty, p) == cudaSuccess;

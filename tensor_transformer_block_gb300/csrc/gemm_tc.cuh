@@ -83,10 +83,9 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
                      unsigned long long timeout_ns, cudaStream_t stream, int kind,
                      const GemmExtra& extra = GemmExtra());
 
-// 0: choose per launch (CTA pairs when there are at least #SM/2 tiles of 256 x 256,
-// two pairs per cluster sharing B where there are two M tiles), 1: always one CTA
-// per 128 x 256 tile, 2: always a CTA pair per 256 x 256 tile, 3: CTA pairs in
-// clusters of two pairs sharing B wherever there are two M tiles.
-void set_gemm_tiling_mode(int mode);
+// 0: choose per launch (CTA pairs when there are at least #SM/2 tiles of 256 x 256),
+// 1: always one CTA per 128 x 256 tile, 2: always a CTA pair per 256 x 256 tile.
+// Returns false (and keeps the mode) for another value.
+bool set_gemm_tiling_mode(int mode);
 
 }  // namespace tpb

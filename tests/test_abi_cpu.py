@@ -126,3 +126,11 @@ def test_golden_head_split_rule(lib, case):
         st = lib.tp_attn_fwd(1, 1, 128, 4096, case["H"], 128, case["N"], 1, 16, 16, 16, None, None, None, 16,
                              None, 0, None)
         assert st == 2
+
+
+def test_gemm_tiling_modes(lib):
+    """Tilings 0-2 are accepted; any other value is rejected and leaves the setting."""
+    for m in (1, 2, 0):
+        assert lib.tp_set_gemm_tiling(m) == 0
+    for m in (3, -1, 4):
+        assert lib.tp_set_gemm_tiling(m) == 2

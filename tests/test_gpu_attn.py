@@ -163,7 +163,7 @@ def test_layer_full_config_sampled():
         assert torch.isfinite(ga[k].float()).all(), k
 
 
-@pytest.mark.parametrize("mode", [1, 2, 3])
+@pytest.mark.parametrize("mode", [1, 2])
 def test_attention_block_each_tiling(mode):
     """The attention projections (split-residual epilogue, shard-sum output GEMM,
     backward GEMMs) under both GEMM tilings."""

@@ -133,7 +133,7 @@ def test_mlp_bf16_h4096_sampled():
     assert_bf16_parity(got2, gc["dW2_rows"], "dW2 rows")
 
 
-@pytest.mark.parametrize("mode", [1, 2, 3])
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("T,h,f,N", [(333, 200, 264, 3), (2048, 1024, 4096, 4), (600, 520, 1040, 5), (1, 64, 64, 8)])
 def test_mlp_bf16_each_tiling(mode, T, h, f, N):
     """Both GEMM tilings (one CTA per 128x256 tile; a CTA pair per 256x256 tile,
