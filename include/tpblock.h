@@ -142,7 +142,10 @@ TP_API int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
  *    device current; make that first call before any stream capture.
  *  - All calls on a device share the one array.  The array is written before it
  *    is read in every call (nothing in it has to start at zero), but calls whose
- *    kernels overlap on the GPU, such as calls on two streams at once, race on it. */
+ *    kernels overlap on the GPU, such as calls on two streams at once, race on it.
+ *  - The device address is kept for the life of the process: do not use the
+ *    library on a device after cudaDeviceReset() on it (the same holds for the
+ *    device error word every call uses). */
 TP_API int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N,
                               const void* X, const void* W1s, const void* W2s, void* Z, void* stream);
 

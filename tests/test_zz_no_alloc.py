@@ -2,9 +2,12 @@
 memory (a plug-in whose host framework owns all allocations, a runtime that
 forbids cudaMalloc once it is serving).  Its activation scratch is a fixed array
 inside the library.  The test calls it through the C-ABI twice in a row, on
-different inputs, and checks each result against tp_mlp_fwd's with the parity
-criteria the other tests use.  The file sorts last so that a run stopping at
-the first failure has already run every other test."""
+different inputs.  Each result must equal tp_mlp_fwd's bit for bit (the same
+kernels run on the same operands; only the scratch address differs) and pass
+the parity criteria the other tests use, and the second call must leave the
+device's free memory unchanged (an allocation inside the call, even one that
+bypasses torch's allocator, would show there).  The file sorts last so that a
+run stopping at the first failure has already run every other test."""
 import pytest
 import torch
 
@@ -24,16 +27,22 @@ def test_noalloc_matches_workspace_path_twice(dtype):
     lib = tp.load_library()
     code = tp.TP_BF16 if dtype == "bf16" else tp.TP_F32
     check = assert_bf16_parity if dtype == "bf16" else assert_f32_parity
-    for (T, h, f, N, seed) in ((2048, 1024, 4096, 4, 0), (333, 200, 264, 3, 7)):
+    for i, (T, h, f, N, seed) in enumerate(((2048, 1024, 4096, 4, 0), (333, 200, 264, 3, 7))):
         inp = inputs.mlp_inputs(T, h, f, N, dtype=dtype, seed=seed, backward=False)
         d = {k: v.cuda() for k, v in inp.items()}
         z_ref = block.mlp_forward(d["X"], d["W1s"], d["W2s"], save=False)["Z"]
-        z = torch.empty_like(z_ref)
+        z = torch.full_like(z_ref, float("nan"))
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         st = lib.tp_mlp_fwd_noalloc(code, T, h, f, N, d["X"].data_ptr(), d["W1s"].data_ptr(),
                                     d["W2s"].data_ptr(), z.data_ptr(), torch.cuda.current_stream().cuda_stream)
         assert st == 0, tp.tp_status_string(st)
         torch.cuda.synchronize()
+        free1 = torch.cuda.mem_get_info()[0]
         assert tp.tp_sync_status() == 0
+        if i > 0:  # the first call may load kernels; the second must not change free memory
+            assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
+        assert torch.equal(z, z_ref), f"noalloc Z differs from tp_mlp_fwd's ({T}, {h}, {f}, {N})"
         check(_np(z), _np(z_ref), f"noalloc Z ({T}, {h}, {f}, {N})")
 
 
