@@ -144,8 +144,9 @@ def describe(w) -> str:
         return (f"pre-norm layer (LN, attention, residual, LN, MLP, residual) fwd+bwd, {w.dtype}, B={w.B} x "
                 f"S={w.S}, h={w.h}, {w.H} heads x d={w.d}, f={w.f}, causal, N={w.N} logical shards; LayerNorm and "
                 f"residual adds not counted in the flops")
-    return (f"attention + MLP layer fwd+bwd, {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, "
-            f"f={w.f}, causal, N={w.N} logical shards")
+    return (f"attention + MLP layer fwd+bwd (tp_attn_mlp_fwd/bwd: the attention output stays in fp16 between "
+            f"the blocks), {w.dtype}, B={w.B} x S={w.S}, h={w.h}, {w.H} heads x d={w.d}, f={w.f}, causal, "
+            f"N={w.N} logical shards")
 
 
 # ------------------------------------------------------------------ clocks
@@ -463,9 +464,8 @@ def run_gpu(args, w) -> None:
     dt = tp.TP_BF16 if w.dtype == "bf16" else tp.TP_F32
     T, h, f, N = w.T, w.h, w.f, w.N
     buf = {}
-    if w.kind in ("mlp", "layer"):
+    if w.kind == "mlp":
         fN = f // N
-        xin = d["X"] if w.kind == "mlp" else None
         buf["Y"] = torch.empty(N, T, fN, dtype=d["W1s"].dtype, device=dev)
         buf["A"] = torch.empty_like(buf["Y"])
         buf["Z"] = torch.empty(T, h, dtype=d["W1s"].dtype, device=dev)
@@ -504,18 +504,20 @@ def run_gpu(args, w) -> None:
         buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
         buf["grads"] = {"dX": torch.empty(T, h, dtype=torch.bfloat16, device=dev),
                         **{"d" + k: torch.empty_like(v) for k, v in p.items()}}
-    if w.kind in ("attn", "layer"):
+    if w.kind == "attn":
         hN = w.H // N
         buf["QKV"] = torch.empty(N, T, tp.QKV_PLANES * hN * w.d, dtype=torch.bfloat16, device=dev)
         buf["O"] = torch.empty(N, T, hN * w.d, dtype=torch.bfloat16, device=dev)
         buf["LSE"] = torch.empty(w.B, w.H, w.S, dtype=torch.float32, device=dev)
         buf["H"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
         buf["aws"] = block.workspace(tp.tp_attn_workspace_bytes(dt, w.B, w.S, h, w.H, w.d, N), dev)
-        if w.kind == "layer":
-            buf["dH"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
-            buf["dWqkv"] = torch.empty_like(d["Wqkv"])
-            buf["dWo"] = torch.empty_like(d["Wo"])
-            buf["dXa"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+    if w.kind == "layer":
+        p = {k: d[k] for k in ("Wqkv", "Wo", "W1s", "W2s")}
+        buf["save"] = block.workspace(tp.tp_attn_mlp_save_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
+        buf["lws"] = block.workspace(tp.tp_attn_mlp_workspace_bytes(dt, w.B, w.S, h, w.H, w.d, f, N), dev)
+        buf["Z"] = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        buf["grads"] = {"dX": torch.empty(T, h, dtype=torch.bfloat16, device=dev),
+                        **{"d" + k: torch.empty_like(v) for k, v in p.items()}}
 
     def step(X, dZ):
         if w.kind == "mlp":
@@ -551,14 +553,13 @@ def run_gpu(args, w) -> None:
             tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, w.causal, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"],
                            buf["LSE"], buf["H"], buf["aws"], stream)
             return buf["H"], None
-        tp.tp_attn_fwd(dt, w.B, w.S, h, w.H, w.d, N, True, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"], buf["LSE"],
-                       buf["H"], buf["aws"], stream)
-        tp.tp_mlp_fwd(dt, T, h, f, N, buf["H"], d["W1s"], d["W2s"], buf["Y"], buf["A"], buf["Z"], buf["mws"], stream)
-        tp.tp_mlp_bwd(dt, T, h, f, N, buf["H"], d["W1s"], d["W2s"], buf["Y"], buf["A"], dZ, buf["dH"], buf["dW1s"],
-                      buf["dW2s"], buf["mws"], stream)
-        tp.tp_attn_bwd(dt, w.B, w.S, h, w.H, w.d, N, True, X, d["Wqkv"], d["Wo"], buf["QKV"], buf["O"], buf["LSE"],
-                       buf["dH"], buf["dXa"], buf["dWqkv"], buf["dWo"], buf["aws"], stream)
-        return buf["Z"], buf["dXa"]
+        gr = buf["grads"]
+        tp.tp_attn_mlp_fwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, X, p["Wqkv"], p["Wo"], p["W1s"], p["W2s"],
+                           buf["save"], buf["Z"], stream)
+        tp.tp_attn_mlp_bwd(dt, w.B, w.S, h, w.H, w.d, f, N, True, X, p["Wqkv"], p["Wo"], p["W1s"], p["W2s"],
+                           buf["save"], dZ, gr["dX"], gr["dWqkv"], gr["dWo"], gr["dW1s"], gr["dW2s"], buf["lws"],
+                           stream)
+        return buf["Z"], gr["dX"]
 
     # L2: flush between steps unless one step's working set is far above L2
     work_bytes = sum(t.numel() * t.element_size() for t in list(d.values()) + list(buf.values())
@@ -662,15 +663,13 @@ def run_gpu(args, w) -> None:
         zkey = "H" if w.kind == "attn" else "Z"
 
         def dx_get():
-            if w.kind in ("lnlayer", "splayer"):
+            if w.kind in ("lnlayer", "splayer", "layer"):
                 return buf["grads"]["dX"]
-            return buf["dXa"] if w.kind == "layer" else buf.get("dX")
+            return buf.get("dX")
 
         def dx_set(t):
-            if w.kind in ("lnlayer", "splayer"):
+            if w.kind in ("lnlayer", "splayer", "layer"):
                 buf["grads"]["dX"] = t
-            elif w.kind == "layer":
-                buf["dXa"] = t
             else:
                 buf["dX"] = t
 

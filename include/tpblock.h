@@ -202,14 +202,15 @@ TP_API size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h
  *  by columns so each shard owns whole heads, W_O split by rows, one all-reduce;
  *  wangyu.me 张量并行 §注意力机制中的张量并行.)
  *   QKV_i = X Wqkv_i                       -> QKV_save [N][T][3][H/N][d] (or ws): planes
- *                                             Q, K, V; Q and K are stored as fp16 (11
- *                                             significant bits, so that the scores
- *                                             Q K^T, which the softmax exponentiates,
- *                                             carry about 2^-11 relative error instead
- *                                             of bf16's 2^-8; |Q|, |K| entries above
- *                                             65504 overflow), V as bf16
- *   O_j   = softmax(mask(Q_j K_j^T / sqrt(d))) V_j, per batch and head j
- *                                          -> O_save [N][T][(H/N)*d] (or ws)
+ *                                             Q, K, V, stored as fp16 (11 significant
+ *                                             bits, so that the scores Q K^T, which the
+ *                                             softmax exponentiates, carry about 2^-11
+ *                                             relative error instead of bf16's 2^-8,
+ *                                             and P V is an fp16 product; entries
+ *                                             above 65504 overflow)
+ *   O_j   = softmax(mask(Q_j K_j^T / sqrt(d))) V_j, per batch and head j; the
+ *           probabilities enter P V as fp16
+ *                                          -> O_save [N][T][(H/N)*d] (or ws), bf16
  *   LSE   = log sum_k exp(Q_j K_j^T/sqrt(d)) per query -> LSE_save [B][H][S] fp32 (or ws)
  *   Z     = sum_i O_i Wo_i                 -> Z [T][h], shard sum on the device
  * X is [B*S][h] (token t = b*S + s).  causal != 0 masks keys after the query. */
@@ -225,8 +226,9 @@ TP_API int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  *   per head: D = rowsum(dO * O), P = exp(S/sqrt(d) - LSE), dV = P^T dO,
  *             dP = dO V^T, dS = P * (dP - D), dQ = dS K / sqrt(d), dK = dS^T Q / sqrt(d)
  *   dWqkv_i = X^T dQKV_i,  dX = sum_i dQKV_i Wqkv_i^T (shard sum on the device)
- *   (dQKV [N][T][3][H/N][d], all bf16, lives in ws; P is recomputed from the
- *   saved fp16 Q, K and LSE)
+ *   (dQKV [N][T][3][H/N][d], all bf16, lives in ws, and so does dO, stored as
+ *   fp16: every product of the core is fp16; P is recomputed from the saved fp16
+ *   Q, K and LSE)
  * QKV_save, O_save, LSE_save are what tp_attn_fwd wrote for the same inputs. */
 TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal,
                 const void* X, const void* Wqkv, const void* Wo,
@@ -247,7 +249,7 @@ TP_API int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d,
  *   Wqkv     [N][h][(H/N + 2 Hkv/N) d]   shard i: its query heads, then its key
  *                                        heads, then its value heads, d columns each
  *   Wo       [N][(H/N) d][h]             as tp_attn_fwd
- *   QKV_save [N][T][(H/N + 2 Hkv/N) d]   Q, K (fp16), V (bf16) as tp_attn_fwd
+ *   QKV_save [N][T][(H/N + 2 Hkv/N) d]   Q, K, V (fp16) as tp_attn_fwd
  *   O_save, LSE_save, Z, dX, dWo         as tp_attn_fwd / tp_attn_bwd
  *   dWqkv    Wqkv's layout; a key/value head's gradient sums its group's query heads */
 TP_API size_t tp_gqa_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N);
@@ -260,6 +262,45 @@ TP_API int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv
                       const void* QKV_save, const void* O_save, const float* LSE_save,
                       const void* dZ, void* dX, void* dWqkv, void* dWo,
                       void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------ attention block then MLP block (layer) */
+
+/* Bytes of the ``save`` buffer tp_attn_mlp_fwd fills and tp_attn_mlp_bwd reads, and
+ * of tp_attn_mlp_bwd's scratch.  0 for invalid sizes (the attention rules and the
+ * MLP rules above apply, with T = B*S). */
+TP_API size_t tp_attn_mlp_save_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N);
+TP_API size_t tp_attn_mlp_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f,
+                                          int N);
+
+/* Transformer layer forward (bf16 inputs, weights and output): the attention
+ * block, then the MLP block on its output, Z = MLP(Attn(X)).  The pages put the
+ * two tensor-parallel blocks one after the other and keep LayerNorm, dropout and
+ * the residuals outside them (io.zouht.com 张量并行 §2.2.2; damodev 3D并行 §1.2.1
+ * and §1.2.2); this call is the two blocks alone.  Attn and MLP compute what
+ * tp_attn_fwd and tp_mlp_fwd compute, with one difference in storage: the
+ * attention output H, the MLP's input, is kept in fp16 instead of bf16, and so is
+ * O.  The MLP's GeLU' is steep where its pre-activations cross zero, so an error
+ * in H reaches the backward's dY amplified; fp16's 11 significant bits keep it an
+ * eighth of bf16's.  The products with an fp16 operand (O Wo, H W1) take fp16
+ * copies of Wo and W1s that this call makes in ``save`` (exact for weights of
+ * magnitude 2^-17 .. 65504; smaller ones round to a multiple of 2^-24).
+ * ``save`` (256-byte aligned, tp_attn_mlp_save_bytes) receives QKV, O, LSE, the
+ * fp16 weight copies, H, Y and A; its layout is private to the library. */
+TP_API int tp_attn_mlp_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N,
+                           int causal, const void* X, const void* Wqkv, const void* Wo,
+                           const void* W1s, const void* W2s, void* save, size_t save_bytes,
+                           void* Z, void* stream);
+
+/* The layer's backward for an upstream dZ: the MLP block's backward on H (dY and
+ * dH kept in fp16), then the attention block's backward with upstream dH.  Every
+ * gradient is written: dX [T][h], dWqkv, dWo, dW1s, dW2s in the forward's layouts
+ * (bf16).  ``save`` is what tp_attn_mlp_fwd wrote for the same inputs; ws:
+ * tp_attn_mlp_workspace_bytes. */
+TP_API int tp_attn_mlp_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N,
+                           int causal, const void* X, const void* Wqkv, const void* Wo,
+                           const void* W1s, const void* W2s, const void* save, size_t save_bytes,
+                           const void* dZ, void* dX, void* dWqkv, void* dWo, void* dW1s, void* dW2s,
+                           void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------ LayerNorm and residuals */
 

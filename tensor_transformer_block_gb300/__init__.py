@@ -9,7 +9,8 @@ that allocates outputs with torch (``block``), and the seeded synthetic inputs
 """
 from ._binding import (  # noqa: F401
     HEADER_PATH, LIB_PATH, QKV_PLANES, STATUS, TP_BF16, TP_F32, TPError, header_functions, load_library,
-    tp_attn_bwd, tp_attn_fwd, tp_attn_workspace_bytes, tp_debug_timeout_probe, tp_device_check,
+    tp_attn_bwd, tp_attn_fwd, tp_attn_mlp_bwd, tp_attn_mlp_fwd, tp_attn_mlp_save_bytes, tp_attn_mlp_workspace_bytes,
+    tp_attn_workspace_bytes, tp_debug_timeout_probe, tp_device_check,
     tp_gmlp_bwd, tp_gmlp_fwd, tp_gmlp_workspace_bytes, tp_gqa_bwd, tp_gqa_fwd, tp_gqa_workspace_bytes, tp_layer_bwd, tp_layer_fwd, tp_layer_save_bytes,
     tp_layer_workspace_bytes, tp_layernorm_bwd, tp_layernorm_fwd, tp_layernorm_workspace_bytes,
     tp_mlp_bwd, tp_mlp_fwd, tp_mlp_fwd_noalloc,

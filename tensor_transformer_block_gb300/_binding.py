@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(HERE, "libtpblock.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "tpblock.h")
 
 TP_F32, TP_BF16 = 0, 1
-QKV_PLANES = 3  # Q (fp16), K (fp16), V (bf16) per (token, head)
+QKV_PLANES = 3  # Q, K, V (fp16 values in 16-bit storage) per (token, head)
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_WORKSPACE",
           5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE"}
 _TORCH_DT = {TP_F32: torch.float32, TP_BF16: torch.bfloat16}
@@ -58,6 +58,11 @@ _SIGS = {
                      i32),
     "tp_sp_layer_fwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32, ctypes.c_float] + [vp] * 10 + [sz, vp, vp], i32),
     "tp_sp_layer_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 8 + [sz] + [vp] * 10 + [vp, sz, vp],
+                        i32),
+    "tp_attn_mlp_save_bytes": ([i32, i64, i64, i64, i32, i32, i64, i32], sz),
+    "tp_attn_mlp_workspace_bytes": ([i32, i64, i64, i64, i32, i32, i64, i32], sz),
+    "tp_attn_mlp_fwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 6 + [sz, vp, vp], i32),
+    "tp_attn_mlp_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 6 + [sz] + [vp] * 6 + [vp, sz, vp],
                         i32),
     "tp_set_gemm_tiling": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
@@ -374,6 +379,40 @@ def tp_attn_bwd(dtype, B, S, h, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, 
         _p(O_save, "O_save", dt, T * H * d), _p(LSE_save, "LSE_save", torch.float32, T * H),
         _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h), _p(dWqkv, "dWqkv", dt, h * 3 * H * d),
         _p(dWo, "dWo", dt, H * d * h), wptr, wbytes, _stream(stream)), "tp_attn_bwd")
+
+
+# ---------------------------------------------------------------- attention block then MLP block
+def tp_attn_mlp_save_bytes(dtype, B, S, h, H, d, f, N) -> int:
+    return load_library().tp_attn_mlp_save_bytes(dtype, B, S, h, H, d, f, N)
+
+
+def tp_attn_mlp_workspace_bytes(dtype, B, S, h, H, d, f, N) -> int:
+    return load_library().tp_attn_mlp_workspace_bytes(dtype, B, S, h, H, d, f, N)
+
+
+def tp_attn_mlp_fwd(dtype, B, S, h, H, d, f, N, causal, X, Wqkv, Wo, W1s, W2s, save, Z, stream=None) -> int:
+    """Z = MLP(Attn(X)); ``save`` receives what the backward needs."""
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    sptr, sbytes = _ws(save, tp_attn_mlp_save_bytes(dtype, B, S, h, H, d, f, N))
+    return _check(load_library().tp_attn_mlp_fwd(
+        dtype, B, S, h, H, d, f, N, 1 if causal else 0, _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, 3 * h * H * d),
+        _p(Wo, "Wo", dt, H * d * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h), sptr, sbytes,
+        _p(Z, "Z", dt, T * h), _stream(stream)), "tp_attn_mlp_fwd")
+
+
+def tp_attn_mlp_bwd(dtype, B, S, h, H, d, f, N, causal, X, Wqkv, Wo, W1s, W2s, save, dZ, dX, dWqkv, dWo, dW1s, dW2s,
+                    ws=None, stream=None) -> int:
+    dt = _TORCH_DT.get(dtype)
+    T = B * S
+    sptr, sbytes = _ws(save, tp_attn_mlp_save_bytes(dtype, B, S, h, H, d, f, N))
+    wptr, wbytes = _ws(ws, tp_attn_mlp_workspace_bytes(dtype, B, S, h, H, d, f, N))
+    return _check(load_library().tp_attn_mlp_bwd(
+        dtype, B, S, h, H, d, f, N, 1 if causal else 0, _p(X, "X", dt, T * h), _p(Wqkv, "Wqkv", dt, 3 * h * H * d),
+        _p(Wo, "Wo", dt, H * d * h), _p(W1s, "W1s", dt, h * f), _p(W2s, "W2s", dt, f * h), sptr, sbytes,
+        _p(dZ, "dZ", dt, T * h), _p(dX, "dX", dt, T * h), _p(dWqkv, "dWqkv", dt, 3 * h * H * d),
+        _p(dWo, "dWo", dt, H * d * h), _p(dW1s, "dW1s", dt, h * f), _p(dW2s, "dW2s", dt, f * h), wptr, wbytes,
+        _stream(stream)), "tp_attn_mlp_bwd")
 
 
 def tp_set_gemm_tiling(mode: int) -> int:

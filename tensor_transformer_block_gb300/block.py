@@ -220,3 +220,34 @@ def prenorm_layer_backward(X, p: dict, save, dZ, B_: int, S: int, causal: bool =
        out["dX"], out["dln1_g"], out["dln1_b"], out["dWqkv"], out["dWo"], out["dln2_g"], out["dln2_b"], out["dW1s"],
        out["dW2s"], ws, stream)
     return out
+
+
+def attn_mlp_forward(X, p: dict, B_: int, S: int, causal: bool = True, save=None, stream=None) -> dict:
+    """Z = MLP(Attn(X)): the attention block then the MLP block in one call (the
+    attention output stays in the library's save buffer, in fp16).  ``p`` holds
+    Wqkv, Wo, W1s, W2s; the returned ``save`` buffer feeds the backward."""
+    N, h, _, hN, d = p["Wqkv"].shape
+    H = N * hN
+    f = N * p["W1s"].shape[2]
+    dt = _dtype(X)
+    if save is None:
+        save = workspace(B.tp_attn_mlp_save_bytes(dt, B_, S, h, H, d, f, N), X.device)
+    Z = torch.empty_like(X)
+    B.tp_attn_mlp_fwd(dt, B_, S, h, H, d, f, N, causal, X, p["Wqkv"], p["Wo"], p["W1s"], p["W2s"], save, Z, stream)
+    return {"Z": Z, "save": save}
+
+
+def attn_mlp_backward(X, p: dict, save, dZ, B_: int, S: int, causal: bool = True, ws=None, stream=None,
+                      out=None) -> dict:
+    N, h, _, hN, d = p["Wqkv"].shape
+    H = N * hN
+    f = N * p["W1s"].shape[2]
+    dt = _dtype(X)
+    if out is None:
+        out = {"dX": torch.empty_like(X), "dWqkv": torch.empty_like(p["Wqkv"]), "dWo": torch.empty_like(p["Wo"]),
+               "dW1s": torch.empty_like(p["W1s"]), "dW2s": torch.empty_like(p["W2s"])}
+    if ws is None:
+        ws = workspace(B.tp_attn_mlp_workspace_bytes(dt, B_, S, h, H, d, f, N), X.device)
+    B.tp_attn_mlp_bwd(dt, B_, S, h, H, d, f, N, causal, X, p["Wqkv"], p["Wo"], p["W1s"], p["W2s"], save, dZ,
+                      out["dX"], out["dWqkv"], out["dWo"], out["dW1s"], out["dW2s"], ws, stream)
+    return out

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtpblock.so")
 
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "attn_fwd.cu", "attn_bwd.cu", "layernorm.cu", "host_util.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_simt.cu", "attn_fwd.cu", "attn_bwd.cu", "layernorm.cu", "host_util.cu", "cast.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

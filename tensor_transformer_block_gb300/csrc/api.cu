@@ -9,6 +9,7 @@
 
 #include "../../include/tpblock.h"
 #include "attn.cuh"
+#include "cast.cuh"
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
 #include "host_util.cuh"
@@ -180,16 +181,20 @@ int tp_debug_timeout_probe(int64_t timeout_ns, void* stream) {
 
 namespace {
 // bf16 MLP forward kernels: a1 then a2.  With ``residual`` (a [T][h] tensor) the
-// row-parallel GEMM's epilogue adds it: Z = residual + sum_i A_i W2_i.
+// row-parallel GEMM's epilogue adds it: Z = residual + sum_i A_i W2_i.  With
+// ``W1_16`` (an fp16 copy of W1s) X holds fp16 values and a1 is an fp16 product.
 int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
-                void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st, Sp sp = Sp()) {
+                void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st, Sp sp = Sp(),
+                const void* W1_16 = nullptr) {
   const int64_t fN = f / N;
   // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard; with
   // sequence-sharded X the copies gather the shards: the pages' all-gather g)
   const tpb::GemmOperand opX = with_sp(tpb::GemmOperand{X, h, T, 1, false, 0, 0}, sp);
-  const tpb::GemmOperand opW1{W1s, fN, h, N, true, 1, 0};
+  const tpb::GemmOperand opW1{W1_16 ? W1_16 : W1s, fN, h, N, true, 1, 0};
+  tpb::GemmExtra e1;
+  e1.ab_f16 = W1_16 != nullptr;
   int rc = tpb::launch_gemm_bf16(tpb::kEpiGelu, opX, opW1, Abuf, Y_save, Y_save != nullptr, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKMlpFc1);
+                                 kWaitTimeoutNs, st, tpb::kKMlpFc1, e1);
   if (rc) return gemm_status(rc);
   // a2: Z = sum_i A_i W2_i   (row-parallel, shards reduced in the accumulator, order 0..N-1)
   const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
@@ -207,17 +212,24 @@ tpb::AttnDims attn_dims(int64_t B, int64_t S, int H, int Hkv, int d, int N, int 
 
 // bf16 MLP backward kernels a3..a6 (dY in ``dY``, an activation-sized scratch).
 // With sequence-sharded X, dZ and dX (``sp``) the GEMMs read and write those
-// tensors in their shards.
+// tensors in their shards.  With ``W1_16`` (an fp16 copy of W1s; X then holds
+// fp16 values) dY is stored in fp16, dW1 and dX are fp16 products and dX is
+// written in fp16.
 int mlp_bwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
                 const void* Y_save, const void* A_save, const void* dZ, void* dX, void* dW1s, void* dW2s, void* dY,
-                unsigned* err, cudaStream_t st, Sp sp) {
+                unsigned* err, cudaStream_t st, Sp sp, const void* W1_16 = nullptr) {
   const int64_t fN = f / N;
+  const bool h16 = W1_16 != nullptr;
+  tpb::GemmExtra e16;
+  e16.ab_f16 = h16;
 
   // a3: dY_i = (dZ W2_i^T) * GeLU'(Y_i)   (the row-split backward needs no reduction)
   const tpb::GemmOperand opdZk = with_sp(tpb::GemmOperand{dZ, h, T, 1, false, 0, 0}, sp);
   const tpb::GemmOperand opW2k{W2s, h, fN, N, false, 1, 0};
+  tpb::GemmExtra e3;
+  e3.c_f16 = h16;
   int rc = tpb::launch_gemm_bf16(tpb::kEpiDGelu, opdZk, opW2k, dY, Y_save, false, T, fN, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKMlpDgelu);
+                                 kWaitTimeoutNs, st, tpb::kKMlpDgelu, e3);
   if (rc) return gemm_status(rc);
   // a4: dW2_i = A_i^T dZ
   const tpb::GemmOperand opAt{A_save, fN, T, N, true, 1, 0};
@@ -229,30 +241,38 @@ int mlp_bwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const voi
   const tpb::GemmOperand opXt = with_sp(tpb::GemmOperand{X, h, T, 1, true, 0, 0}, sp);
   const tpb::GemmOperand opdYn{dY, fN, T, N, true, 1, 0};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdYn, dW1s, nullptr, false, h, fN, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKMlpDw1);
+                             st, tpb::kKMlpDw1, e16);
   if (rc) return gemm_status(rc);
   // a6: dX = sum_i dY_i W1_i^T   (the column split's backward all-reduce, done in the accumulator)
   const tpb::GemmOperand opdYk{dY, fN, T, N, false, 0, 1};
-  const tpb::GemmOperand opW1k{W1s, fN, h, N, false, 0, 1};
+  const tpb::GemmOperand opW1k{h16 ? W1_16 : W1s, fN, h, N, false, 0, 1};
+  tpb::GemmExtra e6 = out_sp(sp);
+  e6.ab_f16 = h16;
+  e6.c_f16 = h16;
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
-                             st, tpb::kKMlpDx, out_sp(sp));
+                             st, tpb::kKMlpDx, e6);
   return gemm_status(rc);
 }
 
 
 // Attention forward kernels: a7, a8, a9 (H query heads, Hkv key/value heads).
 // With ``residual`` ([T][h]) the output projection's epilogue adds it:
-// Z = residual + sum_i O_i Wo_i.
+// Z = residual + sum_i O_i Wo_i.  With ``Wo16`` (an fp16 copy of Wo) O is stored
+// in fp16 and a9 is an fp16 product; ``z_f16`` writes Z in fp16.  With ``Wqkv16``
+// (an fp16 copy of Wqkv) X holds fp16 values and a7 is an fp16 product.
 int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
                  const void* Wqkv, const void* Wo, void* QKV, void* Ob, float* LSE, void* Z, const void* residual,
-                 unsigned* err, cudaStream_t st, Sp sp = Sp()) {
-  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+                 unsigned* err, cudaStream_t st, Sp sp = Sp(), const void* Wo16 = nullptr, bool z_f16 = false,
+                 const void* Wqkv16 = nullptr) {
+  tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+  ad.o_f16 = Wo16 != nullptr;
   const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, kvd = static_cast<int64_t>(ad.hkvN) * d;
-  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); Q and K stored fp16
+  // a7: [Q_i K_i V_i] = X Wqkv_i  (column-parallel by head); Q, K and V stored fp16
   const tpb::GemmOperand opX = with_sp(tpb::GemmOperand{X, h, T, 1, false, 0, 0}, sp);
-  const tpb::GemmOperand opW{Wqkv, hNd + 2 * kvd, h, N, true, 1, 0};
+  const tpb::GemmOperand opW{Wqkv16 ? Wqkv16 : Wqkv, hNd + 2 * kvd, h, N, true, 1, 0};
   tpb::GemmExtra split;
-  split.split_cols = hNd + kvd;
+  split.split_cols = hNd + 2 * kvd;
+  split.ab_f16 = Wqkv16 != nullptr;
   int rc = tpb::launch_gemm_bf16(tpb::kEpiSplit, opX, opW, QKV, nullptr, false, T, hNd + 2 * kvd, N, 1, h, err,
                                  kWaitTimeoutNs, st, tpb::kKAttnQkv, split);
   if (rc) return gemm_status(rc);
@@ -261,35 +281,50 @@ int attn_fwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
   if (rc) return gemm_status(rc);
   // a9: Z = sum_i O_i Wo_i  (row-parallel, shard sum in the accumulator)
   const tpb::GemmOperand opO{Ob, hNd, T, N, false, 0, 1};
-  const tpb::GemmOperand opWo{Wo, h, hNd, N, true, 0, 1};
+  const tpb::GemmOperand opWo{Wo16 ? Wo16 : Wo, h, hNd, N, true, 0, 1};
+  tpb::GemmExtra e9 = out_sp(sp);
+  e9.ab_f16 = Wo16 != nullptr;
+  e9.c_f16 = z_f16;
   rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opO, opWo, Z, residual, false, T, h, 1,
-                             N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut, out_sp(sp));
+                             N, hNd, err, kWaitTimeoutNs, st, tpb::kKAttnOut, e9);
   return gemm_status(rc);
 }
 // Attention backward kernels (scratch [dQKV | dO | Dsum] carved from ``wsb`` per
 // ``w``).  With sequence-sharded X, dZ and dX (``sp``) the GEMMs read and write
-// those tensors in their shards.
+// those tensors in their shards.  With ``Wo16`` (the fp16 copy of Wo the forward
+// used) O and dZ hold fp16 values and dO, dWo are fp16 products.  With
+// ``Wqkv16`` (the fp16 copy of Wqkv) X holds fp16 values: dQKV is stored in fp16,
+// dWqkv and dX are fp16 products and dX is written in fp16.
 int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
                  const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
                  const void* dZ, void* dX, void* dWqkv, void* dWo, char* wsb, const AttnWs& w, unsigned* err,
-                 cudaStream_t st, Sp sp) {
-  const tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+                 cudaStream_t st, Sp sp, const void* Wo16 = nullptr, const void* Wqkv16 = nullptr) {
+  tpb::AttnDims ad = attn_dims(B, S, H, Hkv, d, N, causal);
+  ad.o_f16 = Wo16 != nullptr;
+  ad.dqkv_f16 = Wqkv16 != nullptr;
+  tpb::GemmExtra eq;  // the products with X or Wqkv
+  eq.ab_f16 = Wqkv16 != nullptr;
   const int64_t T = B * S, hNd = static_cast<int64_t>(ad.hN) * d, gw = ad.dqkv_width();
   void* dQKV = wsb;
   void* dO = wsb + w.qkv;
   float* dsum = reinterpret_cast<float*>(wsb + w.qkv + w.o);
 
-  // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ)
+  // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ); fp16
   const tpb::GemmOperand opdZk = with_sp(tpb::GemmOperand{dZ, h, T, 1, false, 0, 0}, sp);
-  const tpb::GemmOperand opWok{Wo, h, hNd, N, false, 1, 0};
+  const tpb::GemmOperand opWok{Wo16 ? Wo16 : Wo, h, hNd, N, false, 1, 0};
+  tpb::GemmExtra edo;
+  edo.ab_f16 = Wo16 != nullptr;
+  edo.c_f16 = true;
   int rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdZk, opWok, dO, nullptr, false, T, hNd, N, 1, h, err,
-                                 kWaitTimeoutNs, st, tpb::kKAttnDo);
+                                 kWaitTimeoutNs, st, tpb::kKAttnDo, edo);
   if (rc) return gemm_status(rc);
   // dWo_i = O_i^T dZ
   const tpb::GemmOperand opOt{O_save, hNd, T, N, true, 1, 0};
   const tpb::GemmOperand opdZn = with_sp(tpb::GemmOperand{dZ, h, T, 1, true, 0, 0}, sp);
+  tpb::GemmExtra ewo;
+  ewo.ab_f16 = Wo16 != nullptr;
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opOt, opdZn, dWo, nullptr, false, hNd, h, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKAttnDwo);
+                             st, tpb::kKAttnDwo, ewo);
   if (rc) return gemm_status(rc);
   // attention core backward -> dQKV
   rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
@@ -298,13 +333,16 @@ int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
   const tpb::GemmOperand opXt = with_sp(tpb::GemmOperand{X, h, T, 1, true, 0, 0}, sp);
   const tpb::GemmOperand opdQn{dQKV, gw, T, N, true, 1, 0};
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opXt, opdQn, dWqkv, nullptr, false, h, gw, N, 1, T, err, kWaitTimeoutNs,
-                             st, tpb::kKAttnDwqkv);
+                             st, tpb::kKAttnDwqkv, eq);
   if (rc) return gemm_status(rc);
   // dX = sum_i dQKV_i Wqkv_i^T  (the column split's backward all-reduce, in the accumulator)
   const tpb::GemmOperand opdQk{dQKV, gw, T, N, false, 0, 1};
-  const tpb::GemmOperand opWk{Wqkv, gw, h, N, false, 0, 1};
+  const tpb::GemmOperand opWk{Wqkv16 ? Wqkv16 : Wqkv, gw, h, N, false, 0, 1};
+  tpb::GemmExtra edx = out_sp(sp);
+  edx.ab_f16 = eq.ab_f16;
+  edx.c_f16 = eq.ab_f16;
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdQk, opWk, dX, nullptr, false, T, h, 1, N, gw, err, kWaitTimeoutNs, st,
-                             tpb::kKAttnDx, out_sp(sp));
+                             tpb::kKAttnDx, edx);
   return gemm_status(rc);
 }
 
@@ -560,18 +598,141 @@ int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
 
 }  // extern "C"
 
+// ------------------------------------------- attention block then MLP block
+namespace {
+// The saved tensors of tp_attn_mlp_fwd, carved from the caller's ``save`` buffer
+// in this order (each region 256-byte aligned): the attention block's QKV (fp16),
+// O (fp16) and LSE; the fp16 copy of Wo; the block output H (fp16), which is the
+// MLP's input; the fp16 copy of W1s; the MLP's Y and A (bf16).
+struct AmSave {
+  size_t qkv, o, lse, wo16, h16, w1_16, y, a, total;
+};
+AmSave am_save(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
+  const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  const AttnWs aw = attn_ws(B, S, H, H, d);
+  const size_t hs = static_cast<size_t>(h), fs = static_cast<size_t>(f), hd = static_cast<size_t>(H) * d;
+  AmSave L;
+  size_t o = 0;
+  L.qkv = o;   o += aw.qkv;
+  L.o = o;     o += aw.o;
+  L.lse = o;   o += aw.lse;
+  L.wo16 = o;  o += round_up(hd * hs * 2, 256);
+  L.h16 = o;   o += round_up(T * hs * 2, 256);
+  L.w1_16 = o; o += round_up(hs * fs * 2, 256);
+  L.y = o;     o += round_up(T * fs * 2, 256);
+  L.a = o;     o += round_up(T * fs * 2, 256);
+  L.total = o;
+  return L;
+}
+// Backward scratch: [block scratch (the MLP's dY, then the attention block's
+// dQKV | dO | Dsum) | dH (fp16)].
+struct AmWs {
+  size_t blk, dh, total;
+};
+AmWs am_ws(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
+  const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  const size_t a = attn_ws(B, S, H, H, d).total, m = round_up(T * static_cast<size_t>(f) * 2, 256);
+  AmWs w;
+  w.blk = 0;
+  w.dh = a > m ? a : m;
+  w.total = w.dh + round_up(T * static_cast<size_t>(h) * 2, 256);
+  return w;
+}
+int am_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  const int c = attn_shape_check(dtype, B, S, h, H, H, d, N);
+  return c != TP_OK ? c : mlp_shape_check(dtype, B * S, h, f, N);
+}
+}  // namespace
+
+extern "C" {
+
+size_t tp_attn_mlp_save_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  if (am_check(dtype, B, S, h, H, d, f, N) != TP_OK) return 0;
+  return am_save(B, S, h, H, d, f).total;
+}
+
+size_t tp_attn_mlp_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
+  if (am_check(dtype, B, S, h, H, d, f, N) != TP_OK) return 0;
+  return am_ws(B, S, h, H, d, f).total;
+}
+
+int tp_attn_mlp_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                    const void* X, const void* Wqkv, const void* Wo, const void* W1s, const void* W2s, void* save,
+                    size_t save_bytes, void* Z, void* stream) {
+  const int sc = am_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wqkv || !Wo || !W1s || !W2s || !save || !Z) return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(W1s) || !al16(W2s) || !al16(Z)) return TP_ERR_ALIGN;
+  const AmSave L = am_save(B, S, h, H, d, f);
+  if (save_bytes < L.total) return TP_ERR_WORKSPACE;
+  if (!al256(save)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* sv = static_cast<char*>(save);
+  // fp16 copies of the two weights whose other operand is an fp16 activation
+  int rc = tpb::launch_bf16_to_f16(Wo, sv + L.wo16, static_cast<long long>(H) * d * h, st);
+  if (rc) return gemm_status(rc);
+  rc = tpb::launch_bf16_to_f16(W1s, sv + L.w1_16, static_cast<long long>(h) * f, st);
+  if (rc) return gemm_status(rc);
+  // H = Attn(X), written in fp16
+  rc = attn_fwd_seq(B, S, h, H, H, d, N, causal, X, Wqkv, Wo, sv + L.qkv, sv + L.o,
+                    reinterpret_cast<float*>(sv + L.lse), sv + L.h16, nullptr, err, st, Sp(), sv + L.wo16, true);
+  if (rc) return rc;
+  // Z = MLP(H)
+  return mlp_fwd_seq(B * S, h, f, N, sv + L.h16, W1s, W2s, sv + L.y, sv + L.a, Z, nullptr, err, st, Sp(),
+                     sv + L.w1_16);
+}
+
+int tp_attn_mlp_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
+                    const void* X, const void* Wqkv, const void* Wo, const void* W1s, const void* W2s,
+                    const void* save, size_t save_bytes, const void* dZ, void* dX, void* dWqkv, void* dWo,
+                    void* dW1s, void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  const int sc = am_check(dtype, B, S, h, H, d, f, N);
+  if (sc != TP_OK) return sc;
+  if (!X || !Wqkv || !Wo || !W1s || !W2s || !save || !dZ || !dX || !dWqkv || !dWo || !dW1s || !dW2s)
+    return TP_ERR_NULL;
+  if (!al16(X) || !al16(Wqkv) || !al16(Wo) || !al16(W1s) || !al16(W2s) || !al16(dZ) || !al16(dX) || !al16(dWqkv) ||
+      !al16(dWo) || !al16(dW1s) || !al16(dW2s))
+    return TP_ERR_ALIGN;
+  const AmSave L = am_save(B, S, h, H, d, f);
+  const AmWs W = am_ws(B, S, h, H, d, f);
+  if (save_bytes < L.total || !ws || ws_bytes < W.total) return TP_ERR_WORKSPACE;
+  if (!al256(save) || !al256(ws)) return TP_ERR_ALIGN;
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
+  if (dc != TP_OK) return dc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const char* sv = static_cast<const char*>(save);
+  char* wb = static_cast<char*>(ws);
+  // MLP block backward on H: dH (fp16) and the MLP's weight gradients
+  int rc = mlp_bwd_seq(B * S, h, f, N, sv + L.h16, W1s, W2s, sv + L.y, sv + L.a, dZ, wb + W.dh, dW1s, dW2s,
+                       wb + W.blk, err, st, Sp(), sv + L.w1_16);
+  if (rc) return rc;
+  // attention block backward with upstream dH
+  return attn_bwd_seq(B, S, h, H, H, d, N, causal, X, Wqkv, Wo, sv + L.qkv, sv + L.o,
+                      reinterpret_cast<const float*>(sv + L.lse), wb + W.dh, dX, dWqkv, dWo, wb + W.blk,
+                      attn_ws(B, S, H, H, d), err, st, Sp(), sv + L.wo16);
+}
+
+}  // extern "C"
+
 // ------------------------------------------------------ LayerNorm + residual
 namespace {
 constexpr float kEpsMin = 0.0f;
 
 // The pre-norm layer's saved tensors, carved from the caller's ``save`` buffer in
-// this order (each region 256-byte aligned).
+// this order (each region 256-byte aligned): LN1(X) (fp16) and its statistics;
+// the attention block's QKV, O (fp16) and LSE; H1 (bf16); LN2(H1) (fp16) and its
+// statistics; the MLP's Y and A (bf16); the fp16 copies of Wqkv, Wo and W1s.
 struct LayerSave {
-  size_t ln1, mean1, rstd1, qkv, o, lse, h1, ln2, mean2, rstd2, y, a, total;
+  size_t ln1, mean1, rstd1, qkv, o, lse, h1, ln2, mean2, rstd2, y, a, wqkv16, wo16, w1_16, total;
 };
 LayerSave layer_save(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
   const size_t th = round_up(T * static_cast<size_t>(h) * 2, 256), tv = round_up(T * 4, 256);
+  const size_t hd = static_cast<size_t>(H) * static_cast<size_t>(d), hs = static_cast<size_t>(h);
   const AttnWs aw = attn_ws(B, S, H, H, d);
   LayerSave L;
   size_t o = 0;
@@ -587,6 +748,9 @@ LayerSave layer_save(int64_t B, int64_t S, int64_t h, int H, int d, int64_t f) {
   L.rstd2 = o; o += tv;
   L.y = o;     o += round_up(T * static_cast<size_t>(f) * 2, 256);
   L.a = o;     o += round_up(T * static_cast<size_t>(f) * 2, 256);
+  L.wqkv16 = o; o += round_up(hs * 3 * hd * 2, 256);
+  L.wo16 = o;   o += round_up(hd * hs * 2, 256);
+  L.w1_16 = o;  o += round_up(hs * static_cast<size_t>(f) * 2, 256);
   L.total = o;
   return L;
 }
@@ -692,18 +856,24 @@ int layer_fwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
   float* rstd1 = reinterpret_cast<float*>(sv + L.rstd1);
   float* mean2 = reinterpret_cast<float*>(sv + L.mean2);
   float* rstd2 = reinterpret_cast<float*>(sv + L.rstd2);
-  // LN1(X) (row by row, so in whatever row order X is stored)
-  int rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st);
+  // fp16 copies of the weights whose other operand is an fp16 activation
+  int rc = tpb::launch_bf16_to_f16(Wqkv, sv + L.wqkv16, static_cast<long long>(h) * 3 * H * d, st);
+  if (!rc) rc = tpb::launch_bf16_to_f16(Wo, sv + L.wo16, static_cast<long long>(H) * d * h, st);
+  if (!rc) rc = tpb::launch_bf16_to_f16(W1s, sv + L.w1_16, static_cast<long long>(h) * f, st);
+  if (rc) return gemm_status(rc);
+  // LN1(X) in fp16 (row by row, so in whatever row order X is stored)
+  rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st, tpb::kLnYF16);
   if (rc) return gemm_status(rc);
   // H1 = X + Attn(LN1(X)): the residual is added in the output projection's epilogue
   rc = attn_fwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
-                    reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st, sp);
+                    reinterpret_cast<float*>(sv + L.lse), sv + L.h1, X, err, st, sp, sv + L.wo16, false,
+                    sv + L.wqkv16);
   if (rc) return rc;
-  // LN2(H1)
-  rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st);
+  // LN2(H1) in fp16
+  rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st, tpb::kLnYF16);
   if (rc) return gemm_status(rc);
   // Z = H1 + MLP(LN2(H1)): the residual is added in the second GEMM's epilogue
-  return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st, sp);
+  return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st, sp, sv + L.w1_16);
 }
 
 int layer_bwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
@@ -734,22 +904,24 @@ int layer_bwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
   void* dLN = wb + W.dln;
   void* dH1 = wb + W.dh1;
   float* part = reinterpret_cast<float*>(wb + W.part);
-  // MLP block backward on LN2(H1): dLN2 -> dLN (dY in the block scratch)
+  // MLP block backward on LN2(H1): dLN2 -> dLN (fp16; dY in the block scratch)
   int rc = mlp_bwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, dZ, dLN, dW1s, dW2s, wb + W.blk, err, st,
-                       sp);
+                       sp, sv + L.w1_16);
   if (rc) return rc;
-  // dH1 = dZ + LN2'(dLN2)   (the residual passes dZ through)
+  // dH1 = dZ + LN2'(dLN2)   (the residual passes dZ through); fp16
   rc = tpb::launch_ln_bwd(sv + L.h1, ln2_g, reinterpret_cast<const float*>(sv + L.mean2),
-                          reinterpret_cast<const float*>(sv + L.rstd2), dLN, dZ, dH1, dln2_g, dln2_b, part, T, h, st);
+                          reinterpret_cast<const float*>(sv + L.rstd2), dLN, dZ, dH1, dln2_g, dln2_b, part, T, h, st,
+                          tpb::kLnDyF16 | tpb::kLnDxF16);
   if (rc) return gemm_status(rc);
-  // attention block backward on LN1(X) with upstream dH1: dLN1 -> dLN
+  // attention block backward on LN1(X) with upstream dH1: dLN1 -> dLN (fp16)
   rc = attn_bwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
                     reinterpret_cast<const float*>(sv + L.lse), dH1, dLN, dWqkv, dWo, wb + W.blk, attn_ws(B, S, H, H, d),
-                    err, st, sp);
+                    err, st, sp, sv + L.wo16, sv + L.wqkv16);
   if (rc) return rc;
   // dX = dH1 + LN1'(dLN1)
   rc = tpb::launch_ln_bwd(X, ln1_g, reinterpret_cast<const float*>(sv + L.mean1),
-                          reinterpret_cast<const float*>(sv + L.rstd1), dLN, dH1, dX, dln1_g, dln1_b, part, T, h, st);
+                          reinterpret_cast<const float*>(sv + L.rstd1), dLN, dH1, dX, dln1_g, dln1_b, part, T, h, st,
+                          tpb::kLnDyF16 | tpb::kLnDrF16);
   return gemm_status(rc);
 }
 

@@ -5,10 +5,11 @@
 // query head j uses key/value head j / (H/Hkv).  Per shard, hN = H/N query and
 // hkvN = Hkv/N key/value heads (io.zouht.com 张量并行 §2.2.1: each shard owns
 // whole heads; with GQA it owns whole groups):
-//   QKV  [N][B][S][W] with W = (hN + 2 hkvN) d: Q (hN heads) and K (hkvN) in fp16,
-//        V (hkvN) in bf16
-//   dQKV [N][B][S][W]: dQ, dK, dV (bf16)
-//   O    [N][B][S][hN][d]
+//   QKV  [N][B][S][W] with W = (hN + 2 hkvN) d: Q (hN heads), K and V (hkvN each),
+//        all fp16
+//   dQKV [N][B][S][W]: dQ, dK, dV (bf16, or fp16 with dqkv_f16)
+//   O    [N][B][S][hN][d]  bf16, or fp16 with o_f16
+//   dO   [N][B][S][hN][d]  fp16
 //   LSE  [B][H][S] fp32          natural-log sum of exp of the scaled scores
 // Global query head j lives in shard i = j / hN as local head jj = j % hN.
 //
@@ -16,7 +17,9 @@
 // exponentiates scores whose range reaches tens of units, where bf16 Q and K would
 // move the largest weights by several percent; fp16 puts the scores within ~2^-11
 // relative and the products Q K^T still run as single tensor-core MMAs (fp16 x
-// fp16, fp32 accumulation).  Entries of Q and K beyond +-65504 would overflow.
+// fp16, fp32 accumulation).  V, the probabilities P, dO and dS are fp16 too, so
+// that every product of the core is an fp16 MMA and the attention output carries
+// an eighth of bf16's rounding error.  Entries beyond +-65504 would overflow.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -28,6 +31,8 @@ namespace tpb {
 struct AttnDims {
   int B, S, H, hN, N, d, causal;
   int Hkv, hkvN;  // key/value heads in total and per shard (= H, hN without grouping)
+  int o_f16 = 0;     // O stored as fp16 (else bf16)
+  int dqkv_f16 = 0;  // dQ, dK, dV stored as fp16 (else bf16)
   // column offsets (elements) of local head jj (query) or kv (key/value) in QKV
   __host__ __device__ int qkv_width() const { return (hN + 2 * hkvN) * d; }
   __host__ __device__ int col_q(int jj) const { return jj * d; }

@@ -8,12 +8,14 @@
 //   dQ = dS K / sqrt(d)                         (k_attn_dq:   one CTA per query block)
 // Each CTA owns its output rows and loops over the blocks it needs, so results
 // are deterministic (no atomics).  P is recomputed from the saved LSE.  Blocks are
-// 128 x 128 (M=128, N=128 tensor-core products); Q, K and dS are fp16 (the fp16
-// products dS^T Q and dS K), P, V and dO bf16.  P and dS never leave TMEM: they are
+// 128 x 128 (M=128, N=128 tensor-core products); Q, K, V, P, dO and dS are fp16,
+// so every product is an fp16 MMA.  P and dS never leave TMEM: they are
 // written over the first halves of the score columns they come from and feed the
 // next products as the TMEM A operand.
 // Warp roles: warp 8 TMA, warp 9 MMA, warps 0-7 elementwise (warp w owns TMEM lanes
 // 32 (w % 4).. and the column half w / 4 of every 128-column block).
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 #include "attn.cuh"
@@ -32,7 +34,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 // one 16-byte vector of O and of dO, so a warp's loads are contiguous, and the
 // group adds its partial dot products with shuffles.  The loop runs whole warps
 // (a group past the last row adds zeros and stores nothing), so every shuffle
-// has all 32 lanes.
+// has all 32 lanes.  dO is fp16; O is fp16 or bf16 (a.o_f16).
+__device__ __forceinline__ float2 f16x2_to_f32(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+__device__ __forceinline__ float dot8(const uint4& x, const uint4& y, bool x_f16) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 yy = f16x2_to_f32(ys[i]);
+    const float2 xx = x_f16 ? f16x2_to_f32(xs[i]) : make_float2(bf16lo_to_f32(xs[i]), bf16hi_to_f32(xs[i]));
+    s = fmaf(xx.x, yy.x, s);
+    s = fmaf(xx.y, yy.y, s);
+  }
+  return s;
+}
 template <int D>
 __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict__ dout, float* __restrict__ dsum,
                             const AttnDims a) {
@@ -47,13 +64,7 @@ __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict
     const long long idx = w * (32 / LPR) + lane / LPR;  // this lane's row
     const bool valid = idx < total;
     float s = 0.0f;
-    if (valid) {
-      const uint4 x = o[idx * LPR + sub], y = dout[idx * LPR + sub];
-      s = bf16lo_to_f32(x.x) * bf16lo_to_f32(y.x) + bf16hi_to_f32(x.x) * bf16hi_to_f32(y.x);
-      s += bf16lo_to_f32(x.y) * bf16lo_to_f32(y.y) + bf16hi_to_f32(x.y) * bf16hi_to_f32(y.y);
-      s += bf16lo_to_f32(x.z) * bf16lo_to_f32(y.z) + bf16hi_to_f32(x.z) * bf16hi_to_f32(y.z);
-      s += bf16lo_to_f32(x.w) * bf16lo_to_f32(y.w) + bf16hi_to_f32(x.w) * bf16hi_to_f32(y.w);
-    }
+    if (valid) s = dot8(o[idx * LPR + sub], dout[idx * LPR + sub], a.o_f16 != 0);
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (valid && sub == 0) {
@@ -75,9 +86,11 @@ struct BwdCommon {
 };
 
 // Writes a warp's 32 accumulator rows x D columns (fp32 in TMEM, times ``mul``)
-// as bf16 into a staging area laid out as D/64 boxes of 32 x 64 (swizzled).
+// as bf16 (or f16: fp16) into a staging area laid out as D/64 boxes of 32 x 64
+// (swizzled).
 template <int D>
-__device__ __forceinline__ void stage_rows_from_tmem(uint32_t taddr, uint32_t stage, int lane, float mul) {
+__device__ __forceinline__ void stage_rows_from_tmem(uint32_t taddr, uint32_t stage, int lane, float mul, bool f16) {
+  auto pk2 = [f16](float x, float y) { return f16 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) {
     uint32_t v[32];
@@ -87,10 +100,10 @@ __device__ __forceinline__ void stage_rows_from_tmem(uint32_t taddr, uint32_t st
 #pragma unroll
     for (int g = 0; g < 4; ++g)
       st_shared_v4(stage + cb * 4096 + lane * 128 + (((g0 + g) ^ static_cast<uint32_t>(lane & 7)) << 4),
-                   pack_bf16x2(__uint_as_float(v[8 * g + 0]) * mul, __uint_as_float(v[8 * g + 1]) * mul),
-                   pack_bf16x2(__uint_as_float(v[8 * g + 2]) * mul, __uint_as_float(v[8 * g + 3]) * mul),
-                   pack_bf16x2(__uint_as_float(v[8 * g + 4]) * mul, __uint_as_float(v[8 * g + 5]) * mul),
-                   pack_bf16x2(__uint_as_float(v[8 * g + 6]) * mul, __uint_as_float(v[8 * g + 7]) * mul));
+                   pk2(__uint_as_float(v[8 * g + 0]) * mul, __uint_as_float(v[8 * g + 1]) * mul),
+                   pk2(__uint_as_float(v[8 * g + 2]) * mul, __uint_as_float(v[8 * g + 3]) * mul),
+                   pk2(__uint_as_float(v[8 * g + 4]) * mul, __uint_as_float(v[8 * g + 5]) * mul),
+                   pk2(__uint_as_float(v[8 * g + 6]) * mul, __uint_as_float(v[8 * g + 7]) * mul));
   }
 }
 
@@ -112,8 +125,8 @@ __device__ __forceinline__ uint32_t half_packed_col(int kk) {
 // ------------------------------------------------------------------ dK / dV
 // One CTA per (128-key block, key/value head, batch); loops over the query heads
 // of the head's group and, for each, over the 128-query blocks whose Q, dO tiles
-// and LSE / Dsum rows are double-buffered.  Per block: S^T = K Q^T (fp16) and
-// dP^T = V dO^T into TMEM; the elementwise warps turn them into P^T (bf16) and
+// and LSE / Dsum rows are double-buffered.  Per block: S^T = K Q^T and
+// dP^T = V dO^T into TMEM; the elementwise warps turn them into P^T (fp16) and
 // dS^T = P^T (dP^T - Dsum) (fp16) in place; dV += P^T dO and dK += dS^T Q with
 // A from TMEM.  Each product has its own barrier so that the elementwise phases
 // overlap the tensor core: P^T is computed while dP^T is, dS^T while dV is, and the
@@ -239,8 +252,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BLK, false, false);   // K Q^T
-      constexpr uint32_t ID_P = idesc_bf16(128, BLK, false, false);  // V dO^T
-      constexpr uint32_t ID_DV = idesc_bf16(128, D, false, true);    // P^T dO
+      constexpr uint32_t ID_P = idesc_f16(128, BLK, false, false);   // V dO^T
+      constexpr uint32_t ID_DV = idesc_f16(128, D, false, true);     // P^T dO
       constexpr uint32_t ID_DK = idesc_f16(128, D, false, true);     // dS^T Q
       auto s_mmas = [&](int st) {  // S^T = K Q^T
 #pragma unroll
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float4* ls4 = reinterpret_cast<const float4*>(lse_s + st * BLK + 64 * half);  // LSE * log2(e)
       const float4* ds4 = reinterpret_cast<const float4*>(dd_s + st * BLK + 64 * half);
       float p[64];
-      // P^T = exp(S^T / sqrt(d) - LSE), bf16, over the first half of these columns
+      // P^T = exp(S^T / sqrt(d) - LSE), fp16, over the first half of these columns
       {
         uint32_t v[2][32];
         tmem_ld32(tmem + trow + cS, v[0]);
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(p[2 * e], p[2 * e + 1]);
+        for (int e = 0; e < 32; ++e) pk[e] = pack_f16x2(p[2 * e], p[2 * e + 1]);
         tmem_st32(tmem + trow + cS, pk);
       }
       tmem_st_wait();
@@ -401,7 +414,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // all MMAs are complete: the Q/dO stages are free for staging (8 warps x CH x 4 KB)
       const uint32_t stage = cm.sb + C::OFF_Q + static_cast<uint32_t>((half * 4 + quad) * C::CH * 4096);
       if (nit > 0)
-        stage_rows_from_tmem<D>((half == 0 ? tDV : tDK) + trow, stage, lane, half == 0 ? 1.0f : scale);
+        stage_rows_from_tmem<D>((half == 0 ? tDV : tDK) + trow, stage, lane, half == 0 ? 1.0f : scale,
+                                a.dqkv_f16 != 0);
       else
         stage_zero_rows<D>(stage, lane);
       fence_proxy_async_smem();
@@ -538,7 +552,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 9) {
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_f16(128, BLK, false, false);   // Q K^T
-      constexpr uint32_t ID_P = idesc_bf16(128, BLK, false, false);  // dO V^T
+      constexpr uint32_t ID_P = idesc_f16(128, BLK, false, false);   // dO V^T
       constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);     // dS K
       auto s_mmas = [&](int st) {
 #pragma unroll
@@ -675,7 +689,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // all MMAs are complete: the Q tile is free for staging
       const uint32_t stQ = sQ + static_cast<uint32_t>(quad * C::CH * 4096);
       if (nkv > 0)
-        stage_rows_from_tmem<D>(trow + 256, stQ, lane, scale);
+        stage_rows_from_tmem<D>(trow + 256, stQ, lane, scale, a.dqkv_f16 != 0);
       else
         stage_zero_rows<D>(stQ, lane);
       fence_proxy_async_smem();
@@ -717,7 +731,7 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   const uint64_t od[4] = {static_cast<uint64_t>(a.hN) * D, S, Bb, Nn};
   const uint32_t box128[4] = {64, 128, 1, 1};
   const uint32_t box32[4] = {64, 32, 1, 1};
-  // 16-bit elements (fp16 Q, K; bf16 V, dO, dQKV): the copies do not interpret them
+  // 16-bit elements (fp16 Q, K, V, dO; O fp16 or bf16; bf16 dQKV): the copies do not interpret them
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_128B;
   if (!encode_tmap(&tq, bf, 4, qkv, qd, box128, sw) || !encode_tmap(&tdo, bf, 4, dout, od, box128, sw) ||

@@ -10,19 +10,20 @@
 // with two shared-memory stages so that the copies of block kv+1 overlap block kv.
 //   warp 8: TMA producer: both Q tiles once; K and V per key block
 //   warp 9: MMA issuer: per block, O_t += P_t V for both tiles (P read from TMEM,
-//           V from shared memory), then S_t = Q_t K^T of the next block for each
-//           tile once that tile's P V has read its P (fp16 Q and K, one MMA per
-//           16 of the head dim)
+//           V from shared memory; fp16 P and V), then S_t = Q_t K^T of the next
+//           block for each tile once that tile's P V has read its P (fp16 Q and K,
+//           one MMA per 16 of the head dim)
 //   warps 0-3 / 4-7: the softmax warpgroup of tile 0 / tile 1, one query row per
-//           thread: masked row max over the block, exp2, P (bf16) written back
+//           thread: masked row max over the block, exp2, P (fp16) written back
 //           over the first half of the same TMEM columns.  The running max is only
 //           moved (and the row of O rescaled in TMEM) when a block's max exceeds
 //           it by more than 8 (log2 units); otherwise the stale max stays,
 //           P <= 2^8, and the final O / l is unchanged because the max cancels.
 //           While one warpgroup works on its softmax the tensor core works on the
 //           other tile.
-// TMEM (512 columns): tile t's scores at 256 t (128 columns; P, 128 bf16 per row,
-// in the first 64 of them), its O at 256 t + 128.  A tile's P V has completed
+// TMEM (512 columns): tile t's scores at 256 t (128 columns; P, 128 fp16 per row,
+// in the first 64 of them), its O at 256 t + 128.  O is written out as fp16 or
+// bf16 (AttnDims::o_f16).  A tile's P V has completed
 // before the next block's scores overwrite its P, so O is never being accumulated
 // while the softmax warps read or rescale it.
 #include <cmath>
@@ -54,9 +55,9 @@ enum : int {
   B_DR = 15, NBARS = 16
 };
 
-// acc + lo + hi of a bf16 pair, each half widened exactly inside the add
-__device__ __forceinline__ float add_bf16x2_f32(float acc, uint32_t pk) {
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.f32.bf16 %0, lo, %0;\n\tadd.f32.bf16 %0, hi, %0;\n\t}"
+// acc + lo + hi of an fp16 pair, each half widened exactly inside the add
+__device__ __forceinline__ float add_f16x2_f32(float acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.f32.f16 %0, lo, %0;\n\tadd.f32.f16 %0, hi, %0;\n\t}"
       : "+f"(acc)
       : "r"(pk));
   return acc;
@@ -186,7 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t ID_S = idesc_f16(128, BKV, false, false);
-      constexpr uint32_t ID_PV = idesc_bf16(128, D, false, true);
+      constexpr uint32_t ID_PV = idesc_f16(128, D, false, true);
       bool ok = mbar_wait(bar(B_QF), 0, wc), any = false;
       // scores of key block 0 for every tile
       if (ok && nkv > 0) {
@@ -305,7 +306,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       const float m_use = (m == -INFINITY) ? 0.0f : m;
-      // P = exp2(s * scale - m) as bf16 (masked scores are -inf: exp2 gives 0),
+      // P = exp2(s * scale - m) as fp16 (masked scores are -inf: exp2 gives 0; P <= 2^8,
+      // and a P below fp16's normal range keeps an absolute error under 2^-25),
       // written over the first 64 of the columns just read
       float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -315,8 +317,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e]), scale_log2, -m_use));
           const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e + 1]), scale_log2, -m_use));
-          pk[e] = pack_bf16x2(p0, p1);
-          ls[e & 3] = add_bf16x2_f32(ls[e & 3], pk[e]);
+          pk[e] = pack_f16x2(p0, p1);
+          ls[e & 3] = add_f16x2_f32(ls[e & 3], pk[e]);
         }
         tmem_st16(tS + 16 * c, pk);
       }
@@ -346,6 +348,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // every MMA of this tile is complete: its Q buffer is free for staging O
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       const uint32_t stage = sQ(t) + static_cast<uint32_t>(quad * C::CH * 4096);
+      const bool of16 = a.o_f16 != 0;
+      auto pk2 = [of16](float x, float y) { return of16 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -355,10 +359,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int g = 0; g < 4; ++g)
           st_shared_v4(stage + cb * 4096 + lane * 128 + (((g0 + g) ^ static_cast<uint32_t>(lane & 7)) << 4),
-                       pack_bf16x2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv),
-                       pack_bf16x2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv),
-                       pack_bf16x2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv),
-                       pack_bf16x2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv));
+                       pk2(__uint_as_float(o[8 * g + 0]) * inv, __uint_as_float(o[8 * g + 1]) * inv),
+                       pk2(__uint_as_float(o[8 * g + 2]) * inv, __uint_as_float(o[8 * g + 3]) * inv),
+                       pk2(__uint_as_float(o[8 * g + 4]) * inv, __uint_as_float(o[8 * g + 5]) * inv),
+                       pk2(__uint_as_float(o[8 * g + 6]) * inv, __uint_as_float(o[8 * g + 7]) * inv));
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -400,7 +404,7 @@ int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsign
   const uint64_t od[4] = {static_cast<uint64_t>(a.hN) * D, static_cast<uint64_t>(a.S), static_cast<uint64_t>(a.B),
                           static_cast<uint64_t>(a.N)};
   const uint32_t obox[4] = {64, 32, 1, 1};
-  // 16-bit elements (fp16 Q and K, bf16 V): the copies do not interpret them
+  // 16-bit elements (fp16 Q, K and V; O fp16 or bf16): the copies do not interpret them
   if (!encode_tmap(&tqkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, qkv, qd, box, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
   if (!encode_tmap(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, o, od, obox, CU_TENSOR_MAP_SWIZZLE_128B)) return 2;
   const int nqb = (a.S + QT * BQ - 1) / (QT * BQ);

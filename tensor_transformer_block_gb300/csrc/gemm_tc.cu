@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == WARP_MMA) {
     if (lane == 0 && leader) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t IDESC = idesc_bf16(C::TILE_M, BN, A_MN, B_MN);
+      const uint32_t IDESC =
+          p.ab_f16 ? idesc_f16(C::TILE_M, BN, A_MN, B_MN) : idesc_bf16(C::TILE_M, BN, A_MN, B_MN);
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true, any = false;
@@ -534,8 +535,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // fully unrolled 64-column body is large enough to evict the MMA
           // warp's instructions from the cache the SM sub-partition shares.
           if (EPI == kEpiStore || EPI == kEpiSplit) {
-            // kEpiSplit: fp16 for the columns before split_cols (whole 64-column chunks)
-            const bool f16 = EPI == kEpiSplit && ccol < p.split_cols;
+            // fp16 for the columns before split_cols (whole 64-column chunks)
+            const bool f16 = ccol < p.split_cols;
             uint32_t r0[32], r1[32];
             tmem_ld32(tcol, r0);
             tmem_ld32(tcol + 32, r1);
@@ -744,10 +745,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int e = 0; e < 4; ++e) {
                   const float a0 = __uint_as_float(v[8 * hh + 2 * e]), a1 = __uint_as_float(v[8 * hh + 2 * e + 1]);
                   const float y0 = bf16lo_to_f32(yy[e]), y1 = bf16hi_to_f32(yy[e]);
-                  if (EPI == kEpiResidual)
-                    o[e] = pack_bf16x2(a0 + y0, a1 + y1);
-                  else
-                    o[e] = pack_bf16x2(a0 * gelu_grad_f(y0), a1 * gelu_grad_f(y1));
+                  const float r0 = EPI == kEpiResidual ? a0 + y0 : a0 * gelu_grad_f(y0);
+                  const float r1 = EPI == kEpiResidual ? a1 + y1 : a1 * gelu_grad_f(y1);
+                  o[e] = p.c_f16 ? pack_f16x2(r0, r1) : pack_bf16x2(r0, r1);
                 }
                 st_shared_v4(addr, o[0], o[1], o[2], o[3]);
               }
@@ -897,6 +897,8 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   if ((A.d0 % 8) || (B.d0 % 8) || (N % 8) || (ldc % 8) || ldc < N) return 1;
   if (ldc != N && (N % 64)) return 1;  // a partial last chunk would not be clipped at N
   if (epi == kEpiSplit && (extra.split_cols % 64)) return 1;
+  // fp16 outputs: the plain store, the dGeLU and the residual epilogues
+  if (extra.c_f16 && epi != kEpiStore && epi != kEpiDGelu && epi != kEpiResidual) return 1;
   const bool gated = epi == kEpiSwiGLU || epi == kEpiDSwiGLU;
   // sequence-sharded operands: the token axis is d1 (A, B) or M (C), d2 = 1, and
   // every box height (128, 64, 32 rows) divides the shard length L
@@ -972,7 +974,11 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.b_zg = B.zg;
   p.b_zs = B.zs;
   p.store_y = (store_y && Yaux) ? 1 : 0;
-  p.split_cols = static_cast<int>(extra.split_cols);
+  // kEpiStore with c_f16: every column fp16 (N < 2^31)
+  p.split_cols = epi == kEpiSplit ? static_cast<int>(extra.split_cols)
+                                  : (epi == kEpiStore && extra.c_f16 ? 0x7fffffff : 0);
+  p.ab_f16 = extra.ab_f16 ? 1 : 0;
+  p.c_f16 = extra.c_f16 ? 1 : 0;
   p.a_spS = A.sp_S;
   p.a_spL = A.sp_L;
   p.b_spS = B.sp_S;

@@ -43,7 +43,9 @@ struct GemmShape {
   int tiles_m, tiles_n;
   int a_zg, a_zs, b_zg, b_zs;  // outer TMA coordinate = g*zg + s*zs
   int store_y;                 // kEpiGelu: also write the pre-activation
-  int split_cols;              // kEpiSplit
+  int split_cols;              // kEpiStore / kEpiSplit: columns < split_cols are stored as fp16
+  int ab_f16;                  // A and B are fp16 (else bf16); one MMA's operands share a type
+  int c_f16;                   // kEpiDGelu, kEpiResidual: the output C is fp16 (else bf16)
   // token remaps (0 = off): the operand's row coordinate t (A, B: d1; C, Yaux: M)
   // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
   int a_spS, a_spL, b_spS, b_spL, c_spS, c_spL;
@@ -75,7 +77,9 @@ struct GemmOperand {
 // the two-part tensors are [G][M][2][N] and ldc must be 0.
 struct GemmExtra {
   int64_t ldc = 0;
-  int64_t split_cols = 0;  // kEpiSplit
+  int64_t split_cols = 0;  // kEpiSplit (a multiple of 64)
+  bool c_f16 = false;      // the whole output C in fp16 (kEpiStore, kEpiDGelu, kEpiResidual)
+  bool ab_f16 = false;     // A and B hold fp16 values (both; tcgen05 kind::f16 takes one type)
   int c_sp_S = 0, c_sp_L = 0;  // sequence-sharded rows of C and Yaux (kEpiStore, kEpiResidual)
 };
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,

@@ -58,6 +58,7 @@ enum KernelKind : int {
   kKLnBwd,          // LayerNorm backward (+ residual gradient), per-CTA partial dgamma / dbeta
   kKLnColsum,       // fixed-order sum of the partial rows -> dgamma, dbeta
   kKProbe,          // timeout probe
+  kKCast,           // bf16 -> fp16 copy of a weight matrix
   kNumKernelKinds
 };
 const char* kernel_kind_name(int k);

@@ -24,6 +24,7 @@
 // geometry depends only on T, h and the device (the grids are the CTAs that fit
 // at once), so the result is bit-reproducible on a given GPU.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "host_util.cuh"
 #include "ln.cuh"
@@ -32,21 +33,28 @@
 namespace tpb {
 namespace {
 
-__device__ __forceinline__ void unpack8(const uint4& q, float (&v)[8]) {
+// Eight 16-bit values of a 16-byte vector, bf16 or (f16) fp16, to fp32 and back.
+__device__ __forceinline__ void unpack8(const uint4& q, float (&v)[8], bool f16 = false) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    v[2 * e] = bf16lo_to_f32(w[e]);
-    v[2 * e + 1] = bf16hi_to_f32(w[e]);
+    if (f16) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+      v[2 * e] = t.x;
+      v[2 * e + 1] = t.y;
+    } else {
+      v[2 * e] = bf16lo_to_f32(w[e]);
+      v[2 * e + 1] = bf16hi_to_f32(w[e]);
+    }
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+__device__ __forceinline__ uint4 pack8(const float (&v)[8], bool f16 = false) {
   uint4 q;
-  q.x = pack_bf16x2(v[0], v[1]);
-  q.y = pack_bf16x2(v[2], v[3]);
-  q.z = pack_bf16x2(v[4], v[5]);
-  q.w = pack_bf16x2(v[6], v[7]);
+  q.x = f16 ? pack_f16x2(v[0], v[1]) : pack_bf16x2(v[0], v[1]);
+  q.y = f16 ? pack_f16x2(v[2], v[3]) : pack_bf16x2(v[2], v[3]);
+  q.z = f16 ? pack_f16x2(v[4], v[5]) : pack_bf16x2(v[4], v[5]);
+  q.w = f16 ? pack_f16x2(v[6], v[7]) : pack_bf16x2(v[6], v[7]);
   return q;
 }
 
@@ -80,8 +88,9 @@ template <int VPT>
 __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
                                                  const uint4* __restrict__ beta, uint4* __restrict__ Y,
                                                  float* __restrict__ mean, float* __restrict__ rstd, int T,
-                                                 int nvec, float inv_h, float eps) {
+                                                 int nvec, float inv_h, float eps, int io) {
   __shared__ float red[64];
+  const bool x16 = io & kLnXF16, y16 = io & kLnYF16;
   int64_t row = blockIdx.x;
   if (row >= T) return;
   // persistent over rows: the next row's vectors are loaded while this one is reduced
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
-      unpack8(cur[k], v[k]);  // zero beyond the row: adds nothing
+      unpack8(cur[k], v[k], x16);  // zero beyond the row: adds nothing
 #pragma unroll
       for (int e = 0; e < 8; ++e) s += v[k][e];
     }
@@ -130,7 +139,7 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
         unpack8(beta[i], b);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = fmaf((v[k][e] - mu) * r, g[e], b[e]);
-        yr[i] = pack8(o);
+        yr[i] = pack8(o, y16);
       }
     }
     if (threadIdx.x == 0) {
@@ -148,8 +157,9 @@ template <int VPT, bool PF>
 __global__ void __launch_bounds__(PF ? 512 : 1024)
     k_ln_bwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma, const float* __restrict__ mean,
              const float* __restrict__ rstd, const uint4* __restrict__ dY, const uint4* __restrict__ dR,
-             uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h) {
+             uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h, int io) {
   __shared__ float red[64];
+  const bool x16 = io & kLnXF16, dy16 = io & kLnDyF16, dr16 = io & kLnDrF16, dx16 = io & kLnDxF16;
   float gm[VPT][8], pg[VPT][8], pb[VPT][8];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -196,8 +206,8 @@ __global__ void __launch_bounds__(PF ? 512 : 1024)
       const int i = threadIdx.x + k * blockDim.x;
       if (i < nvec) {
         float xv[8], dy[8];
-        unpack8(cur.x[k], xv);
-        unpack8(cur.dy[k], dy);
+        unpack8(cur.x[k], xv, x16);
+        unpack8(cur.dy[k], dy, dy16);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           xh[k][e] = (xv[e] - mu) * r;
@@ -223,10 +233,10 @@ __global__ void __launch_bounds__(PF ? 512 : 1024)
       if (i < nvec) {
         float o[8], rr[8];
         // zero without a residual (without the prefetch, loaded only now)
-        unpack8(PF ? cur.dr[k] : (dR ? dR[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u)), rr);
+        unpack8(PF ? cur.dr[k] : (dR ? dR[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u)), rr, dr16);
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = r * (g[k][e] - c1 - xh[k][e] * c2) + rr[e];
-        dX[row * nvec + i] = pack8(o);
+        dX[row * nvec + i] = pack8(o, dx16);
       }
     }
     if (PF) cur = nxt;
@@ -321,7 +331,7 @@ size_t ln_partial_bytes(int64_t T, int64_t h) {
 }
 
 int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, float* mean, float* rstd, int64_t T,
-                  int64_t h, float eps, cudaStream_t st) {
+                  int64_t h, float eps, cudaStream_t st, int io) {
   if (!ln_shape_ok(T, h)) return 1;
   const LnGeom g = ln_fwd_geom(h);
   const int nvec = static_cast<int>(h / 8);
@@ -341,9 +351,9 @@ int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, f
   const int slot = timing_begin(kKLnFwd, st);
   const dim3 grid(static_cast<unsigned>(nb));
   if (g.vpt == 4)
-    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io);
   else
-    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps);
+    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io);
   const bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
@@ -351,7 +361,7 @@ int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, f
 
 int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd, const void* dY,
                   const void* dR, void* dX, void* dgamma, void* dbeta, float* part, int64_t T, int64_t h,
-                  cudaStream_t st) {
+                  cudaStream_t st, int io) {
   if (!ln_shape_ok(T, h)) return 1;
   const LnGeom g = ln_geom(h);
   const int nvec = static_cast<int>(h / 8);
@@ -376,13 +386,13 @@ int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const flo
   int slot = timing_begin(kKLnBwd, st);
   if (g.pf && g.vpt == 2)
     k_ln_bwd<2, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h);
+                                                 inv_h, io);
   else if (g.pf)
     k_ln_bwd<1, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h);
+                                                 inv_h, io);
   else
     k_ln_bwd<2, false><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                  inv_h);
+                                                  inv_h, io);
   bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;

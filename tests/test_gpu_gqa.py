@@ -31,7 +31,7 @@ def _run(B, S, h, H, Hkv, d, N, causal=True, backward=True, seed=0):
 def _check(B, S, h, H, Hkv, d, N, causal=True, backward=True, seed=0):
     inp, r, f, g = _run(B, S, h, H, Hkv, d, N, causal, backward, seed)
     ref = O.gqa_attention_forward(r["X"], r["Wqkv"], r["Wo"], B, S, H, Hkv, causal)
-    # Q and K planes (fp16) and the V plane (bf16): single roundings of the projection
+    # Q, K and V planes (fp16): single roundings of the projection
     T, hn, kvn = B * S, H // N, Hkv // N
     qkv = f["QKV"].detach().reshape(N, T, -1)
     for i in range(N):
@@ -42,7 +42,7 @@ def _check(B, S, h, H, Hkv, d, N, causal=True, backward=True, seed=0):
         as16 = lambda t: t.contiguous().view(torch.float16).to("cpu", torch.float64).numpy()
         assert_bf16_rounded(as16(row[:, :hn * d]), q, "Q (fp16)", rel=2.0 ** -10)
         assert_bf16_rounded(as16(row[:, hn * d:(hn + kvn) * d]), k, "K (fp16)", rel=2.0 ** -10)
-        assert_bf16_rounded(_np(row[:, (hn + kvn) * d:]), v, "V")
+        assert_bf16_rounded(as16(row[:, (hn + kvn) * d:]), v, "V (fp16)", rel=2.0 ** -10)
     assert_attn_parity(_np(f["O"]), ref["O"], "O")
     assert_attn_parity(_np(f["LSE"]).reshape(B * H, S), ref["LSE"].reshape(B * H, S), "LSE")
     assert_attn_parity(_np(f["Z"]), ref["Z"], "Z")

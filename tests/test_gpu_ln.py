@@ -5,7 +5,7 @@ import torch
 
 import tensor_transformer_block_gb300 as tp
 from oracle import tp_oracle as O
-from parity import assert_attn_parity, assert_bf16_rounded, assert_f32_parity, bf16_round
+from parity import assert_attn_parity, assert_bf16_rounded, assert_f32_parity
 from tensor_transformer_block_gb300 import block, inputs
 
 pytestmark = pytest.mark.gpu
@@ -92,11 +92,18 @@ def test_prenorm_layer_reduced():
 
 def test_prenorm_layer_zero_projections_is_identity():
     """With Wo = 0 and W2 = 0 both blocks add exactly zero: Z = X bit for bit (the
-    residual epilogues add a zero accumulator to a bf16 value), and dX = dZ."""
+    residual epilogues add a zero accumulator to a bf16 value), and dX = dZ.  The
+    residual gradient dH1 passes through fp16 storage between the two LayerNorm
+    backwards, which holds every bf16 value of magnitude 2^-14 .. 65504 exactly:
+    there dX = dZ bit for bit; below 2^-14 fp16 is subnormal and the value moves
+    by at most half its spacing, 2^-25."""
     B, S, h, H, d, f, N = 1, 200, 512, 4, 64, 1024, 4
     inp, r, fw, bw = _layer(B, S, h, H, d, f, N, seed=6, zero_out=True)
     assert torch.equal(fw["Z"].cpu(), inp["X"])
-    assert torch.equal(bw["dX"].cpu(), inp["dZ"])
+    dx, dz = bw["dX"].cpu().double(), inp["dZ"].double()
+    normal = dz.abs() >= 2.0 ** -14
+    assert torch.equal(dx[normal], dz[normal])
+    assert float((dx - dz).abs().max()) <= 2.0 ** -25
 
 
 @pytest.mark.parametrize("mode", [1, 2])
@@ -114,21 +121,25 @@ def test_prenorm_layer_each_tiling(mode):
         tp.tp_set_gemm_tiling(0)
 
 
-def test_prenorm_layer_full_size_sampled():
+def test_prenorm_layer_full_size():
     """The pre-norm layer at the full layer size (S=4096, h=8192, 64 heads, f=28672,
-    N=8): Z on sampled token rows; every gradient finite."""
+    N=8): Z on sampled token rows (the oracle's forward restricted to them) and every
+    gradient in full against the oracle's backward, each within the stated 5e-3
+    relative Frobenius error."""
     B, S, h, H, d, f, N = 1, 4096, 8192, 64, 128, 28672, 8
     inp, r, fw, bw = _layer(B, S, h, H, d, f, N)
+    z = _np(fw["Z"])
+    out = {k: _np(v) for k, v in bw.items()}
+    del fw, bw
+    torch.cuda.empty_cache()
     rng = np.random.default_rng(2)
     rows = np.sort(np.concatenate([[0, S - 1], rng.choice(S, 30, replace=False)]))
     ref = O.prenorm_layer_forward_rows(*_args(r), B, S, rows)
-    # The MLP reads LN2 of the bf16 H1 (RMS ~2 here), and its pre-activations'
-    # RMS is ~1.8, so the bf16 storage between the kernels alone moves Z by about
-    # the 5e-3 bound.  The oracle measures that: the Frobenius bound is twice the
-    # error of the oracle itself with LN1(X), H1, LN2(H1) and A rounded to bf16
-    # (at least 5e-3).
-    rs = O.prenorm_layer_forward_rows(*_args(r), B, S, rows, store=bf16_round)
-    floor = float(np.linalg.norm(bf16_round(rs["Z"]) - ref["Z"]) / np.linalg.norm(ref["Z"]))
-    assert_attn_parity(_np(fw["Z"])[rows], ref["Z"], "Z rows", fro_tol=max(5e-3, 2 * floor))
-    for k, v in bw.items():
-        assert torch.isfinite(v.float()).all(), k
+    assert_attn_parity(z[rows], ref["Z"], "Z rows")
+    g = O.prenorm_layer_backward(*_args(r), r["dZ"], B, S)
+    assert_attn_parity(out["dX"], g["dX"], "dX")
+    assert_attn_parity(out["dWqkv"].reshape(N, h, -1), g["dWqkv"].reshape(N, h, -1), "dWqkv")
+    for k in ("dWo", "dW1s", "dW2s"):
+        assert_attn_parity(out[k], g[k], k)
+    for k in ("dln1_g", "dln1_b", "dln2_g", "dln2_b"):
+        assert_attn_parity(out[k][None, :], g[k][None, :], k)
