@@ -61,7 +61,9 @@ typedef enum {
   TP_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed (launch, tensor-map encode, sync) */
   TP_ERR_TIMEOUT = 6,   /* a kernel's bounded wait ran out (reported by tp_sync_status) */
   TP_ERR_ALIGN = 7,     /* a pointer is not 16-byte aligned (ws: 256-byte) */
-  TP_ERR_DEVICE = 8     /* the current device is not a compute capability 10.3 (sm_103) GPU */
+  TP_ERR_DEVICE = 8,    /* the current device is not a compute capability 10.3 (sm_103) GPU */
+  TP_ERR_BOUNDS = 9     /* a debug build's device-side bounds or alignment check failed
+                           (reported by tp_sync_status; release builds never raise it) */
 } tp_status;
 
 typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
@@ -78,7 +80,10 @@ TP_API int tp_device_check(void);
 
 /* Waits for ``stream``, then reads and clears the device error word.
  * Returns TP_ERR_TIMEOUT if any kernel since the last call gave up on a bounded
- * wait, TP_ERR_CUDA if the synchronisation itself failed, TP_OK otherwise. */
+ * wait, TP_ERR_BOUNDS if (in a library built with -DTPBLOCK_DEBUG) a kernel found
+ * an index outside its tensor or a TMA coordinate off its 16-byte boundary and
+ * skipped that access, TP_ERR_CUDA if the synchronisation itself failed, TP_OK
+ * otherwise. */
 TP_API int tp_sync_status(void* stream);
 
 /* ---------------------------------------------------------------- MLP block */
@@ -346,9 +351,18 @@ TP_API size_t tp_layer_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t 
  *   H1 = X + Attn(LN1(X))      (the residual is added in the output projection's
  *                               epilogue, after the shard sum)
  *   Z  = H1 + MLP(LN2(H1))     (likewise in the second MLP GEMM's epilogue)
- * Attn and MLP are exactly tp_attn_fwd and tp_mlp_fwd.  ``save`` (256-byte aligned,
- * tp_layer_save_bytes) receives LN1(X), H1, LN2(H1), their row statistics and the
- * blocks' saved tensors; its layout is private to the library. */
+ * Attn and MLP compute what tp_attn_fwd and tp_mlp_fwd compute.  Inside the layer
+ * the LayerNorm outputs LN1(X) and LN2(H1), the attention output O and, in the
+ * backward, dY, the LayerNorm input gradients, dH1 and dQKV are stored in fp16
+ * (11 significant bits) instead of bf16: LN1(X) feeds the scores the softmax
+ * exponentiates and LN2(H1) the MLP whose GeLU' amplifies errors, and with bf16
+ * there the layer's gradients missed a 5e-3 relative error bound at h = 8192.
+ * The products with an fp16 operand take fp16 copies of Wqkv, Wo and W1s that this
+ * call makes in ``save`` (exact for weights of magnitude 2^-17 .. 65504; smaller
+ * ones round to a multiple of 2^-24).  ``save`` (256-byte aligned,
+ * tp_layer_save_bytes) receives LN1(X), H1 (bf16), LN2(H1), their row statistics,
+ * the blocks' saved tensors and the weight copies; its layout is private to the
+ * library. */
 TP_API int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N,
                         int causal, float eps,
                         const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,

@@ -16,13 +16,14 @@ import re
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libtpblock.so")
+# TPBLOCK_LIB selects another build of the library (the checked libtpblock_debug.so)
+LIB_PATH = os.environ.get("TPBLOCK_LIB") or os.path.join(HERE, "libtpblock.so")
 HEADER_PATH = os.path.join(os.path.dirname(HERE), "include", "tpblock.h")
 
 TP_F32, TP_BF16 = 0, 1
 QKV_PLANES = 3  # Q, K, V (fp16 values in 16-bit storage) per (token, head)
 STATUS = {0: "TP_OK", 1: "TP_ERR_NULL", 2: "TP_ERR_SHAPE", 3: "TP_ERR_DTYPE", 4: "TP_ERR_WORKSPACE",
-          5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE"}
+          5: "TP_ERR_CUDA", 6: "TP_ERR_TIMEOUT", 7: "TP_ERR_ALIGN", 8: "TP_ERR_DEVICE", 9: "TP_ERR_BOUNDS"}
 _TORCH_DT = {TP_F32: torch.float32, TP_BF16: torch.bfloat16}
 
 _lib = None

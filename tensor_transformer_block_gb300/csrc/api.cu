@@ -3,6 +3,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -51,6 +53,29 @@ int check_device(unsigned** err) {
   if (err) *err = g_err_ptr[d];
   return TP_OK;
 }
+
+// An NVTX range (domain "libtpblock") around every C-ABI call, named after the
+// call: a profiler attached to the process sees each call and the kernels it
+// launched inside it.  With no tool attached a range costs a function-pointer
+// check.  NVTX v3 is header-only; a tool is found through the environment.
+nvtxDomainHandle_t trace_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("libtpblock");
+  return d;
+}
+struct TraceRange {
+  explicit TraceRange(const char* name) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(trace_domain(), &a);
+  }
+  ~TraceRange() { nvtxDomainRangePop(trace_domain()); }
+  TraceRange(const TraceRange&) = delete;
+  TraceRange& operator=(const TraceRange&) = delete;
+};
+#define TP_TRACE const TraceRange tp_trace_range_(__func__)
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -144,6 +169,7 @@ const char* tp_status_string(int s) {
     case TP_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
     case TP_ERR_ALIGN: return "pointer not aligned (16 bytes; workspace 256 bytes)";
     case TP_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case TP_ERR_BOUNDS: return "a debug build's device-side bounds or alignment check failed";
     default: return "unknown status";
   }
 }
@@ -151,6 +177,7 @@ const char* tp_status_string(int s) {
 int tp_device_check(void) { return check_device(nullptr); }
 
 int tp_sync_status(void* stream) {
+  TP_TRACE;
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
@@ -162,10 +189,12 @@ int tp_sync_status(void* stream) {
     if (cudaMemcpyToSymbol(g_tp_error_word, &z, sizeof(z)) != cudaSuccess) return TP_ERR_CUDA;
   }
   if (v & tpb::kErrTimeout) return TP_ERR_TIMEOUT;
+  if (v & tpb::kErrBounds) return TP_ERR_BOUNDS;
   return TP_OK;
 }
 
 int tp_debug_timeout_probe(int64_t timeout_ns, void* stream) {
+  TP_TRACE;
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
@@ -359,6 +388,7 @@ size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N)
 
 int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
                const void* W2s, void* Y_save, void* A_save, void* Z, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = mlp_shape_check(dtype, T, h, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;
@@ -417,6 +447,7 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
 int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
                const void* W2s, const void* Y_save, const void* A_save, const void* dZ, void* dX, void* dW1s,
                void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = mlp_shape_check(dtype, T, h, f, N);
   if (sc != TP_OK) return sc;
   if (dtype != TP_BF16) return TP_ERR_DTYPE;
@@ -452,6 +483,7 @@ size_t tp_gmlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N
 
 int tp_gmlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* Wgus,
                 const void* Wds, void* GU_save, void* A_save, void* Z, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = gmlp_shape_check(dtype, T, h, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wgus || !Wds || !Z) return TP_ERR_NULL;
@@ -484,6 +516,7 @@ int tp_gmlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X
 int tp_gmlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* Wgus,
                 const void* Wds, const void* GU_save, const void* A_save, const void* dZ, void* dX, void* dWgus,
                 void* dWds, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = gmlp_shape_check(dtype, T, h, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wgus || !Wds || !GU_save || !A_save || !dZ || !dX || !dWgus || !dWds) return TP_ERR_NULL;
@@ -542,6 +575,7 @@ size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H
 int tp_gqa_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
                const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
                size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = attn_shape_check(dtype, B, S, h, H, Hkv, d, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !Z) return TP_ERR_NULL;
@@ -566,6 +600,7 @@ int tp_gqa_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d
 int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
                 const void* Wqkv, const void* Wo, void* QKV_save, void* O_save, float* LSE_save, void* Z, void* ws,
                 size_t ws_bytes, void* stream) {
+  TP_TRACE;
   return tp_gqa_fwd(dtype, B, S, h, H, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, Z, ws, ws_bytes,
                     stream);
 }
@@ -573,6 +608,7 @@ int tp_attn_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N,
 int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, int causal, const void* X,
                const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
                const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = attn_shape_check(dtype, B, S, h, H, Hkv, d, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !QKV_save || !O_save || !LSE_save || !dZ || !dX || !dWqkv || !dWo) return TP_ERR_NULL;
@@ -592,6 +628,7 @@ int tp_gqa_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv, int d
 int tp_attn_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N, int causal, const void* X,
                 const void* Wqkv, const void* Wo, const void* QKV_save, const void* O_save, const float* LSE_save,
                 const void* dZ, void* dX, void* dWqkv, void* dWo, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   return tp_gqa_bwd(dtype, B, S, h, H, H, d, N, causal, X, Wqkv, Wo, QKV_save, O_save, LSE_save, dZ, dX, dWqkv, dWo,
                     ws, ws_bytes, stream);
 }
@@ -659,6 +696,7 @@ size_t tp_attn_mlp_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, i
 int tp_attn_mlp_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N, int causal,
                     const void* X, const void* Wqkv, const void* Wo, const void* W1s, const void* W2s, void* save,
                     size_t save_bytes, void* Z, void* stream) {
+  TP_TRACE;
   const int sc = am_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !W1s || !W2s || !save || !Z) return TP_ERR_NULL;
@@ -689,6 +727,7 @@ int tp_attn_mlp_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, in
                     const void* X, const void* Wqkv, const void* Wo, const void* W1s, const void* W2s,
                     const void* save, size_t save_bytes, const void* dZ, void* dX, void* dWqkv, void* dWo,
                     void* dW1s, void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   const int sc = am_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !Wqkv || !Wo || !W1s || !W2s || !save || !dZ || !dX || !dWqkv || !dWo || !dW1s || !dW2s)
@@ -790,18 +829,22 @@ size_t tp_layernorm_workspace_bytes(int dtype, int64_t T, int64_t h) {
 
 int tp_layernorm_fwd(int dtype, int64_t T, int64_t h, float eps, const void* X, const void* gamma, const void* beta,
                      void* Y, float* mean, float* rstd, void* stream) {
+  TP_TRACE;
   if (dtype != TP_BF16) return TP_ERR_DTYPE;
   if (!tpb::ln_shape_ok(T, h) || !(eps >= kEpsMin)) return TP_ERR_SHAPE;
   if (!X || !gamma || !beta || !Y || !mean || !rstd) return TP_ERR_NULL;
   if (!al16(X) || !al16(gamma) || !al16(beta) || !al16(Y) || !al16(mean) || !al16(rstd)) return TP_ERR_ALIGN;
-  const int dc = check_device(nullptr);
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
-  return gemm_status(tpb::launch_ln_fwd(X, gamma, beta, Y, mean, rstd, T, h, eps, static_cast<cudaStream_t>(stream)));
+  return gemm_status(
+      tpb::launch_ln_fwd(X, gamma, beta, Y, mean, rstd, T, h, eps, static_cast<cudaStream_t>(stream), 0, err));
 }
 
 int tp_layernorm_bwd(int dtype, int64_t T, int64_t h, const void* X, const void* gamma, const float* mean,
                      const float* rstd, const void* dY, const void* dR, void* dX, void* dgamma, void* dbeta, void* ws,
                      size_t ws_bytes, void* stream) {
+  TP_TRACE;
   if (dtype != TP_BF16) return TP_ERR_DTYPE;
   if (!tpb::ln_shape_ok(T, h)) return TP_ERR_SHAPE;
   if (!X || !gamma || !mean || !rstd || !dY || !dX || !dgamma || !dbeta) return TP_ERR_NULL;
@@ -810,10 +853,11 @@ int tp_layernorm_bwd(int dtype, int64_t T, int64_t h, const void* X, const void*
     return TP_ERR_ALIGN;
   if (!ws || ws_bytes < tp_layernorm_workspace_bytes(dtype, T, h)) return TP_ERR_WORKSPACE;
   if (!al256(ws)) return TP_ERR_ALIGN;
-  const int dc = check_device(nullptr);
+  unsigned* err = nullptr;
+  const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
   return gemm_status(tpb::launch_ln_bwd(X, gamma, mean, rstd, dY, dR, dX, dgamma, dbeta, static_cast<float*>(ws), T,
-                                        h, static_cast<cudaStream_t>(stream)));
+                                        h, static_cast<cudaStream_t>(stream), 0, err));
 }
 
 size_t tp_layer_save_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64_t f, int N) {
@@ -862,7 +906,7 @@ int layer_fwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
   if (!rc) rc = tpb::launch_bf16_to_f16(W1s, sv + L.w1_16, static_cast<long long>(h) * f, st);
   if (rc) return gemm_status(rc);
   // LN1(X) in fp16 (row by row, so in whatever row order X is stored)
-  rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st, tpb::kLnYF16);
+  rc = tpb::launch_ln_fwd(X, ln1_g, ln1_b, sv + L.ln1, mean1, rstd1, T, h, eps, st, tpb::kLnYF16, err);
   if (rc) return gemm_status(rc);
   // H1 = X + Attn(LN1(X)): the residual is added in the output projection's epilogue
   rc = attn_fwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
@@ -870,7 +914,7 @@ int layer_fwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
                     sv + L.wqkv16);
   if (rc) return rc;
   // LN2(H1) in fp16
-  rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st, tpb::kLnYF16);
+  rc = tpb::launch_ln_fwd(sv + L.h1, ln2_g, ln2_b, sv + L.ln2, mean2, rstd2, T, h, eps, st, tpb::kLnYF16, err);
   if (rc) return gemm_status(rc);
   // Z = H1 + MLP(LN2(H1)): the residual is added in the second GEMM's epilogue
   return mlp_fwd_seq(T, h, f, N, sv + L.ln2, W1s, W2s, sv + L.y, sv + L.a, Z, sv + L.h1, err, st, sp, sv + L.w1_16);
@@ -911,7 +955,7 @@ int layer_bwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
   // dH1 = dZ + LN2'(dLN2)   (the residual passes dZ through); fp16
   rc = tpb::launch_ln_bwd(sv + L.h1, ln2_g, reinterpret_cast<const float*>(sv + L.mean2),
                           reinterpret_cast<const float*>(sv + L.rstd2), dLN, dZ, dH1, dln2_g, dln2_b, part, T, h, st,
-                          tpb::kLnDyF16 | tpb::kLnDxF16);
+                          tpb::kLnDyF16 | tpb::kLnDxF16, err);
   if (rc) return gemm_status(rc);
   // attention block backward on LN1(X) with upstream dH1: dLN1 -> dLN (fp16)
   rc = attn_bwd_seq(B, S, h, H, H, d, N, causal, sv + L.ln1, Wqkv, Wo, sv + L.qkv, sv + L.o,
@@ -921,7 +965,7 @@ int layer_bwd_impl(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int
   // dX = dH1 + LN1'(dLN1)
   rc = tpb::launch_ln_bwd(X, ln1_g, reinterpret_cast<const float*>(sv + L.mean1),
                           reinterpret_cast<const float*>(sv + L.rstd1), dLN, dH1, dX, dln1_g, dln1_b, part, T, h, st,
-                          tpb::kLnDyF16 | tpb::kLnDrF16);
+                          tpb::kLnDyF16 | tpb::kLnDrF16, err);
   return gemm_status(rc);
 }
 
@@ -941,6 +985,7 @@ int tp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64
                  const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
                  const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
                  size_t save_bytes, void* Z, void* stream) {
+  TP_TRACE;
   return layer_fwd_impl(dtype, B, S, h, H, d, f, N, causal, eps, X, ln1_g, ln1_b, Wqkv, Wo, ln2_g, ln2_b, W1s, W2s,
                         save, save_bytes, Z, stream, Sp());
 }
@@ -950,6 +995,7 @@ int tp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int64
                  const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
                  void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
                  void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   return layer_bwd_impl(dtype, B, S, h, H, d, f, N, causal, X, ln1_g, Wqkv, Wo, ln2_g, W1s, W2s, save, save_bytes,
                         dZ, dX, dln1_g, dln1_b, dWqkv, dWo, dln2_g, dln2_b, dW1s, dW2s, ws, ws_bytes, stream, Sp());
 }
@@ -958,6 +1004,7 @@ int tp_sp_layer_fwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, in
                     float eps, const void* X, const void* ln1_g, const void* ln1_b, const void* Wqkv, const void* Wo,
                     const void* ln2_g, const void* ln2_b, const void* W1s, const void* W2s, void* save,
                     size_t save_bytes, void* Z, void* stream) {
+  TP_TRACE;
   Sp sp;
   const int sc = layer_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
@@ -971,6 +1018,7 @@ int tp_sp_layer_bwd(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, in
                     const void* W1s, const void* W2s, const void* save, size_t save_bytes, const void* dZ, void* dX,
                     void* dln1_g, void* dln1_b, void* dWqkv, void* dWo, void* dln2_g, void* dln2_b, void* dW1s,
                     void* dW2s, void* ws, size_t ws_bytes, void* stream) {
+  TP_TRACE;
   Sp sp;
   const int sc = layer_check(dtype, B, S, h, H, d, f, N);
   if (sc != TP_OK) return sc;
@@ -1039,6 +1087,7 @@ extern "C" {
 
 int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
                        const void* W2s, void* Z, void* stream) {
+  TP_TRACE;
   const int sc = mlp_shape_check(dtype, T, h, f, N);
   if (sc != TP_OK) return sc;
   if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;

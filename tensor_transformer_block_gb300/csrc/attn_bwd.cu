@@ -52,7 +52,7 @@ __device__ __forceinline__ float dot8(const uint4& x, const uint4& y, bool x_f16
 }
 template <int D>
 __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict__ dout, float* __restrict__ dsum,
-                            const AttnDims a) {
+                            const AttnDims a, unsigned* err) {
   constexpr int LPR = D / 8;  // lanes (16-byte vectors) per row
   static_assert(32 % LPR == 0, "a row's lanes lie in one warp");
   const long long T = static_cast<long long>(a.B) * a.S;
@@ -74,7 +74,8 @@ __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict
       const int jj = static_cast<int>(rem - t * a.hN);
       const long long bb = t / a.S, ss = t - bb * a.S;
       const long long j = shard * a.hN + jj;
-      dsum[(bb * a.H + j) * a.S + ss] = s;
+      const long long di = (bb * a.H + j) * a.S + ss;
+      if (TP_DCHECK(di >= 0 && di < static_cast<long long>(a.B) * a.H * a.S, err)) dsum[di] = s;
     }
   }
 }
@@ -228,8 +229,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(cm.bar(K_QE + st), ph ^ 1u, wc))) break;
       for (int t = lane; t < BLK; t += 32) {
         const int q = q0 + t;
-        lse_s[st * BLK + t] = q < a.S ? lse[row_base + q] * kLog2e : 0.0f;
-        dd_s[st * BLK + t] = q < a.S ? dsum[row_base + q] : 0.0f;
+        const bool in = q < a.S && TP_DCHECK(row_base + q < static_cast<size_t>(a.B) * a.H * a.S, err);
+        lse_s[st * BLK + t] = in ? lse[row_base + q] * kLog2e : 0.0f;
+        dd_s[st * BLK + t] = in ? dsum[row_base + q] : 0.0f;
       }
       __threadfence_block();
       __syncwarp();
@@ -631,8 +633,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int q = q0 + r;
     const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const uint32_t cS = static_cast<uint32_t>(64 * half);
-    const bool qvalid = q < a.S;
     const size_t ridx = (static_cast<size_t>(b) * a.H + j) * a.S + q;
+    const bool qvalid = q < a.S && TP_DCHECK(ridx < static_cast<size_t>(a.B) * a.H * a.S, err);
     const float lse2 = qvalid ? lse[ridx] * kLog2e : 0.0f;
     const float dd = qvalid ? dsum[ridx] : 0.0f;
     bool ok = true;
@@ -744,7 +746,7 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
   int slot = timing_begin(kKAttnDsum, st);
   k_attn_dsum<D><<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(o),
-                                                           static_cast<const uint4*>(dout), dsum, a);
+                                                           static_cast<const uint4*>(dout), dsum, a, err);
   bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;

@@ -55,6 +55,29 @@ enum : int {
   B_DR = 15, NBARS = 16
 };
 
+// max(a, b, c) in one instruction (the three-input form of max.f32)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two fp32 values as one 64-bit operand of the paired fp32 instructions, and back.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// a * b + c on both halves in one instruction (round to nearest)
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // acc + lo + hi of an fp16 pair, each half widened exactly inside the add
 __device__ __forceinline__ float add_f16x2_f32(float acc, uint32_t pk) {
   asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.f32.f16 %0, lo, %0;\n\tadd.f32.f16 %0, hi, %0;\n\t}"
@@ -154,13 +177,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int kiss = 0, viss = 0;  // key blocks whose K / V copies were issued
-      mbar_arrive_expect_tx(bar(B_QF), QT * C::TILE);
+      // every copy's x coordinate is a head's column offset + 64 c (16-byte aligned)
+      const bool coords_ok = TP_DCHECK(cQ % 8 == 0 && cK % 8 == 0 && cV % 8 == 0 && cV + D <= a.qkv_width() &&
+                                           b < a.B && shard < a.N,
+                                       err);
+      if (coords_ok) mbar_arrive_expect_tx(bar(B_QF), QT * C::TILE);
 #pragma unroll
       for (int t = 0; t < QT; ++t)
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
-          tma_load_4d(sQ(t) + c * 16384, &tmQKV, bar(B_QF), cQ + 64 * c, q0 + t * BQ, b, shard);
-      for (int kv = 0; kv < nkv; ++kv) {
+          if (coords_ok) tma_load_4d(sQ(t) + c * 16384, &tmQKV, bar(B_QF), cQ + 64 * c, q0 + t * BQ, b, shard);
+      for (int kv = 0; kv < nkv && coords_ok; ++kv) {
         const int st = kv & 1;
         const uint32_t ph = static_cast<uint32_t>((kv >> 1) & 1);
         if (!mbar_wait(bar(B_KE + st), ph ^ 1u, wc)) break;
@@ -177,7 +204,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         viss = kv + 1;
       }
       // every issued copy lands before the CTA may exit
-      mbar_wait(bar(B_QF), 0, wdrain);
+      if (coords_ok) mbar_wait(bar(B_QF), 0, wdrain);
       for (int k = (kiss > 2 ? kiss - 2 : 0); k < kiss; ++k)
         mbar_wait(bar(B_KF + (k & 1)), static_cast<uint32_t>((k >> 1) & 1), wdrain);
       for (int k = (viss > 2 ? viss - 2 : 0); k < viss; ++k)
@@ -284,12 +311,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int e = 0; e < 32; ++e)
             if (kbase + 32 * c + e > klim) v[c][e] = __float_as_uint(-INFINITY);
       }
-      // row max (raw scores; the scale is positive)
+      // row max (raw scores; the scale is positive), two scores per instruction
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < BKV / 32; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(v[c][e]));
+        for (int e = 0; e < 32; e += 2)
+          mx[(e >> 1) & 3] = fmax3(mx[(e >> 1) & 3], __uint_as_float(v[c][e]), __uint_as_float(v[c][e + 1]));
       const float bmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
       // the running max moves only when the block's exceeds it by the threshold; O
       // is then rescaled after P is written, when the score registers are dead
@@ -309,14 +337,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // P = exp2(s * scale - m) as fp16 (masked scores are -inf: exp2 gives 0; P <= 2^8,
       // and a P below fp16's normal range keeps an absolute error under 2^-25),
       // written over the first 64 of the columns just read
+      // the exponent arguments s * scale - m two at a time (paired fp32 FMA)
       float ls[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      const uint64_t sc2 = f32x2(scale_log2, scale_log2), nm2 = f32x2(-m_use, -m_use);
 #pragma unroll
       for (int c = 0; c < BKV / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e]), scale_log2, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][2 * e + 1]), scale_log2, -m_use));
+          float x0, x1;
+          f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[c][2 * e]), __uint_as_float(v[c][2 * e + 1])), sc2, nm2), x0,
+                      x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
           pk[e] = pack_f16x2(p0, p1);
           ls[e & 3] = add_f16x2_f32(ls[e & 3], pk[e]);
         }
@@ -372,7 +405,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int cb = 0; cb < C::CH; ++cb) tma_store_4d(&tmO, stage + cb * 4096, jj * D + 64 * cb, qrow0, b, shard);
         bulk_commit();
       }
-      if (q < a.S) lse[(static_cast<size_t>(b) * a.H + j) * a.S + q] = (m + log2f(l)) * 0.6931471805599453f;
+      const size_t li = (static_cast<size_t>(b) * a.H + j) * a.S + q;
+      if (q < a.S && TP_DCHECK(li < static_cast<size_t>(a.B) * a.H * a.S, err))
+        lse[li] = (m + log2f(l)) * 0.6931471805599453f;
     }
     __syncwarp();
     if (lane == 0) bulk_wait0();

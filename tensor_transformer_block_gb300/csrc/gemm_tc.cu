@@ -313,6 +313,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sa = sbase + stage * STAGE_BYTES;
             const uint32_t sb = sa + A_BYTES;
             const int kc = kb * BK;
+            // every x coordinate below is kc, arow + 64 j or bcol + 64 j (or 0): a copy
+            // must start on a 16-byte boundary and inside the operand's extent
+            if (!TP_DCHECK(kc % 8 == 0 && arow % 8 == 0 && bcol % 8 == 0 && arow >= 0 && bcol >= 0 &&
+                               arow < p.tiles_m * C::TILE_M && az >= 0 && bz >= 0,
+                           p.err)) {
+              ok = false;
+              break;
+            }
             if (PAIR) {
               const uint32_t fb = mapa_shared(fb_local, lead);  // the even CTA's full barrier counts both
               if (leader) mbar_arrive_expect_tx(fb_local, 2 * STAGE_BYTES);
@@ -500,7 +508,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int col0 = nb * TILE_N + half * WARP_COLS;
       int nch = col0 < p.N ? (p.N - col0 + CW - 1) / CW : 0;
       if (nch > WARP_COLS / CW) nch = WARP_COLS / CW;
-      const bool rows_valid = row0 < p.M && nch > 0;
+      // the staged boxes start at x = col0 + CW j (16-byte aligned) in group g < G;
+      // the condition is the same for every lane of the warp
+      const bool rows_valid =
+          row0 < p.M && nch > 0 && TP_DCHECK(col0 % 8 == 0 && row0 >= 0 && g >= 0 && g < p.G, p.err);
       if ((EPI == kEpiDGelu || EPI == kEpiResidual) && rows_valid) {
         const uint32_t b = ecount & 1u;
         if (lane == 0) {

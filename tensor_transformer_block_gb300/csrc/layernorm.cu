@@ -88,7 +88,7 @@ template <int VPT>
 __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma,
                                                  const uint4* __restrict__ beta, uint4* __restrict__ Y,
                                                  float* __restrict__ mean, float* __restrict__ rstd, int T,
-                                                 int nvec, float inv_h, float eps, int io) {
+                                                 int nvec, float inv_h, float eps, int io, unsigned* err) {
   __shared__ float red[64];
   const bool x16 = io & kLnXF16, y16 = io & kLnYF16;
   int64_t row = blockIdx.x;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
-      if (i < nvec) {
+      if (i < nvec && TP_DCHECK(row * nvec + i < static_cast<int64_t>(T) * nvec, err)) {
         float g[8], b[8], o[8];
         unpack8(gamma[i], g);
         unpack8(beta[i], b);
@@ -157,7 +157,8 @@ template <int VPT, bool PF>
 __global__ void __launch_bounds__(PF ? 512 : 1024)
     k_ln_bwd(const uint4* __restrict__ X, const uint4* __restrict__ gamma, const float* __restrict__ mean,
              const float* __restrict__ rstd, const uint4* __restrict__ dY, const uint4* __restrict__ dR,
-             uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h, int io) {
+             uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h, int io,
+             unsigned* err) {
   __shared__ float red[64];
   const bool x16 = io & kLnXF16, dy16 = io & kLnDyF16, dr16 = io & kLnDrF16, dx16 = io & kLnDxF16;
   float gm[VPT][8], pg[VPT][8], pb[VPT][8];
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(PF ? 512 : 1024)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int i = threadIdx.x + k * blockDim.x;
-      if (i < nvec) {
+      if (i < nvec && TP_DCHECK(row * nvec + i < static_cast<int64_t>(T) * nvec, err)) {
         float o[8], rr[8];
         // zero without a residual (without the prefetch, loaded only now)
         unpack8(PF ? cur.dr[k] : (dR ? dR[row * nvec + i] : make_uint4(0u, 0u, 0u, 0u)), rr, dr16);
@@ -331,7 +332,7 @@ size_t ln_partial_bytes(int64_t T, int64_t h) {
 }
 
 int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, float* mean, float* rstd, int64_t T,
-                  int64_t h, float eps, cudaStream_t st, int io) {
+                  int64_t h, float eps, cudaStream_t st, int io, unsigned* err) {
   if (!ln_shape_ok(T, h)) return 1;
   const LnGeom g = ln_fwd_geom(h);
   const int nvec = static_cast<int>(h / 8);
@@ -351,9 +352,11 @@ int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, f
   const int slot = timing_begin(kKLnFwd, st);
   const dim3 grid(static_cast<unsigned>(nb));
   if (g.vpt == 4)
-    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io);
+    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io,
+                                            err);
   else
-    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io);
+    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io,
+                                            err);
   const bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
@@ -361,7 +364,7 @@ int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, f
 
 int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const float* rstd, const void* dY,
                   const void* dR, void* dX, void* dgamma, void* dbeta, float* part, int64_t T, int64_t h,
-                  cudaStream_t st, int io) {
+                  cudaStream_t st, int io, unsigned* err) {
   if (!ln_shape_ok(T, h)) return 1;
   const LnGeom g = ln_geom(h);
   const int nvec = static_cast<int>(h / 8);
@@ -386,13 +389,13 @@ int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const flo
   int slot = timing_begin(kKLnBwd, st);
   if (g.pf && g.vpt == 2)
     k_ln_bwd<2, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h, io);
+                                                 inv_h, io, err);
   else if (g.pf)
     k_ln_bwd<1, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h, io);
+                                                 inv_h, io, err);
   else
     k_ln_bwd<2, false><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                  inv_h, io);
+                                                  inv_h, io, err);
   bool ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;

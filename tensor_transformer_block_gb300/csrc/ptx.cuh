@@ -10,6 +10,18 @@ namespace tpb {
 
 // Device error word bits (latched with atomicOr, read and cleared by the host).
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrBounds = 2u;  // a debug build's bounds or alignment check failed
+
+// Debug builds (-DTPBLOCK_DEBUG) check indices and TMA coordinates on the device:
+// a failed check latches kErrBounds in the error word and the access is skipped
+// (a skipped copy leaves its barrier short, so the wait for it runs out and the
+// kernel returns through the timeout path).  Release builds compile the checks
+// away.
+#ifdef TPBLOCK_DEBUG
+#define TP_DCHECK(cond, err) ((cond) ? true : (atomicOr((err), ::tpb::kErrBounds), false))
+#else
+#define TP_DCHECK(cond, err) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

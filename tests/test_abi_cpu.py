@@ -34,7 +34,7 @@ def test_exports_every_header_function(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert tp.tp_status_string(s) != "unknown status"
     assert tp.tp_status_string(99) == "unknown status"
     assert tp.tp_version() > 0
