@@ -44,14 +44,14 @@ DEFAULT_WORKLOAD = "mlp_bf16_T8192_h4096_f16384_N8"
 # the sha256 of the kernel source it was taken on; reported as null once the
 # source has changed.
 NCU_TRAFFIC: dict = {
-    k: {"bytes": v, "sha": "549a00c422b99dae", "workload": "mlp_bf16_T8192_h4096_f16384_N8"}
+    k: {"bytes": v, "sha": "00de2e47bef2d6bb", "workload": "mlp_bf16_T8192_h4096_f16384_N8"}
     for k, v in {
-        "mlp.fc1_col_gemm_gelu": 1027684608,
-        "mlp.fc2_row_gemm_shard_sum": 1459828480,
-        "mlp.bwd_dA_gemm_dgelu": 1143380736,
-        "mlp.bwd_dW2_gemm": 1336691200,
-        "mlp.bwd_dW1_gemm": 1295062016,
-        "mlp.bwd_dX_row_gemm_shard_sum": 1470222848,
+        "mlp.fc1_col_gemm_gelu": 1026003712,
+        "mlp.fc2_row_gemm_shard_sum": 1509922304,
+        "mlp.bwd_dA_gemm_dgelu": 1141448960,
+        "mlp.bwd_dW2_gemm": 1326806272,
+        "mlp.bwd_dW1_gemm": 1274430976,
+        "mlp.bwd_dX_row_gemm_shard_sum": 1545751552,
     }.items()
 }
 
