@@ -117,33 +117,54 @@ __device__ __forceinline__ void decode_tile(int t, const GemmShape& p, int& g, i
 // smoothly).  exp2 and the reciprocal are the special-function unit's approximations
 // (about 1 ulp of fp32): the results are rounded to bf16, and the correctly rounded
 // reciprocal cost ~2% of the fused GEMMs' time.
-__device__ __forceinline__ float gelu_sigmoid(float x, float x2, float& oms) {
-  const float a = fminf(x * fmaf(-0.1029432395800235f, x2, -2.302208198144325f), 126.0f);
-  const float e = ex2_approx(a);
-  const float s = rcp_approx(1.0f + e);
-  oms = e * s;  // 1 - s without cancellation
-  return s;
+// Two values are computed at once: the fp32 arithmetic in paired instructions (each
+// half rounded as the scalar instruction rounds it), the clamp, exponential and
+// reciprocal per element.  That halves the issue cost of the fused epilogues' math,
+// which shares its sub-partitions with the MMA and TMA warps.  s and oms = 1 - s
+// (= e^(-2u) s, no cancellation) of the pair x (x2 = x^2):
+__device__ __forceinline__ void gelu_sigmoid2(uint64_t x, uint64_t x2, uint64_t& s, uint64_t& oms) {
+  const uint64_t k3 = f32x2(-0.1029432395800235f, -0.1029432395800235f);
+  const uint64_t k1 = f32x2(-2.302208198144325f, -2.302208198144325f);
+  float a0, a1;
+  f32x2_split(mul_f32x2(x, fma_f32x2(k3, x2, k1)), a0, a1);
+  const float e0 = ex2_approx(fminf(a0, 126.0f)), e1 = ex2_approx(fminf(a1, 126.0f));
+  const uint64_t e = f32x2(e0, e1);
+  float d0, d1;
+  f32x2_split(add_f32x2(f32x2(1.0f, 1.0f), e), d0, d1);
+  s = f32x2(rcp_approx(d0), rcp_approx(d1));
+  oms = mul_f32x2(e, s);
 }
 
-__device__ __forceinline__ float gelu_f(float x) {
-  float oms;
-  return x * gelu_sigmoid(x, x * x, oms);
+// GeLU of two values (the pair (lo, hi) of ``x``)
+__device__ __forceinline__ uint64_t gelu2(uint64_t x) {
+  uint64_t s, oms;
+  gelu_sigmoid2(x, mul_f32x2(x, x), s, oms);
+  return mul_f32x2(x, s);
 }
 
-__device__ __forceinline__ float gelu_grad_f(float x) {
-  const float x2 = x * x;
-  float oms;
-  const float s = gelu_sigmoid(x, x2, oms);
-  return s * fmaf(x * oms, fmaf(0.21406444881780076f, x2, 1.5957691216057308f), 1.0f);
+// da * GeLU'(y) for two values
+__device__ __forceinline__ uint64_t dgelu2(uint64_t da, uint64_t y) {
+  const uint64_t y2 = mul_f32x2(y, y);
+  uint64_t s, oms;
+  gelu_sigmoid2(y, y2, s, oms);
+  const uint64_t d2 = f32x2(0.21406444881780076f, 0.21406444881780076f);
+  const uint64_t d0 = f32x2(1.5957691216057308f, 1.5957691216057308f);
+  const uint64_t g =
+      mul_f32x2(s, fma_f32x2(mul_f32x2(y, oms), fma_f32x2(d2, y2, d0), f32x2(1.0f, 1.0f)));
+  return mul_f32x2(da, g);
 }
 
-// Logistic sigmoid s = 1 / (1 + e^(-x)) and 1 - s = e^(-x) s (no cancellation);
-// silu(x) = x s, silu'(x) = s (1 + x (1 - s)).  The exponent is clamped as above.
-__device__ __forceinline__ void sigmoid_parts(float x, float& s, float& oms) {
-  const float a = fminf(-1.4426950408889634f * x, 126.0f);  // -x log2(e)
-  const float e = ex2_approx(a);
-  s = rcp_approx(1.0f + e);
-  oms = e * s;
+// Logistic sigmoid s = 1 / (1 + e^(-x)) and 1 - s = e^(-x) s (no cancellation) of
+// a pair; silu(x) = x s, silu'(x) = s (1 + x (1 - s)).  Clamped and paired as above.
+__device__ __forceinline__ void sigmoid2(uint64_t x, uint64_t& s, uint64_t& oms) {
+  float a0, a1;
+  f32x2_split(mul_f32x2(f32x2(-1.4426950408889634f, -1.4426950408889634f), x), a0, a1);  // -x log2(e)
+  const float e0 = ex2_approx(fminf(a0, 126.0f)), e1 = ex2_approx(fminf(a1, 126.0f));
+  const uint64_t e = f32x2(e0, e1);
+  float d0, d1;
+  f32x2_split(add_f32x2(f32x2(1.0f, 1.0f), e), d0, d1);
+  s = f32x2(rcp_approx(d0), rcp_approx(d1));
+  oms = mul_f32x2(e, s);
 }
 
 // Tile copies of an operand whose second coordinate c1 may be a token of a
@@ -589,9 +610,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(v[8 * hh + e]);
                 const uint32_t off = soff(c);
-                st_shared_v4(ebuf[0] + off, pack_bf16x2(gelu_f(x[0]), gelu_f(x[1])),
-                             pack_bf16x2(gelu_f(x[2]), gelu_f(x[3])), pack_bf16x2(gelu_f(x[4]), gelu_f(x[5])),
-                             pack_bf16x2(gelu_f(x[6]), gelu_f(x[7])));
+                uint32_t gq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  float g0, g1;
+                  f32x2_split(gelu2(f32x2(x[2 * e], x[2 * e + 1])), g0, g1);
+                  gq[e] = pack_bf16x2(g0, g1);
+                }
+                st_shared_v4(ebuf[0] + off, gq[0], gq[1], gq[2], gq[3]);
                 if (p.store_y)
                   st_shared_v4(ebuf[1] + off, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
                                pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
@@ -621,12 +647,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint32_t a[4], gg[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  float s0, o0, s1, o1;
                   const float g0 = __uint_as_float(vg[8 * hh + 2 * e]), g1 = __uint_as_float(vg[8 * hh + 2 * e + 1]);
-                  sigmoid_parts(g0, s0, o0);
-                  sigmoid_parts(g1, s1, o1);
-                  a[e] = pack_bf16x2(g0 * s0 * __uint_as_float(vu[8 * hh + 2 * e]),
-                                     g1 * s1 * __uint_as_float(vu[8 * hh + 2 * e + 1]));
+                  const uint64_t g2 = f32x2(g0, g1);
+                  uint64_t s2, o2;
+                  sigmoid2(g2, s2, o2);
+                  float a0, a1;
+                  f32x2_split(mul_f32x2(mul_f32x2(g2, s2), f32x2(__uint_as_float(vu[8 * hh + 2 * e]),
+                                                                 __uint_as_float(vu[8 * hh + 2 * e + 1]))),
+                              a0, a1);
+                  a[e] = pack_bf16x2(a0, a1);
                   gg[e] = pack_bf16x2(g0, g1);
                 }
                 const uint32_t off = soff(c);
@@ -700,19 +729,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ld_shared_v4(ebuf[1] + off, uq[0], uq[1], uq[2], uq[3]);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                  float r[2][2];
-#pragma unroll
-                  for (int k2 = 0; k2 < 2; ++k2) {
-                    const float gv = k2 ? bf16hi_to_f32(gq[e]) : bf16lo_to_f32(gq[e]);
-                    const float uv = k2 ? bf16hi_to_f32(uq[e]) : bf16lo_to_f32(uq[e]);
-                    const float da = __uint_as_float(v[8 * hh + 2 * e + k2]);
-                    float sg, om;
-                    sigmoid_parts(gv, sg, om);
-                    r[0][k2] = da * uv * (sg * fmaf(gv, om, 1.0f));  // dG = dA U silu'(G)
-                    r[1][k2] = da * gv * sg;                         // dU = dA silu(G)
-                  }
-                  dg[e] = pack_bf16x2(r[0][0], r[0][1]);
-                  du[e] = pack_bf16x2(r[1][0], r[1][1]);
+                  const uint64_t gv = f32x2(bf16lo_to_f32(gq[e]), bf16hi_to_f32(gq[e]));
+                  const uint64_t uv = f32x2(bf16lo_to_f32(uq[e]), bf16hi_to_f32(uq[e]));
+                  const uint64_t da = f32x2(__uint_as_float(v[8 * hh + 2 * e]), __uint_as_float(v[8 * hh + 2 * e + 1]));
+                  uint64_t sg, om;
+                  sigmoid2(gv, sg, om);
+                  float r0, r1, q0, q1;
+                  // dG = dA U silu'(G), dU = dA silu(G)
+                  f32x2_split(mul_f32x2(mul_f32x2(da, uv), mul_f32x2(sg, fma_f32x2(gv, om, f32x2(1.0f, 1.0f)))), r0,
+                              r1);
+                  f32x2_split(mul_f32x2(mul_f32x2(da, gv), sg), q0, q1);
+                  dg[e] = pack_bf16x2(r0, r1);
+                  du[e] = pack_bf16x2(q0, q1);
                 }
                 st_shared_v4(ebuf[0] + off, dg[0], dg[1], dg[2], dg[3]);
                 st_shared_v4(ebuf[1] + off, du[0], du[1], du[2], du[3]);
@@ -756,8 +784,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 for (int e = 0; e < 4; ++e) {
                   const float a0 = __uint_as_float(v[8 * hh + 2 * e]), a1 = __uint_as_float(v[8 * hh + 2 * e + 1]);
                   const float y0 = bf16lo_to_f32(yy[e]), y1 = bf16hi_to_f32(yy[e]);
-                  const float r0 = EPI == kEpiResidual ? a0 + y0 : a0 * gelu_grad_f(y0);
-                  const float r1 = EPI == kEpiResidual ? a1 + y1 : a1 * gelu_grad_f(y1);
+                  float r0, r1;
+                  if (EPI == kEpiResidual) {
+                    r0 = a0 + y0;
+                    r1 = a1 + y1;
+                  } else {
+                    f32x2_split(dgelu2(f32x2(a0, a1), f32x2(y0, y1)), r0, r1);
+                  }
                   o[e] = p.c_f16 ? pack_f16x2(r0, r1) : pack_bf16x2(r0, r1);
                 }
                 st_shared_v4(addr, o[0], o[1], o[2], o[3]);
