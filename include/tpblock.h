@@ -88,8 +88,15 @@ TP_API int tp_sync_status(void* stream);
 
 /* ---------------------------------------------------------------- MLP block */
 
-/* Bytes of scratch that tp_mlp_fwd (with A_save == NULL) and tp_mlp_bwd need:
- * one [N][T][f/N] activation-sized buffer plus alignment.  0 for invalid sizes. */
+/* Bytes of scratch for tp_mlp_fwd and tp_mlp_bwd: one [N][T][f/N] activation-sized
+ * buffer (A in the forward when A_save is NULL, dY in the backward), rounded up to
+ * 256 bytes, plus, for bf16 shapes whose row-parallel GEMMs (Z, dX) have too few
+ * tiles to fill the GPU (at most 76 tiles of 128 x 256, at least 32 K blocks of
+ * 64), room for their split-K partial sums: 2 x T x h fp32.  The activation-sized
+ * part is required; with the rest present those GEMMs run their K loop (the
+ * shards) in two halves on twice the SMs and a second kernel adds the two fp32
+ * partials in that fixed order (deterministic; a different rounding order than the
+ * unsplit sum).  0 for invalid sizes. */
 TP_API size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N);
 
 /* MLP block forward, Z = sum_i GeLU(X W1_i) W2_i.
@@ -421,7 +428,7 @@ TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
 
 /* Tiling of every GEMM the library launches (process-wide; for tests and
  * measurement): 0 = automatic (default: a CTA pair per 256 x 256 tile through
- * tcgen05 cta_group::2 when there are at least #SM/2 such tiles, else one CTA per
+ * tcgen05 cta_group::2 unless the output has at most 128 rows, then one CTA per
  * 128 x 256 tile), 1 = always one CTA per tile, 2 = always CTA pairs.  Every
  * tiling computes the same products; TP_ERR_SHAPE for another value (the setting
  * is then unchanged).  Each CTA loads only its own tiles: no TMA load is

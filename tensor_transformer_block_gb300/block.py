@@ -32,7 +32,7 @@ def mlp_forward(X, W1s, W2s, save: bool = True, ws=None, stream=None) -> dict:
     Z = torch.empty(T, h, dtype=X.dtype, device=dev)
     Y = torch.empty(N, T, fN, dtype=X.dtype, device=dev) if save else None
     A = torch.empty(N, T, fN, dtype=X.dtype, device=dev) if save else None
-    if A is None and ws is None:
+    if ws is None:  # scratch for A when it is not saved, and split-K partials for small shapes
         ws = workspace(B.tp_mlp_workspace_bytes(dt, T, h, f, N), dev)
     B.tp_mlp_fwd(dt, T, h, f, N, X, W1s, W2s, Y, A, Z, ws, stream)
     return {"Z": Z, "Y": Y, "A": A}

@@ -214,7 +214,7 @@ namespace {
 // ``W1_16`` (an fp16 copy of W1s) X holds fp16 values and a1 is an fp16 product.
 int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
                 void* Y_save, void* Abuf, void* Z, const void* residual, unsigned* err, cudaStream_t st, Sp sp = Sp(),
-                const void* W1_16 = nullptr) {
+                const void* W1_16 = nullptr, void* part_ws = nullptr, size_t part_bytes = 0) {
   const int64_t fN = f / N;
   // a1: Y_i = X W1_i, A_i = GeLU(Y_i)   (column-parallel, one group per shard; with
   // sequence-sharded X the copies gather the shards: the pages' all-gather g)
@@ -229,9 +229,13 @@ int mlp_fwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const voi
   const tpb::GemmOperand opA{Abuf, fN, T, N, false, 0, 1};
   const tpb::GemmOperand opW2{W2s, h, fN, N, true, 0, 1};
   // (sequence-sharded Z: the stores scatter the summed rows to their shards, the
-  // pages' reduce-scatter g*)
+  // pages' reduce-scatter g*).  With ``part_ws`` a launch too small to fill the GPU
+  // splits its K loop (the shards) in two halves added in fixed order.
+  tpb::GemmExtra e2 = out_sp(sp);
+  e2.part_ws = part_ws;
+  e2.part_ws_bytes = part_bytes;
   rc = tpb::launch_gemm_bf16(residual ? tpb::kEpiResidual : tpb::kEpiStore, opA, opW2, Z, residual, false, T, h, 1,
-                             N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2, out_sp(sp));
+                             N, fN, err, kWaitTimeoutNs, st, tpb::kKMlpFc2, e2);
   return gemm_status(rc);
 }
 
@@ -246,7 +250,8 @@ tpb::AttnDims attn_dims(int64_t B, int64_t S, int H, int Hkv, int d, int N, int 
 // written in fp16.
 int mlp_bwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s, const void* W2s,
                 const void* Y_save, const void* A_save, const void* dZ, void* dX, void* dW1s, void* dW2s, void* dY,
-                unsigned* err, cudaStream_t st, Sp sp, const void* W1_16 = nullptr) {
+                unsigned* err, cudaStream_t st, Sp sp, const void* W1_16 = nullptr, void* part_ws = nullptr,
+                size_t part_bytes = 0) {
   const int64_t fN = f / N;
   const bool h16 = W1_16 != nullptr;
   tpb::GemmExtra e16;
@@ -278,6 +283,8 @@ int mlp_bwd_seq(int64_t T, int64_t h, int64_t f, int N, const void* X, const voi
   tpb::GemmExtra e6 = out_sp(sp);
   e6.ab_f16 = h16;
   e6.c_f16 = h16;
+  e6.part_ws = part_ws;
+  e6.part_ws_bytes = part_bytes;
   rc = tpb::launch_gemm_bf16(tpb::kEpiStore, opdYk, opW1k, dX, nullptr, false, T, h, 1, N, fN, err, kWaitTimeoutNs,
                              st, tpb::kKMlpDx, e6);
   return gemm_status(rc);
@@ -380,10 +387,25 @@ int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
 extern "C" {
 
 // ------------------------------------------------------------------ MLP block
+}  // extern "C"
+
+namespace {
+// The MLP workspace: [A (forward, when not saved) or dY (backward) | split-K
+// partials of the two row-parallel GEMMs (Z, dX), for shapes too small to fill
+// the GPU otherwise].
+size_t mlp_act_bytes(int dtype, int64_t T, int64_t f) {
+  return round_up(static_cast<size_t>(T) * static_cast<size_t>(f) * (dtype == TP_F32 ? 4 : 2), 256);
+}
+size_t mlp_part_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N) {
+  return dtype == TP_BF16 ? round_up(tpb::gemm_splitk_bytes(T, h, 1, N, f / N), 256) : 0;
+}
+}  // namespace
+
+extern "C" {
+
 size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f, int N) {
   if (mlp_shape_check(dtype, T, h, f, N) != TP_OK) return 0;
-  const size_t esz = dtype == TP_F32 ? 4 : 2;
-  return round_up(static_cast<size_t>(T) * static_cast<size_t>(f) * esz, 256);
+  return mlp_act_bytes(dtype, T, f) + mlp_part_bytes(dtype, T, h, f, N);
 }
 
 int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
@@ -394,8 +416,8 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
   if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;
   if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Z) || !al16(Y_save) || !al16(A_save)) return TP_ERR_ALIGN;
   void* Abuf = A_save;
-  if (!Abuf) {
-    if (!ws || ws_bytes < tp_mlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+  if (!Abuf) {  // A in the workspace: at least its bytes
+    if (!ws || ws_bytes < mlp_act_bytes(dtype, T, f)) return TP_ERR_WORKSPACE;
     if (!al256(ws)) return TP_ERR_ALIGN;
     Abuf = ws;
   }
@@ -441,7 +463,11 @@ int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
     return gemm_status(tpb::launch_gemm_f32(a2, st, tpb::kKMlpF32Fc2));
   }
 
-  return mlp_fwd_seq(T, h, f, N, X, W1s, W2s, Y_save, Abuf, Z, nullptr, err, st);
+  // the partials region of the workspace, when the caller gave one that holds it
+  void* part = nullptr;
+  const size_t act = mlp_act_bytes(dtype, T, f), pb = mlp_part_bytes(dtype, T, h, f, N);
+  if (pb && ws && al256(ws) && ws_bytes >= act + pb) part = static_cast<char*>(ws) + act;
+  return mlp_fwd_seq(T, h, f, N, X, W1s, W2s, Y_save, Abuf, Z, nullptr, err, st, Sp(), nullptr, part, pb);
 }
 
 int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X, const void* W1s,
@@ -455,13 +481,16 @@ int tp_mlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N, const void* X,
   if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Y_save) || !al16(A_save) || !al16(dZ) || !al16(dX) ||
       !al16(dW1s) || !al16(dW2s))
     return TP_ERR_ALIGN;
-  if (!ws || ws_bytes < tp_mlp_workspace_bytes(dtype, T, h, f, N)) return TP_ERR_WORKSPACE;
+  if (!ws || ws_bytes < mlp_act_bytes(dtype, T, f)) return TP_ERR_WORKSPACE;  // dY
   if (!al256(ws)) return TP_ERR_ALIGN;
   unsigned* err = nullptr;
   const int dc = check_device(&err);
   if (dc != TP_OK) return dc;
+  // the split-K partials region, when the workspace holds it
+  const size_t act = mlp_act_bytes(dtype, T, f), pb = mlp_part_bytes(dtype, T, h, f, N);
+  void* part = (pb && ws_bytes >= act + pb) ? static_cast<char*>(ws) + act : nullptr;
   return mlp_bwd_seq(T, h, f, N, X, W1s, W2s, Y_save, A_save, dZ, dX, dW1s, dW2s, ws, err,
-                     static_cast<cudaStream_t>(stream), Sp());
+                     static_cast<cudaStream_t>(stream), Sp(), nullptr, part, pb);
 }
 
 }  // extern "C"
@@ -1092,7 +1121,7 @@ int tp_mlp_fwd_noalloc(int dtype, int64_t T, int64_t h, int64_t f, int N, const 
   if (sc != TP_OK) return sc;
   if (!X || !W1s || !W2s || !Z) return TP_ERR_NULL;
   if (!al16(X) || !al16(W1s) || !al16(W2s) || !al16(Z)) return TP_ERR_ALIGN;
-  if (tp_mlp_workspace_bytes(dtype, T, h, f, N) > static_cast<size_t>(TP_NOALLOC_SCRATCH_BYTES))
+  if (mlp_act_bytes(dtype, T, f) > static_cast<size_t>(TP_NOALLOC_SCRATCH_BYTES))
     return TP_ERR_WORKSPACE;  // the activation does not fit the fixed scratch array
   unsigned* err = nullptr;
   const int dc = check_device(&err);

@@ -49,7 +49,8 @@ constexpr int GROUP_M = 16;
 
 template <bool PAIR, int EPI>
 struct Cfg {
-  static constexpr int EBUFS = (EPI == kEpiStore || EPI == kEpiSplit) ? 1 : 2;  // staging boxes per warp
+  // staging boxes per warp
+  static constexpr int EBUFS = (EPI == kEpiStore || EPI == kEpiSplit || EPI == kEpiPartial) ? 1 : 2;
   // epilogue chunk: 32 rows x CW columns of bf16 (one box): 64 columns with 128-byte
   // swizzle for the one-box epilogues, 32 columns with 64-byte swizzle for the fused
   // ones, so that either stages 32 KB per CTA
@@ -299,8 +300,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
   const WaitCtx wdrain{p.err, never_flag, p.timeout_ns};
-  const int total = p.G * p.tiles_m * p.tiles_n;
+  const int tiles = p.G * p.tiles_m * p.tiles_n;
+  const int total = tiles * p.ksplit;  // work units: (split, tile), split-major
   const int nk = p.S * p.kb_per_seg;
+  // K blocks [kbeg, kend) of the unit's split
+  auto krange = [&](int t, int& kbeg, int& kend) {
+    const int split = t / tiles;
+    kbeg = split * p.kps;
+    kend = min(nk, kbeg + p.kps);
+  };
 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
@@ -315,17 +323,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int k_spL = a_k_sp ? p.a_spL : p.b_spL;
       const int k_nc = (a_k_sp || b_k_sp) ? (a_k_sp ? p.a_spS : p.b_spS) / k_spL : 1;
       for (int t = unit; t < total && ok; t += nunits) {
-        int g, mb, nb;
-        decode_tile(t, p, g, mb, nb);
+        int g, mb, nb, kbeg, kend;
+        decode_tile(t % tiles, p, g, mb, nb);
+        krange(t, kbeg, kend);
         const int arow = mb * C::TILE_M + static_cast<int>(rank) * BM;
         const int bcol = EPI == kEpiSwiGLU ? nb * TILE_N : nb * BN + static_cast<int>(rank) * C::BN_CTA;
         TokPos apos{0, 0, 0};
         if (a_rows_sp) tok_coords(arow, p.a_spS, p.a_spL, apos.sl, apos.b, apos.c);
-        for (int s = 0; s < p.S && ok; ++s) {
+        // the segments the split's K blocks fall in (a split starts inside a segment only
+        // without sequence-sharded K, where kpos is unused)
+        for (int s = kbeg / p.kb_per_seg; s < p.S && s * p.kb_per_seg < kend && ok; ++s) {
           const int az = g * p.a_zg + s * p.a_zs;
           const int bz = g * p.b_zg + s * p.b_zs;
           TokPos kpos{0, 0, 0};
-          for (int kb = 0; kb < p.kb_per_seg; ++kb) {
+          const int kb_lo = max(0, kbeg - s * p.kb_per_seg), kb_hi = min(p.kb_per_seg, kend - s * p.kb_per_seg);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(bar0 + 8u * (BAR_EMPTY + stage), phase ^ 1u, wc)) {
               ok = false;
               break;
@@ -453,13 +465,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = unit; t < total && ok; t += nunits, ++it) {
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
+        int kbeg, kend;
+        krange(t, kbeg, kend);
         if (!mbar_wait(bar0 + 8u * (BAR_TEMPTY + buf), tph ^ 1u, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t dt = tmem_base + static_cast<uint32_t>(buf * BN);
-        for (int k = 0; k < nk; ++k) {
+        for (int k = kbeg; k < kend; ++k) {
           if (!mbar_wait(bar0 + 8u * (BAR_FULL + stage), phase, wc)) {
             ok = false;
             break;
@@ -471,10 +485,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t ad = A_MN ? sdesc_sw128(sa + kk * 2048, BK * 128, 1024) : sdesc_sw128(sa + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(sb + kk * 2048, BK * 128, 1024) : sdesc_sw128(sb + kk * 32, 16, 1024);
+            const uint32_t acc = ((k - kbeg) | kk) != 0 ? 1u : 0u;
             if (PAIR)
-              tc_mma_bf16_pair(dt, ad, bd, IDESC, (k | kk) != 0 ? 1u : 0u);
+              tc_mma_bf16_pair(dt, ad, bd, IDESC, acc);
             else
-              tc_mma_bf16(dt, ad, bd, IDESC, (k | kk) != 0 ? 1u : 0u);
+              tc_mma_bf16(dt, ad, bd, IDESC, acc);
           }
           any = true;
           if (PAIR)
@@ -522,7 +537,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int t = unit; t < total && ok; t += nunits, ++it) {
       int g, mb, nb;
-      decode_tile(t, p, g, mb, nb);
+      decode_tile(t % tiles, p, g, mb, nb);
+      const int split = t / tiles;
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       const int row0 = mb * C::TILE_M + static_cast<int>(rank) * BM + quad * 32;
@@ -566,7 +582,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // The fused epilogues run as a rolled loop of 16-column TMEM loads: a
           // fully unrolled 64-column body is large enough to evict the MMA
           // warp's instructions from the cache the SM sub-partition shares.
-          if (EPI == kEpiStore || EPI == kEpiSplit) {
+          if (EPI == kEpiPartial) {
+            // fp32 partial sums: two boxes of 32 rows x 32 columns (128-byte rows,
+            // the same swizzle as the bf16 boxes), group split * G + g of the partials
+            uint32_t r0[32], r1[32];
+            tmem_ld32(tcol, r0);
+            tmem_ld32(tcol + 32, r1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb) {
+              if (ccol + 32 * hb >= p.N) break;  // no box that starts past the last column
+              const uint32_t* v = hb ? r1 : r0;
+              const uint32_t sb = ebuf[0];
+              if (lane == 0) bulk_wait_read0();
+              __syncwarp();
+#pragma unroll
+              for (int c = 0; c < 8; ++c) st_shared_v4(sb + soff(c), v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmC, sb, ccol + 32 * hb, row0, split * p.G + g);
+                bulk_commit();
+              }
+            }
+          } else if (EPI == kEpiStore || EPI == kEpiSplit) {
             // fp16 for the columns before split_cols (whole 64-column chunks)
             const bool f16 = ccol < p.split_cols;
             uint32_t r0[32], r1[32];
@@ -867,8 +907,54 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
   if (!a_mn && b_mn && epi == kEpiSwiGLU) return get_kernel<PAIR, false, true, kEpiSwiGLU>();
   if (!a_mn && !b_mn && epi == kEpiDSwiGLU) return get_kernel<PAIR, false, false, kEpiDSwiGLU>();
   if (!a_mn && b_mn && epi == kEpiResidual) return get_kernel<PAIR, false, true, kEpiResidual>();
+  if (!a_mn && b_mn && epi == kEpiPartial) return get_kernel<PAIR, false, true, kEpiPartial>();
+  if (!a_mn && !b_mn && epi == kEpiPartial) return get_kernel<PAIR, false, false, kEpiPartial>();
+  if (a_mn && b_mn && epi == kEpiPartial) return get_kernel<PAIR, true, true, kEpiPartial>();
   return nullptr;
 }
+
+// C[r][c] = fp(sum_{j=0}^{ksplit-1} part[j][r][c] (+ R[r][c])) over the G*M rows of N
+// columns, the splits added in index order (deterministic); 8 columns per thread,
+// 16-byte loads and stores; C and R are [G*M][ldc] 16-bit tensors (R bf16).
+__global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__ part, int ksplit, long long rows,
+                                                       int N, long long ldc, const uint4* __restrict__ R,
+                                                       uint4* __restrict__ C, int c_f16) {
+  const long long per_row = N / 8, n8 = rows * per_row, plane = rows * N;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
+    const long long row = i / per_row;
+    const int col = static_cast<int>(i - row * per_row) * 8;
+    const float* src = part + row * N + col;
+    float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+    for (int j = 1; j < ksplit; ++j) {
+      const float4 x = *reinterpret_cast<const float4*>(src + j * plane);
+      const float4 y = *reinterpret_cast<const float4*>(src + j * plane + 4);
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    }
+    float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const long long o = (row * ldc + col) / 8;
+    if (R) {
+      const uint4 r = R[o];
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] += bf16lo_to_f32(rw[e]);
+        v[2 * e + 1] += bf16hi_to_f32(rw[e]);
+      }
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = c_f16 ? pack_f16x2(v[2 * e], v[2 * e + 1]) : pack_bf16x2(v[2 * e], v[2 * e + 1]);
+    C[o] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// split-K is worth its second kernel when the tiles leave most of the GPU idle and
+// the K loop is long
+constexpr int64_t kSplitMaxTiles = 76;
+constexpr int64_t kSplitMinKBlocks = 32;
+constexpr int kSplit = 2;
 
 // An MN-major operand whose d0 is a multiple of 64: the 64-element chunks of a row
 // become an outer dimension, so a box {64, BK, chunks} lands in shared memory as the
@@ -926,6 +1012,14 @@ int g_tiling_mode = 0;  // 0 automatic, 1 single CTA per tile, 2 CTA pairs
 
 }  // namespace
 
+size_t gemm_splitk_bytes(int64_t M, int64_t N, int G, int S, int64_t Ks) {
+  if (M < 1 || N < 1 || G < 1 || S < 1 || Ks < 1) return 0;
+  const int64_t tiles = static_cast<int64_t>(G) * ((M + 127) / 128) * ((N + 255) / 256);
+  const int64_t nk = static_cast<int64_t>(S) * ((Ks + BK - 1) / BK);
+  if (tiles > kSplitMaxTiles || nk < kSplitMinKBlocks) return 0;
+  return static_cast<size_t>(kSplit) * static_cast<size_t>(G) * static_cast<size_t>(M) * static_cast<size_t>(N) * 4;
+}
+
 bool set_gemm_tiling_mode(int mode) {
   if (mode < 0 || mode > 2) return false;
   g_tiling_mode = mode;
@@ -963,11 +1057,26 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const int64_t tile_n = epi == kEpiSwiGLU ? BN / 2 : BN;
   const int sms = device_sm_count();
   if (sms <= 0) return 2;
-  // pair tiles when there are enough 256 x 256 tiles to give every SM pair work
+  // CTA pairs unless M fits one 128-row tile: a pair stages 32 KB per SM and k-block
+  // against 48 KB for a single CTA's 128 x 256 tile, and the SMs' L2 read bandwidth
+  // (about 64 bytes per clock each) is what a k-block's copies contend for; for a
+  // launch with few tiles both tilings occupy the same number of SMs
   const long long pair_tiles = static_cast<long long>(G) * ((M + 255) / 256) * ((N + tile_n - 1) / tile_n);
-  bool pair = g_tiling_mode >= 2 || (g_tiling_mode == 0 && pair_tiles >= sms / 2);
+  bool pair = g_tiling_mode >= 2 || (g_tiling_mode == 0 && M > 128);
   if (sms < 2) pair = false;
-  KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, epi) : pick_kernel<false>(A.mn_major, B.mn_major, epi);
+  // split-K for launches whose tiles leave most SMs idle: the K loop in two halves,
+  // fp32 partials in the caller's scratch, added in fixed order by k_splitk_reduce
+  // (its units: pair tiles on #SM/2 pairs, or single tiles on #SM CTAs)
+  const size_t split_bytes = gemm_splitk_bytes(M, N, G, S, Ks);
+  const int64_t units1 = pair ? pair_tiles : static_cast<int64_t>(G) * ((M + 127) / 128) * ((N + 255) / 256);
+  const bool split = split_bytes > 0 && extra.part_ws && extra.part_ws_bytes >= split_bytes &&
+                     (reinterpret_cast<uintptr_t>(extra.part_ws) & 255u) == 0 &&
+                     (epi == kEpiStore || epi == kEpiResidual) && extra.c_sp_S == 0 && A.sp_S == 0 && B.sp_S == 0 &&
+                     units1 * kSplit <= (pair ? sms / 2 : sms) &&
+                     (pair ? pick_kernel<true>(A.mn_major, B.mn_major, kEpiPartial)
+                           : pick_kernel<false>(A.mn_major, B.mn_major, kEpiPartial)) != nullptr;
+  const int kepi = split ? static_cast<int>(kEpiPartial) : epi;
+  KernelFn fn = pair ? pick_kernel<true>(A.mn_major, B.mn_major, kepi) : pick_kernel<false>(A.mn_major, B.mn_major, kepi);
   if (!fn) return 2;
   const uint32_t a_rows = 128, b_rows = pair ? Cfg<true, kEpiStore>::BN_CTA : Cfg<false, kEpiStore>::BN_CTA;
   const bool one_box = epi == kEpiStore || epi == kEpiSplit;
@@ -993,7 +1102,13 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
       return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, sdims, sbox, swz);
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, cdims, cbox, swz);
   };
-  if (epi == kEpiDSwiGLU) {
+  if (split) {  // fp32 partials [kSplit][G][M][N], 32 x 32 boxes (128-byte rows)
+    const uint64_t pdims[3] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                               static_cast<uint64_t>(kSplit) * static_cast<uint64_t>(G)};
+    const uint32_t pbox[3] = {32u, 32u, 1u};
+    if (!encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, extra.part_ws, pdims, pbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return 2;
+  } else if (epi == kEpiDSwiGLU) {
     if (!two_part_map(&tc, C, N, M, G, cw, swz)) return 2;
   } else if (!out_map(&tc, C)) {
     return 2;
@@ -1023,6 +1138,11 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
                                   : (epi == kEpiStore && extra.c_f16 ? 0x7fffffff : 0);
   p.ab_f16 = extra.ab_f16 ? 1 : 0;
   p.c_f16 = extra.c_f16 ? 1 : 0;
+  {
+    const int nkb = S * static_cast<int>((Ks + BK - 1) / BK);
+    p.ksplit = split ? kSplit : 1;
+    p.kps = (nkb + p.ksplit - 1) / p.ksplit;
+  }
   p.a_spS = A.sp_S;
   p.a_spL = A.sp_L;
   p.b_spS = B.sp_S;
@@ -1036,7 +1156,8 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   p.b_chunked = b_ch ? 1 : 0;
   p.err = err;
   p.timeout_ns = timeout_ns;
-  const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n;
+  const long long total = static_cast<long long>(G) * p.tiles_m * p.tiles_n * p.ksplit;
+  // with split-K the kind's time covers both kernels (one product per launch)
   const int slot = timing_begin(kind, stream);
   bool ok;
   if (pair) {
@@ -1061,6 +1182,17 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
     const int grid = static_cast<int>(total < sms ? total : sms);
     fn<<<grid, NUM_THREADS, static_cast<size_t>(smem), stream>>>(ta, tb, tc, ty, p);
     ok = cudaGetLastError() == cudaSuccess;
+  }
+  if (ok && split) {
+    const long long rows = static_cast<long long>(G) * M, n8 = rows * (N / 8);
+    long long blocks = (n8 + 255) / 256;
+    if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
+    const int rslot = timing_begin(kKSplitReduce, stream);
+    k_splitk_reduce<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const float*>(extra.part_ws), kSplit, rows, static_cast<int>(N), ldc,
+        epi == kEpiResidual ? static_cast<const uint4*>(Yaux) : nullptr, static_cast<uint4*>(C), p.c_f16);
+    ok = cudaGetLastError() == cudaSuccess;
+    timing_end(rslot, stream);
   }
   timing_end(slot, stream);
   return ok ? 0 : 2;

@@ -33,6 +33,10 @@ enum GemmEpi : int {
   kEpiDSwiGLU = 5,  // Yaux [G][M][2][N] holds G, U; C [G][M][2][N] gets
                     // C(.,0,.) = bf16(acc * U * silu'(G)), C(.,1,.) = bf16(acc * silu(G))
   kEpiResidual = 6,  // C = bf16(acc + R), R = Yaux [G][M][ldc] (a residual connection)
+  // split-K: the fp32 accumulator of one K-split written to partial[split][G][M][N];
+  // a second kernel adds the splits in order 0, 1, ... and applies kEpiStore or
+  // kEpiResidual (chosen by the launcher, never passed in)
+  kEpiPartial = 7,
 };
 
 struct GemmShape {
@@ -45,6 +49,8 @@ struct GemmShape {
   int store_y;                 // kEpiGelu: also write the pre-activation
   int split_cols;              // kEpiStore / kEpiSplit: columns < split_cols are stored as fp16
   int ab_f16;                  // A and B are fp16 (else bf16); one MMA's operands share a type
+  int ksplit;                  // K-splits per output tile (1: none); tile index = split * tiles + tile
+  int kps;                     // 64-wide K blocks per split
   int c_f16;                   // kEpiDGelu, kEpiResidual: the output C is fp16 (else bf16)
   // token remaps (0 = off): the operand's row coordinate t (A, B: d1; C, Yaux: M)
   // is a token b*S + s stored at [s / L][b][s % L] (sequence-sharded layout)
@@ -80,6 +86,11 @@ struct GemmExtra {
   int64_t split_cols = 0;  // kEpiSplit (a multiple of 64)
   bool c_f16 = false;      // the whole output C in fp16 (kEpiStore, kEpiDGelu, kEpiResidual)
   bool ab_f16 = false;     // A and B hold fp16 values (both; tcgen05 kind::f16 takes one type)
+  // scratch for split-K partial sums (kEpiStore / kEpiResidual): when it holds
+  // gemm_splitk_bytes() and the launch has too few tiles to fill the GPU, the K loop
+  // is split in two and the partials added by a second kernel in fixed order
+  void* part_ws = nullptr;
+  size_t part_ws_bytes = 0;
   int c_sp_S = 0, c_sp_L = 0;  // sequence-sharded rows of C and Yaux (kEpiStore, kEpiResidual)
 };
 int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* C, const void* Yaux,
@@ -87,7 +98,11 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
                      unsigned long long timeout_ns, cudaStream_t stream, int kind,
                      const GemmExtra& extra = GemmExtra());
 
-// 0: choose per launch (CTA pairs when there are at least #SM/2 tiles of 256 x 256),
+// Bytes of split-K partials a launch of this shape may use (0: it never splits):
+// launches with at most 76 single-CTA tiles of 128 x 256 and at least 32 K blocks.
+size_t gemm_splitk_bytes(int64_t M, int64_t N, int G, int S, int64_t Ks);
+
+// 0: choose per launch (CTA pairs unless M <= 128),
 // 1: always one CTA per 128 x 256 tile, 2: always a CTA pair per 256 x 256 tile.
 // Returns false (and keeps the mode) for another value.
 bool set_gemm_tiling_mode(int mode);

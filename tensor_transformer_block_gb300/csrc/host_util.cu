@@ -95,7 +95,8 @@ const char* const kKindNames[kNumKernelKinds] = {
     "attn.bwd_dsum", "attn.bwd_core_dkdv", "attn.bwd_core_dq", "attn.bwd_dWqkv_gemm",
     "attn.bwd_dX_row_gemm_shard_sum", "gmlp.fc1_col_gemm_swiglu", "gmlp.fc2_row_gemm_shard_sum",
     "gmlp.bwd_dA_gemm_dswiglu", "gmlp.bwd_dWd_gemm", "gmlp.bwd_dWgu_gemm", "gmlp.bwd_dX_row_gemm_shard_sum",
-    "ln.fwd", "ln.bwd_residual", "ln.bwd_colsum", "debug.timeout_probe", "cast.bf16_to_f16"};
+    "ln.fwd", "ln.bwd_residual", "ln.bwd_colsum", "debug.timeout_probe", "cast.bf16_to_f16",
+    "gemm.splitk_reduce"};
 
 struct Slot {
   int kind;

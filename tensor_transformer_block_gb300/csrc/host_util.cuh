@@ -59,6 +59,7 @@ enum KernelKind : int {
   kKLnColsum,       // fixed-order sum of the partial rows -> dgamma, dbeta
   kKProbe,          // timeout probe
   kKCast,           // bf16 -> fp16 copy of a weight matrix
+  kKSplitReduce,    // fixed-order sum of split-K partials (+ residual), 16-bit output
   kNumKernelKinds
 };
 const char* kernel_kind_name(int k);

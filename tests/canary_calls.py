@@ -53,6 +53,16 @@ def run_calls() -> list:
     tp.tp_mlp_bwd(tp.TP_BF16, T, h, f, N, m["X"], m["W1s"], m["W2s"], Y, A, m["dZ"], g("mlp.dX", (T, h)),
                   g("mlp.dW1s", (N, h, f // N)), g("mlp.dW2s", (N, f // N, h)), ws.t)
     tp.tp_mlp_fwd_noalloc(tp.TP_BF16, T, h, f, N, m["X"], m["W1s"], m["W2s"], g("mlp.Z_noalloc", (T, h)))
+    # a shape whose row-parallel GEMMs split K (fp32 partials in the workspace)
+    Ts, hs, fs, Ns = 1000, 520, 2048, 2
+    ms = {k: v.cuda() for k, v in inputs.mlp_inputs(Ts, hs, fs, Ns, seed=9).items()}
+    wss = _ws(tp.tp_mlp_workspace_bytes(tp.TP_BF16, Ts, hs, fs, Ns))
+    bufs["mlp_split.ws"] = wss
+    Ys, As = g("mlp_split.Y", (Ns, Ts, fs // Ns)), g("mlp_split.A", (Ns, Ts, fs // Ns))
+    tp.tp_mlp_fwd(tp.TP_BF16, Ts, hs, fs, Ns, ms["X"], ms["W1s"], ms["W2s"], Ys, As, g("mlp_split.Z", (Ts, hs)), wss.t)
+    tp.tp_mlp_bwd(tp.TP_BF16, Ts, hs, fs, Ns, ms["X"], ms["W1s"], ms["W2s"], Ys, As, ms["dZ"],
+                  g("mlp_split.dX", (Ts, hs)), g("mlp_split.dW1s", (Ns, hs, fs // Ns)),
+                  g("mlp_split.dW2s", (Ns, fs // Ns, hs)), wss.t)
     m32 = {k: v.cuda() for k, v in inputs.mlp_inputs(64, 256, 1024, 2, dtype="f32", seed=2, backward=False).items()}
     ws32 = _ws(tp.tp_mlp_workspace_bytes(tp.TP_F32, 64, 256, 1024, 2))
     bufs["mlp32.ws"] = ws32
