@@ -206,7 +206,10 @@ TP_API int tp_gmlp_bwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
 
 /* ---------------------------------------------------------- attention block */
 
-/* Bytes of scratch tp_attn_fwd (with NULL saves) and tp_attn_bwd need. */
+/* Bytes of scratch tp_attn_fwd (with NULL saves) and tp_attn_bwd need: the
+ * forward's QKV, O and LSE (or the backward's dQKV, dO and Dsum in the same
+ * regions), plus the backward's dS tiles, B x H x ceil(S/128)^2 x 32 KB (fp16
+ * 128 x 128 tiles of dS, which the dQ kernel multiplies by K). */
 TP_API size_t tp_attn_workspace_bytes(int dtype, int64_t B, int64_t S, int64_t h, int H, int d, int N);
 
 /* Self-attention block forward (bf16), heads split over N shards.

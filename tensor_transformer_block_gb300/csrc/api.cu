@@ -137,18 +137,23 @@ int attn_shape_check(int dtype, int64_t B, int64_t S, int64_t h, int H, int Hkv,
   return TP_OK;
 }
 
-// Workspace of the attention block: [QKV (fp16 Q, K; bf16 V) | O |
-// LSE] in the forward; [dQKV | dO | Dsum] in the backward fits the same regions.
+// Workspace of the attention block: [QKV (fp16 Q, K, V) | O | LSE] in the
+// forward; [dQKV | dO | Dsum | dS tiles] in the backward, the first three in the
+// same regions.  The dS tiles (128 x 128 fp16 per query head, query block and key
+// block) are sized for all block pairs, causal or not: the size queries take no
+// mask flag.
 struct AttnWs {
-  size_t qkv, o, lse, total;
+  size_t qkv, o, lse, ds, total;
 };
 AttnWs attn_ws(int64_t B, int64_t S, int H, int Hkv, int d) {
   const size_t T = static_cast<size_t>(B) * static_cast<size_t>(S);
+  const size_t nb = (static_cast<size_t>(S) + 127) / 128;
   AttnWs w;
   w.qkv = round_up(T * (static_cast<size_t>(H) + 2 * static_cast<size_t>(Hkv)) * static_cast<size_t>(d) * 2, 256);
   w.o = round_up(T * static_cast<size_t>(H) * static_cast<size_t>(d) * 2, 256);
   w.lse = round_up(T * static_cast<size_t>(H) * 4, 256);
-  w.total = w.qkv + w.o + w.lse;
+  w.ds = static_cast<size_t>(B) * static_cast<size_t>(H) * nb * nb * 128 * 128 * 2;
+  w.total = w.qkv + w.o + w.lse + w.ds;
   return w;
 }
 
@@ -344,6 +349,7 @@ int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
   void* dQKV = wsb;
   void* dO = wsb + w.qkv;
   float* dsum = reinterpret_cast<float*>(wsb + w.qkv + w.o);
+  void* dsbuf = wsb + w.qkv + w.o + w.lse;
 
   // dO_i = dZ Wo_i^T   (row-parallel backward: every shard sees the whole dZ); fp16
   const tpb::GemmOperand opdZk = with_sp(tpb::GemmOperand{dZ, h, T, 1, false, 0, 0}, sp);
@@ -363,7 +369,7 @@ int attn_bwd_seq(int64_t B, int64_t S, int64_t h, int H, int Hkv, int d, int N, 
                              st, tpb::kKAttnDwo, ewo);
   if (rc) return gemm_status(rc);
   // attention core backward -> dQKV
-  rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dQKV, err, kWaitTimeoutNs, st);
+  rc = tpb::launch_attn_bwd(ad, QKV_save, O_save, dO, LSE_save, dsum, dsbuf, dQKV, err, kWaitTimeoutNs, st);
   if (rc) return gemm_status(rc);
   // dWqkv_i = X^T dQKV_i
   const tpb::GemmOperand opXt = with_sp(tpb::GemmOperand{X, h, T, 1, true, 0, 0}, sp);

@@ -77,6 +77,24 @@ inline WorkOrder make_work_order(int units, int blocks, int sms) {
   return WorkOrder{units, blocks, group};
 }
 
+// dS tiles written by the dK/dV kernel and read by the dQ kernel: for every
+// (batch, query head, query block qb, key block kb) the core visits, 128 keys x 128
+// queries of fp16 dS^T (key rows, query columns contiguous: 32 KB).  A head's tiles
+// are ordered by query block, then key block: qb (qb + 1) / 2 + kb with the causal
+// mask (kb <= qb), qb * nb + kb without it.
+__host__ __device__ inline long long ds_tiles_per_head(const AttnDims& a) {
+  const long long nb = (a.S + 127) / 128;
+  return a.causal ? nb * (nb + 1) / 2 : nb * nb;
+}
+__host__ __device__ inline long long ds_tiles(const AttnDims& a) {
+  return static_cast<long long>(a.B) * a.H * ds_tiles_per_head(a);
+}
+__host__ __device__ inline long long ds_tile_index(const AttnDims& a, int b, int j, int qb, int kb) {
+  const long long nb = (a.S + 127) / 128;
+  const long long within = a.causal ? static_cast<long long>(qb) * (qb + 1) / 2 + kb : qb * nb + kb;
+  return (static_cast<long long>(b) * a.H + j) * ds_tiles_per_head(a) + within;
+}
+
 // Number of d-wide planes per (token, local head) in QKV without grouping.
 constexpr int kQkvPlanes = 3;
 
@@ -86,7 +104,9 @@ int launch_attn_fwd(const AttnDims& a, const void* qkv, void* o, float* lse, uns
 
 // Backward cores.  Dsum[b][j][s] = sum_e dO * O over the head dim; dqkv gets dQ,
 // dK, dV (a key/value head's gradient summed over the query heads of its group).
+// ``dsbuf``: scratch of ds_tiles(a) x 32 KB (16-byte aligned) for the dS tiles.
 int launch_attn_bwd(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse,
-                    float* dsum, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st);
+                    float* dsum, void* dsbuf, void* dqkv, unsigned* err, unsigned long long timeout_ns,
+                    cudaStream_t st);
 
 }  // namespace tpb

@@ -145,7 +145,8 @@ struct DkdvCfg {
   static constexpr int OFF_Q = 2 * TILE;           // [stage][Q, dO]
   static constexpr int OFF_LSE = OFF_Q + 4 * TILE; // [2][128] fp32
   static constexpr int OFF_DD = OFF_LSE + 1024;    // [2][128] fp32
-  static constexpr int OFF_BAR = OFF_DD + 1024;
+  static constexpr int OFF_STG = OFF_DD + 1024;    // [8 warps] 32 keys x 32 queries fp16: dS^T staging
+  static constexpr int OFF_BAR = OFF_STG + 8 * 2048;
   static constexpr int OFF_MISC = OFF_BAR + K_NB * 8;
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
@@ -155,9 +156,9 @@ struct DkdvCfg {
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
     k_attn_dkdv(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-                const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
-                const float* __restrict__ dsum, const AttnDims a, const float scale_log2, const float scale,
-                const WorkOrder ord, unsigned* err, const unsigned long long timeout_ns) {
+                const __grid_constant__ CUtensorMap tmDQKV, const __grid_constant__ CUtensorMap tmDS,
+                const float* __restrict__ lse, const float* __restrict__ dsum, const AttnDims a, const float scale_log2,
+                const float scale, const WorkOrder ord, unsigned* err, const unsigned long long timeout_ns) {
   using C = DkdvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -409,6 +410,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cm.bar(K_DSF));
+      {
+        // the same dS^T values (the warp's 32 keys x the half's 64 queries) to the dS
+        // tile of (query head, query block, key block), from which k_attn_dq forms dQ:
+        // two 32 x 32 boxes staged in the warp's 2 KB (64-byte rows, 64-byte swizzle)
+        // and written by TMA, after dS^T has been handed to the dK product, so that
+        // the copies overlap it
+        const long long tile = ds_tile_index(a, b, shard * a.hN + jq_of(it), q_start + it % nq, kb);
+        const uint32_t stg = cm.sb + C::OFF_STG + static_cast<uint32_t>(warp * 2048);
+        const bool tile_ok = TP_DCHECK(tile >= 0 && tile < ds_tiles(a), err);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          if (lane == 0) bulk_wait_read0();  // the previous box has left the staging area
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(stg + lane * 64 + ((static_cast<uint32_t>(c) ^ ((lane >> 1) & 3)) << 4), dk[16 * rr + 4 * c],
+                         dk[16 * rr + 4 * c + 1], dk[16 * rr + 4 * c + 2], dk[16 * rr + 4 * c + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && tile_ok) {
+            tma_store_2d(&tmDS, stg, 64 * half + 32 * rr, static_cast<int>(tile * BLK) + quad * 32);
+            bulk_commit();
+          }
+        }
+      }
     }
     if (ok && nit > 0) ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(K_ACC), static_cast<uint32_t>((nit - 1) & 1), wc));
     if (ok) {
@@ -443,50 +469,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ---------------------------------------------------------------------- dQ
-// One CTA per (128-query block, query head, batch); loops over the 128-key blocks
-// of the head's group, K in three shared-memory stages (a stage is free only once
-// the block's dQ product has read it, late in the block) and V in two (free once
-// the block's dP has).  Per block: S = Q K^T (fp16) and
-// dP = dO V^T; the elementwise warps turn them into dS = P (dP - Dsum) (fp16) over
-// the dP columns; dQ += dS K with A from TMEM.  dP / dS alternate between two TMEM
-// buffers, so the next block's S and dP are computed while this block's dS and dQ
-// are: S once this block's S has been read, dP once the dQ product two blocks back
-// has read the dS its buffer held.
-constexpr int kDqKStages = 3;
-enum : int {
-  Q_QF = 0, Q_KF = 1 /* 3 */, Q_KE = 4 /* 3 */, Q_VF = 7 /* 2 */, Q_VE = 9 /* 2 */, Q_SF = 11, Q_SE = 12,
-  Q_DPF = 13 /* 2 */, Q_DSF = 15 /* 2 */, Q_DQE = 17 /* 2 */, Q_DR = 19, Q_NB = 20
-};
+// dQ = sum over key blocks of dS K / sqrt(d), from the dS tiles the dK/dV kernel
+// wrote: no score, probability or dP recomputation, one product per block.  One
+// CTA per (128-query block, query head, batch), heaviest causal blocks first.
+// Each stage holds one key block's dS^T tile (the MMA's A operand, MN-major: two
+// 64-query chunks of 128 key rows) and its K tile (B, MN-major, D/64 chunks); the
+// fp32 accumulator (128 x D) stays in TMEM.
+//   warp 4: TMA producer; warp 5: MMA issuer (one elected thread);
+//   warps 0-3: epilogue (TMEM lane quadrant w), dQ scaled and stored once at the end.
+constexpr int kDqStages = 3;
+constexpr int DQ_THREADS = 192;
+enum : int { Q_F = 0 /* [stage] */, Q_E = kDqStages /* [stage] */, Q_ACC = 2 * kDqStages, Q_DR, Q_NB };
 
 template <int D>
 struct DqCfg {
   static constexpr int CH = D / 64;
-  static constexpr int TILE = CH * 16384;  // 128 rows x D 16-bit values
-  static constexpr int OFF_Q = 0, OFF_DO = TILE;
-  static constexpr int OFF_K = 2 * TILE;                     // [3 stages]
-  static constexpr int OFF_V = OFF_K + kDqKStages * TILE;    // [2 stages]
-  static constexpr int OFF_BAR = OFF_V + 2 * TILE;
+  static constexpr int DS_BYTES = 2 * 16384;       // 128 keys x 128 queries, fp16
+  static constexpr int K_BYTES = CH * 16384;       // 128 keys x D, fp16
+  static constexpr int STAGE = DS_BYTES + K_BYTES;
+  static constexpr int OFF_BAR = kDqStages * STAGE;
   static constexpr int OFF_MISC = OFF_BAR + Q_NB * 8;
   static constexpr int USED = OFF_MISC + 16;
-  static constexpr int SMEM = (USED + 1024 > 122880) ? USED + 1024 : 122880;
-  static_assert(USED + 1024 <= 232448, "shared memory budget");
+  static constexpr int SMEM = USED + 1024;
+  static_assert(SMEM <= 232448, "shared memory budget");
 };
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    k_attn_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDO,
-              const __grid_constant__ CUtensorMap tmDQKV, const float* __restrict__ lse,
-              const float* __restrict__ dsum, const AttnDims a, const float scale_log2, const float scale,
-              const WorkOrder ord, unsigned* err, const unsigned long long timeout_ns) {
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    k_attn_dq(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmDS,
+              const __grid_constant__ CUtensorMap tmDQKV, const AttnDims a, const float scale, const WorkOrder ord,
+              unsigned* err, const unsigned long long timeout_ns) {
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
   const BwdCommon cm{raw + pad, raw + pad + C::OFF_BAR};
-  const uint32_t sQ = cm.sb + C::OFF_Q, sDO = cm.sb + C::OFF_DO;
-  auto sK = [&](int st) { return cm.sb + C::OFF_K + static_cast<uint32_t>(st * C::TILE); };
-  auto sV = [&](int st) { return cm.sb + C::OFF_V + static_cast<uint32_t>(st * C::TILE); };
+  auto sDS = [&](int st) { return cm.sb + static_cast<uint32_t>(st * C::STAGE); };
+  auto sK = [&](int st) { return cm.sb + static_cast<uint32_t>(st * C::STAGE + C::DS_BYTES); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   volatile int* never_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -499,17 +519,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int j = unit % a.H, b = unit / a.H;
   const int shard = j / a.hN, jj = j % a.hN, kvh = jj / a.group();
   const int q0 = qb * BLK;
-  const int nkv = a.causal ? min((min(q0 + BLK, a.S) - 1) / BLK + 1, nb) : nb;
-  const int cQ = a.col_q(jj), cK = a.col_k(kvh), cV = a.col_v(kvh);
+  const int nkv = a.causal ? qb + 1 : nb;
+  const int cK = a.col_k(kvh);
+  const long long tile0 = ds_tile_index(a, b, j, qb, 0);  // the key blocks' tiles are consecutive
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Q_NB; ++i) mbar_init(cm.bar(i), (i == Q_SE || i == Q_DSF || i == Q_DSF + 1) ? 8 : 1);
+    for (int i = 0; i < Q_NB; ++i) mbar_init(cm.bar(i), 1);
     *abort_flag = 0;
     *never_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 128);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -518,187 +539,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
-  // TMEM: S [0, 128), dP / dS buffer 0 [128, 256), dQ [256, +D), dP / dS buffer 1 [384, 512)
 
-  if (warp == 8) {
+  if (warp == 4) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(cm.bar(Q_QF), 2 * C::TILE);
-#pragma unroll
-      for (int c = 0; c < C::CH; ++c) {
-        tma_load_4d(sQ + c * 16384, &tmQKV, cm.bar(Q_QF), cQ + 64 * c, q0, b, shard);
-        tma_load_4d(sDO + c * 16384, &tmDO, cm.bar(Q_QF), jj * D + 64 * c, q0, b, shard);
-      }
-      int kiss = 0, viss = 0;  // key blocks whose K / V copies were issued
-      for (int it = 0; it < nkv; ++it) {
-        const int sk = it % kDqKStages, sv = it & 1;
-        if (!mbar_wait(cm.bar(Q_KE + sk), static_cast<uint32_t>(((it / kDqKStages) & 1) ^ 1), wc)) break;
-        mbar_arrive_expect_tx(cm.bar(Q_KF + sk), C::TILE);
+      const bool coords_ok = TP_DCHECK(cK % 8 == 0 && tile0 >= 0 && tile0 + nkv <= ds_tiles(a), err);
+      int issued = 0;
+      for (int kb = 0; kb < nkv && coords_ok; ++kb) {
+        const int st = kb % kDqStages;
+        if (!mbar_wait(cm.bar(Q_E + st), static_cast<uint32_t>(((kb / kDqStages) & 1) ^ 1), wc)) break;
+        mbar_arrive_expect_tx(cm.bar(Q_F + st), C::STAGE);
+        const int row = static_cast<int>((tile0 + kb) * BLK);
+        tma_load_2d(sDS(st), &tmDS, cm.bar(Q_F + st), 0, row);
+        tma_load_2d(sDS(st) + 16384, &tmDS, cm.bar(Q_F + st), 64, row);
 #pragma unroll
         for (int c = 0; c < C::CH; ++c)
-          tma_load_4d(sK(sk) + c * 16384, &tmQKV, cm.bar(Q_KF + sk), cK + 64 * c, it * BLK, b, shard);
-        kiss = it + 1;
-        if (!mbar_wait(cm.bar(Q_VE + sv), static_cast<uint32_t>(((it >> 1) & 1) ^ 1), wc)) break;
-        mbar_arrive_expect_tx(cm.bar(Q_VF + sv), C::TILE);
-#pragma unroll
-        for (int c = 0; c < C::CH; ++c)
-          tma_load_4d(sV(sv) + c * 16384, &tmQKV, cm.bar(Q_VF + sv), cV + 64 * c, it * BLK, b, shard);
-        viss = it + 1;
+          tma_load_4d(sK(st) + c * 16384, &tmQKV, cm.bar(Q_F + st), cK + 64 * c, kb * BLK, b, shard);
+        issued = kb + 1;
       }
       // every issued copy lands before the CTA may exit
-      mbar_wait(cm.bar(Q_QF), 0, wdrain);
-      for (int k = (kiss > kDqKStages ? kiss - kDqKStages : 0); k < kiss; ++k)
-        mbar_wait(cm.bar(Q_KF + k % kDqKStages), static_cast<uint32_t>((k / kDqKStages) & 1), wdrain);
-      for (int k = (viss > 2 ? viss - 2 : 0); k < viss; ++k)
-        mbar_wait(cm.bar(Q_VF + (k & 1)), static_cast<uint32_t>((k >> 1) & 1), wdrain);
+      for (int k = (issued > kDqStages ? issued - kDqStages : 0); k < issued; ++k)
+        mbar_wait(cm.bar(Q_F + k % kDqStages), static_cast<uint32_t>((k / kDqStages) & 1), wdrain);
     }
-  } else if (warp == 9) {
+  } else if (warp == 5) {
     if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_f16(128, BLK, false, false);   // Q K^T
-      constexpr uint32_t ID_P = idesc_f16(128, BLK, false, false);   // dO V^T
-      constexpr uint32_t ID_DQ = idesc_f16(128, D, false, true);     // dS K
-      auto s_mmas = [&](int st) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
-          tc_mma_bf16(tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK(st) + off, 16, 1024), ID_S,
-                      kk > 0 ? 1u : 0u);
-        }
-      };
-      auto dp_mmas = [&](int st, int buf) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>((kk >> 2) * 16384 + (kk & 3) * 32);
-          tc_mma_bf16(tmem + 128 + 256 * buf, sdesc_sw128(sDO + off, 16, 1024), sdesc_sw128(sV(st) + off, 16, 1024),
-                      ID_P, kk > 0 ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(cm.bar(Q_QF), 0, wc), any = false;
-      if (ok && nkv > 0) {
-        ok = mbar_wait(cm.bar(Q_KF), 0, wc) && mbar_wait(cm.bar(Q_VF), 0, wc);
-        if (ok) {
-          tc_fence_after();
-          s_mmas(0);
-          tc_commit(cm.bar(Q_SF));
-          dp_mmas(0, 0);
-          tc_commit(cm.bar(Q_DPF));
-          tc_commit(cm.bar(Q_VE));
-          any = true;
-        }
-      }
-      for (int it = 0; it < nkv && ok; ++it) {
-        const int st = it & 1, st1 = (it + 1) & 1;  // V stage; also the dP / dS buffer
-        const int sk = it % kDqKStages, sk1 = (it + 1) % kDqKStages;
-        const bool more = it + 1 < nkv;
-        if (more) {
-          // the next block's scores once this block's S has been read
-          if (!mbar_wait(cm.bar(Q_KF + sk1), static_cast<uint32_t>(((it + 1) / kDqKStages) & 1), wc) ||
-              !mbar_wait(cm.bar(Q_SE), static_cast<uint32_t>(it & 1), wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          s_mmas(sk1);
-          tc_commit(cm.bar(Q_SF));
-          // its dP into the other buffer once the dQ product of block it-1 has read it
-          if ((it >= 1 && !mbar_wait(cm.bar(Q_DQE + st1), static_cast<uint32_t>(((it - 1) >> 1) & 1), wc)) ||
-              !mbar_wait(cm.bar(Q_VF + st1), static_cast<uint32_t>(((it + 1) >> 1) & 1), wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          dp_mmas(st1, st1);
-          tc_commit(cm.bar(Q_DPF + st1));
-          tc_commit(cm.bar(Q_VE + st1));
-        }
-        if (!mbar_wait(cm.bar(Q_DSF + st), static_cast<uint32_t>((it >> 1) & 1), wc)) {
+      // D (queries x d) += A (dS: queries x keys, MN-major) B (K: keys x d, MN-major)
+      constexpr uint32_t ID_DQ = idesc_f16(128, D, true, true);
+      bool ok = true, any = false;
+      for (int kb = 0; kb < nkv && ok; ++kb) {
+        const int st = kb % kDqStages;
+        if (!mbar_wait(cm.bar(Q_F + st), static_cast<uint32_t>((kb / kDqStages) & 1), wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BLK / 16; ++kk)
-          tc_mma_bf16_ts(tmem + 256, tmem + 128 + 256 * st + half_packed_col(kk),
-                         sdesc_sw128(sK(sk) + kk * 2048, 16384, 1024), ID_DQ, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(cm.bar(Q_DQE + st));
-        tc_commit(cm.bar(Q_KE + sk));
+          tc_mma_bf16(tmem, sdesc_sw128(sDS(st) + kk * 2048, 16384, 1024), sdesc_sw128(sK(st) + kk * 2048, 16384, 1024),
+                      ID_DQ, (kb > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(cm.bar(Q_E + st));
+        any = true;
       }
+      if (ok && any) tc_commit(cm.bar(Q_ACC));
       if (any) {
         tc_commit(cm.bar(Q_DR));
         mbar_wait(cm.bar(Q_DR), 0, wdrain);
       }
     }
   } else {
-    const int quad = warp & 3, half = warp >> 2;
-    const int r = quad * 32 + lane;
-    const int q = q0 + r;
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t cS = static_cast<uint32_t>(64 * half);
-    const size_t ridx = (static_cast<size_t>(b) * a.H + j) * a.S + q;
-    const bool qvalid = q < a.S && TP_DCHECK(ridx < static_cast<size_t>(a.B) * a.H * a.S, err);
-    const float lse2 = qvalid ? lse[ridx] * kLog2e : 0.0f;
-    const float dd = qvalid ? dsum[ridx] : 0.0f;
-    bool ok = true;
-    for (int it = 0; it < nkv; ++it) {
-      const int kbase = it * BLK + 64 * half;
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_SF), static_cast<uint32_t>(it & 1), wc));
-      if (!ok) break;
+    const int quad = warp;
+    bool ok = nkv == 0 || __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_ACC), 0, wc));
+    if (ok) {
       tc_fence_after();
-      uint32_t vs[2][32];
-      tmem_ld32(trow + cS, vs[0]);
-      tmem_ld32(trow + cS + 32, vs[1]);
-      tmem_ld_wait(vs[0]);
-      tmem_ld_wait(vs[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cm.bar(Q_SE));  // S may be recomputed for the next block
-      const bool need_mask = (a.causal && kbase + 64 > q0) || (kbase + 64 > a.S) || !qvalid;
-      float p[64];
-#pragma unroll
-      for (int kc = 0; kc < 64; ++kc)
-        p[kc] = ex2_approx(fmaf(__uint_as_float(vs[kc >> 5][kc & 31]), scale_log2, -lse2));
-      if (need_mask) {  // warp-uniform: only diagonal and ragged blocks
-#pragma unroll
-        for (int kc = 0; kc < 64; ++kc) {
-          const int key = kbase + kc;
-          if (!qvalid || key >= a.S || (a.causal && key > q)) p[kc] = 0.0f;
-        }
-      }
-      const uint32_t tbuf = trow + 128 + 256 * static_cast<uint32_t>(it & 1);  // this block's dP / dS
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DPF + (it & 1)), static_cast<uint32_t>((it >> 1) & 1), wc));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t vp[2][32];
-      tmem_ld32(tbuf + cS, vp[0]);
-      tmem_ld32(tbuf + cS + 32, vp[1]);
-      tmem_ld_wait(vp[0]);
-      tmem_ld_wait(vp[1]);
-      uint32_t dk[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e)
-        dk[e] = pack_f16x2(p[2 * e] * (__uint_as_float(vp[e >> 4][(2 * e) & 31]) - dd),
-                           p[2 * e + 1] * (__uint_as_float(vp[e >> 4][(2 * e + 1) & 31]) - dd));
-      tmem_st32(tbuf + cS, dk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cm.bar(Q_DSF + (it & 1)));
-    }
-    // the last dQ product (its commit covers every earlier MMA of the issuing thread)
-    if (ok && nkv > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(cm.bar(Q_DQE + ((nkv - 1) & 1)), static_cast<uint32_t>(((nkv - 1) >> 1) & 1), wc));
-    if (ok && half == 0) {
-      tc_fence_after();
-      // all MMAs are complete: the Q tile is free for staging
-      const uint32_t stQ = sQ + static_cast<uint32_t>(quad * C::CH * 4096);
+      // every MMA is complete: stage 0's dS buffer is free for staging
+      const uint32_t stage = sDS(0) + static_cast<uint32_t>(quad * C::CH * 4096);
       if (nkv > 0)
-        stage_rows_from_tmem<D>(trow + 256, stQ, lane, scale, a.dqkv_f16 != 0);
+        stage_rows_from_tmem<D>(tmem + (static_cast<uint32_t>(quad * 32) << 16), stage, lane, scale, a.dqkv_f16 != 0);
       else
-        stage_zero_rows<D>(stQ, lane);
+        stage_zero_rows<D>(stage, lane);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0 && q0 + quad * 32 < a.S) {
 #pragma unroll
-        for (int cb = 0; cb < C::CH; ++cb) tma_store_4d(&tmDQKV, stQ + cb * 4096, jj * D + 64 * cb, q0 + quad * 32, b, shard);
+        for (int cb = 0; cb < C::CH; ++cb)
+          tma_store_4d(&tmDQKV, stage + cb * 4096, jj * D + 64 * cb, q0 + quad * 32, b, shard);
         bulk_commit();
       }
     }
@@ -709,15 +612,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, 128);
   }
 }
 
 template <int D>
 int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse, float* dsum,
-                 void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
+                 void* dsbuf, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(k_attn_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) !=
@@ -725,6 +628,16 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
         cudaFuncSetAttribute(k_attn_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM) != cudaSuccess)
       return 2;
     configured = true;
+  }
+  // the dS tiles: [tiles * 128 key rows][128 query columns] fp16; written in 32 x 32
+  // boxes (64-byte swizzle) by dK/dV, read in 64 x 128 boxes (128-byte swizzle) by dQ
+  CUtensorMap tds, tds_st;
+  {
+    const uint64_t dd[2] = {128u, static_cast<uint64_t>(ds_tiles(a)) * 128u};
+    const uint32_t dbox[2] = {64, 128}, sbox[2] = {32, 32};
+    if (!encode_tmap(&tds, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dsbuf, dd, dbox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&tds_st, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, dsbuf, dd, sbox, CU_TENSOR_MAP_SWIZZLE_64B))
+      return 2;
   }
   const uint64_t S = static_cast<uint64_t>(a.S), Bb = static_cast<uint64_t>(a.B), Nn = static_cast<uint64_t>(a.N);
   CUtensorMap tq, tdo, tdq;
@@ -755,14 +668,13 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   const float scale_log2 = scale * kLog2e;
   const WorkOrder ord_q = make_work_order(a.B * a.H, nb, sms), ord_kv = make_work_order(a.B * a.Hkv, nb, sms);
   slot = timing_begin(kKAttnDkdv, st);
-  k_attn_dkdv<D><<<ord_kv.ctas(), NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale,
-                                                                   ord_kv, err, timeout_ns);
+  k_attn_dkdv<D><<<ord_kv.ctas(), NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq, tdo, tdq, tds_st, lse, dsum, a, scale_log2,
+                                                                   scale, ord_kv, err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
   slot = timing_begin(kKAttnDq, st);
-  k_attn_dq<D><<<ord_q.ctas(), NTHREADS, DqCfg<D>::SMEM, st>>>(tq, tdo, tdq, lse, dsum, a, scale_log2, scale, ord_q,
-                                                             err, timeout_ns);
+  k_attn_dq<D><<<ord_q.ctas(), DQ_THREADS, DqCfg<D>::SMEM, st>>>(tq, tds, tdq, a, scale, ord_q, err, timeout_ns);
   ok = cudaGetLastError() == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
@@ -771,12 +683,14 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
 }  // namespace
 
 int launch_attn_bwd(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse,
-                    float* dsum, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
+                    float* dsum, void* dsbuf, void* dqkv, unsigned* err, unsigned long long timeout_ns,
+                    cudaStream_t st) {
+  if (!dsbuf || (reinterpret_cast<uintptr_t>(dsbuf) & 15u)) return 1;
   if (a.B < 1 || a.S < 1 || a.H < 1 || a.N < 1 || a.hN * a.N != a.H) return 1;
   if (a.Hkv < 1 || a.hkvN * a.N != a.Hkv || a.H % a.Hkv || a.hN % a.hkvN) return 1;
   if (a.H > 65535 || a.B > 65535) return 1;
-  if (a.d == 128) return launch_bwd_d<128>(a, qkv, o, dout, lse, dsum, dqkv, err, timeout_ns, st);
-  if (a.d == 64) return launch_bwd_d<64>(a, qkv, o, dout, lse, dsum, dqkv, err, timeout_ns, st);
+  if (a.d == 128) return launch_bwd_d<128>(a, qkv, o, dout, lse, dsum, dsbuf, dqkv, err, timeout_ns, st);
+  if (a.d == 64) return launch_bwd_d<64>(a, qkv, o, dout, lse, dsum, dsbuf, dqkv, err, timeout_ns, st);
   return 1;
 }
 
