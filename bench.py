@@ -456,6 +456,7 @@ def run_gpu(args, w) -> None:
     if tp.tp_device_check() != 0:
         raise RuntimeError("not an sm_103 GPU")
     tp.tp_set_gemm_tiling(args.gemm_tiling)
+    tp.tp_set_launch_overlap(bool(args.launch_overlap))
 
     inp = inputs.workload_inputs(w)
     inp_tok = inp  # token-major copies (the oracle's layout)
@@ -584,8 +585,11 @@ def run_gpu(args, w) -> None:
     except Exception:
         gpu_id = None
 
-    def timed_region():
-        tp.tp_timing_enable(True)
+    def timed_region(kernel_events: bool):
+        # kernel_events: an event pair around every library kernel (tp_timing_*), for
+        # the per-kernel durations.  Events between the kernels of a step serialise
+        # them (no launch overlap), so the step time is taken in a pass without them.
+        tp.tp_timing_enable(kernel_events)
         barrier()
         torch.cuda.synchronize(dev)
         with ClockSampler(gpu_id) as cs:
@@ -615,9 +619,11 @@ def run_gpu(args, w) -> None:
         tp.tp_timing_enable(False)
         return ms, statistics.median(per), rep, cs.summary()
 
-    ms, ms_median, rep, clocks = timed_region()
+    ms, ms_median, rep_value, clocks = timed_region(False)
     if clocks_rejected(clocks):
-        ms, ms_median, rep, clocks = timed_region()  # re-measured once
+        ms, ms_median, rep_value, clocks = timed_region(False)  # re-measured once
+    # the same K steps again with per-kernel events: the roofline's launch durations
+    ms_ev, _, rep, clocks_ev = timed_region(True)
     if tp.tp_sync_status(stream) != 0:
         raise RuntimeError("device error during the timed region")
     if world > 1:
@@ -649,8 +655,12 @@ def run_gpu(args, w) -> None:
                 "avg_launch_ms": avg_ms, "flops_per_launch": kfl[dom],
                 "peak_source": (f"{'bf16_tflops_sustained' if sustained else 'bf16_tflops'} ({pk['source']}): "
                                 f"timed region {ms:.0f} ms, {'at least' if sustained else 'under'} "
-                                f"{SUSTAINED_REGION_MS:.0f} ms")}
-    launches = sum(v[0] for v in rep.values())
+                                f"{SUSTAINED_REGION_MS:.0f} ms"),
+                "events_pass": {"ms": ms_ev, "sm_mhz": clocks_ev.get("sm_mhz"), "reasons": clocks_ev.get("reasons"),
+                                "what": "avg_launch_ms comes from a second pass of the same steps with a CUDA "
+                                        "event pair around every library kernel on its launch stream; the value "
+                                        "pass runs without them, since events between kernels serialise them"}}
+    launches = sum(v[0] for v in rep_value.values())
 
     # end to end: host buffers, copies inside the timed region.  Two sets of device
     # inputs and outputs: step i+1's inputs are copied in on one stream and step i-1's
@@ -777,6 +787,7 @@ def run_gpu(args, w) -> None:
                 "config": {"workload": w.name, "description": describe(w), "parallelism": "tp" + str(N) +
                            " logical shards on one GPU" + (f", {world} independent replicas" if world > 1 else ""),
                            "flops_per_step": flops,
+                           "launch_overlap": bool(args.launch_overlap),
                            "l2": ("flushed before each step (256 MiB write, outside the step's CUDA events)"
                                   if flush is not None else
                                   f"inputs larger than L2 (step working set {work_bytes / 2**30:.2f} GiB); no flush")},
@@ -810,6 +821,9 @@ def main() -> None:
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--gemm-tiling", type=int, default=0, choices=[0, 1, 2],
                     help="0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile")
+    ap.add_argument("--launch-overlap", type=int, default=1, choices=[0, 1],
+                    help="1: each kernel's prologue overlaps the previous kernel's tail (programmatic "
+                         "dependent launch); 0: ordinary stream order")
     ap.add_argument("--override", action="append", default=[],
                     help="KEY=VALUE shape override of the workload (a smaller case for profiling)")
     args = ap.parse_args()

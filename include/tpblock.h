@@ -438,6 +438,20 @@ TP_API int tp_debug_timeout_probe(int64_t timeout_ns, void* stream);
  * multicast across a cluster. */
 TP_API int tp_set_gemm_tiling(int mode);
 
+/* ------------------------------------------------------- launch overlap */
+
+/* Programmatic dependent launch (process-wide; for tests and measurement).
+ * 1 (default): every kernel is launched with programmatic stream serialisation
+ * (cudaLaunchAttributeProgrammaticStreamSerialization).  Its CTAs may become
+ * resident while the previous kernel in the stream finishes; each runs only its
+ * prologue (barrier set-up, tensor-map prefetch, TMEM allocation) and then waits,
+ * in the PTX griddepcontrol.wait instruction, until that kernel has completed and its
+ * writes are visible, before it reads or writes global memory.  That hides the
+ * launch latency and the prologue between the dependent kernels of a call.
+ * 0: ordinary stream order.  The results are bit-identical either way.
+ * TP_ERR_SHAPE for a value other than 0 or 1 (the setting is then unchanged). */
+TP_API int tp_set_launch_overlap(int on);
+
 /* ---------------------------------------------------------- kernel timing */
 
 /* Every kernel the library launches is counted per kind.  With timing on, a

@@ -14,7 +14,7 @@ from ._binding import (  # noqa: F401
     tp_gmlp_bwd, tp_gmlp_fwd, tp_gmlp_workspace_bytes, tp_gqa_bwd, tp_gqa_fwd, tp_gqa_workspace_bytes, tp_layer_bwd, tp_layer_fwd, tp_layer_save_bytes,
     tp_layer_workspace_bytes, tp_layernorm_bwd, tp_layernorm_fwd, tp_layernorm_workspace_bytes,
     tp_mlp_bwd, tp_mlp_fwd, tp_mlp_fwd_noalloc,
-    tp_mlp_workspace_bytes, tp_set_gemm_tiling, tp_sp_layer_bwd, tp_sp_layer_fwd, tp_status_string,
+    tp_mlp_workspace_bytes, tp_set_gemm_tiling, tp_set_launch_overlap, tp_sp_layer_bwd, tp_sp_layer_fwd, tp_status_string,
     tp_sync_status, tp_timing_enable,
     tp_timing_kinds, tp_timing_name, tp_timing_read, tp_version, timing_report,
 )

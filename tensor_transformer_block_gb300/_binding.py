@@ -66,6 +66,7 @@ _SIGS = {
     "tp_attn_mlp_bwd": ([i32, i64, i64, i64, i32, i32, i64, i32, i32] + [vp] * 6 + [sz] + [vp] * 6 + [vp, sz, vp],
                         i32),
     "tp_set_gemm_tiling": ([i32], i32),
+    "tp_set_launch_overlap": ([i32], i32),
     "tp_timing_enable": ([i32], i32),
     "tp_timing_kinds": ([], i32),
     "tp_timing_name": ([i32], ctypes.c_char_p),
@@ -419,6 +420,12 @@ def tp_attn_mlp_bwd(dtype, B, S, h, H, d, f, N, causal, X, Wqkv, Wo, W1s, W2s, s
 def tp_set_gemm_tiling(mode: int) -> int:
     """0 automatic, 1 one CTA per 128x256 tile, 2 CTA pairs per 256x256 tile."""
     return _check(load_library().tp_set_gemm_tiling(mode), "tp_set_gemm_tiling")
+
+
+def tp_set_launch_overlap(on: bool) -> int:
+    """True (default): each kernel's prologue overlaps the previous kernel's tail
+    (programmatic dependent launch); False: ordinary stream order."""
+    return _check(load_library().tp_set_launch_overlap(1 if on else 0), "tp_set_launch_overlap")
 
 
 # ---------------------------------------------------------------- kernel timing

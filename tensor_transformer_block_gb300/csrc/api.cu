@@ -1071,6 +1071,12 @@ int tp_set_gemm_tiling(int mode) {
   return tpb::set_gemm_tiling_mode(mode) ? TP_OK : TP_ERR_SHAPE;
 }
 
+int tp_set_launch_overlap(int on) {
+  if (on != 0 && on != 1) return TP_ERR_SHAPE;
+  tpb::set_launch_overlap(on != 0);
+  return TP_OK;
+}
+
 int tp_timing_enable(int on) {
   tpb::timing_enable(on != 0);
   return TP_OK;

@@ -53,6 +53,8 @@ __device__ __forceinline__ float dot8(const uint4& x, const uint4& y, bool x_f16
 template <int D>
 __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict__ dout, float* __restrict__ dsum,
                             const AttnDims a, unsigned* err) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   constexpr int LPR = D / 8;  // lanes (16-byte vectors) per row
   static_assert(32 % LPR == 0, "a row's lanes lie in one warp");
   const long long T = static_cast<long long>(a.B) * a.S;
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
   // TMEM: S^T / P^T [0, 128), dP^T / dS^T [128, 256), dV [256, +D), dK [256 + D, +D)
@@ -537,6 +541,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
 
@@ -658,9 +664,8 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   long long blocks = (rows * (D / 8) + 255) / 256;  // D/8 lanes per row
   if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
   int slot = timing_begin(kKAttnDsum, st);
-  k_attn_dsum<D><<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(o),
-                                                           static_cast<const uint4*>(dout), dsum, a, err);
-  bool ok = cudaGetLastError() == cudaSuccess;
+  bool ok = launch_k(k_attn_dsum<D>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1,
+                     static_cast<const uint4*>(o), static_cast<const uint4*>(dout), dsum, a, err) == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
   const int nb = (a.S + BLK - 1) / BLK;
@@ -668,14 +673,13 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
   const float scale_log2 = scale * kLog2e;
   const WorkOrder ord_q = make_work_order(a.B * a.H, nb, sms), ord_kv = make_work_order(a.B * a.Hkv, nb, sms);
   slot = timing_begin(kKAttnDkdv, st);
-  k_attn_dkdv<D><<<ord_kv.ctas(), NTHREADS, DkdvCfg<D>::SMEM, st>>>(tq, tdo, tdq, tds_st, lse, dsum, a, scale_log2,
-                                                                   scale, ord_kv, err, timeout_ns);
-  ok = cudaGetLastError() == cudaSuccess;
+  ok = launch_k(k_attn_dkdv<D>, dim3(ord_kv.ctas()), dim3(NTHREADS), DkdvCfg<D>::SMEM, st, 1, tq, tdo, tdq, tds_st,
+                lse, dsum, a, scale_log2, scale, ord_kv, err, timeout_ns) == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
   slot = timing_begin(kKAttnDq, st);
-  k_attn_dq<D><<<ord_q.ctas(), DQ_THREADS, DqCfg<D>::SMEM, st>>>(tq, tds, tdq, a, scale, ord_q, err, timeout_ns);
-  ok = cudaGetLastError() == cudaSuccess;
+  ok = launch_k(k_attn_dq<D>, dim3(ord_q.ctas()), dim3(DQ_THREADS), DqCfg<D>::SMEM, st, 1, tq, tds, tdq, a, scale,
+                ord_q, err, timeout_ns) == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
 }

@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   const WaitCtx wc{err, abort_flag, timeout_ns};
   const WaitCtx wdrain{err, never_flag, timeout_ns};
 
@@ -430,8 +432,8 @@ int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsign
   const float scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
   const WorkOrder ord = make_work_order(a.B * a.H, nqb, device_sm_count());
   const int slot = timing_begin(kKAttnCore, st);
-  k_attn_fwd<D><<<ord.ctas(), NTHREADS, C::SMEM, st>>>(tqkv, to, a, lse, scale_log2, ord, err, timeout_ns);
-  const bool ok = cudaGetLastError() == cudaSuccess;
+  const bool ok = launch_k(k_attn_fwd<D>, dim3(ord.ctas()), dim3(NTHREADS), C::SMEM, st, 1, tqkv, to, a, lse,
+                           scale_log2, ord, err, timeout_ns) == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
 }

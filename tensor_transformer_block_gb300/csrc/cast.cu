@@ -20,6 +20,8 @@ namespace {
 
 __global__ void __launch_bounds__(256) k_bf16_to_f16(const uint4* __restrict__ in, uint4* __restrict__ out,
                                                      long long n8) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
     const uint4 v = in[i];
@@ -44,8 +46,8 @@ int launch_bf16_to_f16(const void* in, void* out, long long n, cudaStream_t st) 
   long long blocks = (n8 + 255) / 256;
   if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;  // 8 x 256 threads per SM
   const int slot = timing_begin(kKCast, st);
-  k_bf16_to_f16<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(in), static_cast<uint4*>(out), n8);
-  const bool ok = cudaGetLastError() == cudaSuccess;
+  const bool ok = launch_k(k_bf16_to_f16, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1,
+                           static_cast<const uint4*>(in), static_cast<uint4*>(out), n8) == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
 }

@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (PAIR) cluster_sync();  // the peer's barriers are initialised before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
 
   const WaitCtx wc{p.err, abort_flag, p.timeout_ns};
   const WaitCtx wdrain{p.err, never_flag, p.timeout_ns};
@@ -919,6 +921,8 @@ KernelFn pick_kernel(bool a_mn, bool b_mn, int epi) {
 __global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__ part, int ksplit, long long rows,
                                                        int N, long long ldc, const uint4* __restrict__ R,
                                                        uint4* __restrict__ C, int c_f16) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   const long long per_row = N / 8, n8 = rows * per_row, plane = rows * N;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8; i += stride) {
@@ -1161,37 +1165,25 @@ int launch_gemm_bf16(int epi, const GemmOperand& A, const GemmOperand& B, void* 
   const int slot = timing_begin(kind, stream);
   bool ok;
   if (pair) {
-    const int cl = 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cl);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     // persistent pairs: one per two SMs
-    long long units = sms / cl;
+    long long units = sms / 2;
     if (units > total) units = total;
-    cfg.gridDim = dim3(static_cast<unsigned>(cl * units), 1, 1);
-    ok = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, ty, p) == cudaSuccess;
+    ok = launch_k(fn, dim3(static_cast<unsigned>(2 * units)), dim3(NUM_THREADS), static_cast<size_t>(smem), stream, 2,
+                  ta, tb, tc, ty, p) == cudaSuccess;
   } else {
     const int grid = static_cast<int>(total < sms ? total : sms);
-    fn<<<grid, NUM_THREADS, static_cast<size_t>(smem), stream>>>(ta, tb, tc, ty, p);
-    ok = cudaGetLastError() == cudaSuccess;
+    ok = launch_k(fn, dim3(static_cast<unsigned>(grid)), dim3(NUM_THREADS), static_cast<size_t>(smem), stream, 1, ta,
+                  tb, tc, ty, p) == cudaSuccess;
   }
   if (ok && split) {
     const long long rows = static_cast<long long>(G) * M, n8 = rows * (N / 8);
     long long blocks = (n8 + 255) / 256;
     if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
     const int rslot = timing_begin(kKSplitReduce, stream);
-    k_splitk_reduce<<<static_cast<int>(blocks), 256, 0, stream>>>(
-        static_cast<const float*>(extra.part_ws), kSplit, rows, static_cast<int>(N), ldc,
-        epi == kEpiResidual ? static_cast<const uint4*>(Yaux) : nullptr, static_cast<uint4*>(C), p.c_f16);
-    ok = cudaGetLastError() == cudaSuccess;
+    ok = launch_k(k_splitk_reduce, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1,
+                  static_cast<const float*>(extra.part_ws), kSplit, rows, static_cast<int>(N), ldc,
+                  epi == kEpiResidual ? static_cast<const uint4*>(Yaux) : nullptr, static_cast<uint4*>(C),
+                  p.c_f16) == cudaSuccess;
     timing_end(rslot, stream);
   }
   timing_end(slot, stream);

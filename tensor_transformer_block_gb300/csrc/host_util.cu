@@ -1,5 +1,6 @@
 #include "host_util.cuh"
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -121,6 +122,13 @@ cudaEvent_t take_event() {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<bool> g_overlap{true};
+}  // namespace
+
+void set_launch_overlap(bool on) { g_overlap.store(on); }
+bool launch_overlap() { return g_overlap.load(); }
 
 const char* kernel_kind_name(int k) { return (k >= 0 && k < kNumKernelKinds) ? kKindNames[k] : nullptr; }
 

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 namespace tpb {
 
@@ -25,6 +26,45 @@ int device_sm_count();
 
 // Current device's compute capability as major*10+minor, or -1.
 int device_cc();
+
+// Programmatic dependent launch (process-wide, on by default): every kernel is
+// launched with programmatic stream serialisation, so that its prologue overlaps
+// the tail of the kernel before it in the stream (grid_dep_wait in ptx.cuh).  Off,
+// each kernel starts after the previous one has completed; results are the same.
+void set_launch_overlap(bool on);
+bool launch_overlap();
+
+// fn<<<grid, block, smem, st>>>(args...) through cudaLaunchKernelEx, with
+// programmatic stream serialisation while launch_overlap() and, for cluster > 1,
+// clusters of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*fn)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (launch_overlap()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, std::forward<Args>(args)...);
+  if (e != cudaSuccess) (void)cudaGetLastError();  // returned here; not left for a later check
+  return e;
+}
 
 // Kernel launch registry.  Every launch is counted per kernel kind; while
 // timing is on, a pair of CUDA events is recorded on the launch stream around

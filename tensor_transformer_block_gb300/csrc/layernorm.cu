@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(1024) k_ln_fwd(const uint4* __restrict__ X, co
                                                  const uint4* __restrict__ beta, uint4* __restrict__ Y,
                                                  float* __restrict__ mean, float* __restrict__ rstd, int T,
                                                  int nvec, float inv_h, float eps, int io, unsigned* err) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   __shared__ float red[64];
   const bool x16 = io & kLnXF16, y16 = io & kLnYF16;
   int64_t row = blockIdx.x;
@@ -159,6 +161,8 @@ __global__ void __launch_bounds__(PF ? 512 : 1024)
              const float* __restrict__ rstd, const uint4* __restrict__ dY, const uint4* __restrict__ dR,
              uint4* __restrict__ dX, float* __restrict__ part, int T, int nvec, float inv_h, int io,
              unsigned* err) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   __shared__ float red[64];
   const bool x16 = io & kLnXF16, dy16 = io & kLnDyF16, dr16 = io & kLnDrF16, dx16 = io & kLnDxF16;
   float gm[VPT][8], pg[VPT][8], pb[VPT][8];
@@ -265,6 +269,8 @@ constexpr int kColsumWarps = 8;
 __global__ void __launch_bounds__(kColsumWarps * 32) k_ln_colsum(const float* __restrict__ part, int P, int two_h,
                                                                    int h, __nv_bfloat16* dgamma,
                                                                    __nv_bfloat16* dbeta) {
+  grid_dep_wait();  // the previous kernel in the stream has completed
+  grid_dep_launch();
   __shared__ float red[kColsumWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * 32 + lane;
@@ -351,13 +357,8 @@ int launch_ln_fwd(const void* X, const void* gamma, const void* beta, void* Y, f
   if (nb > T) nb = T;
   const int slot = timing_begin(kKLnFwd, st);
   const dim3 grid(static_cast<unsigned>(nb));
-  if (g.vpt == 4)
-    k_ln_fwd<4><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io,
-                                            err);
-  else
-    k_ln_fwd<1><<<grid, g.threads, 0, st>>>(x, ga, be, y, mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io,
-                                            err);
-  const bool ok = cudaGetLastError() == cudaSuccess;
+  const bool ok = launch_k(g.vpt == 4 ? k_ln_fwd<4> : k_ln_fwd<1>, grid, dim3(g.threads), 0, st, 1, x, ga, be, y,
+                           mean, rstd, static_cast<int>(T), nvec, inv_h, eps, io, err) == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
 }
@@ -387,24 +388,16 @@ int launch_ln_bwd(const void* X, const void* gamma, const float* mean, const flo
   const auto* dr = static_cast<const uint4*>(dR);
   auto* dx = static_cast<uint4*>(dX);
   int slot = timing_begin(kKLnBwd, st);
-  if (g.pf && g.vpt == 2)
-    k_ln_bwd<2, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h, io, err);
-  else if (g.pf)
-    k_ln_bwd<1, true><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                 inv_h, io, err);
-  else
-    k_ln_bwd<2, false><<<grid, g.threads, 0, st>>>(x, ga, mean, rstd, dy, dr, dx, part, static_cast<int>(T), nvec,
-                                                  inv_h, io, err);
-  bool ok = cudaGetLastError() == cudaSuccess;
+  bool ok = launch_k(g.pf ? (g.vpt == 2 ? k_ln_bwd<2, true> : k_ln_bwd<1, true>) : k_ln_bwd<2, false>,
+                     dim3(static_cast<unsigned>(grid)), dim3(g.threads), 0, st, 1, x, ga, mean, rstd, dy, dr, dx, part,
+                     static_cast<int>(T), nvec, inv_h, io, err) == cudaSuccess;
   timing_end(slot, st);
   if (!ok) return 2;
   slot = timing_begin(kKLnColsum, st);
   const int two_h = static_cast<int>(2 * h);
-  k_ln_colsum<<<(two_h + 31) / 32, kColsumWarps * 32, 0, st>>>(part, grid, two_h, static_cast<int>(h),
-                                                    static_cast<__nv_bfloat16*>(dgamma),
-                                                    static_cast<__nv_bfloat16*>(dbeta));
-  ok = cudaGetLastError() == cudaSuccess;
+  ok = launch_k(k_ln_colsum, dim3(static_cast<unsigned>((two_h + 31) / 32)), dim3(kColsumWarps * 32), 0, st, 1,
+                static_cast<const float*>(part), grid, two_h, static_cast<int>(h),
+                static_cast<__nv_bfloat16*>(dgamma), static_cast<__nv_bfloat16*>(dbeta)) == cudaSuccess;
   timing_end(slot, st);
   return ok ? 0 : 2;
 }

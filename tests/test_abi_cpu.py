@@ -134,3 +134,11 @@ def test_gemm_tiling_modes(lib):
         assert lib.tp_set_gemm_tiling(m) == 0
     for m in (3, -1, 4):
         assert lib.tp_set_gemm_tiling(m) == 2
+
+
+def test_launch_overlap_setting(lib):
+    """Overlap 0 and 1 are accepted; any other value is rejected."""
+    for v in (0, 1):
+        assert lib.tp_set_launch_overlap(v) == 0
+    for v in (2, -1):
+        assert lib.tp_set_launch_overlap(v) == 2

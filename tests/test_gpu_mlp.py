@@ -50,7 +50,12 @@ def test_mlp_f32_forward_full_config():
     assert_f32_parity(_np(fwd["A"]), ref["A"], "A")
 
 
-@pytest.mark.parametrize("T,h,f,N", [(77, 40, 96, 3), (130, 264, 520, 5), (1, 8, 16, 2)])
+@pytest.mark.parametrize("T,h,f,N", [
+    (77, 40, 96, 3),      # K split over 2 (fc1) and 4 (fc2, one CTA of the cluster idle) CTAs
+    (130, 264, 520, 5),   # ragged tiles, K split over 8
+    (1, 8, 16, 2),        # one K slice: no split
+    (1024, 512, 4096, 2), # fc1 enough tiles for every SM: no split; fc2 split over 2
+])
 def test_mlp_f32_forward_ragged(T, h, f, N):
     inp, r, fwd, _ = _run(T, h, f, N, dtype="f32", backward=False, seed=3)
     ref = O.mlp_forward(r["X"], r["W1s"], r["W2s"])
