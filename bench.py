@@ -44,14 +44,14 @@ DEFAULT_WORKLOAD = "mlp_bf16_T8192_h4096_f16384_N8"
 # the sha256 of the kernel source it was taken on; reported as null once the
 # source has changed.
 NCU_TRAFFIC: dict = {
-    k: {"bytes": v, "sha": "00de2e47bef2d6bb", "workload": "mlp_bf16_T8192_h4096_f16384_N8"}
+    k: {"bytes": v, "sha": "04b6bb428e76ec66", "workload": "mlp_bf16_T8192_h4096_f16384_N8"}
     for k, v in {
-        "mlp.fc1_col_gemm_gelu": 1026003712,
-        "mlp.fc2_row_gemm_shard_sum": 1509922304,
-        "mlp.bwd_dA_gemm_dgelu": 1141448960,
-        "mlp.bwd_dW2_gemm": 1326806272,
-        "mlp.bwd_dW1_gemm": 1274430976,
-        "mlp.bwd_dX_row_gemm_shard_sum": 1545751552,
+        "mlp.fc1_col_gemm_gelu": 1030209280,
+        "mlp.fc2_row_gemm_shard_sum": 1446737920,
+        "mlp.bwd_dA_gemm_dgelu": 1140733952,
+        "mlp.bwd_dW2_gemm": 1330707456,
+        "mlp.bwd_dW1_gemm": 1317489920,
+        "mlp.bwd_dX_row_gemm_shard_sum": 1448254464,
     }.items()
 }
 
