@@ -735,10 +735,11 @@ def run_gpu(args, w) -> None:
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e2e_run(args.steps, e0)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        with ClockSampler(gpu_id) as cs_e2e:
+            e0.record(stream)
+            e2e_run(args.steps, e0)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
         barrier()
         buf[zkey] = z0
         if dx0 is not None:
@@ -750,6 +751,7 @@ def run_gpu(args, w) -> None:
             ems = float(t.item())
         e2e = {"value": world * flops * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
+               "clocks": cs_e2e.summary(),
                "path": "pinned host -> device copies of each step's inputs on a copy stream, tp_* C-ABI calls on "
                        "the compute stream, device -> pinned host copies of each step's outputs on a second copy "
                        "stream; inputs and outputs double-buffered on the device so that the copies of the "

@@ -235,8 +235,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int t = lane; t < BLK; t += 32) {
         const int q = q0 + t;
         const bool in = q < a.S && TP_DCHECK(row_base + q < static_cast<size_t>(a.B) * a.H * a.S, err);
-        lse_s[st * BLK + t] = in ? lse[row_base + q] * kLog2e : 0.0f;
-        dd_s[st * BLK + t] = in ? dsum[row_base + q] : 0.0f;
+        // negated, so that the elementwise phases add them with paired fp32 instructions
+        lse_s[st * BLK + t] = in ? -(lse[row_base + q] * kLog2e) : 0.0f;
+        dd_s[st * BLK + t] = in ? -dsum[row_base + q] : 0.0f;
       }
       __threadfence_block();
       __syncwarp();
@@ -352,8 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = (a.causal && q0 < k0 + BLK) || (q0 + 64 > a.S) || (k0 + BLK > a.S);
-      const float4* ls4 = reinterpret_cast<const float4*>(lse_s + st * BLK + 64 * half);  // LSE * log2(e)
-      const float4* ds4 = reinterpret_cast<const float4*>(dd_s + st * BLK + 64 * half);
+      const float4* ls4 = reinterpret_cast<const float4*>(lse_s + st * BLK + 64 * half);  // -LSE * log2(e)
+      const float4* ds4 = reinterpret_cast<const float4*>(dd_s + st * BLK + 64 * half);  // -Dsum
       float p[64];
       // P^T = exp(S^T / sqrt(d) - LSE), fp16, over the first half of these columns
       {
@@ -362,14 +363,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(tmem + trow + cS + 32, v[1]);
         tmem_ld_wait(v[0]);
         tmem_ld_wait(v[1]);
+        // the exponent arguments s * scale - LSE two at a time (paired fp32 FMA; each
+        // half rounded as the scalar FMA rounds it)
+        const uint64_t sc2 = f32x2(scale_log2, scale_log2);
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 l4 = ls4[c4];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 4; u += 2) {
             const int qc = 4 * c4 + u;
-            p[qc] = ex2_approx(fmaf(__uint_as_float(v[qc >> 5][qc & 31]), scale_log2, -lv[u]));
+            float x0, x1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(v[qc >> 5][qc & 31]), __uint_as_float(v[qc >> 5][(qc + 1) & 31])),
+                                  sc2, u == 0 ? f32x2(l4.x, l4.y) : f32x2(l4.z, l4.w)),
+                        x0, x1);
+            p[qc] = ex2_approx(x0);
+            p[qc + 1] = ex2_approx(x1);
           }
         }
       }
@@ -399,14 +407,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld32(tmem + trow + 128 + cS + 32, v[1]);
         tmem_ld_wait(v[0]);
         tmem_ld_wait(v[1]);
+        // P * (dP - Dsum) two at a time (paired fp32 add and multiply)
 #pragma unroll
         for (int c4 = 0; c4 < 16; ++c4) {
           const float4 d4 = ds4[c4];
-          const int qc = 4 * c4;
-          dk[2 * c4] = pack_f16x2(p[qc] * (__uint_as_float(v[qc >> 5][qc & 31]) - d4.x),
-                                  p[qc + 1] * (__uint_as_float(v[qc >> 5][(qc + 1) & 31]) - d4.y));
-          dk[2 * c4 + 1] = pack_f16x2(p[qc + 2] * (__uint_as_float(v[qc >> 5][(qc + 2) & 31]) - d4.z),
-                                      p[qc + 3] * (__uint_as_float(v[qc >> 5][(qc + 3) & 31]) - d4.w));
+#pragma unroll
+          for (int u = 0; u < 4; u += 2) {
+            const int qc = 4 * c4 + u;
+            const uint64_t t = add_f32x2(f32x2(__uint_as_float(v[qc >> 5][qc & 31]),
+                                               __uint_as_float(v[qc >> 5][(qc + 1) & 31])),
+                                         u == 0 ? f32x2(d4.x, d4.y) : f32x2(d4.z, d4.w));
+            float y0, y1;
+            f32x2_split(mul_f32x2(f32x2(p[qc], p[qc + 1]), t), y0, y1);
+            dk[2 * c4 + u / 2] = pack_f16x2(y0, y1);
+          }
         }
       }
       tmem_st32(tmem + trow + 128 + cS, dk);
