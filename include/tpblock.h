@@ -112,8 +112,11 @@ TP_API size_t tp_mlp_workspace_bytes(int dtype, int64_t T, int64_t h, int64_t f,
  *   Z      [T][h]                 output, the shard partial sums added on the device
  *                                 in order i = 0..N-1 in one fp32 accumulator
  * GeLU_tanh(x) = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated in fp32.
- * TP_F32: every tensor fp32, FFMA accumulation.  TP_BF16: bf16 tensors, fp32
- * accumulation, outputs rounded to bf16 once. */
+ * TP_F32: every tensor fp32, FFMA accumulation; when the output tiles would leave
+ * most SMs idle (few tokens) each tile's K loop (shard 0..N-1, then K within a
+ * shard) is split into up to 8 contiguous ranges whose fp32 partial sums are added
+ * in range order, so the order stays fixed for a shape.  TP_BF16: bf16 tensors,
+ * fp32 accumulation, outputs rounded to bf16 once. */
 TP_API int tp_mlp_fwd(int dtype, int64_t T, int64_t h, int64_t f, int N,
                const void* X, const void* W1s, const void* W2s,
                void* Y_save, void* A_save, void* Z,
