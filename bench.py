@@ -792,7 +792,10 @@ def run_gpu(args, w) -> None:
                            "launch_overlap": bool(args.launch_overlap),
                            "l2": ("flushed before each step (256 MiB write, outside the step's CUDA events)"
                                   if flush is not None else
-                                  f"inputs larger than L2 (step working set {work_bytes / 2**30:.2f} GiB); no flush")},
+                                  (f"inputs larger than L2 (step working set {work_bytes / 2**30:.2f} GiB); no flush"
+                                   if work_bytes > (129 << 20) else
+                                   f"not flushed (--l2 none; the step working set, {work_bytes / 2**30:.2f} GiB, "
+                                   f"fits in L2)"))},
                 "pct_of_peak": {"of_measured_burst": value / world / pk["bf16_tflops"],
                                 "of_measured_sustained": value / world / pk["bf16_tflops_sustained"],
                                 "peaks": pk["source"], "of_nominal_dense": value / world / nominal,
