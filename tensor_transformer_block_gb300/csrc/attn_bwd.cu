@@ -641,14 +641,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 template <int D>
 int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* dout, const float* lse, float* dsum,
                  void* dsbuf, void* dqkv, unsigned* err, unsigned long long timeout_ns, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(k_attn_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvCfg<D>::SMEM) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_attn_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg<D>::SMEM) != cudaSuccess)
-      return 2;
-    configured = true;
-  }
+  static std::atomic<bool> configured_kv[kMaxDevices], configured_q[kMaxDevices];
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(k_attn_dkdv<D>), DkdvCfg<D>::SMEM, configured_kv) ||
+      !set_smem_limit_once(reinterpret_cast<const void*>(k_attn_dq<D>), DqCfg<D>::SMEM, configured_q))
+    return 2;
   // the dS tiles: [tiles * 128 key rows][128 query columns] fp16; written in 32 x 32
   // boxes (64-byte swizzle) by dK/dV, read in 64 x 128 boxes (128-byte swizzle) by dQ
   CUtensorMap tds, tds_st;

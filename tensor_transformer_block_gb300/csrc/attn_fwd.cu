@@ -412,12 +412,8 @@ template <int D>
 int launch_fwd_d(const AttnDims& a, const void* qkv, void* o, float* lse, unsigned* err, unsigned long long timeout_ns,
                  cudaStream_t st) {
   using C = FwdCfg<D>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-      return 2;
-    configured = true;
-  }
+  static std::atomic<bool> configured[kMaxDevices];
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(k_attn_fwd<D>), C::SMEM, configured)) return 2;
   CUtensorMap tqkv, to;
   const uint64_t qd[4] = {static_cast<uint64_t>(a.qkv_width()), static_cast<uint64_t>(a.S),
                           static_cast<uint64_t>(a.B), static_cast<uint64_t>(a.N)};

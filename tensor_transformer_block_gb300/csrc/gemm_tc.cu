@@ -881,20 +881,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, GemmShape);
 
-constexpr int kMaxDev = 64;
-
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 KernelFn get_kernel() {
-  static bool configured[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  static std::atomic<bool> configured[kMaxDevices];
   auto fn = &k_gemm<PAIR, A_MN, B_MN, EPI>;
-  if (!configured[dev]) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<PAIR, EPI>::SMEM_ALLOC) !=
-        cudaSuccess)
-      return nullptr;
-    configured[dev] = true;
-  }
+  if (!set_smem_limit_once(reinterpret_cast<const void*>(fn), Cfg<PAIR, EPI>::SMEM_ALLOC, configured)) return nullptr;
   return fn;
 }
 

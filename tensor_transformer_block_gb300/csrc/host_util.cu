@@ -25,7 +25,6 @@ void load_encode() {
     g_encode = reinterpret_cast<EncodeTiledFn>(fn);
 }
 
-constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices] = {0};
 
 }  // namespace
@@ -126,6 +125,15 @@ cudaEvent_t take_event() {
 namespace {
 std::atomic<bool> g_overlap{true};
 }  // namespace
+
+bool set_smem_limit_once(const void* fn, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (done[dev].load()) return true;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done[dev].store(true);
+  return true;
+}
 
 void set_launch_overlap(bool on) { g_overlap.store(on); }
 bool launch_overlap() { return g_overlap.load(); }

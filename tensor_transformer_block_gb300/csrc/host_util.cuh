@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <atomic>
 #include <utility>
 
 namespace tpb {
@@ -23,6 +24,12 @@ bool encode_tmap_strided(CUtensorMap* map, int rank, const void* base, const uin
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int device_sm_count();
+
+// Raises a kernel's dynamic shared-memory limit to ``bytes`` on the current device,
+// once per device (the attribute belongs to the device's context); ``done`` is the
+// kernel's own per-device flag array.  False if the device or the call fails.
+constexpr int kMaxDevices = 64;
+bool set_smem_limit_once(const void* fn, int bytes, std::atomic<bool> (&done)[kMaxDevices]);
 
 // Current device's compute capability as major*10+minor, or -1.
 int device_cc();
