@@ -146,7 +146,7 @@ def run_calls() -> list:
 
 
 if __name__ == "__main__":
-    # child process: the library chosen by TPBLOCK_LIB; prints the verdict
+    # child process: the library chosen by TPBLOCK_LIB; prints the result
     torch.cuda.set_device(0)
     hit = run_calls()
     st = tp.tp_sync_status()
