@@ -100,6 +100,30 @@ def kernel_flops(w) -> dict:
     return out
 
 
+# ------------------------------------------------------------ replicas (N > 1)
+def dist_env() -> tuple:
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the whole job ends with its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, ms: float, world: int) -> float:
+    """Every rank runs the same step on its own GPU (independent replicas, weak
+    scaling): the job does world x steps steps in the slowest rank's time."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 def step_flops(w) -> float:
     T, h, f = w.T, w.h, w.f
     tot = 0.0
@@ -303,8 +327,7 @@ def cpu_baseline(w, inp_np, target_s: float = 15.0) -> dict:
 
 
 def run_reference(args, w) -> None:
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    if dist_env()[1] != 0:  # rank 0 alone times the oracle; the other ranks exit without work
         return
     inp_np = oracle_inputs(w)
     rows = calibrate_rows(w, inp_np, 3.0)
@@ -444,9 +467,7 @@ def run_gpu(args, w) -> None:
     import tensor_transformer_block_gb300 as tp
     from tensor_transformer_block_gb300 import block, inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if world > 1:
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -626,12 +647,9 @@ def run_gpu(args, w) -> None:
     ms_ev, _, rep, clocks_ev = timed_region(True)
     if tp.tp_sync_status(stream) != 0:
         raise RuntimeError("device error during the timed region")
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     flops = step_flops(w)
-    value = world * flops * args.steps / (ms / 1e3) / 1e12
+    value = whole_job_tflops(flops, args.steps, ms, world)
 
     # the dominant kernel: largest share of event-measured time in the timed region
     pk = peaks()
@@ -744,12 +762,8 @@ def run_gpu(args, w) -> None:
         buf[zkey] = z0
         if dx0 is not None:
             dx_set(dx0)
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * flops * args.steps / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_tflops(flops, args.steps, ems, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems / args.steps,
                "clocks": cs_e2e.summary(),
                "path": "pinned host -> device copies of each step's inputs on a copy stream, tp_* C-ABI calls on "
