@@ -70,14 +70,14 @@ __global__ void k_attn_dsum(const uint4* __restrict__ o, const uint4* __restrict
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (valid && sub == 0) {
-      const long long shard = idx / (T * a.hN);
-      const long long rem = idx - shard * T * a.hN;
-      const long long t = rem / a.hN;
-      const int jj = static_cast<int>(rem - t * a.hN);
-      const long long bb = t / a.S, ss = t - bb * a.S;
-      const long long j = shard * a.hN + jj;
-      const long long di = (bb * a.H + j) * a.S + ss;
-      if (TP_DCHECK(di >= 0 && di < static_cast<long long>(a.B) * a.H * a.S, err)) dsum[di] = s;
+      // row idx = (shard T + t) hN + jj -> Dsum[b][head][s]; 32-bit (the launcher
+      // keeps B S H below 2^31), three divisions per row instead of 64-bit ones
+      const uint32_t ui = static_cast<uint32_t>(idx), hN = static_cast<uint32_t>(a.hN);
+      const uint32_t q = ui / hN, jj = ui - q * hN;
+      const uint32_t T32 = static_cast<uint32_t>(T), shard = q / T32, t = q - shard * T32;
+      const uint32_t S32 = static_cast<uint32_t>(a.S), bb = t / S32, ss = t - bb * S32;
+      const uint32_t di = (bb * static_cast<uint32_t>(a.H) + shard * hN + jj) * S32 + ss;
+      if (TP_DCHECK(di < static_cast<uint32_t>(a.B * a.H * a.S), err)) dsum[di] = s;
     }
   }
 }
@@ -671,6 +671,7 @@ int launch_bwd_d(const AttnDims& a, const void* qkv, const void* o, const void* 
 
   const long long rows = static_cast<long long>(a.N) * a.B * a.S * a.hN;
   const int sms = device_sm_count();
+  if (rows >= (1ll << 31)) return 1;                // Dsum's 32-bit row indices
   long long blocks = (rows * (D / 8) + 255) / 256;  // D/8 lanes per row
   if (blocks > static_cast<long long>(sms) * 8) blocks = static_cast<long long>(sms) * 8;
   int slot = timing_begin(kKAttnDsum, st);
